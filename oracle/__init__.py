@@ -1,0 +1,53 @@
+"""CPU oracle for the MoE dispatch / experts / combine layer.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import, call or
+execute anything in this package: only the test suite, the smoke check in
+``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` use it.  It shares
+no code with the CUDA library (no kernels, headers, helpers, tables or
+constants); the only thing both sides share is the seeded input generator in
+``synthetic``, which holds none of the method's arithmetic.
+
+It is a plain, slow, obviously-correct restatement of what the pages define:
+
+* "feat: add hybridep (NVIDIA-NeMo/Automodel #1333)" -- top-k indices become a
+  multihot ``routing_map`` plus fp32 ``probs`` (Changelog; review of
+  ``dispatch()``: fp32 probs, ``tokens_per_expert``, ``pad_multiple``,
+  ``num_permuted_tokens = tokens_per_expert.sum()``; review asking for tests of
+  ``_indices_to_multihot``: basic, topk=1, all -1, partial -1, single token,
+  duplicate expert assignments).
+* "Add the deepep expert-parallel implementation (huggingface/transformers
+  #49638)" -- What this adds: Expanded layout (one row per (token, local
+  expert) slot, grouped by expert, carrying the slot's routing weight; the
+  experts apply the weights, the combine only sums); Eager vs captured (exact
+  received rows vs a worst-case buffer whose spare rows are zeroed and sent to
+  a sentinel expert that the experts skip); Training (the combine's backward is
+  a dispatch along the forward layout; routing-weight gradients go back through
+  the combine); Benchmarks (experts are bf16 grouped GEMMs).
+
+Floating point: expert math in fp64 from the exact bf16 values, with the
+roundings the layer itself has (h and y to bf16); combine sums in fp32 in a
+fixed order and rounds once to bf16.
+
+Every function is pinned by ``tests/test_oracle_*.py`` against something other
+than itself (hand-written cases, library routines, closed forms, brute force,
+finite differences).  No function here is "parity unpinned".
+"""
+from .bf16 import (bf16_bits_to_f64, bf16_bits_to_f32, f64_to_bf16_bits,
+                   f32_to_bf16_bits, bf16_round_f64)
+from .moe_oracle import (OracleIndexError, OracleCapacityError, sentinel_expert,
+                         route_to_multihot, counts_and_offsets, build_layout,
+                         dispatch, expert_forward_f64, grouped_experts, combine,
+                         combine_backward, routing_weight_grad,
+                         expert_backward_f64, grouped_experts_backward,
+                         dispatch_backward, route_to_multihot_backward,
+                         layer_forward, layer_backward, worst_case_capacity)
+
+__all__ = [
+    "bf16_bits_to_f64", "bf16_bits_to_f32", "f64_to_bf16_bits", "f32_to_bf16_bits",
+    "bf16_round_f64", "OracleIndexError", "OracleCapacityError", "sentinel_expert",
+    "route_to_multihot", "counts_and_offsets", "build_layout", "dispatch",
+    "expert_forward_f64", "grouped_experts", "combine", "combine_backward",
+    "routing_weight_grad", "expert_backward_f64", "grouped_experts_backward",
+    "dispatch_backward", "route_to_multihot_backward", "layer_forward",
+    "layer_backward", "worst_case_capacity",
+]
