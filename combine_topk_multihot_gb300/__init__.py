@@ -1,0 +1,16 @@
+"""Single-GPU MoE dispatch / experts / combine for GB300 (sm_103a).
+
+The compute path is the CUDA library ``_lib/libmoe.so`` (C ABI in
+``include/moe.h``); this package is its Python binding.  Importing it fails
+loudly if the library has not been built -- there is no CPU fallback.
+"""
+from .moe import (Layout, MoEError, ForwardResult, worst_case_rows, moe_route_to_multihot,
+                  moe_dispatch, moe_grouped_experts, moe_combine, moe_combine_backward,
+                  moe_dispatch_backward, moe_route_to_multihot_backward, moe_layer_forward)
+from . import _native
+
+__all__ = [
+    "Layout", "MoEError", "ForwardResult", "worst_case_rows", "moe_route_to_multihot",
+    "moe_dispatch", "moe_grouped_experts", "moe_combine", "moe_combine_backward",
+    "moe_dispatch_backward", "moe_route_to_multihot_backward", "moe_layer_forward", "_native",
+]

@@ -1,0 +1,282 @@
+// The C ABI declared in include/moe.h: argument validation on the host, then
+// the launches.  No allocation, no global state besides per-device caches of
+// immutable device properties and the thread-local error text.
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+moe_status fail(moe_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+moe_status cuda_fail(cudaError_t err, const char* where) {
+  return fail(MOE_ERR_CUDA, "%s: %s", where, cudaGetErrorString(err));
+}
+
+constexpr int MAX_DEVICES = 64;
+int g_cc_ok[MAX_DEVICES];    // 0 unknown, 1 compute capability 10.3, -1 other
+int g_sms[MAX_DEVICES];
+
+moe_status check_device() {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
+  if (dev < 0 || dev >= MAX_DEVICES) return fail(MOE_ERR_DEVICE, "device ordinal %d unsupported", dev);
+  if (g_cc_ok[dev] == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if ((err = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (err = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(err, "cudaDeviceGetAttribute");
+    g_sms[dev] = sms;
+    g_cc_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    if (g_cc_ok[dev] < 0) {
+      return fail(MOE_ERR_DEVICE, "device %d has compute capability %d.%d; this library is built for 10.3 (sm_103a)",
+                  dev, major, minor);
+    }
+  }
+  if (g_cc_ok[dev] < 0) return fail(MOE_ERR_DEVICE, "device %d is not compute capability 10.3", dev);
+  return MOE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define MOE_REQUIRE(cond, st, ...) \
+  do {                             \
+    if (!(cond)) return fail(st, __VA_ARGS__); \
+  } while (0)
+
+moe_status check_routing_shape(int32_t T, int32_t K, int32_t E) {
+  MOE_REQUIRE(T >= 0, MOE_ERR_INVALID_ARG, "T must be >= 0 (got %d)", T);
+  MOE_REQUIRE(E >= 1 && E <= 1024, MOE_ERR_UNSUPPORTED_SHAPE, "E must be in [1, 1024] (got %d)", E);
+  MOE_REQUIRE(E % 4 == 0, MOE_ERR_UNSUPPORTED_SHAPE, "E must be a multiple of 4 (got %d)", E);
+  MOE_REQUIRE(K >= 1 && K <= E && K <= 127, MOE_ERR_UNSUPPORTED_SHAPE,
+              "K must be in [1, min(E, 127)] (got K=%d, E=%d)", K, E);
+  return MOE_OK;
+}
+
+moe_status check_hidden(int32_t H) {
+  MOE_REQUIRE(H > 0 && H % 256 == 0, MOE_ERR_UNSUPPORTED_SHAPE,
+              "the hidden size must be a positive multiple of 256 (got %d)", H);
+  return MOE_OK;
+}
+
+moe_status check_layout(const moe_layout* L) {
+  MOE_REQUIRE(L != nullptr, MOE_ERR_INVALID_ARG, "layout is NULL");
+  moe_status st = check_routing_shape(L->T, L->K, L->E);
+  if (st != MOE_OK) return st;
+  MOE_REQUIRE(L->pad_multiple >= 1, MOE_ERR_INVALID_ARG, "pad_multiple must be >= 1 (got %d)",
+              L->pad_multiple);
+  MOE_REQUIRE(L->capacity >= 0, MOE_ERR_INVALID_ARG, "capacity must be >= 0");
+  const int64_t worst = static_cast<int64_t>(L->T) * L->K +
+                        static_cast<int64_t>(L->E) * (L->pad_multiple - 1);
+  MOE_REQUIRE(worst < (int64_t(1) << 31) && L->capacity < (int64_t(1) << 31),
+              MOE_ERR_UNSUPPORTED_SHAPE, "row counts must fit in int32");
+  MOE_REQUIRE(L->tokens_per_expert && L->offsets && L->totals && L->status && L->workspace,
+              MOE_ERR_INVALID_ARG, "layout has a NULL count/offset/total/status/workspace pointer");
+  MOE_REQUIRE(L->capacity == 0 || (L->row_token && L->row_expert && L->row_weight),
+              MOE_ERR_INVALID_ARG, "layout has a NULL row buffer");
+  MOE_REQUIRE(L->T == 0 || L->token_row, MOE_ERR_INVALID_ARG, "layout has a NULL token_row");
+  MOE_REQUIRE(aligned16(L->workspace), MOE_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  return MOE_OK;
+}
+
+}  // namespace
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return 148;
+  if (g_sms[dev] == 0) {
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    g_sms[dev] = sms > 0 ? sms : 148;
+  }
+  return g_sms[dev];
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(moe_status status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "MOE_ERR_UNSUPPORTED_SHAPE";
+    case MOE_ERR_CAPACITY: return "MOE_ERR_CAPACITY";
+    case MOE_ERR_BAD_INDEX: return "MOE_ERR_BAD_INDEX";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+const char* moe_last_error(void) { return g_last_error; }
+
+moe_status moe_device_check(void) { return check_device(); }
+
+int64_t moe_worst_case_rows(int32_t T, int32_t E, int32_t K, int32_t pad_multiple) {
+  if (T < 0 || E < 1 || K < 1 || pad_multiple < 1) return -1;
+  return static_cast<int64_t>(T) * K + static_cast<int64_t>(E) * (pad_multiple - 1);
+}
+
+moe_status moe_layout_workspace_bytes(int32_t T, int32_t E, size_t* bytes) {
+  MOE_REQUIRE(bytes != nullptr, MOE_ERR_INVALID_ARG, "bytes is NULL");
+  MOE_REQUIRE(T >= 0 && E >= 1, MOE_ERR_INVALID_ARG, "bad T/E");
+  const size_t b = static_cast<size_t>(layout_chunks(T)) * E * sizeof(int32_t);
+  *bytes = ((b + 255) / 256) * 256 + 256;
+  return MOE_OK;
+}
+
+moe_status moe_route_to_multihot(const int64_t* topk_idx, const float* topk_probs, int32_t T,
+                                 int32_t K, int32_t E, uint8_t* routing_map, float* probs,
+                                 int8_t* winner_slot, int32_t* status, moe_stream_t stream) {
+  moe_status st = check_routing_shape(T, K, E);
+  if (st != MOE_OK) return st;
+  MOE_REQUIRE(T == 0 || (topk_idx && topk_probs && routing_map && probs && winner_slot && status),
+              MOE_ERR_INVALID_ARG, "moe_route_to_multihot: NULL pointer");
+  MOE_REQUIRE(aligned16(routing_map) && aligned16(probs) && aligned16(winner_slot),
+              MOE_ERR_INVALID_ARG, "moe_route_to_multihot: outputs must be 16-byte aligned");
+  if ((st = check_device()) != MOE_OK) return st;
+  cudaError_t err = launch_multihot(topk_idx, topk_probs, T, K, E, routing_map, probs, winner_slot,
+                                    status, stream);
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_route_to_multihot launch");
+}
+
+moe_status moe_dispatch(const moe_bf16* x, const uint8_t* routing_map, const float* probs,
+                        int32_t H, const moe_layout* L, moe_bf16* x_disp, int64_t* rows_host,
+                        moe_stream_t stream) {
+  moe_status st = check_layout(L);
+  if (st != MOE_OK) return st;
+  if ((st = check_hidden(H)) != MOE_OK) return st;
+  MOE_REQUIRE(L->T == 0 || (x && routing_map && probs), MOE_ERR_INVALID_ARG,
+              "moe_dispatch: NULL input");
+  MOE_REQUIRE(L->capacity == 0 || x_disp, MOE_ERR_INVALID_ARG, "moe_dispatch: NULL x_disp");
+  MOE_REQUIRE(aligned16(x) && aligned16(x_disp) && aligned16(routing_map), MOE_ERR_INVALID_ARG,
+              "moe_dispatch: x, x_disp and routing_map must be 16-byte aligned");
+  const int64_t worst = moe_worst_case_rows(L->T, L->E, L->K, L->pad_multiple);
+  if (!rows_host && L->capacity < worst)
+    return fail(MOE_ERR_CAPACITY,
+                "sync-free dispatch needs capacity >= T*K + E*(pad_multiple-1) = %lld rows (got %lld)",
+                static_cast<long long>(worst), static_cast<long long>(L->capacity));
+  if ((st = check_device()) != MOE_OK) return st;
+
+  int* chunk_counts = static_cast<int*>(L->workspace);
+  cudaError_t err = launch_layout_counts(routing_map, *L, chunk_counts, stream);
+  if (err != cudaSuccess) return cuda_fail(err, "moe_dispatch: counts");
+  if (rows_host) {
+    int32_t tot[2] = {0, 0}, dev_status = 0;
+    if ((err = cudaMemcpyAsync(tot, L->totals, sizeof(tot), cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
+        (err = cudaMemcpyAsync(&dev_status, L->status, sizeof(int32_t), cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
+        (err = cudaStreamSynchronize(stream)) != cudaSuccess)
+      return cuda_fail(err, "moe_dispatch: reading the row counts");
+    rows_host[0] = tot[0];
+    rows_host[1] = tot[1];
+    if (dev_status & MOE_DEVERR_BAD_INDEX)
+      return fail(MOE_ERR_BAD_INDEX, "an expert index outside [-1, E) was seen");
+    if (tot[0] > L->capacity)
+      return fail(MOE_ERR_CAPACITY, "the layout needs %d rows, capacity is %lld", tot[0],
+                  static_cast<long long>(L->capacity));
+  }
+  if ((err = launch_layout_place(routing_map, probs, *L, chunk_counts, stream)) != cudaSuccess)
+    return cuda_fail(err, "moe_dispatch: placement");
+  if ((err = launch_row_gather(x, *L, H, x_disp, true, nullptr, nullptr, stream)) != cudaSuccess)
+    return cuda_fail(err, "moe_dispatch: gather");
+  return MOE_OK;
+}
+
+moe_status moe_grouped_experts(const moe_bf16* x_disp, const moe_layout* L, int32_t H, int32_t I,
+                               const moe_bf16* W1, const moe_bf16* W2, moe_bf16* h,
+                               moe_bf16* y_disp, moe_bf16* o_save, moe_bf16* gu_save,
+                               moe_stream_t stream) {
+  moe_status st = check_layout(L);
+  if (st != MOE_OK) return st;
+  if ((st = check_hidden(H)) != MOE_OK) return st;
+  MOE_REQUIRE(I > 0 && I % 128 == 0, MOE_ERR_UNSUPPORTED_SHAPE,
+              "the intermediate size must be a positive multiple of 128 (got %d)", I);
+  MOE_REQUIRE(L->capacity == 0 || (x_disp && W1 && W2 && h && y_disp), MOE_ERR_INVALID_ARG,
+              "moe_grouped_experts: NULL pointer");
+  MOE_REQUIRE(aligned16(x_disp) && aligned16(W1) && aligned16(W2) && aligned16(h) &&
+                  aligned16(y_disp) && aligned16(o_save) && aligned16(gu_save),
+              MOE_ERR_INVALID_ARG, "moe_grouped_experts: pointers must be 16-byte aligned");
+  if ((st = check_device()) != MOE_OK) return st;
+  cudaError_t err = launch_experts_forward(x_disp, *L, H, I, W1, W2, h, y_disp, o_save, gu_save, stream);
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_grouped_experts launch");
+}
+
+moe_status moe_combine(const moe_bf16* y_disp, const moe_layout* L, int32_t H, moe_bf16* out,
+                       moe_stream_t stream) {
+  moe_status st = check_layout(L);
+  if (st != MOE_OK) return st;
+  if ((st = check_hidden(H)) != MOE_OK) return st;
+  MOE_REQUIRE(L->T == 0 || (y_disp && out), MOE_ERR_INVALID_ARG, "moe_combine: NULL pointer");
+  MOE_REQUIRE(aligned16(y_disp) && aligned16(out), MOE_ERR_INVALID_ARG,
+              "moe_combine: pointers must be 16-byte aligned");
+  if ((st = check_device()) != MOE_OK) return st;
+  cudaError_t err = launch_combine(y_disp, *L, H, out, nullptr, nullptr, stream);
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_combine launch");
+}
+
+moe_status moe_combine_backward(const moe_bf16* grad_out, const moe_bf16* o_save,
+                                const moe_layout* L, int32_t H, moe_bf16* grad_y, float* grad_w,
+                                moe_stream_t stream) {
+  moe_status st = check_layout(L);
+  if (st != MOE_OK) return st;
+  if ((st = check_hidden(H)) != MOE_OK) return st;
+  MOE_REQUIRE(L->capacity == 0 || (grad_out && grad_y), MOE_ERR_INVALID_ARG,
+              "moe_combine_backward: NULL pointer");
+  MOE_REQUIRE(!grad_w || o_save, MOE_ERR_INVALID_ARG,
+              "moe_combine_backward: grad_w needs o_save");
+  MOE_REQUIRE(aligned16(grad_out) && aligned16(grad_y) && aligned16(o_save), MOE_ERR_INVALID_ARG,
+              "moe_combine_backward: pointers must be 16-byte aligned");
+  if ((st = check_device()) != MOE_OK) return st;
+  cudaError_t err = launch_row_gather(grad_out, *L, H, grad_y, false, o_save, grad_w, stream);
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_combine_backward launch");
+}
+
+moe_status moe_dispatch_backward(const moe_bf16* grad_x_disp, const float* grad_w,
+                                 const moe_layout* L, int32_t H, moe_bf16* grad_x,
+                                 float* grad_probs, moe_stream_t stream) {
+  moe_status st = check_layout(L);
+  if (st != MOE_OK) return st;
+  if ((st = check_hidden(H)) != MOE_OK) return st;
+  MOE_REQUIRE(L->T == 0 || (grad_x_disp && grad_x), MOE_ERR_INVALID_ARG,
+              "moe_dispatch_backward: NULL pointer");
+  MOE_REQUIRE(aligned16(grad_x_disp) && aligned16(grad_x) && aligned16(grad_probs),
+              MOE_ERR_INVALID_ARG, "moe_dispatch_backward: pointers must be 16-byte aligned");
+  if ((st = check_device()) != MOE_OK) return st;
+  cudaError_t err = launch_combine(grad_x_disp, *L, H, grad_x, grad_w, grad_probs, stream);
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_dispatch_backward launch");
+}
+
+moe_status moe_route_to_multihot_backward(const float* grad_probs, const int64_t* topk_idx,
+                                          const int8_t* winner_slot, int32_t T, int32_t K,
+                                          int32_t E, float* grad_topk_probs, moe_stream_t stream) {
+  moe_status st = check_routing_shape(T, K, E);
+  if (st != MOE_OK) return st;
+  MOE_REQUIRE(T == 0 || (grad_probs && topk_idx && winner_slot && grad_topk_probs),
+              MOE_ERR_INVALID_ARG, "moe_route_to_multihot_backward: NULL pointer");
+  if ((st = check_device()) != MOE_OK) return st;
+  cudaError_t err = launch_multihot_backward(grad_probs, topk_idx, winner_slot, T, K, E,
+                                             grad_topk_probs, stream);
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_route_to_multihot_backward launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,122 @@
+// a6 / a10: combine -- each token's rows summed back into place, no weights.
+//
+// "Add the deepep expert-parallel implementation (huggingface/transformers
+// #49638)", What this adds, Expanded layout: the routing weights are applied
+// inside the experts, so the combine is a plain sum.  It runs in fp32 from +0.0 over
+// the token's rows in ascending expert order (token_row order), with one
+// rounding to bf16 at the end, so the result is independent of scheduling.
+// Training: the dispatch's backward is this same sum on the gradient rows;
+// the routing-weight gradient of each row is scattered to grad_probs[t, e].
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+
+namespace {
+
+__device__ __forceinline__ int pick4(const int (&a)[4], int j) {
+  return j == 0 ? a[0] : j == 1 ? a[1] : j == 2 ? a[2] : a[3];
+}
+
+__device__ __forceinline__ void acc_add(float (&acc)[8], const uint4& v) {
+  acc[0] += bf16_lo(v.x);
+  acc[1] += bf16_hi(v.x);
+  acc[2] += bf16_lo(v.y);
+  acc[3] += bf16_hi(v.y);
+  acc[4] += bf16_lo(v.z);
+  acc[5] += bf16_hi(v.z);
+  acc[6] += bf16_lo(v.w);
+  acc[7] += bf16_hi(v.w);
+}
+
+__device__ __forceinline__ uint4 acc_pack(const float (&acc)[8]) {
+  return make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                    pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+}
+
+// One warp per token.  Lane l holds token_row entries l, l+32, l+64, l+96.
+// Each lane owns H/256 16-byte column vectors; two are processed at a time,
+// and up to four rows are loaded before they are added (in row order) so that
+// eight 16-byte loads per lane are in flight.
+template <bool SCATTER>
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ rows,
+                                                      const int* __restrict__ token_row, int T,
+                                                      int K, int H, uint16_t* __restrict__ out,
+                                                      const int* __restrict__ row_expert,
+                                                      const float* __restrict__ grad_w,
+                                                      float* __restrict__ grad_probs, int E) {
+  const int lane = threadIdx.x & 31;
+  const int V = H >> 8;
+  const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long t = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       t < T; t += nwarps) {
+    int tr[4];
+    int n = 0;
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const int k = lane + 32 * jj;
+      tr[jj] = k < K ? token_row[t * K + k] : -1;
+      n += __popc(__ballot_sync(FULL_MASK, tr[jj] >= 0));
+    }
+    uint4* o = reinterpret_cast<uint4*>(out + t * H);
+    for (int v0 = 0; v0 < V; v0 += 2) {
+      const bool two = v0 + 1 < V;
+      float a0[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float a1[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int j0 = 0; j0 < n; j0 += 4) {
+        uint4 b0[4], b1[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int j = j0 + i;
+          const int r = __shfl_sync(FULL_MASK, pick4(tr, j >> 5), j & 31);
+          if (j < n) {
+            const uint4* src = reinterpret_cast<const uint4*>(rows + static_cast<long long>(r) * H);
+            b0[i] = __ldg(src + lane + 32 * v0);
+            if (two) b1[i] = __ldg(src + lane + 32 * (v0 + 1));
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (j0 + i < n) {
+            acc_add(a0, b0[i]);
+            if (two) acc_add(a1, b1[i]);
+          }
+        }
+      }
+      o[lane + 32 * v0] = acc_pack(a0);
+      if (two) o[lane + 32 * (v0 + 1)] = acc_pack(a1);
+    }
+    if (SCATTER && grad_probs) {
+      float* gp = grad_probs + t * E;
+      for (int e = lane * 4; e < E; e += 128)
+        *reinterpret_cast<float4*>(gp + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+      __syncwarp();
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int r = tr[jj];
+        if (r >= 0) gp[row_expert[r]] = grad_w ? grad_w[r] : 0.f;
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const uint16_t* rows, const moe_layout& L, int H, uint16_t* out,
+                           const float* grad_w, float* grad_probs, cudaStream_t s) {
+  if (L.T == 0) return cudaSuccess;
+  const int threads = 256;
+  const long long need = (static_cast<long long>(L.T) + 7) / 8;
+  const int blocks = static_cast<int>(need < 8LL * sm_count() ? need : 8LL * sm_count());
+  if (grad_probs) {
+    combine_kernel<true><<<blocks, threads, 0, s>>>(rows, L.token_row, L.T, L.K, H, out,
+                                                    L.row_expert, grad_w, grad_probs, L.E);
+  } else {
+    combine_kernel<false><<<blocks, threads, 0, s>>>(rows, L.token_row, L.T, L.K, H, out,
+                                                     nullptr, nullptr, nullptr, L.E);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

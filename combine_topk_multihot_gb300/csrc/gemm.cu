@@ -1,0 +1,427 @@
+// a5: the SwiGLU experts as two grouped GEMMs on the 5th-generation tensor
+// cores (tcgen05.mma, accumulators in tensor memory, operands staged by TMA).
+//
+// "Add the deepep expert-parallel implementation (huggingface/transformers
+// #49638)": Expanded layout -- an expert computes only the rows routed to it,
+// and the routing weight scales each row's output inside the expert step;
+// Eager vs captured -- unused rows carry the sentinel expert id and are never
+// computed; Benchmarks -- the experts are bf16 grouped GEMMs.  The SwiGLU form (gate, up, down) is the expert of the Qwen3-MoE
+// layer shapes benchmarked there.
+//
+//   GEMM1 (per expert e, over its rows):  [g | u] = x_disp W1[e]^T,
+//          epilogue h = bf16(silu(g) * u)            (optionally g, u saved)
+//   GEMM2:  o = h W2[e]^T,  epilogue y = bf16(w_row * o)   (optionally o saved)
+//
+// Design (one CTA per SM, persistent):
+//   * the tile list is built on the device from tokens_per_expert / offsets,
+//     so no host sync is needed and the launch can be graph-captured; pad and
+//     spare rows are never computed;
+//   * warp 0 issues TMA loads into a 4-stage shared-memory ring (128-byte
+//     swizzle), warp 1 owns the tensor memory and issues tcgen05.mma
+//     (128 x 256 x 16 per instruction), warps 2-5 are the epilogue;
+//   * two 256-column fp32 accumulators in tensor memory let the epilogue of
+//     one tile overlap the MMAs of the next;
+//   * every wait is bounded; a timeout sets MOE_DEVERR_TIMEOUT and the CTA
+//     drains its in-flight work, frees tensor memory and exits.
+
+#include <cstdio>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128;          // rows per tile (tensor-memory lanes)
+constexpr int BN = 256;          // accumulator columns per tile
+constexpr int BK = 64;           // bf16 elements per 128-byte swizzled row
+constexpr int UMMA_K = 16;       // K per tcgen05.mma for 16-bit inputs
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;           // 16 KiB
+constexpr int B_BYTES = BN * BK * 2;           // 32 KiB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES; // 48 KiB
+constexpr int NUM_THREADS = 192;
+constexpr int TMEM_COLS = 2 * BN;              // double-buffered accumulator
+constexpr int MAX_E = 1024;
+constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+
+enum Epilogue { EPI_SWIGLU = 0, EPI_WEIGHTED = 1 };
+
+struct GemmArgs {
+  const int* counts;       // [E] rows of each expert
+  const int* offsets;      // [E+1] group start rows
+  const float* row_weight; // [C]
+  int E;
+  int k_blocks;            // contraction length / BK
+  int n_tiles;             // N tiles per expert
+  int b_rows_per_expert;   // rows of B per expert (2I or H)
+  int b_tile_step;         // B row step per N tile (128 for GEMM1, 256 for GEMM2)
+  int b_second_off;        // row offset of the second 128-row B box (I or 128)
+  uint16_t* out0;          // GEMM1: h [C, I]     GEMM2: y [C, H]
+  int ld0;
+  uint16_t* out1;          // GEMM1: gu_save [C, 2I] (nullable)   GEMM2: o_save [C, H] (nullable)
+  int ld1;
+  int I;                   // GEMM1: offset of the up half in gu_save
+  int* status;
+};
+
+struct Smem {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int total_tiles;
+  int offsets[MAX_E + 1];
+  int counts[MAX_E];
+  int tile_prefix[MAX_E + 1];
+};
+
+constexpr size_t SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + sizeof(Smem);
+
+struct Tile {
+  int e, mt, nt;
+};
+
+__device__ __forceinline__ Tile decode_tile(const Smem& s, int E, int n_tiles, int tile) {
+  int lo = 0, hi = E;  // tile_prefix[lo] <= tile < tile_prefix[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s.tile_prefix[mid] <= tile) lo = mid; else hi = mid;
+  }
+  const int local = tile - s.tile_prefix[lo];
+  Tile t;
+  t.e = lo;
+  t.mt = local / n_tiles;
+  t.nt = local - t.mt * n_tiles;
+  return t;
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
+
+template <int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* tiles = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  Smem& s = *reinterpret_cast<Smem*>(tiles + STAGES * STAGE_BYTES);
+  const uint32_t tiles_u32 = smem_u32(tiles);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = args.E;
+
+  // ---- set-up: barriers, tensor memory, the device-side tile list
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(smem_u32(&s.full[i]), 1);
+      mbar_init(smem_u32(&s.empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&s.tfull[i]), 1);
+      mbar_init(smem_u32(&s.tempty[i]), 4);
+    }
+    mbar_init(smem_u32(&s.drain), 1);
+    s.abort = 0;
+    mbar_fence_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(&s.tmem_base), TMEM_COLS);
+  for (int e = threadIdx.x; e <= E; e += NUM_THREADS) s.offsets[e] = args.offsets[e];
+  for (int e = threadIdx.x; e < E; e += NUM_THREADS) s.counts[e] = args.counts[e];
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of per-expert tile counts
+    int running = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int n = e < E ? ((s.counts[e] + BM - 1) / BM) * args.n_tiles : 0;
+      int incl = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(FULL_MASK, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (e < E) s.tile_prefix[e] = running + incl - n;
+      running += __shfl_sync(FULL_MASK, incl, 31);
+    }
+    if (lane == 0) {
+      s.tile_prefix[E] = running;
+      s.total_tiles = running;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const int total = s.total_tiles;
+  const uint32_t tmem_base = s.tmem_base;
+  volatile int* abort_flag = &s.abort;
+
+  if (warp == 0) {
+    // ================= TMA producer =================
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const Tile t = decode_tile(s, E, args.n_tiles, tile);
+        const int a_row = s.offsets[t.e] + t.mt * BM;
+        const int b_row = t.e * args.b_rows_per_expert + t.nt * args.b_tile_step;
+        for (int kb = 0; kb < args.k_blocks; ++kb) {
+          if (!mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, abort_flag)) { ok = false; break; }
+          const uint32_t full = smem_u32(&s.full[stage]);
+          const uint32_t a_dst = tiles_u32 + stage * STAGE_BYTES;
+          const uint32_t b_dst = a_dst + A_BYTES;
+          mbar_arrive_expect_tx(full, STAGE_BYTES);
+          tma_load_2d(a_dst, &tmA, kb * BK, a_row, full);
+          tma_load_2d(b_dst, &tmB, kb * BK, b_row, full);
+          tma_load_2d(b_dst + B_BYTES / 2, &tmB, kb * BK, b_row + args.b_second_off, full);
+          ++issued;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // drain: wait for the loads of the last (up to STAGES) issued stages
+        for (int i = 0; i < STAGES && i < issued; ++i) {
+          if (--stage < 0) { stage = STAGES - 1; phase ^= 1u; }
+          mbar_wait_drain(smem_u32(&s.full[stage]), phase);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================= MMA issuer =================
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++local) {
+        const int buf = local & 1;
+        const uint32_t use = (local >> 1) & 1;
+        if (!mbar_wait(smem_u32(&s.tempty[buf]), use ^ 1u, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * BN;
+        for (int kb = 0; kb < args.k_blocks; ++kb) {
+          if (!mbar_wait(smem_u32(&s.full[stage]), phase, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = tiles_u32 + stage * STAGE_BYTES;
+          const uint64_t a_desc = sdesc_k_sw128(a_addr);
+          const uint64_t b_desc = sdesc_k_sw128(a_addr + A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            // advance along K inside the 128-byte swizzled row: 32 bytes per step
+            tc_mma_bf16(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, IDESC, (kb | kk) != 0);
+          }
+          tc_commit(smem_u32(&s.empty[stage]));
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (ok) tc_commit(smem_u32(&s.tfull[buf]));
+      }
+      // make sure every MMA this thread issued has finished before anyone
+      // frees tensor memory or shared memory
+      tc_commit(smem_u32(&s.drain));
+      if (!mbar_wait_drain(smem_u32(&s.drain), 0)) *abort_flag = 1;
+    }
+    __syncwarp();
+  } else {
+    // ================= epilogue (warps 2..5 -> TMEM lanes 32*(warp%4)) =================
+    const int q = warp & 3;
+    const int r_in_tile = q * 32 + lane;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
+      const Tile t = decode_tile(s, E, args.n_tiles, tile);
+      const int buf = local & 1;
+      const uint32_t use = (local >> 1) & 1;
+      if (!mbar_wait(smem_u32(&s.tfull[buf]), use, abort_flag)) break;
+      tc_fence_after();
+      const int group_row = t.mt * BM + r_in_tile;
+      const bool valid = group_row < s.counts[t.e];
+      const long long row = static_cast<long long>(s.offsets[t.e]) + group_row;
+      const uint32_t tb = tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
+      if (EPI == EPI_SWIGLU) {
+        // columns [0,128) gate, [128,256) up, for h columns nt*128 + [0,128)
+        const int col0 = t.nt * (BN / 2);
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld32(tb + c, g);
+          tmem_ld32(tb + BN / 2 + c, u);
+          tmem_ld_wait();
+          if (valid) {
+            uint32_t hv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+              const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+              hv[i] = pack_bf16x2(silu(g0) * u0, silu(g1) * u1);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(args.out0 + row * args.ld0 + col0 + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
+            if (args.out1) {
+              uint4* dg = reinterpret_cast<uint4*>(args.out1 + row * args.ld1 + col0 + c);
+              uint4* du = reinterpret_cast<uint4*>(args.out1 + row * args.ld1 + args.I + col0 + c);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                dg[i] = make_uint4(pack_bf16x2(__uint_as_float(g[8 * i + 0]), __uint_as_float(g[8 * i + 1])),
+                                   pack_bf16x2(__uint_as_float(g[8 * i + 2]), __uint_as_float(g[8 * i + 3])),
+                                   pack_bf16x2(__uint_as_float(g[8 * i + 4]), __uint_as_float(g[8 * i + 5])),
+                                   pack_bf16x2(__uint_as_float(g[8 * i + 6]), __uint_as_float(g[8 * i + 7])));
+                du[i] = make_uint4(pack_bf16x2(__uint_as_float(u[8 * i + 0]), __uint_as_float(u[8 * i + 1])),
+                                   pack_bf16x2(__uint_as_float(u[8 * i + 2]), __uint_as_float(u[8 * i + 3])),
+                                   pack_bf16x2(__uint_as_float(u[8 * i + 4]), __uint_as_float(u[8 * i + 5])),
+                                   pack_bf16x2(__uint_as_float(u[8 * i + 6]), __uint_as_float(u[8 * i + 7])));
+              }
+            }
+          }
+        }
+      } else {
+        const int col0 = t.nt * BN;
+        const float w = valid ? args.row_weight[row] : 0.f;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(tb + c, o);
+          tmem_ld_wait();
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(args.out0 + row * args.ld0 + col0 + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              float f[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) f[k] = __uint_as_float(o[8 * i + k]);
+              dst[i] = make_uint4(pack_bf16x2(w * f[0], w * f[1]), pack_bf16x2(w * f[2], w * f[3]),
+                                  pack_bf16x2(w * f[4], w * f[5]), pack_bf16x2(w * f[6], w * f[7]));
+            }
+            if (args.out1) {
+              uint4* dso = reinterpret_cast<uint4*>(args.out1 + row * args.ld1 + col0 + c);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                float f[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) f[k] = __uint_as_float(o[8 * i + k]);
+                dso[i] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                    pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&s.tempty[buf]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+  if (threadIdx.x == 0 && s.abort) report(args.status, MOE_DEVERR_TIMEOUT);
+}
+
+// ---------------------------------------------------------------- host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// A row-major bf16 matrix [rows, cols] read as 128-row x 64-column boxes with
+// the 128-byte swizzle; out-of-range rows read as zero.
+bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {BK, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int EPI>
+cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args,
+                        cudaStream_t s) {
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    err = cudaFuncSetAttribute(grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(SMEM_BYTES));
+    if (err != cudaSuccess) return err;
+    if (dev >= 0 && dev < 64) configured[dev] = true;
+  }
+  grouped_gemm_kernel<EPI><<<sm_count(), NUM_THREADS, SMEM_BYTES, s>>>(a, b, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_experts_forward(const uint16_t* x_disp, const moe_layout& L, int H, int I,
+                                   const uint16_t* W1, const uint16_t* W2, uint16_t* h,
+                                   uint16_t* y, uint16_t* o_save, uint16_t* gu_save,
+                                   cudaStream_t s) {
+  if (L.capacity == 0) return cudaSuccess;
+  const uint64_t C = static_cast<uint64_t>(L.capacity);
+  CUtensorMap mA1, mB1, mA2, mB2;
+  if (!make_map(&mA1, x_disp, C, H) || !make_map(&mB1, W1, static_cast<uint64_t>(L.E) * 2 * I, H) ||
+      !make_map(&mA2, h, C, I) || !make_map(&mB2, W2, static_cast<uint64_t>(L.E) * H, I))
+    return cudaErrorInvalidValue;
+
+  GemmArgs g1{};
+  g1.counts = L.tokens_per_expert;
+  g1.offsets = L.offsets;
+  g1.row_weight = L.row_weight;
+  g1.E = L.E;
+  g1.k_blocks = H / BK;
+  g1.n_tiles = I / (BN / 2);
+  g1.b_rows_per_expert = 2 * I;
+  g1.b_tile_step = BN / 2;
+  g1.b_second_off = I;
+  g1.out0 = h;
+  g1.ld0 = I;
+  g1.out1 = gu_save;
+  g1.ld1 = 2 * I;
+  g1.I = I;
+  g1.status = L.status;
+  cudaError_t err = launch_gemm<EPI_SWIGLU>(mA1, mB1, g1, s);
+  if (err != cudaSuccess) return err;
+
+  GemmArgs g2 = g1;
+  g2.k_blocks = I / BK;
+  g2.n_tiles = H / BN;
+  g2.b_rows_per_expert = H;
+  g2.b_tile_step = BN;
+  g2.b_second_off = BN / 2;
+  g2.out0 = y;
+  g2.ld0 = H;
+  g2.out1 = o_save;
+  g2.ld1 = H;
+  return launch_gemm<EPI_WEIGHTED>(mA2, mB2, g2, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,47 @@
+// Internal launchers (host side).  The public C ABI in moe.h validates the
+// arguments and calls these; they only size grids and launch.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "moe.h"
+
+namespace moe {
+
+int sm_count();  // SMs of the current device (cached)
+
+// Tokens per chunk of the layout's histogram / placement passes.
+constexpr int LAYOUT_CHUNK = 32;
+
+inline int64_t layout_chunks(int32_t T) { return (T + LAYOUT_CHUNK - 1) / LAYOUT_CHUNK; }
+
+cudaError_t launch_multihot(const int64_t* topk_idx, const float* topk_probs, int T, int K, int E,
+                            uint8_t* routing_map, float* probs, int8_t* winner, int* status,
+                            cudaStream_t s);
+cudaError_t launch_multihot_backward(const float* grad_probs, const int64_t* topk_idx,
+                                     const int8_t* winner, int T, int K, int E, float* grad_topk,
+                                     cudaStream_t s);
+
+// Counts and offsets (a2).  chunk_counts is [E][chunks] int32 scratch.
+cudaError_t launch_layout_counts(const uint8_t* routing_map, const moe_layout& L,
+                                 int* chunk_counts, cudaStream_t s);
+// Stable placement of every (token, expert) pair (a3).
+cudaError_t launch_layout_place(const uint8_t* routing_map, const float* probs,
+                                const moe_layout& L, const int* chunk_base, cudaStream_t s);
+// Row gather x -> x_disp plus pad / spare row metadata (a4); also the combine
+// backward's gather (a7) with the optional routing-weight gradient (a8).
+cudaError_t launch_row_gather(const uint16_t* src, const moe_layout& L, int H, uint16_t* dst,
+                              bool write_row_meta, const uint16_t* o_save, float* grad_w,
+                              cudaStream_t s);
+// Per-token ordered sum of rows (a6 / a10), optional grad_probs scatter.
+cudaError_t launch_combine(const uint16_t* rows, const moe_layout& L, int H, uint16_t* out,
+                           const float* grad_w, float* grad_probs, cudaStream_t s);
+
+// tcgen05 grouped GEMMs of the experts (a5).
+cudaError_t launch_experts_forward(const uint16_t* x_disp, const moe_layout& L, int H, int I,
+                                   const uint16_t* W1, const uint16_t* W2, uint16_t* h,
+                                   uint16_t* y, uint16_t* o_save, uint16_t* gu_save,
+                                   cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,210 @@
+"""Python binding of the C ABI: argument marshalling only.
+
+Every step of the path runs in the CUDA library; PyTorch only allocates the
+device buffers and supplies the current stream.  The function names are the
+C entry points' names.  Pages cited:
+
+  [HEP] "feat: add hybridep (NVIDIA-NeMo/Automodel #1333)"
+  [DEP] "Add the deepep expert-parallel implementation (huggingface/transformers #49638)"
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import _native as N
+
+
+class MoEError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {N.status_string(code)}: {N.last_error()}")
+
+
+def _check(code: int, where: str):
+    if code != N.MOE_OK:
+        raise MoEError(code, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the library must be contiguous")
+    return ctypes.c_void_p(t.data_ptr()) if t.numel() else None
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _bf16(t: torch.Tensor, name: str) -> torch.Tensor:
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16")
+    return t
+
+
+def worst_case_rows(T: int, E: int, K: int, pad_multiple: int) -> int:
+    return int(N.lib.moe_worst_case_rows(T, E, K, pad_multiple))
+
+
+class Layout:
+    """The expanded layout of one forward + backward, in caller-owned device
+    buffers ([HEP]'s dispatch handle, made explicit; [DEP] Custom ops)."""
+
+    def __init__(self, T: int, E: int, K: int, pad_multiple: int, capacity: int,
+                 device="cuda", status: Optional[torch.Tensor] = None):
+        dev = torch.device(device)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.T, self.E, self.K, self.pad_multiple, self.capacity = T, E, K, pad_multiple, capacity
+        self.tokens_per_expert = torch.empty(E, **i32)
+        self.offsets = torch.empty(E + 1, **i32)
+        self.totals = torch.empty(2, **i32)
+        self.row_token = torch.empty(capacity, **i32)
+        self.row_expert = torch.empty(capacity, **i32)
+        self.row_weight = torch.empty(capacity, dtype=torch.float32, device=dev)
+        self.token_row = torch.empty(T * K, **i32)
+        self.status = status if status is not None else torch.zeros(1, **i32)
+        nbytes = ctypes.c_size_t(0)
+        _check(N.lib.moe_layout_workspace_bytes(T, E, ctypes.byref(nbytes)), "moe_layout_workspace_bytes")
+        self.workspace = torch.empty(nbytes.value, dtype=torch.uint8, device=dev)
+        self.c = N.MoeLayout(
+            T, E, K, pad_multiple, capacity,
+            self.tokens_per_expert.data_ptr(), self.offsets.data_ptr(), self.totals.data_ptr(),
+            self.row_token.data_ptr() if capacity else None,
+            self.row_expert.data_ptr() if capacity else None,
+            self.row_weight.data_ptr() if capacity else None,
+            self.token_row.data_ptr() if T * K else None,
+            self.status.data_ptr(), self.workspace.data_ptr())
+
+    @property
+    def ref(self):
+        return ctypes.byref(self.c)
+
+
+def moe_route_to_multihot(topk_idx: torch.Tensor, topk_probs: torch.Tensor, E: int,
+                          status: torch.Tensor, stream=None):
+    """a1: returns (routing_map uint8 [T,E], probs fp32 [T,E], winner_slot int8 [T,E])."""
+    T, K = topk_idx.shape
+    assert topk_idx.dtype == torch.int64 and topk_probs.dtype == torch.float32
+    dev = topk_idx.device
+    routing_map = torch.empty(T, E, dtype=torch.uint8, device=dev)
+    probs = torch.empty(T, E, dtype=torch.float32, device=dev)
+    winner = torch.empty(T, E, dtype=torch.int8, device=dev)
+    _check(N.lib.moe_route_to_multihot(_ptr(topk_idx), _ptr(topk_probs), T, K, E,
+                                       _ptr(routing_map), _ptr(probs), _ptr(winner),
+                                       _ptr(status), _stream(stream)), "moe_route_to_multihot")
+    return routing_map, probs, winner
+
+
+def moe_dispatch(x: torch.Tensor, routing_map: torch.Tensor, probs: torch.Tensor, layout: Layout,
+                 host_sync: bool = True, x_disp: Optional[torch.Tensor] = None, stream=None):
+    """a2-a4: fills ``layout`` and returns (x_disp [C, H], (R, N) or None)."""
+    _bf16(x, "x")
+    H = x.shape[1]
+    if x_disp is None:
+        x_disp = torch.empty(layout.capacity, H, dtype=torch.bfloat16, device=x.device)
+    rows = (ctypes.c_int64 * 2)() if host_sync else None
+    _check(N.lib.moe_dispatch(_ptr(x), _ptr(routing_map), _ptr(probs), H, layout.ref,
+                              _ptr(x_disp), rows, _stream(stream)), "moe_dispatch")
+    return x_disp, ((int(rows[0]), int(rows[1])) if host_sync else None)
+
+
+def moe_grouped_experts(x_disp: torch.Tensor, layout: Layout, W1: torch.Tensor, W2: torch.Tensor,
+                        save_o: bool = False, save_gu: bool = False, out=None, stream=None):
+    """a5: returns dict(h, y, o (or None), gu (or None)), each [C, *] bf16."""
+    E, twoI, H = W1.shape
+    I = twoI // 2
+    C = layout.capacity
+    dev = x_disp.device
+    o = out or {}
+    h = o.get("h") if o.get("h") is not None else torch.empty(C, I, dtype=torch.bfloat16, device=dev)
+    y = o.get("y") if o.get("y") is not None else torch.empty(C, H, dtype=torch.bfloat16, device=dev)
+    o_save = (o.get("o") if o.get("o") is not None else torch.empty(C, H, dtype=torch.bfloat16, device=dev)) if save_o else None
+    gu = (o.get("gu") if o.get("gu") is not None else torch.empty(C, 2 * I, dtype=torch.bfloat16, device=dev)) if save_gu else None
+    _check(N.lib.moe_grouped_experts(_ptr(x_disp), layout.ref, H, I, _ptr(W1), _ptr(W2), _ptr(h),
+                                     _ptr(y), _ptr(o_save), _ptr(gu), _stream(stream)),
+           "moe_grouped_experts")
+    return {"h": h, "y": y, "o": o_save, "gu": gu}
+
+
+def moe_combine(y_disp: torch.Tensor, layout: Layout, out: Optional[torch.Tensor] = None, stream=None):
+    """a6: out [T, H] bf16."""
+    H = y_disp.shape[1]
+    if out is None:
+        out = torch.empty(layout.T, H, dtype=torch.bfloat16, device=y_disp.device)
+    _check(N.lib.moe_combine(_ptr(y_disp), layout.ref, H, _ptr(out), _stream(stream)), "moe_combine")
+    return out
+
+
+def moe_combine_backward(grad_out: torch.Tensor, layout: Layout, o_save: Optional[torch.Tensor] = None,
+                         stream=None):
+    """a7 (+a8 when o_save is given): returns (grad_y [C, H], grad_w [C] or None)."""
+    H = grad_out.shape[1]
+    grad_y = torch.empty(layout.capacity, H, dtype=torch.bfloat16, device=grad_out.device)
+    grad_w = (torch.empty(layout.capacity, dtype=torch.float32, device=grad_out.device)
+              if o_save is not None else None)
+    _check(N.lib.moe_combine_backward(_ptr(grad_out), _ptr(o_save), layout.ref, H, _ptr(grad_y),
+                                      _ptr(grad_w), _stream(stream)), "moe_combine_backward")
+    return grad_y, grad_w
+
+
+def moe_dispatch_backward(grad_x_disp: torch.Tensor, layout: Layout,
+                          grad_w: Optional[torch.Tensor] = None, stream=None):
+    """a10 (+ grad_w scatter): returns (grad_x [T, H], grad_probs [T, E] or None)."""
+    H = grad_x_disp.shape[1]
+    dev = grad_x_disp.device
+    grad_x = torch.empty(layout.T, H, dtype=torch.bfloat16, device=dev)
+    grad_probs = (torch.empty(layout.T, layout.E, dtype=torch.float32, device=dev)
+                  if grad_w is not None else None)
+    _check(N.lib.moe_dispatch_backward(_ptr(grad_x_disp), _ptr(grad_w), layout.ref, H, _ptr(grad_x),
+                                       _ptr(grad_probs), _stream(stream)), "moe_dispatch_backward")
+    return grad_x, grad_probs
+
+
+def moe_route_to_multihot_backward(grad_probs: torch.Tensor, topk_idx: torch.Tensor,
+                                   winner_slot: torch.Tensor, stream=None):
+    """Multihot backward: grad_topk_probs [T, K] fp32."""
+    T, K = topk_idx.shape
+    E = grad_probs.shape[1]
+    g = torch.empty(T, K, dtype=torch.float32, device=grad_probs.device)
+    _check(N.lib.moe_route_to_multihot_backward(_ptr(grad_probs), _ptr(topk_idx), _ptr(winner_slot),
+                                                T, K, E, _ptr(g), _stream(stream)),
+           "moe_route_to_multihot_backward")
+    return g
+
+
+@dataclass
+class ForwardResult:
+    out: torch.Tensor
+    layout: Layout
+    routing_map: torch.Tensor
+    probs: torch.Tensor
+    winner_slot: torch.Tensor
+    x_disp: torch.Tensor
+    h: torch.Tensor
+    y: torch.Tensor
+    o: Optional[torch.Tensor]
+    gu: Optional[torch.Tensor]
+    rows: Optional[tuple]
+
+
+def moe_layer_forward(x, topk_idx, topk_probs, W1, W2, pad_multiple: int, host_sync: bool = True,
+                      capacity: Optional[int] = None, save_for_backward: bool = False,
+                      layout: Optional[Layout] = None, stream=None) -> ForwardResult:
+    """a1..a6 in order: multihot, dispatch, grouped experts, combine."""
+    T, K = topk_idx.shape
+    E = W1.shape[0]
+    if layout is None:
+        C = capacity if capacity is not None else worst_case_rows(T, E, K, pad_multiple)
+        layout = Layout(T, E, K, pad_multiple, C, device=x.device)
+    rmap, probs, win = moe_route_to_multihot(topk_idx, topk_probs, E, layout.status, stream)
+    x_disp, rows = moe_dispatch(x, rmap, probs, layout, host_sync=host_sync, stream=stream)
+    ex = moe_grouped_experts(x_disp, layout, W1, W2, save_o=save_for_backward,
+                             save_gu=save_for_backward, stream=stream)
+    out = moe_combine(ex["y"], layout, stream=stream)
+    return ForwardResult(out, layout, rmap, probs, win, x_disp, ex["h"], ex["y"], ex["o"], ex["gu"], rows)

@@ -1,0 +1,244 @@
+/*
+ * moe.h -- C ABI of the single-GPU MoE dispatch / experts / combine path for
+ * GB300 (sm_103a).
+ *
+ * What the path computes is defined by two pages:
+ *   [HEP] "feat: add hybridep (NVIDIA-NeMo/Automodel #1333)" -- Changelog and
+ *         the review of dispatch(): top-k indices become a multihot
+ *         routing_map with fp32 probs, dispatch returns tokens_per_expert and
+ *         pads each expert's rows to pad_multiple, and the number of permuted
+ *         rows is tokens_per_expert.sum().
+ *   [DEP] "Add the deepep expert-parallel implementation
+ *         (huggingface/transformers #49638)" -- What this adds: Expanded
+ *         layout (each (token, expert) pair has its own row; rows are grouped
+ *         per expert and carry the pair's weight, which the experts apply;
+ *         the combine adds rows without weights); Eager vs captured (either
+ *         the exact row count is read back to the host, or a buffer sized
+ *         for any routing is used without a sync, its unused rows zero and
+ *         owned by a sentinel expert that is never computed); Custom ops and
+ *         Training (the combine's gradient is a dispatch along the same
+ *         layout; the routing weights get gradients through the combine);
+ *         Usage (the hidden size must be a multiple of 256).
+ *
+ * Conventions for every entry point:
+ *   - Pointers named in a signature are DEVICE pointers unless the comment
+ *     says "host".  The caller owns all memory; the library allocates nothing
+ *     (no cudaMalloc, no pinned buffers), keeps no state between calls and
+ *     holds no handles.  Row buffers hold `capacity` rows.
+ *   - bf16 tensors are passed as raw bit patterns (moe_bf16), row-major,
+ *     with the last dimension contiguous and rows packed (no row stride).
+ *     Every pointer must be 16-byte aligned.
+ *   - Every call is asynchronous and ordered on `stream` (a cudaStream_t;
+ *     NULL is the legacy default stream), except moe_dispatch in host-synced
+ *     mode, which synchronises `stream` once.
+ *   - Every call validates its arguments on the host and returns a
+ *     moe_status; it never aborts the process.  moe_last_error() gives a
+ *     human-readable detail of the last failure on the calling thread.
+ *   - Errors found on the device (an expert index outside [-1, E), a
+ *     capacity overflow, a bounded wait that ran out) are OR-ed into the
+ *     caller's device status word as MOE_DEVERR_* bits; kernels never trap.
+ *     The caller zeroes the word before first use and reads it when it
+ *     chooses (host-synced moe_dispatch reads it at its sync).
+ *   - Shapes: H % 256 == 0, I % 128 == 0, 1 <= K <= min(E, 127),
+ *     E <= 1024 with E % 4 == 0, pad_multiple >= 1, T >= 0, and
+ *     T*K + E*(pad_multiple-1) < 2^31.  The device must be compute capability 10.3.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16;                 /* raw bfloat16 bit pattern            */
+typedef struct CUstream_st* moe_stream_t;  /* the same type as cudaStream_t       */
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,        /* null pointer, negative size, misalignment     */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2,  /* H % 256, I % 128, K > 127, E > 1024 ...        */
+  MOE_ERR_CAPACITY = 3,           /* the layout needs more rows than `capacity`     */
+  MOE_ERR_BAD_INDEX = 4,          /* an expert index outside [-1, E) was seen       */
+  MOE_ERR_TIMEOUT = 5,            /* a bounded device-side wait ran out             */
+  MOE_ERR_DEVICE = 6,             /* the current device is not compute cap. 10.3    */
+  MOE_ERR_CUDA = 7                /* a CUDA runtime / driver call failed            */
+} moe_status;
+
+/* Bits of the device status word (int32, OR-ed by kernels). */
+#define MOE_DEVERR_BAD_INDEX 1
+#define MOE_DEVERR_CAPACITY  2
+#define MOE_DEVERR_TIMEOUT   4
+
+/* Name of a status code (static string). */
+MOE_API const char* moe_status_string(moe_status status);
+
+/* Detail of the last failing call on this thread (thread-local, static storage). */
+MOE_API const char* moe_last_error(void);
+
+/* MOE_OK if the current CUDA device is compute capability 10.3, else MOE_ERR_DEVICE. */
+MOE_API moe_status moe_device_check(void);
+
+/* Rows a sync-free buffer needs so that no routing can overflow it:
+ * T*K (every slot valid) + E*(pad_multiple-1) (every group padded).
+ * [DEP] Eager vs captured: the sync-free buffer is sized for the worst case. */
+MOE_API int64_t moe_worst_case_rows(int32_t T, int32_t E, int32_t K, int32_t pad_multiple);
+
+/*
+ * The expanded layout of one forward + backward: the "handle" that
+ * [HEP]'s hybrid_ep_dispatch returns, made explicit as caller-owned device
+ * buffers ([DEP] Custom ops: the handle is passed as tensors).  Written by
+ * moe_dispatch, read by every later call.  All pointers are device pointers.
+ */
+typedef struct moe_layout {
+  int32_t T, E, K, pad_multiple;
+  int64_t capacity;            /* C: rows in every row buffer below                  */
+  int32_t* tokens_per_expert;  /* [E]    exact number of tokens routed to each expert */
+  int32_t* offsets;            /* [E+1]  start row of each expert's group; groups are
+                                           padded to a multiple of pad_multiple       */
+  int32_t* totals;             /* [2]    R = offsets[E] rows used, N = valid rows     */
+  int32_t* row_token;          /* [C]    token of each row; -1 on pad / spare rows    */
+  int32_t* row_expert;         /* [C]    expert of each row; E (the sentinel) on pad /
+                                           spare rows                                  */
+  float*   row_weight;         /* [C]    fp32 routing weight of the row's slot; 0 on
+                                           pad / spare rows                            */
+  int32_t* token_row;          /* [T*K]  each token's rows in ascending expert order,
+                                           then -1                                     */
+  int32_t* status;             /* [1]    device status word (MOE_DEVERR_* bits)        */
+  void*    workspace;          /* moe_layout_workspace_bytes(T, E) bytes of scratch   */
+} moe_layout;
+
+/* Bytes of scratch moe_dispatch needs in moe_layout.workspace (256-byte aligned). */
+MOE_API moe_status moe_layout_workspace_bytes(int32_t T, int32_t E, size_t* bytes);
+
+/*
+ * a1. Top-k -> multihot.  [HEP] Changelog (the HybridEP preprocessing turns
+ * top-k indices into multihot routing metadata) and the review of dispatch()
+ * (probs are fp32).
+ *   topk_idx     [T, K] int64: expert of each slot, -1 = no expert (dropped).
+ *   topk_probs   [T, K] fp32:  the slot's routing weight.
+ *   routing_map  [T, E] uint8 (out): 1 where token t is routed to expert e.
+ *   probs        [T, E] fp32  (out): the weight of that pair, 0 elsewhere.
+ *   winner_slot  [T, E] int8  (out): the slot k that set the pair, -1 elsewhere.
+ *   status       [1] int32 device status word.
+ * Slots are taken in order k = 0..K-1, so when one token names the same
+ * expert twice the pair is set once and the last such slot's prob wins.  An
+ * index outside [-1, E) sets MOE_DEVERR_BAD_INDEX and is treated as -1.
+ */
+MOE_API moe_status moe_route_to_multihot(const int64_t* topk_idx, const float* topk_probs,
+                                 int32_t T, int32_t K, int32_t E,
+                                 uint8_t* routing_map, float* probs, int8_t* winner_slot,
+                                 int32_t* status, moe_stream_t stream);
+
+/*
+ * a2-a4. Counts, padded offsets, the expanded layout, and the row gather.
+ * [HEP] review of dispatch(): tokens_per_expert, pad_multiple, the number of
+ * permuted rows; [DEP] Expanded layout; Eager vs captured.
+ *   x            [T, H] bf16 tokens.
+ *   routing_map, probs: as written by moe_route_to_multihot.
+ *   L            layout to fill (its pointers and sizes are read on the host).
+ *   x_disp       [C, H] bf16 (out): x_disp[r] = x[row_token[r]] bit for bit;
+ *                pad and spare rows are zero.
+ *   rows_host    HOST int64[2] or NULL.
+ *     non-NULL = host-synced (eager) mode: the call synchronises `stream`
+ *       after the counts, writes rows_host[0] = R (rows used) and
+ *       rows_host[1] = N (valid rows), returns MOE_ERR_BAD_INDEX if the
+ *       status word has MOE_DEVERR_BAD_INDEX, or MOE_ERR_CAPACITY (before
+ *       writing any row) if R > capacity.
+ *     NULL = sync-free mode: capacity must be >= moe_worst_case_rows(...)
+ *       (checked on the host, else MOE_ERR_CAPACITY); nothing is read back,
+ *       rows R..C-1 become spare rows (zero, sentinel expert), and the call
+ *       can be captured in a CUDA graph.
+ * Within an expert's group the rows are in ascending token order.
+ */
+MOE_API moe_status moe_dispatch(const moe_bf16* x, const uint8_t* routing_map, const float* probs,
+                        int32_t H, const moe_layout* L, moe_bf16* x_disp,
+                        int64_t* rows_host, moe_stream_t stream);
+
+/*
+ * a5. Grouped SwiGLU experts that apply the routing weight.  [DEP] Expanded
+ * layout (the experts apply the routing weights); Benchmarks (bf16 grouped GEMMs).
+ *   x_disp  [C, H] bf16 rows (moe_dispatch's output).
+ *   W1      [E, 2I, H] bf16: per expert, rows 0..I-1 gate, rows I..2I-1 up.
+ *   W2      [E, H, I] bf16: per expert, the down projection.
+ *   h       [C, I] bf16 (out, required): h = bf16(silu(x Wg^T) * (x Wu^T)).
+ *   y_disp  [C, H] bf16 (out): y = bf16(w_r * (h W2^T)), fp32 accumulation.
+ *   o_save  [C, H] bf16 (out, nullable): bf16(h W2^T), the pre-weight output
+ *           the routing-weight gradient needs.
+ *   gu_save [C, 2I] bf16 (out, nullable): bf16 of the gate and up
+ *           pre-activations, which the expert backward needs.
+ * Only the N valid rows are computed and written; pad and spare rows
+ * (sentinel expert) are skipped and their output rows are left untouched.
+ * The row counts are read on the device, so the call never synchronises and
+ * can be captured.
+ */
+MOE_API moe_status moe_grouped_experts(const moe_bf16* x_disp, const moe_layout* L,
+                               int32_t H, int32_t I,
+                               const moe_bf16* W1, const moe_bf16* W2,
+                               moe_bf16* h, moe_bf16* y_disp,
+                               moe_bf16* o_save, moe_bf16* gu_save,
+                               moe_stream_t stream);
+
+/*
+ * a6. Combine: out[t] = bf16(sum over t's rows of fp32(y_disp[row])), adding
+ * in ascending expert order from +0.0 in fp32, one final rounding; no weights
+ * ([DEP] Expanded layout: the combine is a plain sum).  A token with no rows
+ * gets +0.  Pad and spare rows are never read.
+ *   y_disp [C, H] bf16; out [T, H] bf16 (out).
+ */
+MOE_API moe_status moe_combine(const moe_bf16* y_disp, const moe_layout* L, int32_t H,
+                       moe_bf16* out, moe_stream_t stream);
+
+/*
+ * a7 + a8. Combine backward and the routing-weight gradient.  [DEP] Training:
+ * the combine's backward dispatches along the forward layout, and the
+ * weight gradients go back through the combine.
+ *   grad_out [T, H] bf16: dL/d out.
+ *   o_save   [C, H] bf16 (nullable): moe_grouped_experts' o_save.
+ *   grad_y   [C, H] bf16 (out): grad_y[r] = grad_out[row_token[r]] bit for
+ *            bit; zero on pad / spare rows.
+ *   grad_w   [C] fp32 (out, nullable; needs o_save): grad_w[r] =
+ *            sum_h grad_y[r,h] * o[r,h] in fp32; zero on pad / spare rows.
+ */
+MOE_API moe_status moe_combine_backward(const moe_bf16* grad_out, const moe_bf16* o_save,
+                                const moe_layout* L, int32_t H,
+                                moe_bf16* grad_y, float* grad_w, moe_stream_t stream);
+
+/*
+ * a10 + the weight-gradient scatter.  [DEP] Training (both the tokens and
+ * the routing weights receive gradients).
+ *   grad_x_disp [C, H] bf16: dL/d x_disp.
+ *   grad_x      [T, H] bf16 (out): the combine applied to grad_x_disp (same
+ *               order and rounding as moe_combine).
+ *   grad_w      [C] fp32 (nullable) and grad_probs [T, E] fp32 (out,
+ *               nullable): grad_probs[t, e] = grad_w[row of (t, e)], 0 where
+ *               t is not routed to e.
+ */
+MOE_API moe_status moe_dispatch_backward(const moe_bf16* grad_x_disp, const float* grad_w,
+                                 const moe_layout* L, int32_t H,
+                                 moe_bf16* grad_x, float* grad_probs, moe_stream_t stream);
+
+/*
+ * Multihot backward: grad_topk_probs[t, k] = grad_probs[t, topk_idx[t, k]]
+ * when slot k is valid and is the slot that set the pair (winner_slot), else 0.
+ *   grad_probs [T, E] fp32, topk_idx [T, K] int64, winner_slot [T, E] int8;
+ *   grad_topk_probs [T, K] fp32 (out).
+ */
+MOE_API moe_status moe_route_to_multihot_backward(const float* grad_probs, const int64_t* topk_idx,
+                                          const int8_t* winner_slot,
+                                          int32_t T, int32_t K, int32_t E,
+                                          float* grad_topk_probs, moe_stream_t stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* MOE_GB300_H */

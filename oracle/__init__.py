@@ -9,20 +9,21 @@ constants); the only thing both sides share is the seeded input generator in
 
 It is a plain, slow, obviously-correct restatement of what the pages define:
 
-* "feat: add hybridep (NVIDIA-NeMo/Automodel #1333)" -- top-k indices become a
-  multihot ``routing_map`` plus fp32 ``probs`` (Changelog; review of
-  ``dispatch()``: fp32 probs, ``tokens_per_expert``, ``pad_multiple``,
-  ``num_permuted_tokens = tokens_per_expert.sum()``; review asking for tests of
-  ``_indices_to_multihot``: basic, topk=1, all -1, partial -1, single token,
-  duplicate expert assignments).
+* "feat: add hybridep (NVIDIA-NeMo/Automodel #1333)" -- the preprocessing
+  that maps top-k indices to a multihot ``routing_map`` with fp32 ``probs``
+  (Changelog; review of ``dispatch()``: fp32 probs, ``tokens_per_expert``,
+  ``pad_multiple``, the permuted-row total as the sum of the counts; the
+  review's list of multihot test cases: basic, topk=1, all -1, partial -1,
+  single token, a token naming one expert twice).
 * "Add the deepep expert-parallel implementation (huggingface/transformers
-  #49638)" -- What this adds: Expanded layout (one row per (token, local
-  expert) slot, grouped by expert, carrying the slot's routing weight; the
-  experts apply the weights, the combine only sums); Eager vs captured (exact
-  received rows vs a worst-case buffer whose spare rows are zeroed and sent to
-  a sentinel expert that the experts skip); Training (the combine's backward is
-  a dispatch along the forward layout; routing-weight gradients go back through
-  the combine); Benchmarks (experts are bf16 grouped GEMMs).
+  #49638)" -- What this adds: Expanded layout (every (token, expert) pair gets
+  its own row, rows are grouped per expert and carry the pair's weight; the
+  weight is applied inside the experts and the combine just adds rows up);
+  Eager vs captured (either the exact row count read back to the host, or a
+  buffer big enough for any routing whose unused rows are zero and belong to
+  a sentinel expert that no expert computes); Training (the combine's gradient
+  is a dispatch along the same layout, and the routing weights get gradients
+  through the combine); Benchmarks (the experts are bf16 grouped GEMMs).
 
 Floating point: expert math in fp64 from the exact bf16 values, with the
 roundings the layer itself has (h and y to bf16); combine sums in fp32 in a

@@ -50,13 +50,14 @@ def sentinel_expert(E: int) -> int:
 def worst_case_capacity(T: int, E: int, K: int, P: int) -> int:
     """Rows a sync-free buffer needs for any routing: all T*K slots valid, and
     every expert's group padded by at most P-1 rows ([DEP] Eager vs captured:
-    the rows are sized for the worst case so they cannot overflow)."""
+    the sync-free buffer holds enough rows for any routing)."""
     return T * K + E * (P - 1)
 
 
 # --------------------------------------------------------------------------
-# a1: top-k -> multihot   ([HEP] Changelog: "converts top-k indices to
-# multihot routing metadata"; review of dispatch(): probs are fp32)
+# a1: top-k -> multihot   ([HEP] Changelog: the HybridEP preprocessing step
+# that maps top-k indices to multihot routing data; review of dispatch():
+# probs are fp32)
 # --------------------------------------------------------------------------
 def route_to_multihot(topk_idx: np.ndarray, topk_probs: np.ndarray, E: int):
     """Returns routing_map uint8 [T, E], probs fp32 [T, E], winner_slot int8 [T, E].
@@ -160,7 +161,7 @@ def build_layout(routing_map: np.ndarray, probs: np.ndarray, K: int, P: int,
 # --------------------------------------------------------------------------
 def dispatch(x_bits: np.ndarray, row_token: np.ndarray) -> np.ndarray:
     """x_disp[r] = x[row_token[r]] bit for bit; rows with token -1 are zero.
-    ([DEP] Expanded layout; spare rows "are zeroed")."""
+    ([DEP] Expanded layout; Eager vs captured: spare rows hold zeros)."""
     x_bits = np.asarray(x_bits, dtype=np.uint16)
     row_token = np.asarray(row_token)
     out = np.zeros((row_token.shape[0], x_bits.shape[1]), dtype=np.uint16)
@@ -171,7 +172,8 @@ def dispatch(x_bits: np.ndarray, row_token: np.ndarray) -> np.ndarray:
 
 # --------------------------------------------------------------------------
 # a5: SwiGLU experts that apply the routing weight   ([DEP] Expanded layout:
-# "the experts ... apply the weights"; Benchmarks: experts are bf16 grouped GEMMs)
+# the routing weight is applied inside the experts; Benchmarks: the experts
+# are bf16 grouped GEMMs)
 # --------------------------------------------------------------------------
 def _silu(z: np.ndarray) -> np.ndarray:
     with np.errstate(over="ignore"):
@@ -228,7 +230,7 @@ def grouped_experts(x_disp_bits, row_expert, row_weight, W1_bits, W2_bits, I,
 
 # --------------------------------------------------------------------------
 # a6 / a10: combine (and the dispatch's backward)   ([DEP] Expanded layout:
-# "the combine only sums")
+# the combine is a plain sum, with no weights)
 # --------------------------------------------------------------------------
 def combine(y_bits: np.ndarray, token_row: np.ndarray) -> np.ndarray:
     """out[t] = bf16( ((0 + y[r_0]) + y[r_1]) + ... ) with fp32 adds over the
@@ -247,14 +249,14 @@ def combine(y_bits: np.ndarray, token_row: np.ndarray) -> np.ndarray:
 
 def combine_backward(grad_out_bits: np.ndarray, row_token: np.ndarray) -> np.ndarray:
     """d out / d y: grad_y[r] = grad_out[row_token[r]], zero on pad / spare
-    rows ([DEP] Training: "the combine's backward dispatches along the
-    forward's layout")."""
+    rows ([DEP] Training: the combine's gradient is a dispatch that follows
+    the forward's layout)."""
     return dispatch(grad_out_bits, row_token)
 
 
 # --------------------------------------------------------------------------
-# a8: routing-weight gradient   ([DEP] Training: "Gradients reach ... the
-# routing weights")
+# a8: routing-weight gradient   ([DEP] Training: the routing weights receive
+# gradients too)
 # --------------------------------------------------------------------------
 def routing_weight_grad(grad_y_bits, o_bits, row_expert, E) -> np.ndarray:
     """y_r = w_r * o_r, so dL/dw_r = sum_h grad_y[r, h] * o[r, h] (fp64 sum,
