@@ -1,0 +1,413 @@
+"""Benchmark of the MoE dispatch -> experts -> combine layer on GB300.
+
+One step = one forward pass of the whole layer (multihot, counts/offsets,
+layout + dispatch gather, grouped SwiGLU experts, combine) over one batch of
+the configured layer; with a backward config (h4096) the step also runs the
+backward entry points.  Four distinct layers (weights, tokens, routing) are
+cycled so the working set does not sit in L2 (each layer's weights alone are
+larger than the 126 MB L2).
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synthetic  # noqa: E402
+
+MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def peaks():
+    try:
+        with open(MEASURED_PEAKS) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """The slowest rank's time: an all-reduce MAX over ranks."""
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- algorithmic work
+
+def algorithmic(cfg, counts: np.ndarray, R: int, N: int, C: int, backward: bool):
+    """Bytes / flops the layer's steps must move, per call (definitions in the design doc)."""
+    T, H, E, K, I = cfg.T, cfg.H, cfg.E, cfg.K, cfg.I
+    active = int((counts > 0).sum())
+    meta_disp = T * E * 1 + 4 * N + 12 * C + 4 * T * K + 8 * (E + 1)
+    disp = T * H * 2 + C * H * 2 + meta_disp
+    comb = N * H * 2 + T * H * 2 + 4 * T * K
+    w_bytes = active * (2 * I * H + H * I) * 2
+    ex_bytes = w_bytes + N * H * 2 + 2 * N * I * 2 + N * H * 2
+    ex_flops = 6.0 * N * H * I
+    out = {"dispatch_bytes": disp, "combine_bytes": comb, "experts_bytes": ex_bytes,
+           "experts_flops": ex_flops, "multihot_bytes": T * K * 12 + T * E * 6}
+    if backward:
+        out["combine_bwd_bytes"] = T * H * 2 + C * H * 2 + N * H * 2 + 4 * C
+        out["dispatch_bwd_bytes"] = N * H * 2 + T * H * 2 + T * E * 4
+    return out
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, world, rank, local):
+    import combine_topk_multihot_gb300 as moe
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = synthetic.CONFIGS[args.config]
+    T, H, E, K, I, P = cfg.T, cfg.H, cfg.E, cfg.K, cfg.I, cfg.P
+    host_sync = not cfg.sync_free
+    n_layers = args.layers
+
+    layers = []
+    for l in range(n_layers):
+        s = cfg.seed + 7919 * l + 104729 * rank
+        x = synthetic.make_tokens(T, H, s, device=dev)
+        idx, p = synthetic.make_routing(T, E, K, s, cfg.zipf_s, cfg.drop)
+        W1, W2 = synthetic.make_weights(E, H, I, s, device=dev)
+        layers.append({"x": x, "topk_idx": idx.to(dev), "topk_probs": p.to(dev), "W1": W1, "W2": W2})
+    worst = moe.worst_case_rows(T, E, K, P)
+    # host-synced mode: buffers sized once to the largest R over the layers, as
+    # a caching allocator would hold them; sync-free: the worst case
+    C = worst
+    lay = moe.Layout(T, E, K, P, C, device=dev)
+    x_disp = torch.empty(C, H, dtype=torch.bfloat16, device=dev)
+    bufs = {"h": torch.empty(C, I, dtype=torch.bfloat16, device=dev),
+            "y": torch.empty(C, H, dtype=torch.bfloat16, device=dev)}
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    # find the exact rows of each layer, then size the buffers to the largest
+    rows = []
+    for L in layers:
+        rmap, probs, _ = moe.moe_route_to_multihot(L["topk_idx"], L["topk_probs"], E, lay.status)
+        _, rc = moe.moe_dispatch(L["x"], rmap, probs, lay, host_sync=True, x_disp=x_disp)
+        rows.append(rc)
+        L["counts"] = lay.tokens_per_expert.cpu().numpy()
+    if host_sync:
+        C = max(r[0] for r in rows)
+        lay = moe.Layout(T, E, K, P, C, device=dev)
+        x_disp = torch.empty(C, H, dtype=torch.bfloat16, device=dev)
+        bufs = {"h": torch.empty(C, I, dtype=torch.bfloat16, device=dev),
+                "y": torch.empty(C, H, dtype=torch.bfloat16, device=dev)}
+
+    stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    launches_per_step = 1 + 4 + 2 + 1
+
+    def step(L, events=None):
+        if events: events[0].record(stream)
+        rmap, probs, _ = moe.moe_route_to_multihot(L["topk_idx"], L["topk_probs"], E, lay.status)
+        if events: events[1].record(stream)
+        moe.moe_dispatch(L["x"], rmap, probs, lay, host_sync=host_sync, x_disp=x_disp)
+        if events: events[2].record(stream)
+        moe.moe_grouped_experts(x_disp, lay, L["W1"], L["W2"], out=bufs)
+        if events: events[3].record(stream)
+        moe.moe_combine(bufs["y"], lay, out=out)
+        if events: events[4].record(stream)
+
+    for i in range(args.warmup):
+        step(layers[i % n_layers])
+    torch.cuda.synchronize()
+    barrier(world)
+
+    step_events = [[ev() for _ in range(5)] for _ in range(args.steps)]
+    t0, t1 = ev(), ev()
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        barrier(world)
+        t0.record(stream)
+        for i in range(args.steps):
+            step(layers[i % n_layers], step_events[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = t0.elapsed_time(t1)
+    ms_max = max_over_ranks(ms, world)
+    per = {k: [] for k in ("multihot", "dispatch", "experts", "combine")}
+    for e5 in step_events:
+        for j, k in enumerate(per):
+            per[k].append(e5[j].elapsed_time(e5[j + 1]))
+    status = int(lay.status.item())
+    if status:
+        raise RuntimeError(f"device status word set: {status}")
+
+    # ---- end to end through the public API with host buffers
+    pin = lambda t: t.cpu().pin_memory()
+    host = [{k: pin(L[k]) for k in ("x", "topk_idx", "topk_probs")} for L in layers]
+    out_host = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+    d_in = {k: torch.empty_like(layers[0][k]) for k in ("x", "topk_idx", "topk_probs")}
+    h2d = sum(v.numel() * v.element_size() for v in host[0].values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step(i):
+        hs = host[i % n_layers]
+        for k in d_in:
+            d_in[k].copy_(hs[k], non_blocking=True)
+        L = dict(layers[i % n_layers])
+        L.update(d_in)
+        step(L)
+        out_host.copy_(out, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+
+    # ---- roofline of the dominant step (the experts' two grouped GEMM launches)
+    hbm, bf16_burst, bf16_sust, src = peaks()
+    work = [algorithmic(cfg, L["counts"], r[0], r[1], C, cfg.backward) for L, r in zip(layers, rows)]
+    mean = lambda key: float(np.mean([w[key] for w in work]))
+    # per-step averages over the timed steps (layer i % n_layers)
+    steps_w = [work[i % n_layers] for i in range(args.steps)]
+    ex_us = 1e3 * float(np.mean(per["experts"]))
+    ex_bytes = float(np.mean([w["experts_bytes"] for w in steps_w]))
+    ex_flops = float(np.mean([w["experts_flops"] for w in steps_w]))
+    t_hbm = ex_bytes / (hbm * 1e9)
+    t_tc = ex_flops / (bf16_burst * 1e12)
+    if t_hbm >= t_tc:
+        roof = {"bound": "hbm", "achieved": ex_bytes / (ex_us * 1e-6) / 1e9, "peak": hbm, "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": ex_flops / (ex_us * 1e-6) / 1e12, "peak": bf16_burst, "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = "experts: grouped_gemm_kernel<0> (gate/up + SwiGLU) + grouped_gemm_kernel<1> (down x weight)"
+    roof["peak_source"] = src
+    roof["tensor_frac_of_burst"] = ex_flops / (ex_us * 1e-6) / 1e12 / bf16_burst
+
+    disp_us = 1e3 * float(np.mean(per["dispatch"]))
+    comb_us = 1e3 * float(np.mean(per["combine"]))
+    kernels = {
+        "multihot_us": 1e3 * float(np.mean(per["multihot"])),
+        "dispatch_us": disp_us,
+        "experts_us": ex_us,
+        "combine_us": comb_us,
+        "dispatch_GBs": float(np.mean([w["dispatch_bytes"] for w in steps_w])) / (disp_us * 1e-6) / 1e9,
+        "combine_GBs": float(np.mean([w["combine_bytes"] for w in steps_w])) / (comb_us * 1e-6) / 1e9,
+        "experts_TFLOPs": ex_flops / (ex_us * 1e-6) / 1e12,
+        "rows_used": [r[0] for r in rows], "rows_valid": [r[1] for r in rows], "capacity": C,
+    }
+    kernels["dispatch_frac_hbm"] = kernels["dispatch_GBs"] / hbm
+    kernels["combine_frac_hbm"] = kernels["combine_GBs"] / hbm
+
+    tokens = T * world * args.steps
+    res = {
+        "metric": "MoE layer tokens/sec (dispatch+experts+combine)",
+        "value": tokens / (ms_max * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_max / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) tokens, softmax top-k routing, N(0,0.02) weights)",
+        "config": {"workload": cfg.name, "T": T, "H": H, "E": E, "top_k": K, "I": I,
+                   "pad_multiple": P, "mode": "host-synced" if host_sync else "sync-free",
+                   "layers_cycled": n_layers, "l2": "inputs larger than L2 (4 distinct layers cycled, >1.2 GB weights each)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": roof,
+        "kernels": kernels,
+    }
+    res["clocks"] = clk.summary()
+    return res
+
+
+# ----------------------------------------------------------------------------- the oracle on the CPU
+
+def oracle_sample(cfg, budget_s: float, rank: int = 0):
+    """Times the CPU oracle on the first tokens of one layer of ``cfg``,
+    growing the sample until it takes about ``budget_s``.  Returns
+    (tokens/s, tokens sampled, seconds, threads)."""
+    import oracle as O
+    s = cfg.seed + 104729 * rank
+    x = synthetic.make_tokens(cfg.T, cfg.H, s)
+    idx, p = synthetic.make_routing(cfg.T, cfg.E, cfg.K, s, cfg.zipf_s, cfg.drop)
+    W1, W2 = synthetic.make_weights(cfg.E, cfg.H, cfg.I, s)
+    b = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    xb, W1b, W2b = b(x), b(W1), b(W2)
+    n = min(cfg.T, 16)
+    while True:
+        t0 = time.perf_counter()
+        O.layer_forward(xb[:n], idx[:n].numpy(), p[:n].numpy(), W1b, W2b, cfg.I, cfg.P)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s / 4 or n >= cfg.T:
+            break
+        n = min(cfg.T, max(n * 2, int(n * budget_s / 4 / max(dt, 1e-3))))
+    threads = torch.get_num_threads()
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        threads = max([i.get("num_threads", 1) for i in info] + [1])
+    except Exception:
+        pass
+    return n / dt, n, dt, threads
+
+
+def run_reference(args, world, rank):
+    cfg = synthetic.CONFIGS[args.config]
+    if rank != 0:
+        return None
+    vals = []
+    for i in range(args.warmup + args.steps):
+        v, n, dt, threads = oracle_sample(cfg, budget_s=args.ref_budget)
+        if i >= args.warmup:
+            vals.append((v, n, dt))
+    v = float(np.median([a for a, _, _ in vals]))
+    n = vals[0][1]
+    dt = float(np.mean([c for _, _, c in vals]))
+    return {
+        "impl": "reference",
+        "metric": "MoE layer tokens/sec (dispatch+experts+combine)",
+        "value": v, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "top_k": cfg.K,
+                   "I": cfg.I, "pad_multiple": cfg.P},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"first {n} tokens of the {cfg.name} layer (all {cfg.E} experts' weights), per step"},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="qwen3_30b_a3b", choices=sorted(synthetic.CONFIGS))
+    ap.add_argument("--layers", type=int, default=4)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=8.0, help="seconds of oracle work per reference step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+    else:
+        res = run_ours(args, world, rank, local)
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            cfg = synthetic.CONFIGS[args.config]
+            v, n, dt, threads = oracle_sample(cfg, budget_s=args.cpu_budget)
+            res["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                   "sample": f"first {n} tokens of the {cfg.name} layer, all {cfg.E} experts' weights, {dt:.1f} s"}
+    if rank == 0 and res is not None:
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

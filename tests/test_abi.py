@@ -17,8 +17,8 @@ def _declared_symbols():
 
 @pytest.fixture(scope="module")
 def lib():
-    from combine_topk_multihot_gb300.build import build
-    path = build()
+    import __graft_entry__
+    path = __graft_entry__._build_module().build()
     return ctypes.CDLL(path)
 
 

@@ -160,8 +160,8 @@ def _experts_case(moe, T, H, E, K, I, P, seed, drop=0.0, save=True):
     idx, p = random_routing(T, E, K, seed=seed, drop=drop)
     gen = torch.Generator().manual_seed(seed)
     x = torch.randn(T, H, generator=gen).to(torch.bfloat16)
-    W1 = (torch.randn(E, 2 * I, H, generator=gen) * 0.05).to(torch.bfloat16)
-    W2 = (torch.randn(E, H, I, generator=gen) * 0.05).to(torch.bfloat16)
+    W1 = (torch.randn(E, 2 * I, H, generator=gen) * 0.02).to(torch.bfloat16)
+    W2 = (torch.randn(E, H, I, generator=gen) * 0.02).to(torch.bfloat16)
     C = O.worst_case_capacity(T, E, K, P)
     fwd = moe.moe_layer_forward(x.to(DEV), idx.to(DEV), p.to(DEV), W1.to(DEV), W2.to(DEV), P,
                                 capacity=C, save_for_backward=save)
@@ -183,7 +183,7 @@ def test_experts_match_oracle(moe, T, H, E, K, I, P):
     assert np.array_equal(xd, O.dispatch(bits(x), Lr["row_token"]))
     y, h, o = O.grouped_experts(xd, Lr["row_expert"], Lr["row_weight"], bits(W1), bits(W2), I)
     valid = Lr["row_token"] >= 0
-    assert_gemm_close(bits(fwd.h)[valid], h[valid], "h")
+    assert_gemm_close(bits(fwd.h)[valid], h[valid], "h", intermediate=True)
     assert_gemm_close(bits(fwd.y)[valid], y[valid], "y")
     assert_gemm_close(bits(fwd.o)[valid], o[valid], "o_save")
     # gate / up pre-activations
@@ -192,7 +192,7 @@ def test_experts_match_oracle(moe, T, H, E, K, I, P):
     re = Lr["row_expert"][valid]
     W1f = O.bf16_bits_to_f64(bits(W1))
     gu_ref = np.stack([X[i] @ W1f[re[i]].T for i in range(X.shape[0])]) if X.shape[0] else np.zeros((0, 2 * I))
-    assert_gemm_close(gu, O.f64_to_bf16_bits(gu_ref), "gu_save")
+    assert_gemm_close(gu, O.f64_to_bf16_bits(gu_ref), "gu_save", intermediate=True)
     # the layer output: combine of the GPU's own y is bit-exact ...
     y_gpu = bits(fwd.y).copy()
     y_gpu[~valid] = 0
@@ -207,8 +207,8 @@ def test_experts_skip_sentinel_rows(moe):
     T, H, E, K, I, P = 90, 256, 8, 2, 128, 16
     idx, p = random_routing(T, E, K, seed=9, drop=0.3)
     x = torch.randn(T, H).to(torch.bfloat16).to(DEV)
-    W1 = (torch.randn(E, 2 * I, H) * 0.05).to(torch.bfloat16).to(DEV)
-    W2 = (torch.randn(E, H, I) * 0.05).to(torch.bfloat16).to(DEV)
+    W1 = (torch.randn(E, 2 * I, H) * 0.02).to(torch.bfloat16).to(DEV)
+    W2 = (torch.randn(E, H, I) * 0.02).to(torch.bfloat16).to(DEV)
     C = O.worst_case_capacity(T, E, K, P)
     fwd = moe.moe_layer_forward(x, idx.to(DEV), p.to(DEV), W1, W2, P, capacity=C)
     nan = torch.full((C, H), float("nan"), dtype=torch.bfloat16, device=DEV)
@@ -246,7 +246,7 @@ def test_experts_full_size_sampled_rows(moe, name):
     assert np.array_equal(xd[rows], bits(inp["x"])[rt[rows]])
     y, h, o = O.grouped_experts(xd, re, L.row_weight.cpu().numpy(), bits(inp["W1"]), bits(inp["W2"]),
                                 cfg.I, rows=rows)
-    assert_gemm_close(bits(fwd.h)[rows], h[rows], "h")
+    assert_gemm_close(bits(fwd.h)[rows], h[rows], "h", intermediate=True)
     assert_gemm_close(bits(fwd.y)[rows], y[rows], "y")
     # combine at full size: bit-exact against the oracle on the GPU's y
     y_gpu = bits(fwd.y).copy()
