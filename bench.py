@@ -335,14 +335,20 @@ def oracle_sample(cfg, budget_s: float, rank: int = 0):
     W1, W2 = synthetic.make_weights(cfg.E, cfg.H, cfg.I, s)
     b = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
     xb, W1b, W2b = b(x), b(W1), b(W2)
+    # calibrate on a small sample, then run one sample sized to take ~budget_s
     n = min(cfg.T, 16)
     while True:
         t0 = time.perf_counter()
         O.layer_forward(xb[:n], idx[:n].numpy(), p[:n].numpy(), W1b, W2b, cfg.I, cfg.P)
         dt = time.perf_counter() - t0
-        if dt >= budget_s / 4 or n >= cfg.T:
+        if dt >= budget_s / 8 or n >= cfg.T:
             break
-        n = min(cfg.T, max(n * 2, int(n * budget_s / 4 / max(dt, 1e-3))))
+        n = min(cfg.T, n * 4)
+    if n < cfg.T and dt < budget_s * 0.7:
+        n = min(cfg.T, max(n, int(n * budget_s / max(dt, 1e-3))))
+        t0 = time.perf_counter()
+        O.layer_forward(xb[:n], idx[:n].numpy(), p[:n].numpy(), W1b, W2b, cfg.I, cfg.P)
+        dt = time.perf_counter() - t0
     threads = torch.get_num_threads()
     try:
         import threadpoolctl
@@ -387,7 +393,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="qwen3_30b_a3b", choices=sorted(synthetic.CONFIGS))
     ap.add_argument("--layers", type=int, default=4)
-    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=8.0, help="seconds of oracle work per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -3,7 +3,8 @@
 Bit-exact: multihot, counts, offsets, the layout, the dispatched rows, the
 combine (given the same expert outputs), the backward gathers and scatters.
 Within the bf16 GEMM tolerance (max |err| <= 2e-2, rel L2 <= 5e-3): the
-expert outputs h and y, and the layer output.
+expert outputs y and o and the layer output; the intermediates h and the
+gate/up pre-activations use the same bound scaled by max(1, |ref|).
 """
 import numpy as np
 import pytest
@@ -259,8 +260,15 @@ def test_forward_is_deterministic(moe):
     T, H, E, K, I, P = 700, 512, 16, 4, 256, 8
     a = _experts_case(moe, T, H, E, K, I, P, seed=5)[-1]
     b = _experts_case(moe, T, H, E, K, I, P, seed=5)[-1]
-    for name in ("x_disp", "h", "y", "out"):
+    for name in ("row_token", "row_expert", "row_weight", "token_row", "offsets"):
+        assert torch.equal(getattr(a.layout, name), getattr(b.layout, name)), name
+    for name in ("x_disp", "out"):
         assert torch.equal(getattr(a, name).view(torch.int16), getattr(b, name).view(torch.int16)), name
+    # h and y are written on the valid rows only (pad / spare rows are skipped)
+    valid = a.layout.row_token >= 0
+    for name in ("h", "y"):
+        assert torch.equal(getattr(a, name)[valid].view(torch.int16),
+                           getattr(b, name)[valid].view(torch.int16)), name
 
 
 # ----------------------------------------------------------------- backward a7, a8, a10, multihot
