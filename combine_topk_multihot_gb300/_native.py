@@ -34,6 +34,7 @@ MOE_ERR_CUDA = 7
 MOE_DEVERR_BAD_INDEX = 1
 MOE_DEVERR_CAPACITY = 2
 MOE_DEVERR_TIMEOUT = 4
+MOE_STATIC_SCRATCH_INTS = 262144
 
 
 class MoeLayout(ctypes.Structure):
@@ -59,6 +60,7 @@ SIGNATURES = {
     "moe_layout_workspace_bytes": (c_int32, [c_int32, c_int32, ctypes.POINTER(c_size_t)]),
     "moe_route_to_multihot": (c_int32, [_P, _P, c_int32, c_int32, c_int32, _P, _P, _P, _P, _P]),
     "moe_dispatch": (c_int32, [_P, _P, _P, c_int32, _LP, _P, ctypes.POINTER(c_int64), _P]),
+    "moe_dispatch_static_scratch": (c_int32, [_P, _P, _P, c_int32, _LP, _P, ctypes.POINTER(c_int64), _P]),
     "moe_grouped_experts": (c_int32, [_P, _LP, c_int32, c_int32, _P, _P, _P, _P, _P, _P, _P]),
     "moe_combine": (c_int32, [_P, _LP, c_int32, _P, _P]),
     "moe_combine_backward": (c_int32, [_P, _P, _LP, c_int32, _P, _P, _P]),

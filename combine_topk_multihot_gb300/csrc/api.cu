@@ -97,6 +97,8 @@ moe_status check_layout(const moe_layout* L) {
 
 }  // namespace
 
+moe_status set_last_error(moe_status st, const char* text) { return fail(st, "%s", text); }
+
 int sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return 148;

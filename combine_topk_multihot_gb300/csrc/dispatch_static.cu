@@ -1,0 +1,96 @@
+// moe_dispatch_static_scratch: moe_dispatch for callers that cannot allocate
+// device memory.
+//
+// moe_dispatch needs a small scratch buffer for its per-chunk expert counters
+// (moe_layout.workspace, E * ceil(T/32) int32).  Some callers have no way to
+// get one: a plugin inside an inference engine that owns every byte of the
+// device pool and hands a layer only its declared inputs and outputs, or a
+// serving loop that must never call cudaMalloc because it can synchronise the
+// device and stall every stream.  This entry point takes its scratch from a
+// fixed array that lives in the library's own device memory instead.
+//
+// The array below is a file-scope __device__ variable: every GPU on which
+// the library is loaded holds its 1 MiB from load until the process exits.
+// Host code only knows the symbol, not its device address, so the address is
+// looked up once per device with cudaGetSymbolAddress and handed to the
+// kernels through the layout's workspace pointer.
+
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+
+namespace {
+
+constexpr long long STATIC_SCRATCH_INTS = MOE_STATIC_SCRATCH_INTS;  // 1 MiB of int32 counters
+
+static __device__ __align__(256) int g_dispatch_scratch[STATIC_SCRATCH_INTS];
+
+constexpr int MAX_DEVICES = 64;
+std::mutex g_scratch_mu;
+int* g_scratch_ptr[MAX_DEVICES];  // device address of g_dispatch_scratch, per device
+
+// Device address of the static scratch on the current device; looked up on
+// the first call for that device.
+moe_status static_scratch(int** out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) {
+    char msg[160];
+    snprintf(msg, sizeof(msg), "moe_dispatch_static_scratch: cudaGetDevice: %s", cudaGetErrorString(err));
+    return set_last_error(MOE_ERR_CUDA, msg);
+  }
+  if (dev < 0 || dev >= MAX_DEVICES)
+    return set_last_error(MOE_ERR_DEVICE, "moe_dispatch_static_scratch: device ordinal out of range");
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_dispatch_scratch);
+    if (err != cudaSuccess || p == nullptr) {
+      char msg[200];
+      snprintf(msg, sizeof(msg),
+               "moe_dispatch_static_scratch: cudaGetSymbolAddress of the static scratch failed: %s",
+               cudaGetErrorString(err));
+      return set_last_error(MOE_ERR_CUDA, msg);
+    }
+    g_scratch_ptr[dev] = static_cast<int*>(p);
+  }
+  *out = g_scratch_ptr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status moe_dispatch_static_scratch(const moe_bf16* x, const uint8_t* routing_map,
+                                                  const float* probs, int32_t H,
+                                                  const moe_layout* L, moe_bf16* x_disp,
+                                                  int64_t* rows_host, moe_stream_t stream) {
+  if (L == nullptr) return set_last_error(MOE_ERR_INVALID_ARG, "moe_dispatch_static_scratch: layout is NULL");
+  if (L->T < 0 || L->E < 1)
+    return set_last_error(MOE_ERR_INVALID_ARG, "moe_dispatch_static_scratch: bad T or E");
+  const long long needed = layout_chunks(L->T) * static_cast<long long>(L->E);
+  if (needed > STATIC_SCRATCH_INTS) {
+    char msg[256];
+    snprintf(msg, sizeof(msg),
+             "moe_dispatch_static_scratch: E * ceil(T/32) = %lld counters exceeds the static "
+             "scratch of %lld (T=%d, E=%d); use moe_dispatch with a caller-provided workspace",
+             needed, STATIC_SCRATCH_INTS, L->T, L->E);
+    return set_last_error(MOE_ERR_UNSUPPORTED_SHAPE, msg);
+  }
+  int* scratch = nullptr;
+  moe_status st = static_scratch(&scratch);
+  if (st != MOE_OK) return st;
+  // Same call as moe_dispatch; only the counters' scratch differs.  Every
+  // counter the kernels read is written earlier in the same call, so nothing
+  // in the array has to start at zero.
+  moe_layout with_scratch = *L;
+  with_scratch.workspace = scratch;
+  return moe_dispatch(x, routing_map, probs, H, &with_scratch, x_disp, rows_host, stream);
+}

@@ -11,6 +11,9 @@ namespace moe {
 
 int sm_count();  // SMs of the current device (cached)
 
+// Records `text` as this thread's moe_last_error() and returns `st`.
+moe_status set_last_error(moe_status st, const char* text);
+
 // Tokens per chunk of the layout's histogram / placement passes.
 constexpr int LAYOUT_CHUNK = 32;
 

@@ -164,6 +164,36 @@ MOE_API moe_status moe_dispatch(const moe_bf16* x, const uint8_t* routing_map, c
                         int64_t* rows_host, moe_stream_t stream);
 
 /*
+ * moe_dispatch without caller-provided scratch.  The pages have no
+ * counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory -- for example a plugin inside an inference engine
+ * that owns the whole device pool and passes a layer only its declared
+ * inputs and outputs, or a serving loop that must not call cudaMalloc
+ * because it can synchronise the device.
+ *
+ * Arguments, results and errors are those of moe_dispatch, except that
+ * L->workspace is ignored (it may be NULL): the per-chunk expert counters
+ * live in a static device array inside the library, MOE_STATIC_SCRATCH_INTS
+ * int32 (1 MiB) per GPU, held from library load until the process exits.
+ *   - Limit: E * ceil(T / 32) <= MOE_STATIC_SCRATCH_INTS (E = 128 allows
+ *     T <= 65536); larger sizes return MOE_ERR_UNSUPPORTED_SHAPE before any
+ *     work is queued.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents
+ *     (every counter a call reads is written earlier in that call, so nothing
+ *     needs clearing).  Calls whose work overlaps on the GPU -- on different
+ *     streams, or from different host threads without ordering -- race on it
+ *     and must be serialised by the caller.
+ *   - No device memory is allocated or freed.
+ */
+#define MOE_STATIC_SCRATCH_INTS 262144
+MOE_API moe_status moe_dispatch_static_scratch(const moe_bf16* x, const uint8_t* routing_map,
+                                               const float* probs, int32_t H,
+                                               const moe_layout* L, moe_bf16* x_disp,
+                                               int64_t* rows_host, moe_stream_t stream);
+
+/*
  * a5. Grouped SwiGLU experts that apply the routing weight.  [DEP] Expanded
  * layout (the experts apply the routing weights); Benchmarks (bf16 grouped GEMMs).
  *   x_disp  [C, H] bf16 rows (moe_dispatch's output).
