@@ -145,6 +145,12 @@ def algorithmic(cfg, counts: np.ndarray, R: int, N: int, C: int, backward: bool)
     if backward:
         out["combine_bwd_bytes"] = T * H * 2 + C * H * 2 + N * H * 2 + 4 * C
         out["dispatch_bwd_bytes"] = N * H * 2 + T * H * 2 + T * E * 4
+        # scale, dgrad1 (W2, gu), dgrad2 (W1), wgrad2, wgrad1 (fp32 dW written)
+        out["experts_bwd_bytes"] = (w_bytes + 2 * w_bytes  # weights read, fp32 dW written
+                                    + N * H * 2 * 4        # grad_y, G_o (w + 2 r), x_disp
+                                    + N * 2 * I * 2 * 4    # gu read, G_gu (w + 2 r)
+                                    + N * I * 2 + N * H * 2)  # h read, grad_x_disp written
+        out["experts_bwd_flops"] = 12.0 * N * H * I
     return out
 
 
@@ -192,25 +198,47 @@ def run_ours(args, world, rank, local):
 
     stream = torch.cuda.current_stream()
     ev = lambda: torch.cuda.Event(enable_timing=True)
+    bwd = cfg.backward
+    stages = ["multihot", "dispatch", "experts", "combine"]
     launches_per_step = 1 + 4 + 2 + 1
+    if bwd:
+        stages += ["combine_bwd", "experts_bwd", "dispatch_bwd", "multihot_bwd"]
+        launches_per_step += 1 + 5 + 1 + 1
+        bufs["o"] = torch.empty(C, H, dtype=torch.bfloat16, device=dev)
+        bufs["gu"] = torch.empty(C, 2 * I, dtype=torch.bfloat16, device=dev)
+        for l, L in enumerate(layers):
+            L["grad_out"] = synthetic.make_grad_out(T, H, cfg.seed + 7919 * l + 104729 * rank, device=dev)
 
     def step(L, events=None):
-        if events: events[0].record(stream)
-        rmap, probs, _ = moe.moe_route_to_multihot(L["topk_idx"], L["topk_probs"], E, lay.status)
-        if events: events[1].record(stream)
+        rec = (lambda j: events[j].record(stream)) if events else (lambda j: None)
+        rec(0)
+        rmap, probs, win = moe.moe_route_to_multihot(L["topk_idx"], L["topk_probs"], E, lay.status)
+        rec(1)
         moe.moe_dispatch(L["x"], rmap, probs, lay, host_sync=host_sync, x_disp=x_disp)
-        if events: events[2].record(stream)
-        moe.moe_grouped_experts(x_disp, lay, L["W1"], L["W2"], out=bufs)
-        if events: events[3].record(stream)
+        rec(2)
+        moe.moe_grouped_experts(x_disp, lay, L["W1"], L["W2"], out=bufs, save_o=bwd, save_gu=bwd)
+        rec(3)
         moe.moe_combine(bufs["y"], lay, out=out)
-        if events: events[4].record(stream)
+        rec(4)
+        if bwd:
+            grad_y, grad_w = moe.moe_combine_backward(L["grad_out"], lay, o_save=bufs["o"])
+            rec(5)
+            gxd, dW1, dW2 = moe.moe_grouped_experts_backward(grad_y, x_disp, bufs["h"], bufs["gu"], lay,
+                                                             L["W1"], L["W2"])
+            rec(6)
+            grad_x, grad_probs = moe.moe_dispatch_backward(gxd, lay, grad_w)
+            rec(7)
+            moe.moe_route_to_multihot_backward(grad_probs, L["topk_idx"], win)
+            rec(8)
+            return grad_x
+        return None
 
     for i in range(args.warmup):
         step(layers[i % n_layers])
     torch.cuda.synchronize()
     barrier(world)
 
-    step_events = [[ev() for _ in range(5)] for _ in range(args.steps)]
+    step_events = [[ev() for _ in range(len(stages) + 1)] for _ in range(args.steps)]
     t0, t1 = ev(), ev()
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
@@ -223,21 +251,23 @@ def run_ours(args, world, rank, local):
     barrier(world)
     ms = t0.elapsed_time(t1)
     ms_max = max_over_ranks(ms, world)
-    per = {k: [] for k in ("multihot", "dispatch", "experts", "combine")}
-    for e5 in step_events:
-        for j, k in enumerate(per):
-            per[k].append(e5[j].elapsed_time(e5[j + 1]))
+    per = {k: [] for k in stages}
+    for evs in step_events:
+        for j, k in enumerate(stages):
+            per[k].append(evs[j].elapsed_time(evs[j + 1]))
     status = int(lay.status.item())
     if status:
         raise RuntimeError(f"device status word set: {status}")
 
     # ---- end to end through the public API with host buffers
     pin = lambda t: t.cpu().pin_memory()
-    host = [{k: pin(L[k]) for k in ("x", "topk_idx", "topk_probs")} for L in layers]
+    in_keys = ("x", "topk_idx", "topk_probs") + (("grad_out",) if bwd else ())
+    host = [{k: pin(L[k]) for k in in_keys} for L in layers]
     out_host = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
-    d_in = {k: torch.empty_like(layers[0][k]) for k in ("x", "topk_idx", "topk_probs")}
+    gx_host = torch.empty(T, H, dtype=torch.bfloat16).pin_memory() if bwd else None
+    d_in = {k: torch.empty_like(layers[0][k]) for k in in_keys}
     h2d = sum(v.numel() * v.element_size() for v in host[0].values())
-    d2h = out_host.numel() * out_host.element_size()
+    d2h = out_host.numel() * out_host.element_size() * (2 if bwd else 1)
 
     def e2e_step(i):
         hs = host[i % n_layers]
@@ -245,8 +275,10 @@ def run_ours(args, world, rank, local):
             d_in[k].copy_(hs[k], non_blocking=True)
         L = dict(layers[i % n_layers])
         L.update(d_in)
-        step(L)
+        gx = step(L)
         out_host.copy_(out, non_blocking=True)
+        if bwd:
+            gx_host.copy_(gx, non_blocking=True)
 
     for i in range(args.warmup):
         e2e_step(i)
@@ -269,6 +301,10 @@ def run_ours(args, world, rank, local):
     ex_us = 1e3 * float(np.mean(per["experts"]))
     ex_bytes = float(np.mean([w["experts_bytes"] for w in steps_w]))
     ex_flops = float(np.mean([w["experts_flops"] for w in steps_w]))
+    if bwd:  # the dominant work is the experts' forward + backward GEMMs
+        ex_us += 1e3 * float(np.mean(per["experts_bwd"]))
+        ex_bytes += float(np.mean([w["experts_bwd_bytes"] for w in steps_w]))
+        ex_flops += float(np.mean([w["experts_bwd_flops"] for w in steps_w]))
     t_hbm = ex_bytes / (hbm * 1e9)
     t_tc = ex_flops / (bf16_burst * 1e12)
     if t_hbm >= t_tc:
@@ -277,7 +313,8 @@ def run_ours(args, world, rank, local):
         roof = {"bound": "tensor", "achieved": ex_flops / (ex_us * 1e-6) / 1e12, "peak": bf16_burst, "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = None
-    roof["kernel"] = "experts: grouped_gemm_kernel<0> (gate/up + SwiGLU) + grouped_gemm_kernel<1> (down x weight)"
+    roof["kernel"] = ("experts: grouped_gemm_kernel<0> (gate/up + SwiGLU) + grouped_gemm_kernel<1> (down x weight)"
+                      + (" + the backward's scale_rows + 4 bwd_gemm_kernel launches" if bwd else ""))
     roof["peak_source"] = src
     roof["tensor_frac_of_burst"] = ex_flops / (ex_us * 1e-6) / 1e12 / bf16_burst
 
@@ -291,6 +328,7 @@ def run_ours(args, world, rank, local):
         "dispatch_GBs": float(np.mean([w["dispatch_bytes"] for w in steps_w])) / (disp_us * 1e-6) / 1e9,
         "combine_GBs": float(np.mean([w["combine_bytes"] for w in steps_w])) / (comb_us * 1e-6) / 1e9,
         "experts_TFLOPs": ex_flops / (ex_us * 1e-6) / 1e12,
+        **({k + "_us": 1e3 * float(np.mean(per[k])) for k in stages[4:]} if bwd else {}),
         "rows_used": [r[0] for r in rows], "rows_valid": [r[1] for r in rows], "capacity": C,
     }
     kernels["dispatch_frac_hbm"] = kernels["dispatch_GBs"] / hbm
@@ -298,7 +336,7 @@ def run_ours(args, world, rank, local):
 
     tokens = T * world * args.steps
     res = {
-        "metric": "MoE layer tokens/sec (dispatch+experts+combine)",
+        "metric": "MoE layer tokens/sec (dispatch+experts+combine)" + (", forward + backward" if bwd else ""),
         "value": tokens / (ms_max * 1e-3),
         "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,

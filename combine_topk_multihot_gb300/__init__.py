@@ -6,11 +6,13 @@ loudly if the library has not been built -- there is no CPU fallback.
 """
 from .moe import (Layout, MoEError, ForwardResult, worst_case_rows, moe_route_to_multihot,
                   moe_dispatch, moe_grouped_experts, moe_combine, moe_combine_backward,
-                  moe_dispatch_backward, moe_route_to_multihot_backward, moe_layer_forward)
+                  moe_dispatch_backward, moe_route_to_multihot_backward, moe_layer_forward,
+                  moe_grouped_experts_backward)
 from . import _native
 
 __all__ = [
     "Layout", "MoEError", "ForwardResult", "worst_case_rows", "moe_route_to_multihot",
     "moe_dispatch", "moe_grouped_experts", "moe_combine", "moe_combine_backward",
-    "moe_dispatch_backward", "moe_route_to_multihot_backward", "moe_layer_forward", "_native",
+    "moe_dispatch_backward", "moe_route_to_multihot_backward", "moe_layer_forward",
+    "moe_grouped_experts_backward", "_native",
 ]

@@ -281,4 +281,37 @@ moe_status moe_route_to_multihot_backward(const float* grad_probs, const int64_t
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_route_to_multihot_backward launch");
 }
 
+moe_status moe_experts_backward_workspace_bytes(int64_t capacity, int32_t H, int32_t I,
+                                                size_t* bytes) {
+  MOE_REQUIRE(bytes != nullptr, MOE_ERR_INVALID_ARG, "bytes is NULL");
+  MOE_REQUIRE(capacity >= 0 && H > 0 && I > 0, MOE_ERR_INVALID_ARG, "bad capacity / H / I");
+  *bytes = experts_backward_workspace(capacity, H, I);
+  return MOE_OK;
+}
+
+moe_status moe_grouped_experts_backward(const moe_bf16* grad_y, const moe_bf16* x_disp,
+                                        const moe_bf16* h, const moe_bf16* gu_save,
+                                        const moe_layout* L, int32_t H, int32_t I,
+                                        const moe_bf16* W1, const moe_bf16* W2,
+                                        moe_bf16* grad_x_disp, float* dW1, float* dW2,
+                                        void* workspace, moe_stream_t stream) {
+  moe_status st = check_layout(L);
+  if (st != MOE_OK) return st;
+  if ((st = check_hidden(H)) != MOE_OK) return st;
+  MOE_REQUIRE(I > 0 && I % 128 == 0, MOE_ERR_UNSUPPORTED_SHAPE,
+              "the intermediate size must be a positive multiple of 128 (got %d)", I);
+  MOE_REQUIRE(W1 && W2 && dW1 && dW2 && workspace, MOE_ERR_INVALID_ARG,
+              "moe_grouped_experts_backward: NULL weight, weight-gradient or workspace pointer");
+  MOE_REQUIRE(L->capacity == 0 || (grad_y && x_disp && h && gu_save && grad_x_disp),
+              MOE_ERR_INVALID_ARG, "moe_grouped_experts_backward: NULL row buffer");
+  MOE_REQUIRE(aligned16(grad_y) && aligned16(x_disp) && aligned16(h) && aligned16(gu_save) &&
+                  aligned16(W1) && aligned16(W2) && aligned16(grad_x_disp) && aligned16(dW1) &&
+                  aligned16(dW2),
+              MOE_ERR_INVALID_ARG, "moe_grouped_experts_backward: pointers must be 16-byte aligned");
+  if ((st = check_device()) != MOE_OK) return st;
+  cudaError_t err = launch_experts_backward(grad_y, x_disp, h, gu_save, *L, H, I, W1, W2,
+                                            grad_x_disp, dW1, dW2, workspace, stream);
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_grouped_experts_backward launch");
+}
+
 }  // extern "C"

@@ -251,6 +251,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll 1
         for (int c = 0; c < BN / 2; c += 32) {
           uint32_t g[32], u[32];
+          __syncwarp();
           tmem_ld32(tb + c, g);
           tmem_ld32(tb + BN / 2 + c, u);
           tmem_ld_wait();
@@ -289,6 +290,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           uint32_t o[32];
+          __syncwarp();
           tmem_ld32(tb + c, o);
           tmem_ld_wait();
           if (valid) {
@@ -330,36 +332,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // ---------------------------------------------------------------- host side
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
 // A row-major bf16 matrix [rows, cols] read as 128-row x 64-column boxes with
 // the 128-byte swizzle; out-of-range rows read as zero.
 bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {BK, 128};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return make_tma_2d_bf16(map, base, rows, cols, 128);
 }
 
 template <int EPI>

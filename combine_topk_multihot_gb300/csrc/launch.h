@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "moe.h"
@@ -10,6 +11,13 @@
 namespace moe {
 
 int sm_count();  // SMs of the current device (cached)
+
+// Tensor map of a row-major bf16 matrix [rows, cols] (cols contiguous) read as
+// boxes of box_rows x 64 columns with the 128-byte swizzle; reads past the
+// last row return zeros.  False if the driver entry point is missing or the
+// encoding is rejected.
+bool make_tma_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                      uint32_t box_rows);
 
 // Records `text` as this thread's moe_last_error() and returns `st`.
 moe_status set_last_error(moe_status st, const char* text);
@@ -46,5 +54,14 @@ cudaError_t launch_experts_forward(const uint16_t* x_disp, const moe_layout& L, 
                                    const uint16_t* W1, const uint16_t* W2, uint16_t* h,
                                    uint16_t* y, uint16_t* o_save, uint16_t* gu_save,
                                    cudaStream_t s);
+
+// tcgen05 grouped GEMMs of the expert backward (a9); workspace holds G_o [C, H]
+// and G_gu [C, 2I] (bf16).
+size_t experts_backward_workspace(long long capacity, int H, int I);
+cudaError_t launch_experts_backward(const uint16_t* grad_y, const uint16_t* x_disp,
+                                    const uint16_t* h, const uint16_t* gu_save, const moe_layout& L,
+                                    int H, int I, const uint16_t* W1, const uint16_t* W2,
+                                    uint16_t* grad_x_disp, float* dW1, float* dW2, void* workspace,
+                                    cudaStream_t s);
 
 }  // namespace moe

@@ -178,6 +178,27 @@ def moe_route_to_multihot_backward(grad_probs: torch.Tensor, topk_idx: torch.Ten
     return g
 
 
+def moe_grouped_experts_backward(grad_y: torch.Tensor, x_disp: torch.Tensor, h: torch.Tensor,
+                                 gu_save: torch.Tensor, layout: Layout, W1: torch.Tensor,
+                                 W2: torch.Tensor, stream=None):
+    """a9: returns (grad_x_disp [C, H] bf16, dW1 [E, 2I, H] fp32, dW2 [E, H, I] fp32)."""
+    E, twoI, H = W1.shape
+    I = twoI // 2
+    dev = grad_y.device
+    nbytes = ctypes.c_size_t(0)
+    _check(N.lib.moe_experts_backward_workspace_bytes(layout.capacity, H, I, ctypes.byref(nbytes)),
+           "moe_experts_backward_workspace_bytes")
+    ws = torch.empty(nbytes.value, dtype=torch.uint8, device=dev)
+    grad_x_disp = torch.empty(layout.capacity, H, dtype=torch.bfloat16, device=dev)
+    dW1 = torch.empty(E, 2 * I, H, dtype=torch.float32, device=dev)
+    dW2 = torch.empty(E, H, I, dtype=torch.float32, device=dev)
+    _check(N.lib.moe_grouped_experts_backward(_ptr(grad_y), _ptr(x_disp), _ptr(h), _ptr(gu_save),
+                                              layout.ref, H, I, _ptr(W1), _ptr(W2), _ptr(grad_x_disp),
+                                              _ptr(dW1), _ptr(dW2), _ptr(ws), _stream(stream)),
+           "moe_grouped_experts_backward")
+    return grad_x_disp, dW1, dW2
+
+
 @dataclass
 class ForwardResult:
     out: torch.Tensor

@@ -267,6 +267,33 @@ MOE_API moe_status moe_route_to_multihot_backward(const float* grad_probs, const
                                           int32_t T, int32_t K, int32_t E,
                                           float* grad_topk_probs, moe_stream_t stream);
 
+/*
+ * a9. Expert backward: the dgrad and wgrad of the SwiGLU experts.  [DEP]
+ * Training (both the tokens and the routing weights receive gradients; the
+ * routing-weight part is moe_combine_backward's grad_w).  With
+ * G_o = w_r * grad_y (y = w_r * o moves the weight onto the gradient):
+ *   dW2[e] = sum_r G_o[r]^T h[r];  G_h = G_o W2[e];
+ *   G_g = G_h * u * silu'(g),  G_u = G_h * silu(g)  (g, u: gate / up pre-activations);
+ *   dW1[e] = sum_r [G_g | G_u][r]^T x_disp[r];  grad_x_disp = [G_g | G_u] W1[e].
+ *   grad_y [C, H] bf16 (moe_combine_backward's output); x_disp [C, H], h [C, I]
+ *     and gu_save [C, 2I] bf16 from the forward (gu_save is required here).
+ *   W1, W2: as in moe_grouped_experts.
+ *   grad_x_disp [C, H] bf16 (out): written on the valid rows only.
+ *   dW1 [E, 2I, H], dW2 [E, H, I] fp32 (out): fully overwritten, fp32
+ *     accumulation; an expert with no rows gets zeros.
+ *   workspace: moe_experts_backward_workspace_bytes(capacity, H, I) bytes,
+ *     caller-owned scratch for G_o and [G_g | G_u] (bf16).
+ * Row counts are read on the device: no host sync.
+ */
+MOE_API moe_status moe_experts_backward_workspace_bytes(int64_t capacity, int32_t H, int32_t I,
+                                                        size_t* bytes);
+MOE_API moe_status moe_grouped_experts_backward(const moe_bf16* grad_y, const moe_bf16* x_disp,
+                                                const moe_bf16* h, const moe_bf16* gu_save,
+                                                const moe_layout* L, int32_t H, int32_t I,
+                                                const moe_bf16* W1, const moe_bf16* W2,
+                                                moe_bf16* grad_x_disp, float* dW1, float* dW2,
+                                                void* workspace, moe_stream_t stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

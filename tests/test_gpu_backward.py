@@ -1,0 +1,111 @@
+"""GPU parity of the expert backward (a9) against the fp64 oracle.
+
+The GPU's own forward outputs (x_disp, h) and combine-backward output
+(grad_y) feed both sides, so the test isolates the backward GEMMs.  The
+oracle recomputes the gate / up pre-activations exactly; the GPU reads the
+bf16 copies its forward saved.  grad_x_disp (bf16) and dW1 / dW2 (fp32) must
+satisfy max |err| <= 2e-2 and rel L2 <= 5e-3; experts with no rows must get
+exactly zero weight gradients.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synthetic
+from tests._util import (GEMM_MAX_ABS, GEMM_REL_L2, assert_gemm_close, bits, random_routing)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def moe():
+    assert torch.cuda.is_available(), "GPU tests need a GPU"
+    import combine_topk_multihot_gb300 as m
+    return m
+
+
+def _assert_f32_close(gpu: np.ndarray, ref: np.ndarray, what: str):
+    g = gpu.astype(np.float64)
+    r = ref.astype(np.float64)
+    assert np.isfinite(g).all(), what
+    err = np.abs(g - r).max() if g.size else 0.0
+    den = np.linalg.norm(r)
+    rel = np.linalg.norm(g - r) / den if den > 0 else np.linalg.norm(g - r)
+    assert err <= GEMM_MAX_ABS and rel <= GEMM_REL_L2, f"{what}: max|err|={err:.3g} rel_l2={rel:.3g}"
+
+
+def _run(moe, T, H, E, K, I, P, seed, drop=0.0):
+    idx, p = random_routing(T, E, K, seed=seed, drop=drop)
+    gen = torch.Generator().manual_seed(seed)
+    x = torch.randn(T, H, generator=gen).to(torch.bfloat16)
+    W1 = (torch.randn(E, 2 * I, H, generator=gen) * 0.02).to(torch.bfloat16)
+    W2 = (torch.randn(E, H, I, generator=gen) * 0.02).to(torch.bfloat16)
+    grad_out = torch.randn(T, H, generator=gen).to(torch.bfloat16)
+    C = O.worst_case_capacity(T, E, K, P)
+    d = lambda t: t.to(DEV)
+    fwd = moe.moe_layer_forward(d(x), d(idx), d(p), d(W1), d(W2), P, capacity=C, save_for_backward=True)
+    grad_y, grad_w = moe.moe_combine_backward(d(grad_out), fwd.layout, o_save=fwd.o)
+    gxd, dW1, dW2 = moe.moe_grouped_experts_backward(grad_y, fwd.x_disp, fwd.h, fwd.gu, fwd.layout,
+                                                     d(W1), d(W2))
+    torch.cuda.synchronize()
+    assert int(fwd.layout.status.item()) == 0
+    return dict(fwd=fwd, grad_y=grad_y, gxd=gxd, dW1=dW1, dW2=dW2, W1=W1, W2=W2)
+
+
+@pytest.mark.parametrize("T,H,E,K,I,P,drop", [
+    (64, 256, 8, 2, 128, 16, 0.0),      # the tiny layer: BN = 128 for dgrad1 and wgrad2
+    (300, 512, 8, 2, 256, 16, 0.0),     # 2 N tiles, ragged 64-row K tails in wgrad
+    (1000, 256, 4, 2, 128, 1, 0.0),     # several 128-row tiles, unaligned groups
+    (20, 512, 12, 1, 384, 1, 0.0),      # empty experts, I = 384 (BN 128 in dgrad1)
+    (260, 768, 12, 3, 256, 128, 0.2),   # padded groups, drops, 3 N tiles in dgrad2
+])
+def test_expert_backward_matches_oracle(moe, T, H, E, K, I, P, drop):
+    r = _run(moe, T, H, E, K, I, P, seed=T + 3 * H, drop=drop)
+    L = r["fwd"].layout
+    re = L.row_expert.cpu().numpy()
+    rw = L.row_weight.cpu().numpy()
+    valid = L.row_token.cpu().numpy() >= 0
+    gx_ref, dW1_ref, dW2_ref = O.grouped_experts_backward(
+        bits(r["grad_y"]), bits(r["fwd"].x_disp), bits(r["fwd"].h), re, rw,
+        bits(r["W1"]), bits(r["W2"]), I)
+    assert_gemm_close(bits(r["gxd"])[valid], gx_ref[valid], "grad_x_disp")
+    dW1 = r["dW1"].cpu().numpy()
+    dW2 = r["dW2"].cpu().numpy()
+    _assert_f32_close(dW1, dW1_ref, "dW1")
+    _assert_f32_close(dW2, dW2_ref, "dW2")
+    counts = L.tokens_per_expert.cpu().numpy()
+    for e in np.flatnonzero(counts == 0):
+        assert not dW1[e].any() and not dW2[e].any(), f"expert {e} has no rows"
+
+
+def test_expert_backward_full_size_h4096_sampled(moe):
+    """The h4096 layer (T 16384, H 4096, I 1536, E 128, top-8) forward +
+    backward in the benchmark's configuration; the oracle checks every row and
+    both weight gradients of the largest and the smallest non-empty expert."""
+    cfg = synthetic.CONFIGS["h4096"]
+    T, H, E, K, I, P = cfg.T, cfg.H, cfg.E, cfg.K, cfg.I, cfg.P
+    x = synthetic.make_tokens(T, H, cfg.seed, device=DEV)
+    idx, p = synthetic.make_routing(T, E, K, cfg.seed)
+    W1, W2 = synthetic.make_weights(E, H, I, cfg.seed, device=DEV)
+    grad_out = synthetic.make_grad_out(T, H, cfg.seed, device=DEV)
+    fwd = moe.moe_layer_forward(x, idx.to(DEV), p.to(DEV), W1, W2, P, host_sync=True,
+                                save_for_backward=True)
+    grad_y, grad_w = moe.moe_combine_backward(grad_out, fwd.layout, o_save=fwd.o)
+    gxd, dW1, dW2 = moe.moe_grouped_experts_backward(grad_y, fwd.x_disp, fwd.h, fwd.gu, fwd.layout, W1, W2)
+    torch.cuda.synchronize()
+    L = fwd.layout
+    counts = L.tokens_per_expert.cpu().numpy()
+    offs = L.offsets.cpu().numpy()
+    rw = L.row_weight.cpu().numpy()
+    nz = np.flatnonzero(counts)
+    for e in {int(nz[np.argmax(counts[nz])]), int(nz[np.argmin(counts[nz])])}:
+        rows = np.arange(offs[e], offs[e] + counts[e])
+        f = O.bf16_bits_to_f64
+        dX, d1, d2 = O.expert_backward_f64(f(bits(fwd.x_disp[rows])), f(bits(fwd.h[rows])),
+                                           f(bits(grad_y[rows])), rw[rows],
+                                           f(bits(W1[e])), f(bits(W2[e])), I)
+        assert_gemm_close(bits(gxd[rows]), O.f64_to_bf16_bits(dX), f"grad_x_disp e={e}")
+        _assert_f32_close(dW1[e].cpu().numpy(), d1.astype(np.float32), f"dW1 e={e}")
+        _assert_f32_close(dW2[e].cpu().numpy(), d2.astype(np.float32), f"dW2 e={e}")
