@@ -35,10 +35,12 @@ __device__ __forceinline__ uint4 acc_pack(const float (&acc)[8]) {
                     pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
 }
 
-// One warp per token.  Lane l holds token_row entries l, l+32, l+64, l+96.
-// Each lane owns H/256 16-byte column vectors; two are processed at a time,
-// and up to four rows are loaded before they are added (in row order) so that
-// eight 16-byte loads per lane are in flight.
+// One warp per (token, 512-byte column chunk): lane l sums the 16-byte vector
+// at column chunk v of each of the token's rows.  All of the token's rows
+// (up to 8 at a time) are loaded before they are added, in row order, so an
+// item costs one memory round trip; T * H/256 items keep every SM busy even
+// at small T.  With SCATTER, the warp of chunk 0 also writes the token's
+// grad_probs row.
 template <bool SCATTER>
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ rows,
                                                       const int* __restrict__ token_row, int T,
@@ -47,47 +49,37 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
                                                       const float* __restrict__ grad_w,
                                                       float* __restrict__ grad_probs, int E) {
   const int lane = threadIdx.x & 31;
-  const int V = H >> 8;
+  const int V = H >> 8;  // 512-byte chunks per row
+  const long long items = static_cast<long long>(T) * V;
   const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-  for (long long t = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-       t < T; t += nwarps) {
+  for (long long it = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       it < items; it += nwarps) {
+    const long long t = it / V;
+    const int v = static_cast<int>(it - t * V);
     int tr[4];
     int n = 0;
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
       const int k = lane + 32 * jj;
-      tr[jj] = k < K ? token_row[t * K + k] : -1;
+      tr[jj] = k < K ? __ldg(token_row + t * K + k) : -1;
       n += __popc(__ballot_sync(FULL_MASK, tr[jj] >= 0));
     }
-    uint4* o = reinterpret_cast<uint4*>(out + t * H);
-    for (int v0 = 0; v0 < V; v0 += 2) {
-      const bool two = v0 + 1 < V;
-      float a0[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      float a1[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int j0 = 0; j0 < n; j0 += 4) {
-        uint4 b0[4], b1[4];
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j0 = 0; j0 < n; j0 += 8) {
+      uint4 b[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int j = j0 + i;
-          const int r = __shfl_sync(FULL_MASK, pick4(tr, j >> 5), j & 31);
-          if (j < n) {
-            const uint4* src = reinterpret_cast<const uint4*>(rows + static_cast<long long>(r) * H);
-            b0[i] = __ldg(src + lane + 32 * v0);
-            if (two) b1[i] = __ldg(src + lane + 32 * (v0 + 1));
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          if (j0 + i < n) {
-            acc_add(a0, b0[i]);
-            if (two) acc_add(a1, b1[i]);
-          }
-        }
+      for (int i = 0; i < 8; ++i) {
+        const int j = j0 + i;
+        const int r = __shfl_sync(FULL_MASK, pick4(tr, j >> 5), j & 31);
+        if (j < n)
+          b[i] = __ldg(reinterpret_cast<const uint4*>(rows + static_cast<long long>(r) * H) + lane + 32 * v);
       }
-      o[lane + 32 * v0] = acc_pack(a0);
-      if (two) o[lane + 32 * (v0 + 1)] = acc_pack(a1);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (j0 + i < n) acc_add(acc, b[i]);
     }
-    if (SCATTER && grad_probs) {
+    reinterpret_cast<uint4*>(out + t * H)[lane + 32 * v] = acc_pack(acc);
+    if (SCATTER && grad_probs && v == 0) {
       float* gp = grad_probs + t * E;
       for (int e = lane * 4; e < E; e += 128)
         *reinterpret_cast<float4*>(gp + e) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -107,7 +99,8 @@ cudaError_t launch_combine(const uint16_t* rows, const moe_layout& L, int H, uin
                            const float* grad_w, float* grad_probs, cudaStream_t s) {
   if (L.T == 0) return cudaSuccess;
   const int threads = 256;
-  const long long need = (static_cast<long long>(L.T) + 7) / 8;
+  const long long items = static_cast<long long>(L.T) * (H >> 8);
+  const long long need = (items + 7) / 8;
   const int blocks = static_cast<int>(need < 8LL * sm_count() ? need : 8LL * sm_count());
   if (grad_probs) {
     combine_kernel<true><<<blocks, threads, 0, s>>>(rows, L.token_row, L.T, L.K, H, out,

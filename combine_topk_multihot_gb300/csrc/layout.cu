@@ -117,45 +117,64 @@ __global__ void __launch_bounds__(1024) layout_scan_kernel(int* __restrict__ chu
   }
 }
 
-// Stable placement.  The chunk's map is staged in shared memory; each token's
-// set experts are turned into ballot masks so a pair's position j inside the
-// token's row list is a popcount; then the thread of expert e walks the
-// chunk's tokens in order and assigns consecutive rows of its group.
+// Stable placement.  A chunk is 32 tokens, so the tokens of the chunk that go
+// to expert e form one 32-bit mask, and a pair's rank inside its expert's
+// group is (the chunk's start in the group) + popcount(mask below the token).
+// The chunk's map is staged in shared memory and turned into both bit
+// matrices: experts per token (ballots) and tokens per expert (a transpose of
+// it); then one warp per token places the token's pairs, lane l taking the
+// experts l, l+32, ...  A pair's position j in token_row is the popcount of the
+// token's expert mask below it.
 __global__ void __launch_bounds__(256) layout_place_kernel(
     const uint8_t* __restrict__ map, const float* __restrict__ probs, int T, int E, int K,
     int chunks, const int* __restrict__ chunk_base, const int* __restrict__ offsets,
     long long capacity, int* __restrict__ row_token, int* __restrict__ row_expert,
     float* __restrict__ row_weight, int* __restrict__ token_row, int* __restrict__ status) {
+  static_assert(LAYOUT_CHUNK == 32, "one 32-bit token mask per expert");
   extern __shared__ __align__(16) uint8_t smem[];
   const int c = blockIdx.x;
   const long long t0 = static_cast<long long>(c) * LAYOUT_CHUNK;
   const int nt = static_cast<int>(min(static_cast<long long>(LAYOUT_CHUNK), T - t0));
   const int E4 = E >> 2, EW = (E + 31) >> 5;
-  uint32_t* s_map32 = reinterpret_cast<uint32_t*>(smem);
-  uint32_t* s_mask = s_map32 + LAYOUT_CHUNK * E4;
+  uint32_t* s_map32 = reinterpret_cast<uint32_t*>(smem);     // [32][E] bytes
+  uint32_t* s_emask = s_map32 + LAYOUT_CHUNK * E4;             // [32][EW]: experts of each token
+  uint32_t* s_tmask = s_emask + LAYOUT_CHUNK * EW;             // [E]: tokens of each expert
+  int* s_base = reinterpret_cast<int*>(s_tmask + E);           // [E]: first row of this chunk's pairs
   const uint8_t* s_map = smem;
   const uint32_t* words = reinterpret_cast<const uint32_t*>(map + t0 * E);
   for (int i = threadIdx.x; i < nt * E4; i += blockDim.x) s_map32[i] = words[i];
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    s_base[e] = offsets[e] + chunk_base[static_cast<long long>(e) * chunks + c];
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  for (int tl = warp; tl < nt; tl += nwarps) {
+  for (int tl = warp; tl < LAYOUT_CHUNK; tl += nwarps) {
     for (int seg = 0; seg < EW; ++seg) {
       const int e = seg * 32 + lane;
-      const bool b = e < E && s_map[tl * E + e] != 0;
+      const bool b = tl < nt && e < E && s_map[tl * E + e] != 0;
       const uint32_t m = __ballot_sync(FULL_MASK, b);
-      if (lane == 0) s_mask[tl * EW + seg] = m;
+      if (lane == 0) s_emask[tl * EW + seg] = m;
     }
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    long long row = static_cast<long long>(offsets[e]) + chunk_base[static_cast<long long>(e) * chunks + c];
-    const int seg = e >> 5;
-    const uint32_t below = (1u << (e & 31)) - 1u;
-    for (int tl = 0; tl < nt; ++tl) {
-      if (s_map[tl * E + e]) {
-        int j = __popc(s_mask[tl * EW + seg] & below);
-        for (int s2 = 0; s2 < seg; ++s2) j += __popc(s_mask[tl * EW + s2]);
-        const long long t = t0 + tl;
+    const int seg = e >> 5, bit = e & 31;
+    uint32_t m = 0;
+#pragma unroll 8
+    for (int tl = 0; tl < LAYOUT_CHUNK; ++tl) m |= ((s_emask[tl * EW + seg] >> bit) & 1u) << tl;
+    s_tmask[e] = m;
+  }
+  __syncthreads();
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int tl = warp; tl < nt; tl += nwarps) {
+    const long long t = t0 + tl;
+    const uint32_t below_t = (1u << tl) - 1u;
+    int j_base = 0;
+    for (int seg = 0; seg < EW; ++seg) {
+      const uint32_t em = s_emask[tl * EW + seg];
+      const int e = seg * 32 + lane;
+      if ((em >> lane) & 1u) {
+        const long long row = static_cast<long long>(s_base[e]) + __popc(s_tmask[e] & below_t);
+        const int j = j_base + __popc(em & lt);
         if (row < capacity && j < K) {
           row_token[row] = static_cast<int>(t);
           row_expert[row] = e;
@@ -164,14 +183,10 @@ __global__ void __launch_bounds__(256) layout_place_kernel(
         } else {
           report(status, row < capacity ? MOE_DEVERR_BAD_INDEX : MOE_DEVERR_CAPACITY);
         }
-        ++row;
       }
+      j_base += __popc(em);
     }
-  }
-  for (int tl = threadIdx.x; tl < nt; tl += blockDim.x) {
-    int n = 0;
-    for (int s2 = 0; s2 < EW; ++s2) n += __popc(s_mask[tl * EW + s2]);
-    for (int j = n; j < K; ++j) token_row[(t0 + tl) * K + j] = -1;
+    for (int j = j_base + lane; j < K; j += 32) token_row[t * K + j] = -1;
   }
 }
 
@@ -278,7 +293,8 @@ cudaError_t launch_layout_place(const uint8_t* routing_map, const float* probs,
   const int chunks = static_cast<int>(layout_chunks(L.T));
   if (chunks == 0) return cudaSuccess;
   const size_t smem = static_cast<size_t>(LAYOUT_CHUNK) * L.E +
-                      static_cast<size_t>(LAYOUT_CHUNK) * ((L.E + 31) / 32) * sizeof(uint32_t);
+                      static_cast<size_t>(LAYOUT_CHUNK) * ((L.E + 31) / 32) * sizeof(uint32_t) +
+                      static_cast<size_t>(L.E) * (sizeof(uint32_t) + sizeof(int));
   layout_place_kernel<<<chunks, 256, smem, s>>>(routing_map, probs, L.T, L.E, L.K, chunks,
                                                 chunk_base, L.offsets, L.capacity, L.row_token,
                                                 L.row_expert, L.row_weight, L.token_row, L.status);

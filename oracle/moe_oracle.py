@@ -272,27 +272,31 @@ def routing_weight_grad(grad_y_bits, o_bits, row_expert, E) -> np.ndarray:
 # --------------------------------------------------------------------------
 # a9: expert backward (chain rule written out)
 # --------------------------------------------------------------------------
-def expert_backward_f64(X, h, GY, w, W1e, W2e, I):
+def expert_backward_f64(X, h, GY, w, W1e, W2e, I, rnd=bf16_round_f64):
     """Gradients of one expert's rows, in fp64.
 
     Forward: g = X Wg^T, u = X Wu^T, h = silu(g) u, o = h W2^T, y = w o.
     Given dL/dy = GY and the forward's h:
-      G_o = w * GY;  dW2 = G_o^T h;  G_h = G_o W2;
+      G_o = rnd(w * GY);  dW2 = G_o^T h;  G_h = G_o W2;
       silu'(g) = s (1 + g (1 - s)) with s = sigmoid(g);
-      G_g = G_h * u * silu'(g);  G_u = G_h * silu(g);
-      dW1 = [G_g | G_u]^T X;  dX = [G_g | G_u] W1.
-    Returns (dX [n, H], dW1 [2I, H], dW2 [H, I]).
+      G_g = G_h * u * silu'(g);  G_u = G_h * silu(g);  G_gu = rnd([G_g | G_u]);
+      dW1 = G_gu^T X;  dX = G_gu W1.
+    The experts are bf16 GEMMs, so the operands of the backward GEMMs (G_o,
+    G_gu) and the gate / up values the forward hands to the backward are bf16:
+    ``rnd`` rounds exactly there (g, u = rnd(X Wg^T), rnd(X Wu^T)); every product
+    and sum is exact fp64.  Pass the identity to get the real-valued chain rule.
+    Returns (dX [n, H], dW1 [2I, H], dW2 [H, I]), dX unrounded.
     """
     w = np.asarray(w, dtype=np.float64)[:, None]
-    G_o = w * GY
+    G_o = rnd(w * GY)
     dW2 = G_o.T @ h
     G_h = G_o @ W2e
-    g = X @ W1e[:I].T
-    u = X @ W1e[I:].T
+    g = rnd(X @ W1e[:I].T)
+    u = rnd(X @ W1e[I:].T)
     with np.errstate(over="ignore"):
         s = 1.0 / (1.0 + np.exp(-g))
     dsilu = s * (1.0 + g * (1.0 - s))
-    G_gu = np.concatenate([G_h * u * dsilu, G_h * (g * s)], axis=1)
+    G_gu = rnd(np.concatenate([G_h * u * dsilu, G_h * (g * s)], axis=1))
     dW1 = G_gu.T @ X
     dX = G_gu @ W1e
     return dX, dW1, dW2

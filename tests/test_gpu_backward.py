@@ -2,10 +2,10 @@
 
 The GPU's own forward outputs (x_disp, h) and combine-backward output
 (grad_y) feed both sides, so the test isolates the backward GEMMs.  The
-oracle recomputes the gate / up pre-activations exactly; the GPU reads the
-bf16 copies its forward saved.  grad_x_disp (bf16) must satisfy max |err| <=
-2e-2 and rel L2 <= 5e-3; dW1 / dW2 (fp32 sums over an expert's rows) the same
-rel L2 and a max error scaled by max(1, |ref|); experts with no rows must get
+oracle recomputes the gate / up pre-activations and rounds them to bf16, as
+the GPU's saved copies are; G_o and G_gu are bf16 on both sides (they are
+the operands of bf16 GEMMs).  grad_x_disp (bf16) and dW1 / dW2 (fp32) must
+satisfy max |err| <= 2e-2 and rel L2 <= 5e-3; experts with no rows must get
 exactly zero weight gradients.
 """
 import numpy as np
@@ -28,13 +28,11 @@ def moe():
 
 
 def _assert_f32_close(gpu: np.ndarray, ref: np.ndarray, what: str):
-    """fp32 weight gradients are sums over an expert's rows, so their size grows
-    with the row count; the max-error bound scales with it: |err| <=
-    2e-2 * max(1, |ref|).  The rel L2 bound is the fixed 5e-3."""
+    """max |err| <= 2e-2 and rel L2 <= 5e-3 on the fp32 weight gradients."""
     g = gpu.astype(np.float64)
     r = ref.astype(np.float64)
     assert np.isfinite(g).all(), what
-    err = (np.abs(g - r) / np.maximum(1.0, np.abs(r))).max() if g.size else 0.0
+    err = np.abs(g - r).max() if g.size else 0.0
     den = np.linalg.norm(r)
     rel = np.linalg.norm(g - r) / den if den > 0 else np.linalg.norm(g - r)
     assert err <= GEMM_MAX_ABS and rel <= GEMM_REL_L2, f"{what}: max|err|={err:.3g} rel_l2={rel:.3g}"
