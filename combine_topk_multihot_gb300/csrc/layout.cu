@@ -73,17 +73,35 @@ __global__ void __launch_bounds__(1024) layout_scan_kernel(int* __restrict__ chu
   __shared__ int s_count[1024];
   __shared__ int s_wsum[32], s_wcnt[32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // One warp per expert; lane l owns the contiguous chunks [l*per, (l+1)*per):
+  // a batched load pass for its sum, one warp scan of the sums, then a
+  // batched pass that writes the exclusive starts.
+  const int per = (chunks + 31) >> 5;
   for (int e = warp; e < E; e += 32) {
     int* row = chunk_counts + static_cast<long long>(e) * chunks;
-    int running = 0;
-    for (int c0 = 0; c0 < chunks; c0 += 32) {
-      const int c = c0 + lane;
-      const int v = c < chunks ? row[c] : 0;
-      const int incl = warp_inclusive_scan(v, lane);
-      if (c < chunks) row[c] = running + incl - v;
-      running += __shfl_sync(FULL_MASK, incl, 31);
+    const int c0 = min(chunks, lane * per), c1 = min(chunks, c0 + per);
+    int sum = 0;
+    for (int c = c0; c < c1; c += 8) {
+      int v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = c + i < c1 ? row[c + i] : 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sum += v[i];
     }
-    if (lane == 0) s_count[e] = running;
+    const int incl = warp_inclusive_scan(sum, lane);
+    int run = incl - sum;
+    for (int c = c0; c < c1; c += 8) {
+      int v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = c + i < c1 ? row[c + i] : 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (c + i < c1) row[c + i] = run;
+        run += v[i];
+      }
+    }
+    const int total = __shfl_sync(FULL_MASK, incl, 31);
+    if (lane == 0) s_count[e] = total;
   }
   __syncthreads();
   const int e = threadIdx.x;

@@ -180,8 +180,10 @@ def moe_route_to_multihot_backward(grad_probs: torch.Tensor, topk_idx: torch.Ten
 
 def moe_grouped_experts_backward(grad_y: torch.Tensor, x_disp: torch.Tensor, h: torch.Tensor,
                                  gu_save: torch.Tensor, layout: Layout, W1: torch.Tensor,
-                                 W2: torch.Tensor, stream=None):
-    """a9: returns (grad_x_disp [C, H] bf16, dW1 [E, 2I, H] fp32, dW2 [E, H, I] fp32)."""
+                                 W2: torch.Tensor, stream=None, return_operands: bool = False):
+    """a9: returns (grad_x_disp [C, H] bf16, dW1 [E, 2I, H] fp32, dW2 [E, H, I] fp32),
+    plus, with return_operands, views of the workspace's G_o [C, H] and
+    [G_g | G_u] [C, 2I] (bf16, valid rows)."""
     E, twoI, H = W1.shape
     I = twoI // 2
     dev = grad_y.device
@@ -196,7 +198,15 @@ def moe_grouped_experts_backward(grad_y: torch.Tensor, x_disp: torch.Tensor, h: 
                                               layout.ref, H, I, _ptr(W1), _ptr(W2), _ptr(grad_x_disp),
                                               _ptr(dW1), _ptr(dW2), _ptr(ws), _stream(stream)),
            "moe_grouped_experts_backward")
-    return grad_x_disp, dW1, dW2
+    if not return_operands:
+        return grad_x_disp, dW1, dW2
+    C = layout.capacity
+    base = (-ws.data_ptr()) % 256
+    go_bytes = C * H * 2
+    gu_off = base + (go_bytes + 255) // 256 * 256
+    G_o = ws[base:base + go_bytes].view(torch.bfloat16).view(C, H)
+    G_gu = ws[gu_off:gu_off + C * 2 * I * 2].view(torch.bfloat16).view(C, 2 * I)
+    return grad_x_disp, dW1, dW2, G_o, G_gu
 
 
 @dataclass

@@ -282,7 +282,10 @@ MOE_API moe_status moe_route_to_multihot_backward(const float* grad_probs, const
  *   dW1 [E, 2I, H], dW2 [E, H, I] fp32 (out): fully overwritten, fp32
  *     accumulation; an expert with no rows gets zeros.
  *   workspace: moe_experts_backward_workspace_bytes(capacity, H, I) bytes,
- *     caller-owned scratch for G_o and [G_g | G_u] (bf16).
+ *     caller-owned scratch.  On return it holds the backward GEMMs' bf16
+ *     operands on the valid rows: G_o [C, H] from the workspace's first
+ *     256-byte boundary, then [G_g | G_u] [C, 2I] from the next 256-byte
+ *     boundary after C*H*2 bytes.
  * Row counts are read on the device: no host sync.
  */
 MOE_API moe_status moe_experts_backward_workspace_bytes(int64_t capacity, int32_t H, int32_t I,

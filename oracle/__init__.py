@@ -40,6 +40,8 @@ from .moe_oracle import (OracleIndexError, OracleCapacityError, sentinel_expert,
                          dispatch, expert_forward_f64, grouped_experts, combine,
                          combine_backward, routing_weight_grad,
                          expert_backward_f64, grouped_experts_backward,
+                         backward_scale, backward_gate_up, backward_swiglu,
+                         backward_gemms,
                          dispatch_backward, route_to_multihot_backward,
                          layer_forward, layer_backward, worst_case_capacity)
 
@@ -49,6 +51,7 @@ __all__ = [
     "route_to_multihot", "counts_and_offsets", "build_layout", "dispatch",
     "expert_forward_f64", "grouped_experts", "combine", "combine_backward",
     "routing_weight_grad", "expert_backward_f64", "grouped_experts_backward",
+    "backward_scale", "backward_gate_up", "backward_swiglu", "backward_gemms",
     "dispatch_backward", "route_to_multihot_backward", "layer_forward",
     "layer_backward", "worst_case_capacity",
 ]

@@ -272,34 +272,49 @@ def routing_weight_grad(grad_y_bits, o_bits, row_expert, E) -> np.ndarray:
 # --------------------------------------------------------------------------
 # a9: expert backward (chain rule written out)
 # --------------------------------------------------------------------------
+def backward_scale(GY, w, rnd=bf16_round_f64):
+    """G_o = rnd(w * GY): y = w o, so dL/do = w dL/dy (rounded to bf16, the
+    operand type of the backward GEMMs)."""
+    return rnd(np.asarray(w, dtype=np.float64)[:, None] * GY)
+
+
+def backward_gate_up(X, W1e, I, rnd=bf16_round_f64):
+    """The forward's gate and up pre-activations as handed to the backward:
+    g = rnd(X Wg^T), u = rnd(X Wu^T)."""
+    return rnd(X @ W1e[:I].T), rnd(X @ W1e[I:].T)
+
+
+def backward_swiglu(G_o, W2e, g, u, rnd=bf16_round_f64):
+    """G_h = G_o W2;  G_g = G_h * u * silu'(g),  G_u = G_h * silu(g) with
+    silu'(g) = s (1 + g (1 - s)), s = sigmoid(g).  Returns rnd([G_g | G_u])."""
+    G_h = G_o @ W2e
+    with np.errstate(over="ignore"):
+        s = 1.0 / (1.0 + np.exp(-g))
+    dsilu = s * (1.0 + g * (1.0 - s))
+    return rnd(np.concatenate([G_h * u * dsilu, G_h * (g * s)], axis=1))
+
+
+def backward_gemms(G_o, G_gu, X, h, W1e):
+    """dX = G_gu W1;  dW1 = G_gu^T X;  dW2 = G_o^T h (exact fp64)."""
+    return G_gu @ W1e, G_gu.T @ X, G_o.T @ h
+
+
 def expert_backward_f64(X, h, GY, w, W1e, W2e, I, rnd=bf16_round_f64):
     """Gradients of one expert's rows, in fp64.
 
     Forward: g = X Wg^T, u = X Wu^T, h = silu(g) u, o = h W2^T, y = w o.
-    Given dL/dy = GY and the forward's h:
-      G_o = rnd(w * GY);  dW2 = G_o^T h;  G_h = G_o W2;
-      silu'(g) = s (1 + g (1 - s)) with s = sigmoid(g);
-      G_g = G_h * u * silu'(g);  G_u = G_h * silu(g);  G_gu = rnd([G_g | G_u]);
-      dW1 = G_gu^T X;  dX = G_gu W1.
-    The experts are bf16 GEMMs, so the operands of the backward GEMMs (G_o,
-    G_gu) and the gate / up values the forward hands to the backward are bf16:
-    ``rnd`` rounds exactly there (g, u = rnd(X Wg^T), rnd(X Wu^T)); every product
-    and sum is exact fp64.  Pass the identity to get the real-valued chain rule.
-    Returns (dX [n, H], dW1 [2I, H], dW2 [H, I]), dX unrounded.
+    Given dL/dy = GY and the forward's h, the chain rule in four steps:
+    backward_scale (G_o), backward_gate_up (g, u), backward_swiglu (G_gu =
+    [G_g | G_u]), backward_gemms (dX, dW1, dW2).  The experts are bf16 GEMMs,
+    so the operands of the backward GEMMs (G_o, G_gu) and the gate / up values
+    the forward hands to the backward are bf16: ``rnd`` rounds exactly there;
+    every product and sum is exact fp64.  Pass the identity to get the
+    real-valued chain rule.  Returns (dX [n, H], dW1 [2I, H], dW2 [H, I]).
     """
-    w = np.asarray(w, dtype=np.float64)[:, None]
-    G_o = rnd(w * GY)
-    dW2 = G_o.T @ h
-    G_h = G_o @ W2e
-    g = rnd(X @ W1e[:I].T)
-    u = rnd(X @ W1e[I:].T)
-    with np.errstate(over="ignore"):
-        s = 1.0 / (1.0 + np.exp(-g))
-    dsilu = s * (1.0 + g * (1.0 - s))
-    G_gu = rnd(np.concatenate([G_h * u * dsilu, G_h * (g * s)], axis=1))
-    dW1 = G_gu.T @ X
-    dX = G_gu @ W1e
-    return dX, dW1, dW2
+    G_o = backward_scale(GY, w, rnd)
+    g, u = backward_gate_up(X, W1e, I, rnd)
+    G_gu = backward_swiglu(G_o, W2e, g, u, rnd)
+    return backward_gemms(G_o, G_gu, X, h, W1e)
 
 
 def grouped_experts_backward(grad_y_bits, x_disp_bits, h_bits, row_expert,

@@ -1,12 +1,21 @@
 """GPU parity of the expert backward (a9) against the fp64 oracle.
 
-The GPU's own forward outputs (x_disp, h) and combine-backward output
-(grad_y) feed both sides, so the test isolates the backward GEMMs.  The
-oracle recomputes the gate / up pre-activations and rounds them to bf16, as
-the GPU's saved copies are; G_o and G_gu are bf16 on both sides (they are
-the operands of bf16 GEMMs).  grad_x_disp (bf16) and dW1 / dW2 (fp32) must
-satisfy max |err| <= 2e-2 and rel L2 <= 5e-3; experts with no rows must get
-exactly zero weight gradients.
+The GPU's own forward outputs (x_disp, h, the saved gate/up values) and
+combine-backward output (grad_y) feed both sides, so the test isolates the
+backward.  It checks the backward stage by stage:
+
+* the bf16 GEMM operands the GPU builds -- G_o = bf16(w * grad_y) and
+  G_gu = bf16([G_g | G_u]) -- against the oracle's steps on the same inputs
+  (intermediate tolerance, as for h);
+* the GEMMs themselves -- grad_x_disp, dW1, dW2 -- against exact fp64 products
+  of the GPU's own operands: max |err| <= 2e-2 and rel L2 <= 5e-3;
+* end to end against the independent oracle (exact chain rule with bf16
+  operands): rel L2 <= 5e-3.  A fixed max-error bound does not apply end to
+  end: one intermediate that rounds to the neighbouring bf16 value (its fp32
+  and fp64 values straddle a rounding boundary) shifts a whole row of dW by
+  ulp(G) * |x|, which exceeds 2e-2 where G is large.
+
+Experts with no rows must get exactly zero weight gradients.
 """
 import numpy as np
 import pytest
@@ -27,15 +36,39 @@ def moe():
     return m
 
 
-def _assert_f32_close(gpu: np.ndarray, ref: np.ndarray, what: str):
-    """max |err| <= 2e-2 and rel L2 <= 5e-3 on the fp32 weight gradients."""
+def _close(gpu: np.ndarray, ref: np.ndarray, what: str, max_abs=GEMM_MAX_ABS):
     g = gpu.astype(np.float64)
     r = ref.astype(np.float64)
     assert np.isfinite(g).all(), what
     err = np.abs(g - r).max() if g.size else 0.0
     den = np.linalg.norm(r)
     rel = np.linalg.norm(g - r) / den if den > 0 else np.linalg.norm(g - r)
-    assert err <= GEMM_MAX_ABS and rel <= GEMM_REL_L2, f"{what}: max|err|={err:.3g} rel_l2={rel:.3g}"
+    assert (max_abs is None or err <= max_abs) and rel <= GEMM_REL_L2, \
+        f"{what}: max|err|={err:.3g} rel_l2={rel:.3g}"
+
+
+def _check_expert(e, rows, x_disp, h, gu, grad_y, rw, W1e, W2e, I, gxd, dW1e, dW2e, G_o, G_gu):
+    f = O.bf16_bits_to_f64
+    rt = torch.as_tensor(rows)
+    X, Hs, GY = f(bits(x_disp[rt])), f(bits(h[rt])), f(bits(grad_y[rt]))
+    W1f, W2f = f(bits(W1e)), f(bits(W2e))
+    go_gpu, ggu_gpu = f(bits(G_o[rt])), f(bits(G_gu[rt]))
+    # stage: the bf16 operands
+    assert_gemm_close(bits(G_o[rt]), O.f64_to_bf16_bits(O.backward_scale(GY, rw[rows])),
+                      f"G_o e={e}", intermediate=True)
+    gg = f(bits(gu[rt]))
+    ref_gu = O.backward_swiglu(go_gpu, W2f, gg[:, :I], gg[:, I:])
+    assert_gemm_close(bits(G_gu[rt]), O.f64_to_bf16_bits(ref_gu), f"G_gu e={e}", intermediate=True)
+    # stage: the GEMMs on the GPU's own operands
+    dX, d1, d2 = O.backward_gemms(go_gpu, ggu_gpu, X, Hs, W1f)
+    assert_gemm_close(bits(gxd[rt]), O.f64_to_bf16_bits(dX), f"grad_x_disp e={e}")
+    _close(dW1e, d1, f"dW1 e={e}")
+    _close(dW2e, d2, f"dW2 e={e}")
+    # end to end against the independent oracle
+    dX, d1, d2 = O.expert_backward_f64(X, Hs, GY, rw[rows], W1f, W2f, I)
+    _close(f(bits(gxd[rt])), dX, f"grad_x_disp e2e e={e}", max_abs=None)
+    _close(dW1e, d1, f"dW1 e2e e={e}", max_abs=None)
+    _close(dW2e, d2, f"dW2 e2e e={e}", max_abs=None)
 
 
 def _run(moe, T, H, E, K, I, P, seed, drop=0.0):
@@ -49,11 +82,11 @@ def _run(moe, T, H, E, K, I, P, seed, drop=0.0):
     d = lambda t: t.to(DEV)
     fwd = moe.moe_layer_forward(d(x), d(idx), d(p), d(W1), d(W2), P, capacity=C, save_for_backward=True)
     grad_y, grad_w = moe.moe_combine_backward(d(grad_out), fwd.layout, o_save=fwd.o)
-    gxd, dW1, dW2 = moe.moe_grouped_experts_backward(grad_y, fwd.x_disp, fwd.h, fwd.gu, fwd.layout,
-                                                     d(W1), d(W2))
+    gxd, dW1, dW2, G_o, G_gu = moe.moe_grouped_experts_backward(
+        grad_y, fwd.x_disp, fwd.h, fwd.gu, fwd.layout, d(W1), d(W2), return_operands=True)
     torch.cuda.synchronize()
     assert int(fwd.layout.status.item()) == 0
-    return dict(fwd=fwd, grad_y=grad_y, gxd=gxd, dW1=dW1, dW2=dW2, W1=W1, W2=W2)
+    return dict(fwd=fwd, grad_y=grad_y, gxd=gxd, dW1=dW1, dW2=dW2, W1=W1, W2=W2, G_o=G_o, G_gu=G_gu)
 
 
 @pytest.mark.parametrize("T,H,E,K,I,P,drop", [
@@ -65,21 +98,20 @@ def _run(moe, T, H, E, K, I, P, seed, drop=0.0):
 ])
 def test_expert_backward_matches_oracle(moe, T, H, E, K, I, P, drop):
     r = _run(moe, T, H, E, K, I, P, seed=T + 3 * H, drop=drop)
-    L = r["fwd"].layout
-    re = L.row_expert.cpu().numpy()
+    fwd = r["fwd"]
+    L = fwd.layout
+    counts = L.tokens_per_expert.cpu().numpy()
+    offs = L.offsets.cpu().numpy()
     rw = L.row_weight.cpu().numpy()
-    valid = L.row_token.cpu().numpy() >= 0
-    gx_ref, dW1_ref, dW2_ref = O.grouped_experts_backward(
-        bits(r["grad_y"]), bits(r["fwd"].x_disp), bits(r["fwd"].h), re, rw,
-        bits(r["W1"]), bits(r["W2"]), I)
-    assert_gemm_close(bits(r["gxd"])[valid], gx_ref[valid], "grad_x_disp")
     dW1 = r["dW1"].cpu().numpy()
     dW2 = r["dW2"].cpu().numpy()
-    _assert_f32_close(dW1, dW1_ref, "dW1")
-    _assert_f32_close(dW2, dW2_ref, "dW2")
-    counts = L.tokens_per_expert.cpu().numpy()
-    for e in np.flatnonzero(counts == 0):
-        assert not dW1[e].any() and not dW2[e].any(), f"expert {e} has no rows"
+    for e in range(E):
+        if counts[e] == 0:
+            assert not dW1[e].any() and not dW2[e].any(), f"expert {e} has no rows"
+            continue
+        rows = np.arange(offs[e], offs[e] + counts[e])
+        _check_expert(e, rows, fwd.x_disp, fwd.h, fwd.gu, r["grad_y"], rw, r["W1"][e], r["W2"][e], I,
+                      r["gxd"], dW1[e], dW2[e], r["G_o"], r["G_gu"])
 
 
 def test_expert_backward_full_size_h4096_sampled(moe):
@@ -95,7 +127,8 @@ def test_expert_backward_full_size_h4096_sampled(moe):
     fwd = moe.moe_layer_forward(x, idx.to(DEV), p.to(DEV), W1, W2, P, host_sync=True,
                                 save_for_backward=True)
     grad_y, grad_w = moe.moe_combine_backward(grad_out, fwd.layout, o_save=fwd.o)
-    gxd, dW1, dW2 = moe.moe_grouped_experts_backward(grad_y, fwd.x_disp, fwd.h, fwd.gu, fwd.layout, W1, W2)
+    gxd, dW1, dW2, G_o, G_gu = moe.moe_grouped_experts_backward(
+        grad_y, fwd.x_disp, fwd.h, fwd.gu, fwd.layout, W1, W2, return_operands=True)
     torch.cuda.synchronize()
     L = fwd.layout
     counts = L.tokens_per_expert.cpu().numpy()
@@ -104,10 +137,5 @@ def test_expert_backward_full_size_h4096_sampled(moe):
     nz = np.flatnonzero(counts)
     for e in {int(nz[np.argmax(counts[nz])]), int(nz[np.argmin(counts[nz])])}:
         rows = np.arange(offs[e], offs[e] + counts[e])
-        f = O.bf16_bits_to_f64
-        dX, d1, d2 = O.expert_backward_f64(f(bits(fwd.x_disp[rows])), f(bits(fwd.h[rows])),
-                                           f(bits(grad_y[rows])), rw[rows],
-                                           f(bits(W1[e])), f(bits(W2[e])), I)
-        assert_gemm_close(bits(gxd[rows]), O.f64_to_bf16_bits(dX), f"grad_x_disp e={e}")
-        _assert_f32_close(dW1[e].cpu().numpy(), d1.astype(np.float32), f"dW1 e={e}")
-        _assert_f32_close(dW2[e].cpu().numpy(), d2.astype(np.float32), f"dW2 e={e}")
+        _check_expert(e, rows, fwd.x_disp, fwd.h, fwd.gu, grad_y, rw, W1[e], W2[e], I, gxd,
+                      dW1[e].cpu().numpy(), dW2[e].cpu().numpy(), G_o, G_gu)
