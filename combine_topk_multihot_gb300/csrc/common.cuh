@@ -65,9 +65,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Returns false if
-// the CTA-wide abort flag is raised or the wait runs past WAIT_LIMIT_NS (in
+// the CTA-wide abort flag is raised or the wait runs past `limit_ns` (in
 // which case it raises the flag itself).  Never spins unboundedly.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned long long limit_ns = WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   while (true) {
@@ -75,7 +76,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+    if (global_timer_ns() - t0 > limit_ns) {
       *abort_flag = 1;
       return false;
     }

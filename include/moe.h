@@ -297,6 +297,17 @@ MOE_API moe_status moe_grouped_experts_backward(const moe_bf16* grad_y, const mo
                                                 moe_bf16* grad_x_disp, float* dW1, float* dW2,
                                                 void* workspace, moe_stream_t stream);
 
+/*
+ * Failure-detection self-test.  Runs one CTA whose wait on an mbarrier can
+ * never complete, using the bounded-wait helper of the pipelined kernels with
+ * a limit of limit_ns (0 < limit_ns <= 1 s).  The wait gives up, the kernel
+ * ORs MOE_DEVERR_TIMEOUT into *status (device) and, if waited_ns (device,
+ * nullable) is given, stores how long it waited; then it returns normally.
+ * Asynchronous on `stream`.
+ */
+MOE_API moe_status moe_selftest_wait_timeout(int32_t* status, int64_t limit_ns, uint64_t* waited_ns,
+                                             moe_stream_t stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif
