@@ -40,8 +40,10 @@ cudaError_t launch_layout_counts(const uint8_t* routing_map, const moe_layout& L
 // Stable placement of every (token, expert) pair (a3).
 cudaError_t launch_layout_place(const uint8_t* routing_map, const float* probs,
                                 const moe_layout& L, const int* chunk_base, cudaStream_t s);
-// Row gather x -> x_disp plus pad / spare row metadata (a4); also the combine
-// backward's gather (a7) with the optional routing-weight gradient (a8).
+// Rows of the expanded layout from token rows (a4: x -> x_disp, plus the pad /
+// spare rows' metadata when from_offsets); also the combine backward (a7)
+// with the optional routing-weight gradient (a8).  Each token row is read
+// once and scattered to the token's rows; pad / spare rows are zeroed.
 cudaError_t launch_row_gather(const uint16_t* src, const moe_layout& L, int H, uint16_t* dst,
                               bool write_row_meta, const uint16_t* o_save, float* grad_w,
                               cudaStream_t s);

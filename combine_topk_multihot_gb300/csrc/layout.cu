@@ -61,77 +61,80 @@ __device__ __forceinline__ int warp_inclusive_scan(int v, int lane) {
   return v;
 }
 
-// One block of 1024 threads.  Turns the [E][chunks] counts into each chunk's
-// exclusive start inside its expert's group (in place), then scans the padded
-// group sizes over the experts: offsets[e], offsets[E] = R, and N = sum counts.
-__global__ void __launch_bounds__(1024) layout_scan_kernel(int* __restrict__ chunk_counts, int E,
-                                                           int chunks, int P, long long capacity,
-                                                           int* __restrict__ tokens_per_expert,
-                                                           int* __restrict__ offsets,
-                                                           int* __restrict__ totals,
-                                                           int* __restrict__ status) {
-  __shared__ int s_count[1024];
-  __shared__ int s_wsum[32], s_wcnt[32];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  // One warp per expert; lane l owns the contiguous chunks [l*per, (l+1)*per):
-  // a batched load pass for its sum, one warp scan of the sums, then a
-  // batched pass that writes the exclusive starts.
-  const int per = (chunks + 31) >> 5;
-  for (int e = warp; e < E; e += 32) {
-    int* row = chunk_counts + static_cast<long long>(e) * chunks;
-    const int c0 = min(chunks, lane * per), c1 = min(chunks, c0 + per);
-    int sum = 0;
-    for (int c = c0; c < c1; c += 8) {
-      int v[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = c + i < c1 ? row[c + i] : 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) sum += v[i];
-    }
-    const int incl = warp_inclusive_scan(sum, lane);
-    int run = incl - sum;
-    for (int c = c0; c < c1; c += 8) {
-      int v[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = c + i < c1 ? row[c + i] : 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (c + i < c1) row[c + i] = run;
-        run += v[i];
-      }
-    }
-    const int total = __shfl_sync(FULL_MASK, incl, 31);
-    if (lane == 0) s_count[e] = total;
-  }
-  __syncthreads();
-  const int e = threadIdx.x;
-  const int cnt = e < E ? s_count[e] : 0;
-  const int padded = e < E ? ((cnt + P - 1) / P) * P : 0;
-  int v = warp_inclusive_scan(padded, lane);
-  int n = warp_inclusive_scan(cnt, lane);
-  if (lane == 31) {
-    s_wsum[warp] = v;
-    s_wcnt[warp] = n;
-  }
+// Block-wide exclusive scan of one value per thread (blockDim.x a multiple of
+// 32, at most 1024); returns the exclusive prefix and writes the block total.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int incl = warp_inclusive_scan(v, lane);
+  if (lane == 31) s_warp[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    const int a = s_wsum[lane], b = s_wcnt[lane];
-    const int ia = warp_inclusive_scan(a, lane), ib = warp_inclusive_scan(b, lane);
-    s_wsum[lane] = ia - a;
-    s_wcnt[lane] = ib - b;
+    const int w = lane < nwarps ? s_warp[lane] : 0;
+    const int wi = warp_inclusive_scan(w, lane);
+    s_warp[lane] = wi - w;
+    if (lane == 31) s_warp[32] = wi;
   }
   __syncthreads();
-  v += s_wsum[warp];
-  n += s_wcnt[warp];
-  if (e < E) {
-    offsets[e] = v - padded;
-    tokens_per_expert[e] = cnt;
+  const int excl = incl - v + s_warp[warp];
+  *total = s_warp[32];
+  return excl;
+}
+
+// One CTA per expert: the expert's per-chunk counts become each chunk's
+// exclusive start inside the expert's group (in place), and the total is the
+// expert's token count.  Thread i owns a contiguous run of chunks.
+__global__ void __launch_bounds__(256) layout_expert_scan_kernel(int* __restrict__ chunk_counts,
+                                                                 int chunks,
+                                                                 int* __restrict__ tokens_per_expert) {
+  __shared__ int s_warp[33];
+  const int e = blockIdx.x;
+  int* row = chunk_counts + static_cast<long long>(e) * chunks;
+  const int per = (chunks + blockDim.x - 1) / blockDim.x;
+  const int c0 = min(chunks, static_cast<int>(threadIdx.x) * per), c1 = min(chunks, c0 + per);
+  int sum = 0;
+  for (int c = c0; c < c1; c += 8) {
+    int v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = c + i < c1 ? row[c + i] : 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sum += v[i];
   }
-  if (e == E - 1) {
-    offsets[E] = v;
-    totals[0] = v;
-    totals[1] = n;
-    if (v > capacity) report(status, MOE_DEVERR_CAPACITY);
+  int total;
+  int run = block_exclusive_scan(sum, s_warp, &total);
+  for (int c = c0; c < c1; c += 8) {
+    int v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = c + i < c1 ? row[c + i] : 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (c + i < c1) row[c + i] = run;
+      run += v[i];
+    }
+  }
+  if (threadIdx.x == 0) tokens_per_expert[e] = total;
+}
+
+// One CTA of 1024 threads: offsets[e] = exclusive prefix of the counts padded
+// to multiples of P; offsets[E] = R = totals[0]; totals[1] = N.
+__global__ void __launch_bounds__(1024) layout_offsets_kernel(const int* __restrict__ tokens_per_expert,
+                                                              int E, int P, long long capacity,
+                                                              int* __restrict__ offsets,
+                                                              int* __restrict__ totals,
+                                                              int* __restrict__ status) {
+  __shared__ int s_warp[33];
+  const int e = threadIdx.x;
+  const int cnt = e < E ? tokens_per_expert[e] : 0;
+  const int padded = e < E ? ((cnt + P - 1) / P) * P : 0;
+  int R, N;
+  const int excl = block_exclusive_scan(padded, s_warp, &R);
+  __syncthreads();
+  block_exclusive_scan(cnt, s_warp, &N);
+  if (e < E) offsets[e] = excl;
+  if (e == 0) {
+    offsets[E] = R;
+    totals[0] = R;
+    totals[1] = N;
+    if (R > capacity) report(status, MOE_DEVERR_CAPACITY);
   }
 }
 
@@ -208,86 +211,106 @@ __global__ void __launch_bounds__(256) layout_place_kernel(
   }
 }
 
-// Row gather, one warp per row, each lane moving H/256 16-byte vectors.
-//   FROM_OFFSETS: decide valid / pad / spare from offsets and counts (dispatch,
-//     where the pad rows' metadata is written here), else from row_token (the
-//     combine backward, after dispatch wrote every row's metadata).
-//   DOT: also grad_w[r] = <src[t], o_save[r]> in fp32 (routing-weight gradient).
-template <bool FROM_OFFSETS, bool DOT>
-__global__ void __launch_bounds__(256) row_gather_kernel(
-    const uint16_t* __restrict__ src, int H, int E, long long C, const int* __restrict__ offsets,
+// Dispatch (and the combine's backward) as a scatter, one warp per item.
+//   Items [0, T) are tokens: the warp reads the token's source row once from
+//   memory -- later passes over it hit L1 -- and writes it to each of the
+//   token's rows (token_row).  Reading each token once matters when [T, H]
+//   no longer fits in L2: a per-row gather would fetch it K times from DRAM.
+//   With DOT it also forms grad_w[r] = <src[t], o_save[r]> in fp32.
+//   Items [T, T + C) are rows: a pad or spare row is zeroed (and grad_w = 0).
+//   With META the row's validity comes from offsets / counts and the pad and
+//   spare rows get their metadata here (token -1, the sentinel expert, weight
+//   0); without it, from row_token (the combine's backward, after dispatch).
+template <bool META, bool DOT>
+__global__ void __launch_bounds__(256) row_scatter_kernel(
+    const uint16_t* __restrict__ src, int T, int K, int H, int E, long long C,
+    const int* __restrict__ token_row, const int* __restrict__ offsets,
     const int* __restrict__ counts, int* __restrict__ row_token, int* __restrict__ row_expert,
     float* __restrict__ row_weight, uint16_t* __restrict__ dst, const uint16_t* __restrict__ o_save,
     float* __restrict__ grad_w) {
-  extern __shared__ int s_meta[];  // offsets [E+1], counts [E]
+  extern __shared__ int s_meta[];  // META: offsets [E+1], counts [E]
   int* s_off = s_meta;
   int* s_cnt = s_meta + E + 1;
-  if (FROM_OFFSETS) {
+  if (META) {
     for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = offsets[i];
     for (int i = threadIdx.x; i < E; i += blockDim.x) s_cnt[i] = counts[i];
     __syncthreads();
   }
   const int lane = threadIdx.x & 31;
   const int V = H >> 8;  // 16-byte vectors per lane
+  const long long items = T + C;
   const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-  const int R = FROM_OFFSETS ? s_off[E] : 0;
-  for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-       r < C; r += nwarps) {
-    int t = -1;
-    if (FROM_OFFSETS) {
-      if (r < R) {
-        int lo = 0, hi = E;  // s_off[lo] <= r < s_off[hi]
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if (s_off[mid] <= r) lo = mid; else hi = mid;
-        }
-        if (r - s_off[lo] < s_cnt[lo]) t = row_token[r];
-      }
-      if (t < 0 && lane == 0) {
-        row_token[r] = -1;
-        row_expert[r] = E;
-        row_weight[r] = 0.f;
-      }
-    } else {
-      t = row_token[r];
-    }
-    uint4* d = reinterpret_cast<uint4*>(dst + r * H);
-    float dot = 0.f;
-    if (t >= 0) {
-      const uint4* s = reinterpret_cast<const uint4*>(src + static_cast<long long>(t) * H);
-      const uint4* o = DOT ? reinterpret_cast<const uint4*>(o_save + r * H) : nullptr;
-      for (int v0 = 0; v0 < V; v0 += 8) {
-        uint4 buf[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (v0 + i < V) buf[i] = __ldg(s + lane + 32 * (v0 + i));
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (v0 + i < V) d[lane + 32 * (v0 + i)] = buf[i];
-        if (DOT) {
+  const int R = META ? s_off[E] : 0;
+  for (long long it = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       it < items; it += nwarps) {
+    if (it < T) {
+      const long long t = it;
+      const uint4* s = reinterpret_cast<const uint4*>(src + t * H);
+      for (int j = 0; j < K; ++j) {
+        const int r = __ldg(token_row + t * K + j);
+        if (r < 0) break;
+        uint4* d = reinterpret_cast<uint4*>(dst + static_cast<long long>(r) * H);
+        const uint4* o = DOT ? reinterpret_cast<const uint4*>(o_save + static_cast<long long>(r) * H) : nullptr;
+        float dot = 0.f;
+        for (int v0 = 0; v0 < V; v0 += 8) {
+          uint4 buf[8], ob[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             if (v0 + i < V) {
-              const uint4 ov = __ldg(o + lane + 32 * (v0 + i));
-              const uint32_t g[4] = {buf[i].x, buf[i].y, buf[i].z, buf[i].w};
-              const uint32_t q[4] = {ov.x, ov.y, ov.z, ov.w};
+              buf[i] = __ldg(s + lane + 32 * (v0 + i));
+              if (DOT) ob[i] = __ldg(o + lane + 32 * (v0 + i));
+            }
+          }
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                dot = fmaf(bf16_lo(g[k]), bf16_lo(q[k]), dot);
-                dot = fmaf(bf16_hi(g[k]), bf16_hi(q[k]), dot);
+          for (int i = 0; i < 8; ++i) {
+            if (v0 + i < V) {
+              d[lane + 32 * (v0 + i)] = buf[i];
+              if (DOT) {
+                const uint32_t g[4] = {buf[i].x, buf[i].y, buf[i].z, buf[i].w};
+                const uint32_t q[4] = {ob[i].x, ob[i].y, ob[i].z, ob[i].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  dot = fmaf(bf16_lo(g[k]), bf16_lo(q[k]), dot);
+                  dot = fmaf(bf16_hi(g[k]), bf16_hi(q[k]), dot);
+                }
               }
             }
           }
         }
+        if (DOT) {
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(FULL_MASK, dot, off);
+          if (lane == 0) grad_w[r] = dot;
+        }
       }
     } else {
+      const long long r = it - T;
+      bool pad;
+      if (META) {
+        pad = true;
+        if (r < R) {
+          int lo = 0, hi = E;  // s_off[lo] <= r < s_off[hi]
+          while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_off[mid] <= r) lo = mid; else hi = mid;
+          }
+          pad = r - s_off[lo] >= s_cnt[lo];
+        }
+      } else {
+        pad = __ldg(row_token + r) < 0;
+      }
+      if (!pad) continue;
+      if (lane == 0) {
+        if (META) {
+          row_token[r] = -1;
+          row_expert[r] = E;
+          row_weight[r] = 0.f;
+        }
+        if (DOT) grad_w[r] = 0.f;
+      }
+      uint4* d = reinterpret_cast<uint4*>(dst + r * H);
       const uint4 z = make_uint4(0, 0, 0, 0);
       for (int v = 0; v < V; ++v) d[lane + 32 * v] = z;
-    }
-    if (DOT) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(FULL_MASK, dot, o);
-      if (lane == 0) grad_w[r] = t >= 0 ? dot : 0.f;
     }
   }
 }
@@ -301,8 +324,10 @@ cudaError_t launch_layout_counts(const uint8_t* routing_map, const moe_layout& L
     layout_count_kernel<<<chunks, 256, L.E * sizeof(int), s>>>(routing_map, L.T, L.E, chunks,
                                                                 chunk_counts);
   }
-  layout_scan_kernel<<<1, 1024, 0, s>>>(chunk_counts, L.E, chunks, L.pad_multiple, L.capacity,
-                                        L.tokens_per_expert, L.offsets, L.totals, L.status);
+  if (chunks > 0) layout_expert_scan_kernel<<<L.E, 256, 0, s>>>(chunk_counts, chunks, L.tokens_per_expert);
+  else cudaMemsetAsync(L.tokens_per_expert, 0, L.E * sizeof(int), s);
+  layout_offsets_kernel<<<1, 1024, 0, s>>>(L.tokens_per_expert, L.E, L.pad_multiple, L.capacity,
+                                           L.offsets, L.totals, L.status);
   return cudaGetLastError();
 }
 
@@ -323,21 +348,24 @@ cudaError_t launch_row_gather(const uint16_t* src, const moe_layout& L, int H, u
                               bool from_offsets, const uint16_t* o_save, float* grad_w,
                               cudaStream_t s) {
   const long long C = L.capacity;
-  if (C == 0) return cudaSuccess;
+  const long long items = static_cast<long long>(L.T) + C;
+  if (items == 0) return cudaSuccess;
   const int threads = 256;
-  const long long need = (C + 7) / 8;
+  const long long need = (items + 7) / 8;
   const int blocks = static_cast<int>(need < 8LL * sm_count() ? need : 8LL * sm_count());
-  const size_t smem = from_offsets ? (2 * L.E + 1) * sizeof(int) : 0;
   if (from_offsets) {
-    row_gather_kernel<true, false><<<blocks, threads, smem, s>>>(
-        src, H, L.E, C, L.offsets, L.tokens_per_expert, L.row_token, L.row_expert, L.row_weight,
-        dst, nullptr, nullptr);
+    const size_t smem = (2 * L.E + 1) * sizeof(int);
+    row_scatter_kernel<true, false><<<blocks, threads, smem, s>>>(
+        src, L.T, L.K, H, L.E, C, L.token_row, L.offsets, L.tokens_per_expert, L.row_token,
+        L.row_expert, L.row_weight, dst, nullptr, nullptr);
   } else if (grad_w) {
-    row_gather_kernel<false, true><<<blocks, threads, 0, s>>>(
-        src, H, L.E, C, nullptr, nullptr, L.row_token, nullptr, nullptr, dst, o_save, grad_w);
+    row_scatter_kernel<false, true><<<blocks, threads, 0, s>>>(
+        src, L.T, L.K, H, L.E, C, L.token_row, nullptr, nullptr, L.row_token, nullptr, nullptr,
+        dst, o_save, grad_w);
   } else {
-    row_gather_kernel<false, false><<<blocks, threads, 0, s>>>(
-        src, H, L.E, C, nullptr, nullptr, L.row_token, nullptr, nullptr, dst, nullptr, nullptr);
+    row_scatter_kernel<false, false><<<blocks, threads, 0, s>>>(
+        src, L.T, L.K, H, L.E, C, L.token_row, nullptr, nullptr, L.row_token, nullptr, nullptr,
+        dst, nullptr, nullptr);
   }
   return cudaGetLastError();
 }
