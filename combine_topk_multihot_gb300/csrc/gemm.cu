@@ -80,7 +80,10 @@ struct Smem {
   int tile_prefix[MAX_E + 1];
 };
 
-constexpr size_t SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + sizeof(Smem);
+// Epilogue staging for TMA stores: per epilogue warp, two 32 x 32 bf16 boxes.
+constexpr int STAGING_BYTES = 4 * 2 * 32 * 64;
+constexpr size_t SMEM_BYTES =
+    1024 /*alignment slack*/ + STAGES * STAGE_BYTES + STAGING_BYTES + sizeof(Smem);
 
 struct Tile {
   int e, mt, nt;
@@ -105,12 +108,14 @@ __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g));
 template <int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmOut, const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* tiles = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  Smem& s = *reinterpret_cast<Smem*>(tiles + STAGES * STAGE_BYTES);
+  Smem& s = *reinterpret_cast<Smem*>(tiles + STAGES * STAGE_BYTES + STAGING_BYTES);
   const uint32_t tiles_u32 = smem_u32(tiles);
+  const uint32_t staging_u32 = tiles_u32 + STAGES * STAGE_BYTES;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = args.E;
@@ -130,6 +135,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_fence_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmOut);
   }
   if (warp == 1) tmem_alloc(smem_u32(&s.tmem_base), TMEM_COLS);
   for (int e = threadIdx.x; e <= E; e += NUM_THREADS) s.offsets[e] = args.offsets[e];
@@ -235,6 +241,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int q = warp & 3;
     const int r_in_tile = q * 32 + lane;
     int local = 0;
+    // Staged TMA store of one 32-row x 32-column bf16 box: each lane writes its
+    // row (64 bytes) into one of the warp's two staging buffers, then lane 0
+    // stores the box.  Used only when all 32 rows of the warp are valid.
+    const uint32_t my_staging = staging_u32 + (warp - 2) * 2 * 2048;
+    uint32_t n_staged = 0;
+    int warp_row0 = 0;
+    auto store_staged = [&](const uint32_t (&v)[16], int col) {
+      const uint32_t buf = my_staging + (n_staged & 1) * 2048;
+      if (lane == 0) tma_store_wait_read<1>();
+      __syncwarp();
+      const uint32_t dst = buf + lane * 64;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 16 * i), "r"(v[4 * i]),
+                     "r"(v[4 * i + 1]), "r"(v[4 * i + 2]), "r"(v[4 * i + 3])
+                     : "memory");
+      fence_async_shared();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&tmOut, buf, col, warp_row0);
+        tma_store_commit();
+      }
+      ++n_staged;
+    };
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
       const Tile t = decode_tile(s, E, args.n_tiles, tile);
       const int buf = local & 1;
@@ -243,7 +273,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       const int group_row = t.mt * BM + r_in_tile;
       const bool valid = group_row < s.counts[t.e];
+      const bool full_warp = __all_sync(FULL_MASK, valid);
       const long long row = static_cast<long long>(s.offsets[t.e]) + group_row;
+      warp_row0 = s.offsets[t.e] + t.mt * BM + q * 32;
       const uint32_t tb = tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
       if (EPI == EPI_SWIGLU) {
         // columns [0,128) gate, [128,256) up, for h columns nt*128 + [0,128)
@@ -263,10 +295,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
               hv[i] = pack_bf16x2(silu(g0) * u0, silu(g1) * u1);
             }
-            uint4* dst = reinterpret_cast<uint4*>(args.out0 + row * args.ld0 + col0 + c);
+            if (!full_warp) {
+              uint4* dst = reinterpret_cast<uint4*>(args.out0 + row * args.ld0 + col0 + c);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
+              for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
+            } else {
+              store_staged(hv, col0 + c);
+            }
             if (args.out1) {
               uint4* dg = reinterpret_cast<uint4*>(args.out1 + row * args.ld1 + col0 + c);
               uint4* du = reinterpret_cast<uint4*>(args.out1 + row * args.ld1 + args.I + col0 + c);
@@ -294,14 +330,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld32(tb + c, o);
           tmem_ld_wait();
           if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(args.out0 + row * args.ld0 + col0 + c);
+            uint32_t yv[16];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              float f[8];
+            for (int i = 0; i < 16; ++i)
+              yv[i] = pack_bf16x2(w * __uint_as_float(o[2 * i]), w * __uint_as_float(o[2 * i + 1]));
+            if (!full_warp) {
+              uint4* dst = reinterpret_cast<uint4*>(args.out0 + row * args.ld0 + col0 + c);
 #pragma unroll
-              for (int k = 0; k < 8; ++k) f[k] = __uint_as_float(o[8 * i + k]);
-              dst[i] = make_uint4(pack_bf16x2(w * f[0], w * f[1]), pack_bf16x2(w * f[2], w * f[3]),
-                                  pack_bf16x2(w * f[4], w * f[5]), pack_bf16x2(w * f[6], w * f[7]));
+              for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(yv[4 * i], yv[4 * i + 1], yv[4 * i + 2], yv[4 * i + 3]);
+            } else {
+              store_staged(yv, col0 + c);
             }
             if (args.out1) {
               uint4* dso = reinterpret_cast<uint4*>(args.out1 + row * args.ld1 + col0 + c);
@@ -321,6 +360,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&s.tempty[buf]));
     }
+    if (lane == 0) tma_store_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -339,8 +380,8 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols) 
 }
 
 template <int EPI>
-cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args,
-                        cudaStream_t s) {
+cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
+                        const GemmArgs& args, cudaStream_t s) {
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -351,7 +392,7 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmAr
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  grouped_gemm_kernel<EPI><<<sm_count(), NUM_THREADS, SMEM_BYTES, s>>>(a, b, args);
+  grouped_gemm_kernel<EPI><<<sm_count(), NUM_THREADS, SMEM_BYTES, s>>>(a, b, out, args);
   return cudaGetLastError();
 }
 
@@ -363,9 +404,10 @@ cudaError_t launch_experts_forward(const uint16_t* x_disp, const moe_layout& L, 
                                    cudaStream_t s) {
   if (L.capacity == 0) return cudaSuccess;
   const uint64_t C = static_cast<uint64_t>(L.capacity);
-  CUtensorMap mA1, mB1, mA2, mB2;
+  CUtensorMap mA1, mB1, mA2, mB2, mH, mY;
   if (!make_map(&mA1, x_disp, C, H) || !make_map(&mB1, W1, static_cast<uint64_t>(L.E) * 2 * I, H) ||
-      !make_map(&mA2, h, C, I) || !make_map(&mB2, W2, static_cast<uint64_t>(L.E) * H, I))
+      !make_map(&mA2, h, C, I) || !make_map(&mB2, W2, static_cast<uint64_t>(L.E) * H, I) ||
+      !make_tma_store_2d_bf16(&mH, h, C, I) || !make_tma_store_2d_bf16(&mY, y, C, H))
     return cudaErrorInvalidValue;
 
   GemmArgs g1{};
@@ -384,7 +426,7 @@ cudaError_t launch_experts_forward(const uint16_t* x_disp, const moe_layout& L, 
   g1.ld1 = 2 * I;
   g1.I = I;
   g1.status = L.status;
-  cudaError_t err = launch_gemm<EPI_SWIGLU>(mA1, mB1, g1, s);
+  cudaError_t err = launch_gemm<EPI_SWIGLU>(mA1, mB1, mH, g1, s);
   if (err != cudaSuccess) return err;
 
   GemmArgs g2 = g1;
@@ -397,7 +439,7 @@ cudaError_t launch_experts_forward(const uint16_t* x_disp, const moe_layout& L, 
   g2.ld0 = H;
   g2.out1 = o_save;
   g2.ld1 = H;
-  return launch_gemm<EPI_WEIGHTED>(mA2, mB2, g2, s);
+  return launch_gemm<EPI_WEIGHTED>(mA2, mB2, mY, g2, s);
 }
 
 }  // namespace moe

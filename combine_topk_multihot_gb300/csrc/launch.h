@@ -19,6 +19,10 @@ int sm_count();  // SMs of the current device (cached)
 bool make_tma_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                       uint32_t box_rows);
 
+// Tensor map for TMA stores of 32-row x 32-column bf16 boxes (64-byte rows,
+// no swizzle) into a row-major [rows, cols] matrix.
+bool make_tma_store_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols);
+
 // Records `text` as this thread's moe_last_error() and returns `st`.
 moe_status set_last_error(moe_status st, const char* text);
 
