@@ -134,6 +134,38 @@ __device__ __forceinline__ void fence_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// TMA stores of 32-row boxes of 64-byte rows that a warp holds one row per
+// lane (lane i holds row i as 16 words).  Each box goes through one half of
+// the warp's 4 KiB staging area (the halves alternate, recycled with
+// wait_group.read), then lane 0 stores it with the given tensor map.
+struct StagedStore {
+  uint32_t base;
+  uint32_t n;
+  int lane;
+  __device__ __forceinline__ void box(const CUtensorMap* map, const uint32_t* v, int x, int y) {
+    const uint32_t buf = base + (n & 1) * 2048;
+    if (lane == 0) tma_store_wait_read<1>();
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(buf + lane * 64 + 16 * i),
+                   "r"(v[4 * i]), "r"(v[4 * i + 1]), "r"(v[4 * i + 2]), "r"(v[4 * i + 3])
+                   : "memory");
+    fence_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(map, buf, x, y);
+      tma_store_commit();
+    }
+    ++n;
+  }
+  // Waits for every store this warp issued (call before the CTA exits).
+  __device__ __forceinline__ void finish() {
+    if (lane == 0) tma_store_wait_all();
+    __syncwarp();
+  }
+};
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),

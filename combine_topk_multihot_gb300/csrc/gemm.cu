@@ -14,11 +14,17 @@
 //
 // Design (one CTA per SM, persistent):
 //   * the tile list is built on the device from tokens_per_expert / offsets,
-//     so no host sync is needed and the launch can be graph-captured; pad and
-//     spare rows are never computed;
-//   * warp 0 issues TMA loads into a 4-stage shared-memory ring (128-byte
-//     swizzle), warp 1 owns the tensor memory and issues tcgen05.mma
-//     (128 x 256 x 16 per instruction), warps 2-5 are the epilogue;
+//     so no host sync is needed and the launch can be graph-captured; an
+//     expert's rows are covered by ceil(count / 128) tiles; only the valid
+//     rows are written, plus -- when the gate/up values are saved for the
+//     backward -- the pad rows of the expert's group, which come out as zeros
+//     (x_disp's pad rows are zero) and let the backward skip masking them;
+//     spare rows are never written;
+//   * warp 0 issues TMA loads into a 4-stage (3 for large E) shared-memory
+//     ring (128-byte swizzle), warp 1 owns the tensor memory and issues
+//     tcgen05.mma (128 x 256 x 16 per instruction), warps 2-9 are the
+//     epilogue: two warps per 32-lane quarter of tensor memory, each taking
+//     half of the tile's columns, so the epilogue keeps up with the MMAs;
 //   * two 256-column fp32 accumulators in tensor memory let the epilogue of
 //     one tile overlap the MMAs of the next;
 //   * every wait is bounded; a timeout sets MOE_DEVERR_TIMEOUT and the CTA
@@ -37,13 +43,14 @@ constexpr int BM = 128;          // rows per tile (tensor-memory lanes)
 constexpr int BN = 256;          // accumulator columns per tile
 constexpr int BK = 64;           // bf16 elements per 128-byte swizzled row
 constexpr int UMMA_K = 16;       // K per tcgen05.mma for 16-bit inputs
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;           // 16 KiB
 constexpr int B_BYTES = BN * BK * 2;           // 32 KiB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES; // 48 KiB
-constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARPS = 8;                   // two per TMEM lane quarter
+constexpr int NUM_THREADS = 32 * (2 + EPI_WARPS);
 constexpr int TMEM_COLS = 2 * BN;              // double-buffered accumulator
-constexpr int MAX_E = 1024;
+constexpr int MAX_STAGES = 4;
+constexpr int SMEM_LIMIT = 232448;             // dynamic shared memory per CTA
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 
 enum Epilogue { EPI_SWIGLU = 0, EPI_WEIGHTED = 1 };
@@ -63,39 +70,42 @@ struct GemmArgs {
   uint16_t* out1;          // GEMM1: gu_save [C, 2I] (nullable)   GEMM2: o_save [C, H] (nullable)
   int ld1;
   int I;                   // GEMM1: offset of the up half in gu_save
+  int write_pad;           // also write the pad rows of each expert's group (zeros)
   int* status;
 };
 
+// Barriers and scalars; the per-expert tables (offsets [E+1], counts [E],
+// tile_prefix [E+1]) follow it in shared memory, sized by E.
 struct Smem {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
   int total_tiles;
-  int offsets[MAX_E + 1];
-  int counts[MAX_E];
-  int tile_prefix[MAX_E + 1];
 };
 
 // Epilogue staging for TMA stores: per epilogue warp, two 32 x 32 bf16 boxes.
-constexpr int STAGING_BYTES = 4 * 2 * 32 * 64;
-constexpr size_t SMEM_BYTES =
-    1024 /*alignment slack*/ + STAGES * STAGE_BYTES + STAGING_BYTES + sizeof(Smem);
+constexpr int STAGING_BYTES = EPI_WARPS * 2 * 32 * 64;
+
+constexpr size_t smem_bytes(int stages, int E) {
+  return 1024 /*alignment slack*/ + static_cast<size_t>(stages) * STAGE_BYTES + STAGING_BYTES +
+         sizeof(Smem) + static_cast<size_t>(3 * E + 2) * sizeof(int);
+}
 
 struct Tile {
   int e, mt, nt;
 };
 
-__device__ __forceinline__ Tile decode_tile(const Smem& s, int E, int n_tiles, int tile) {
+__device__ __forceinline__ Tile decode_tile(const int* tile_prefix, int E, int n_tiles, int tile) {
   int lo = 0, hi = E;  // tile_prefix[lo] <= tile < tile_prefix[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (s.tile_prefix[mid] <= tile) lo = mid; else hi = mid;
+    if (tile_prefix[mid] <= tile) lo = mid; else hi = mid;
   }
-  const int local = tile - s.tile_prefix[lo];
+  const int local = tile - tile_prefix[lo];
   Tile t;
   t.e = lo;
   t.mt = local / n_tiles;
@@ -105,7 +115,7 @@ __device__ __forceinline__ Tile decode_tile(const Smem& s, int E, int n_tiles, i
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
 
-template <int EPI>
+template <int EPI, int STAGES>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
@@ -114,6 +124,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* tiles = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   Smem& s = *reinterpret_cast<Smem*>(tiles + STAGES * STAGE_BYTES + STAGING_BYTES);
+  int* s_off = reinterpret_cast<int*>(&s + 1);  // [E+1]
+  int* s_cnt = s_off + args.E + 1;              // [E]
+  int* s_pre = s_cnt + args.E;                  // [E+1] tile prefix
   const uint32_t tiles_u32 = smem_u32(tiles);
   const uint32_t staging_u32 = tiles_u32 + STAGES * STAGE_BYTES;
 
@@ -128,7 +141,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.tfull[i]), 1);
-      mbar_init(smem_u32(&s.tempty[i]), 4);
+      mbar_init(smem_u32(&s.tempty[i]), EPI_WARPS);
     }
     mbar_init(smem_u32(&s.drain), 1);
     s.abort = 0;
@@ -138,25 +151,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tmOut);
   }
   if (warp == 1) tmem_alloc(smem_u32(&s.tmem_base), TMEM_COLS);
-  for (int e = threadIdx.x; e <= E; e += NUM_THREADS) s.offsets[e] = args.offsets[e];
-  for (int e = threadIdx.x; e < E; e += NUM_THREADS) s.counts[e] = args.counts[e];
+  for (int e = threadIdx.x; e <= E; e += NUM_THREADS) s_off[e] = args.offsets[e];
+  for (int e = threadIdx.x; e < E; e += NUM_THREADS) s_cnt[e] = args.counts[e];
   __syncthreads();
   if (warp == 0) {  // exclusive scan of per-expert tile counts
     int running = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
       const int e = e0 + lane;
-      const int n = e < E ? ((s.counts[e] + BM - 1) / BM) * args.n_tiles : 0;
+      const int n = e < E ? ((s_cnt[e] + BM - 1) / BM) * args.n_tiles : 0;
       int incl = n;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int v = __shfl_up_sync(FULL_MASK, incl, o);
         if (lane >= o) incl += v;
       }
-      if (e < E) s.tile_prefix[e] = running + incl - n;
+      if (e < E) s_pre[e] = running + incl - n;
       running += __shfl_sync(FULL_MASK, incl, 31);
     }
     if (lane == 0) {
-      s.tile_prefix[E] = running;
+      s_pre[E] = running;
       s.total_tiles = running;
     }
   }
@@ -176,8 +189,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       long long issued = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const Tile t = decode_tile(s, E, args.n_tiles, tile);
-        const int a_row = s.offsets[t.e] + t.mt * BM;
+        const Tile t = decode_tile(s_pre, E, args.n_tiles, tile);
+        const int a_row = s_off[t.e] + t.mt * BM;
         const int b_row = t.e * args.b_rows_per_expert + t.nt * args.b_tile_step;
         for (int kb = 0; kb < args.k_blocks; ++kb) {
           if (!mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, abort_flag)) { ok = false; break; }
@@ -238,13 +251,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else {
     // ================= epilogue (warps 2..5 -> TMEM lanes 32*(warp%4)) =================
+    // warps 2..9: lane quarter q = warp % 4 of TMEM, column half (warp - 2) / 4
     const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r_in_tile = q * 32 + lane;
     int local = 0;
     // Staged TMA store of one 32-row x 32-column bf16 box: each lane writes its
     // row (64 bytes) into one of the warp's two staging buffers, then lane 0
     // stores the box.  Used only when all 32 rows of the warp are valid.
-    const uint32_t my_staging = staging_u32 + (warp - 2) * 2 * 2048;
+    const uint32_t my_staging = staging_u32 + (warp - 2) * 2 * 2048;  // two 2 KiB boxes
     uint32_t n_staged = 0;
     int warp_row0 = 0;
     auto store_staged = [&](const uint32_t (&v)[16], int col) {
@@ -266,22 +281,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ++n_staged;
     };
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
-      const Tile t = decode_tile(s, E, args.n_tiles, tile);
+      const Tile t = decode_tile(s_pre, E, args.n_tiles, tile);
       const int buf = local & 1;
       const uint32_t use = (local >> 1) & 1;
       if (!mbar_wait(smem_u32(&s.tfull[buf]), use, abort_flag)) break;
       tc_fence_after();
       const int group_row = t.mt * BM + r_in_tile;
-      const bool valid = group_row < s.counts[t.e];
+      // rows written: the valid rows, plus (write_pad) the pad rows of the
+      // expert's group, which come out zero from the zero pad rows of x_disp
+      const bool valid = group_row < (args.write_pad ? s_off[t.e + 1] - s_off[t.e] : s_cnt[t.e]);
       const bool full_warp = __all_sync(FULL_MASK, valid);
-      const long long row = static_cast<long long>(s.offsets[t.e]) + group_row;
-      warp_row0 = s.offsets[t.e] + t.mt * BM + q * 32;
+      const long long row = static_cast<long long>(s_off[t.e]) + group_row;
+      warp_row0 = s_off[t.e] + t.mt * BM + q * 32;
       const uint32_t tb = tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
       if (EPI == EPI_SWIGLU) {
         // columns [0,128) gate, [128,256) up, for h columns nt*128 + [0,128)
         const int col0 = t.nt * (BN / 2);
 #pragma unroll 1
-        for (int c = 0; c < BN / 2; c += 32) {
+        for (int c = half * (BN / 4); c < (half + 1) * (BN / 4); c += 32) {
           uint32_t g[32], u[32];
           __syncwarp();
           tmem_ld32(tb + c, g);
@@ -324,7 +341,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int col0 = t.nt * BN;
         const float w = valid ? args.row_weight[row] : 0.f;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
           uint32_t o[32];
           __syncwarp();
           tmem_ld32(tb + c, o);
@@ -379,21 +396,32 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols) 
   return make_tma_2d_bf16(map, base, rows, cols, 128);
 }
 
-template <int EPI>
-cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
-                        const GemmArgs& args, cudaStream_t s) {
+template <int EPI, int STAGES>
+cudaError_t launch_gemm_stages(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
+                               const GemmArgs& args, cudaStream_t s) {
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    err = cudaFuncSetAttribute(grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(SMEM_BYTES));
+    err = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, STAGES>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  grouped_gemm_kernel<EPI><<<sm_count(), NUM_THREADS, SMEM_BYTES, s>>>(a, b, out, args);
+  grouped_gemm_kernel<EPI, STAGES><<<sm_count(), NUM_THREADS, smem_bytes(STAGES, args.E), s>>>(
+      a, b, out, args);
   return cudaGetLastError();
+}
+
+// Four pipeline stages when they fit beside the staging and the per-expert
+// tables (E up to about 200), else three.
+template <int EPI>
+cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
+                        const GemmArgs& args, cudaStream_t s) {
+  if (smem_bytes(4, args.E) <= static_cast<size_t>(SMEM_LIMIT))
+    return launch_gemm_stages<EPI, 4>(a, b, out, args, s);
+  return launch_gemm_stages<EPI, 3>(a, b, out, args, s);
 }
 
 }  // namespace
@@ -425,6 +453,7 @@ cudaError_t launch_experts_forward(const uint16_t* x_disp, const moe_layout& L, 
   g1.out1 = gu_save;
   g1.ld1 = 2 * I;
   g1.I = I;
+  g1.write_pad = gu_save != nullptr;  // training: the backward reads the pad rows
   g1.status = L.status;
   cudaError_t err = launch_gemm<EPI_SWIGLU>(mA1, mB1, mH, g1, s);
   if (err != cudaSuccess) return err;

@@ -21,10 +21,11 @@
 //     (leading byte offset), 8-deep K groups 1 KiB apart (stride byte offset),
 //     and the instruction descriptor's transpose bit set for that operand.
 //   * K over an expert's rows (wgrad).  Each tile's contraction runs over the
-//     rows of one expert, so the last 64-row block may reach into the next
-//     expert's rows; the MMA warp zeroes those K lines of both operands in
-//     shared memory before issuing the MMAs.  An expert with no rows gets
-//     zero weight gradients.
+//     rows of one expert, so the last 64-row block may reach past them.  When
+//     the groups are padded to a multiple of 64 rows those are the expert's
+//     own pad rows, zero in every operand; otherwise the MMA warp zeroes those
+//     K lines of both operands in shared memory before issuing the MMAs.  An
+//     expert with no rows gets zero weight gradients.
 
 #include "common.cuh"
 #include "launch.h"
@@ -36,8 +37,9 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int UMMA_K = 16;
-constexpr int NUM_THREADS = 192;
-constexpr int MAX_E = 1024;
+constexpr int EPI_WARPS = 8;              // two per TMEM lane quarter
+constexpr int NUM_THREADS = 32 * (2 + EPI_WARPS);
+constexpr int SMEM_LIMIT = 232448;
 constexpr int A_BYTES = BM * BK * 2;      // 16 KiB
 constexpr int MN_BOX_BYTES = 64 * BK * 2; // 8 KiB: 64 MN x 64 K, MN-major
 constexpr int TMEM_COLS = 512;
@@ -48,7 +50,7 @@ template <int BN>
 struct Cfg {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int MAX_STAGES = BN == 256 ? 4 : 6;
 };
 
 struct BwdArgs {
@@ -65,9 +67,12 @@ struct BwdArgs {
   const uint16_t* gu;        // EPI_DSWIGLU: gate / up pre-activations [C, 2I]
   int I;
   float* out_f32;            // K-grouped: [E, m_total, n_total]
+  int zero_tail;             // K-grouped: zero the K lines past an expert's count
   int* status;
 };
 
+// Barriers and scalars; the per-expert tables (offsets [E+1], counts [E],
+// tile_prefix [E+1]) follow it in shared memory, sized by E.
 struct Smem {
   uint64_t full[6];
   uint64_t empty[6];
@@ -77,14 +82,16 @@ struct Smem {
   uint32_t tmem_base;
   int abort;
   int total_tiles;
-  int offsets[MAX_E + 1];
-  int counts[MAX_E];
-  int tile_prefix[MAX_E + 1];
 };
 
+// Epilogue staging for TMA stores: 4 KiB per epilogue warp (two boxes of
+// 32 rows x 64 bytes: 32 bf16 or 16 fp32 columns).
+constexpr int STAGING_BYTES = EPI_WARPS * 4096;
+
 template <int BN>
-constexpr size_t smem_bytes() {
-  return 1024 + Cfg<BN>::STAGES * Cfg<BN>::STAGE_BYTES + sizeof(Smem);
+constexpr size_t smem_bytes(int stages, int E) {
+  return 1024 + static_cast<size_t>(stages) * Cfg<BN>::STAGE_BYTES + STAGING_BYTES + sizeof(Smem) +
+         static_cast<size_t>(3 * E + 2) * sizeof(int);
 }
 
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -101,13 +108,13 @@ struct Tile {
   int e, mt, nt;
 };
 
-__device__ __forceinline__ Tile decode(const Smem& s, int E, int n_tiles, int tile) {
+__device__ __forceinline__ Tile decode(const int* tile_prefix, int E, int n_tiles, int tile) {
   int lo = 0, hi = E;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (s.tile_prefix[mid] <= tile) lo = mid; else hi = mid;
+    if (tile_prefix[mid] <= tile) lo = mid; else hi = mid;
   }
-  const int local = tile - s.tile_prefix[lo];
+  const int local = tile - tile_prefix[lo];
   Tile t;
   t.e = lo;
   t.mt = local / n_tiles;
@@ -126,11 +133,10 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
 //   A is K-major (rows of the expert), B is MN-major (the expert's weight).
 // GROUP_K = true: tiles are (expert, M block, N block); both operands are
 //   MN-major slices of the expert's rows, the contraction runs over the rows.
-template <bool GROUP_K, int BN, int EPI>
+template <bool GROUP_K, int BN, int EPI, int STAGES>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const BwdArgs args) {
-  constexpr int STAGES = Cfg<BN>::STAGES;
+                    const __grid_constant__ CUtensorMap tmOut, const BwdArgs args) {
   constexpr int STAGE_BYTES = Cfg<BN>::STAGE_BYTES;
   constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN) | (GROUP_K ? (1u << 15) : 0u) | (1u << 16);
   // K-major A: 8-row groups 1 KiB apart, next 16-wide K slice 32 bytes on.
@@ -144,8 +150,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* tiles = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  Smem& s = *reinterpret_cast<Smem*>(tiles + STAGES * STAGE_BYTES);
+  Smem& s = *reinterpret_cast<Smem*>(tiles + STAGES * STAGE_BYTES + STAGING_BYTES);
+  int* s_off = reinterpret_cast<int*>(&s + 1);  // [E+1]
+  int* s_cnt = s_off + args.E + 1;              // [E]
+  int* s_pre = s_cnt + args.E;                  // [E+1]
   const uint32_t tiles_u32 = smem_u32(tiles);
+  const uint32_t staging_u32 = tiles_u32 + STAGES * STAGE_BYTES;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = args.E;
 
@@ -156,35 +166,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.tfull[i]), 1);
-      mbar_init(smem_u32(&s.tempty[i]), 4);
+      mbar_init(smem_u32(&s.tempty[i]), EPI_WARPS);
     }
     mbar_init(smem_u32(&s.drain), 1);
     s.abort = 0;
     mbar_fence_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmOut);
   }
   if (warp == 1) tmem_alloc(smem_u32(&s.tmem_base), TMEM_COLS);
-  for (int e = threadIdx.x; e <= E; e += NUM_THREADS) s.offsets[e] = args.offsets[e];
-  for (int e = threadIdx.x; e < E; e += NUM_THREADS) s.counts[e] = args.counts[e];
+  for (int e = threadIdx.x; e <= E; e += NUM_THREADS) s_off[e] = args.offsets[e];
+  for (int e = threadIdx.x; e < E; e += NUM_THREADS) s_cnt[e] = args.counts[e];
   __syncthreads();
   if (warp == 0) {
     int running = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
       const int e = e0 + lane;
       int n = 0;
-      if (e < E) n = GROUP_K ? args.m_tiles * args.n_tiles : ((s.counts[e] + BM - 1) / BM) * args.n_tiles;
+      if (e < E) n = GROUP_K ? args.m_tiles * args.n_tiles : ((s_cnt[e] + BM - 1) / BM) * args.n_tiles;
       int incl = n;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int v = __shfl_up_sync(FULL_MASK, incl, o);
         if (lane >= o) incl += v;
       }
-      if (e < E) s.tile_prefix[e] = running + incl - n;
+      if (e < E) s_pre[e] = running + incl - n;
       running += __shfl_sync(FULL_MASK, incl, 31);
     }
     if (lane == 0) {
-      s.tile_prefix[E] = running;
+      s_pre[E] = running;
       s.total_tiles = running;
     }
   }
@@ -204,8 +215,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       long long issued = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const Tile t = decode(s, E, args.n_tiles, tile);
-        const int kbs = GROUP_K ? (s.counts[t.e] + BK - 1) / BK : args.k_blocks;
+        const Tile t = decode(s_pre, E, args.n_tiles, tile);
+        const int kbs = GROUP_K ? (s_cnt[t.e] + BK - 1) / BK : args.k_blocks;
         for (int kb = 0; kb < kbs; ++kb) {
           if (!mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, abort_flag)) { ok = false; break; }
           const uint32_t full = smem_u32(&s.full[stage]);
@@ -213,14 +224,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t b_dst = a_dst + A_BYTES;
           mbar_arrive_expect_tx(full, STAGE_BYTES);
           if (GROUP_K) {
-            const int k_row = s.offsets[t.e] + kb * BK;
+            const int k_row = s_off[t.e] + kb * BK;
             tma_load_2d(a_dst, &tmA, t.mt * BM, k_row, full);
             tma_load_2d(a_dst + MN_BOX_BYTES, &tmA, t.mt * BM + 64, k_row, full);
 #pragma unroll
             for (int j = 0; j < BN / 64; ++j)
               tma_load_2d(b_dst + j * MN_BOX_BYTES, &tmB, t.nt * BN + 64 * j, k_row, full);
           } else {
-            tma_load_2d(a_dst, &tmA, kb * BK, s.offsets[t.e] + t.mt * BM, full);
+            tma_load_2d(a_dst, &tmA, kb * BK, s_off[t.e] + t.mt * BM, full);
             const int k_row = t.e * args.b_rows_per_expert + kb * BK;
 #pragma unroll
             for (int j = 0; j < BN / 64; ++j)
@@ -245,8 +256,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int local = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++local) {
-      const Tile t = decode(s, E, args.n_tiles, tile);
-      const int count = s.counts[t.e];
+      const Tile t = decode(s_pre, E, args.n_tiles, tile);
+      const int count = s_cnt[t.e];
       const int kbs = GROUP_K ? (count + BK - 1) / BK : args.k_blocks;
       const int buf = local & 1;
       const uint32_t use = (local >> 1) & 1;
@@ -258,7 +269,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t a_addr = tiles_u32 + stage * STAGE_BYTES;
         if (GROUP_K) {
           const int valid = count - kb * BK;
-          if (valid < BK) {
+          if (valid < BK && args.zero_tail) {
             // zero K lines [valid, 64) of the two A boxes and the BN/64 B boxes
             const int lines = BK - valid;
             const int per_box = lines * 8;  // 16-byte chunks
@@ -299,24 +310,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     __syncwarp();
   } else {
-    // ================= epilogue =================
+    // ================= epilogue (warps 2..9) =================
+    // Warp w reads TMEM lane quarter w % 4 and takes column half (w - 2) / 4
+    // of each tile.  A warp whose 32 rows are all written stores 32-row boxes
+    // through TMA; a warp with rows past the group stores its rows directly.
     const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r_in_tile = q * 32 + lane;
+    StagedStore st{staging_u32 + (warp - 2) * 4096, 0u, lane};
     int local = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
-      const Tile t = decode(s, E, args.n_tiles, tile);
+      const Tile t = decode(s_pre, E, args.n_tiles, tile);
       const int buf = local & 1;
       const uint32_t use = (local >> 1) & 1;
       if (!mbar_wait(smem_u32(&s.tfull[buf]), use, abort_flag)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
       if (GROUP_K) {
-        const int m_row = t.mt * BM + r_in_tile;
-        float* dst = args.out_f32 +
-                     (static_cast<long long>(t.e) * args.m_total + m_row) * args.n_total + t.nt * BN;
-        const bool empty = s.counts[t.e] == 0;
+        // dW rows of expert e: rows (e * m_total + m) of the [E * m_total, n_total] output
+        const int out_row0 = t.e * args.m_total + t.mt * BM + q * 32;
+        const bool empty = s_cnt[t.e] == 0;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
           uint32_t v[32];
           __syncwarp();
           if (!empty) {
@@ -326,34 +341,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0u;
           }
-          float4* d4 = reinterpret_cast<float4*>(dst + c);
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+          st.box(&tmOut, v, t.nt * BN + c, out_row0);
+          st.box(&tmOut, v + 16, t.nt * BN + c + 16, out_row0);
         }
       } else {
+        // rows written: the expert's group (valid and pad rows) inside the tile
         const int group_row = t.mt * BM + r_in_tile;
-        const bool valid = group_row < s.counts[t.e];
-        const long long row = static_cast<long long>(s.offsets[t.e]) + group_row;
+        const bool valid = group_row < s_off[t.e + 1] - s_off[t.e];
+        const bool full_warp = __all_sync(FULL_MASK, valid);
+        const long long row = static_cast<long long>(s_off[t.e]) + group_row;
+        const int warp_row0 = s_off[t.e] + t.mt * BM + q * 32;
         const int col0 = t.nt * BN;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
           uint32_t v[32];
           __syncwarp();
           tmem_ld32(tb + c, v);
           tmem_ld_wait();
-          if (valid && EPI == EPI_DSWIGLU) {
+          if (!__any_sync(FULL_MASK, valid)) continue;
+          if (EPI == EPI_DSWIGLU) {
+            uint32_t og[16], ou[16];
+            uint4 g4[4], u4[4];
             const uint4* gp = reinterpret_cast<const uint4*>(args.gu + row * (2 * args.I) + col0 + c);
             const uint4* up = reinterpret_cast<const uint4*>(args.gu + row * (2 * args.I) + args.I + col0 + c);
-            uint4* dg = reinterpret_cast<uint4*>(args.out_bf16 + row * args.ld_out + col0 + c);
-            uint4* du = reinterpret_cast<uint4*>(args.out_bf16 + row * args.ld_out + args.I + col0 + c);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const uint4 g4 = gp[i], u4 = up[i];
-              const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w};
-              const uint32_t uw[4] = {u4.x, u4.y, u4.z, u4.w};
-              uint32_t og[4], ou[4];
+              g4[i] = valid ? gp[i] : make_uint4(0, 0, 0, 0);
+              u4[i] = valid ? up[i] : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t gw[4] = {g4[i].x, g4[i].y, g4[i].z, g4[i].w};
+              const uint32_t uw[4] = {u4[i].x, u4[i].y, u4[i].z, u4[i].w};
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
                 float rg[2], ru[2];
@@ -367,20 +386,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                   rg[hlf] = gh * u * dsilu;
                   ru[hlf] = gh * g * sg;
                 }
-                og[k] = pack_bf16x2(rg[0], rg[1]);
-                ou[k] = pack_bf16x2(ru[0], ru[1]);
+                og[4 * i + k] = pack_bf16x2(rg[0], rg[1]);
+                ou[4 * i + k] = pack_bf16x2(ru[0], ru[1]);
               }
-              dg[i] = make_uint4(og[0], og[1], og[2], og[3]);
-              du[i] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
             }
-          } else if (valid) {
-            uint4* d4 = reinterpret_cast<uint4*>(args.out_bf16 + row * args.ld_out + col0 + c);
+            if (full_warp) {
+              st.box(&tmOut, og, col0 + c, warp_row0);
+              st.box(&tmOut, ou, args.I + col0 + c, warp_row0);
+            } else if (valid) {
+              uint4* dg = reinterpret_cast<uint4*>(args.out_bf16 + row * args.ld_out + col0 + c);
+              uint4* du = reinterpret_cast<uint4*>(args.out_bf16 + row * args.ld_out + args.I + col0 + c);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              d4[i] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * i + 0]), __uint_as_float(v[8 * i + 1])),
-                                 pack_bf16x2(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
-                                 pack_bf16x2(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
-                                 pack_bf16x2(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])));
+              for (int i = 0; i < 4; ++i) {
+                dg[i] = make_uint4(og[4 * i], og[4 * i + 1], og[4 * i + 2], og[4 * i + 3]);
+                du[i] = make_uint4(ou[4 * i], ou[4 * i + 1], ou[4 * i + 2], ou[4 * i + 3]);
+              }
+            }
+          } else {
+            uint32_t ov[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              ov[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+            if (full_warp) {
+              st.box(&tmOut, ov, col0 + c, warp_row0);
+            } else if (valid) {
+              uint4* d4 = reinterpret_cast<uint4*>(args.out_bf16 + row * args.ld_out + col0 + c);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                d4[i] = make_uint4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
+            }
           }
         }
       }
@@ -388,6 +422,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&s.tempty[buf]));
     }
+    st.finish();
   }
 
   tc_fence_before();
@@ -397,21 +432,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0 && s.abort) report(args.status, MOE_DEVERR_TIMEOUT);
 }
 
-// G_o[r] = bf16(w_r * grad_y[r]) on the valid rows (one warp per row).
+// G_o[r] = bf16(w_r * grad_y[r]) on the valid rows and 0 on the pad rows
+// (rows below R = totals[0] with no token); one warp per row.
 __global__ void __launch_bounds__(256) scale_rows_kernel(const uint16_t* __restrict__ grad_y,
                                                          const int* __restrict__ row_token,
                                                          const float* __restrict__ row_weight,
+                                                         const int* __restrict__ totals,
                                                          long long C, int H,
                                                          uint16_t* __restrict__ g_o) {
+  const long long R = totals[0];
   const int lane = threadIdx.x & 31;
   const int V = H >> 8;
   const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-       r < C; r += nwarps) {
-    if (row_token[r] < 0) continue;
+       r < C && r < R; r += nwarps) {
+    uint4* dst = reinterpret_cast<uint4*>(g_o + r * H);
+    if (row_token[r] < 0) {
+      for (int v = lane; v < 32 * V; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
     const float w = row_weight[r];
     const uint4* src = reinterpret_cast<const uint4*>(grad_y + r * H);
-    uint4* dst = reinterpret_cast<uint4*>(g_o + r * H);
     for (int v = lane; v < 32 * V; v += 32) {
       const uint4 a = __ldg(src + v);
       dst[v] = make_uint4(pack_bf16x2(w * bf16_lo(a.x), w * bf16_hi(a.x)),
@@ -422,33 +463,43 @@ __global__ void __launch_bounds__(256) scale_rows_kernel(const uint16_t* __restr
   }
 }
 
-template <bool GROUP_K, int BN, int EPI>
-cudaError_t launch_bwd(const CUtensorMap& a, const CUtensorMap& b, const BwdArgs& args,
-                       cudaStream_t s) {
+template <bool GROUP_K, int BN, int EPI, int STAGES>
+cudaError_t launch_bwd_stages(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
+                              const BwdArgs& args, cudaStream_t s) {
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  constexpr size_t bytes = smem_bytes<BN>();
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    err = cudaFuncSetAttribute(bwd_gemm_kernel<GROUP_K, BN, EPI>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    err = cudaFuncSetAttribute(bwd_gemm_kernel<GROUP_K, BN, EPI, STAGES>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  bwd_gemm_kernel<GROUP_K, BN, EPI><<<sm_count(), NUM_THREADS, bytes, s>>>(a, b, args);
+  bwd_gemm_kernel<GROUP_K, BN, EPI, STAGES><<<sm_count(), NUM_THREADS, smem_bytes<BN>(STAGES, args.E), s>>>(
+      a, b, out, args);
   return cudaGetLastError();
 }
 
+// The deepest ring that fits beside the staging and the per-expert tables.
+template <bool GROUP_K, int BN, int EPI>
+cudaError_t launch_bwd(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
+                       const BwdArgs& args, cudaStream_t s) {
+  constexpr int MS = Cfg<BN>::MAX_STAGES;
+  if (smem_bytes<BN>(MS, args.E) <= static_cast<size_t>(SMEM_LIMIT))
+    return launch_bwd_stages<GROUP_K, BN, EPI, MS>(a, b, out, args, s);
+  return launch_bwd_stages<GROUP_K, BN, EPI, MS - 1>(a, b, out, args, s);
+}
+
 template <bool GROUP_K, int EPI>
-cudaError_t launch_bwd_bn(int n_total, const CUtensorMap& a, const CUtensorMap& b, BwdArgs args,
-                          cudaStream_t s) {
+cudaError_t launch_bwd_bn(int n_total, const CUtensorMap& a, const CUtensorMap& b,
+                          const CUtensorMap& out, BwdArgs args, cudaStream_t s) {
   if (n_total % 256 == 0) {
     args.n_tiles = n_total / 256;
-    return launch_bwd<GROUP_K, 256, EPI>(a, b, args, s);
+    return launch_bwd<GROUP_K, 256, EPI>(a, b, out, args, s);
   }
   args.n_tiles = n_total / 128;
-  return launch_bwd<GROUP_K, 128, EPI>(a, b, args, s);
+  return launch_bwd<GROUP_K, 128, EPI>(a, b, out, args, s);
 }
 
 }  // namespace
@@ -473,7 +524,7 @@ cudaError_t launch_experts_backward(const uint16_t* grad_y, const uint16_t* x_di
   if (C > 0) {
     const long long need = (C + 7) / 8;
     const int blocks = static_cast<int>(need < 8LL * sm_count() ? need : 8LL * sm_count());
-    scale_rows_kernel<<<blocks, 256, 0, s>>>(grad_y, L.row_token, L.row_weight, C, H, g_o);
+    scale_rows_kernel<<<blocks, 256, 0, s>>>(grad_y, L.row_token, L.row_weight, L.totals, C, H, g_o);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
@@ -488,9 +539,10 @@ cudaError_t launch_experts_backward(const uint16_t* grad_y, const uint16_t* x_di
 
   if (C > 0) {
     // dgrad1: G_gu = SwiGLU'(G_o W2)
-    CUtensorMap mA, mB;
+    CUtensorMap mA, mB, mO;
     if (!make_tma_2d_bf16(&mA, g_o, C, H, 128) ||
-        !make_tma_2d_bf16(&mB, W2, static_cast<uint64_t>(E) * H, I, 64))
+        !make_tma_2d_bf16(&mB, W2, static_cast<uint64_t>(E) * H, I, 64) ||
+        !make_tma_store_2d_bf16(&mO, g_gu, C, 2 * I))
       return cudaErrorInvalidValue;
     BwdArgs a = base;
     a.k_blocks = H / BK;
@@ -498,50 +550,63 @@ cudaError_t launch_experts_backward(const uint16_t* grad_y, const uint16_t* x_di
     a.out_bf16 = g_gu;
     a.ld_out = 2 * I;
     a.gu = gu_save;
-    err = launch_bwd_bn<false, EPI_DSWIGLU>(I, mA, mB, a, s);
+    err = launch_bwd_bn<false, EPI_DSWIGLU>(I, mA, mB, mO, a, s);
     if (err != cudaSuccess) return err;
 
     // dgrad2: grad_x_disp = G_gu W1
     if (!make_tma_2d_bf16(&mA, g_gu, C, 2 * I, 128) ||
-        !make_tma_2d_bf16(&mB, W1, static_cast<uint64_t>(E) * 2 * I, H, 64))
+        !make_tma_2d_bf16(&mB, W1, static_cast<uint64_t>(E) * 2 * I, H, 64) ||
+        !make_tma_store_2d_bf16(&mO, grad_x_disp, C, H))
       return cudaErrorInvalidValue;
     a = base;
     a.k_blocks = 2 * I / BK;
     a.b_rows_per_expert = 2 * I;
     a.out_bf16 = grad_x_disp;
     a.ld_out = H;
-    err = launch_bwd_bn<false, EPI_BF16>(H, mA, mB, a, s);
+    err = launch_bwd_bn<false, EPI_BF16>(H, mA, mB, mO, a, s);
     if (err != cudaSuccess) return err;
   }
 
   // wgrad2: dW2[e] = G_o^T h     (M = H, N = I, K = the expert's rows)
   {
-    CUtensorMap mA, mB;
+    CUtensorMap mA, mB, mO;
     const uint64_t rows = C > 0 ? static_cast<uint64_t>(C) : 1;
     if (!make_tma_2d_bf16(&mA, C > 0 ? static_cast<const void*>(g_o) : static_cast<const void*>(dW2), rows, H, 64) ||
-        !make_tma_2d_bf16(&mB, C > 0 ? static_cast<const void*>(h) : static_cast<const void*>(dW2), rows, I, 64))
+        !make_tma_2d_bf16(&mB, C > 0 ? static_cast<const void*>(h) : static_cast<const void*>(dW2), rows, I, 64) ||
+        !make_tma_store_2d_f32(&mO, dW2, static_cast<uint64_t>(E) * H, I))
       return cudaErrorInvalidValue;
     BwdArgs a = base;
     a.m_tiles = H / BM;
+    // With groups padded to a multiple of 64 rows, an expert's last K block
+    // holds only its own pad rows, which are zero in every operand (x_disp by
+    // the dispatch, h and the gate/up values by the forward, G_o and G_gu
+    // here); otherwise the lines past the count are zeroed in shared memory.
+    a.zero_tail = (L.pad_multiple % BK) != 0;
     a.m_total = H;
     a.n_total = I;
     a.out_f32 = dW2;
-    err = launch_bwd_bn<true, EPI_F32>(I, mA, mB, a, s);
+    err = launch_bwd_bn<true, EPI_F32>(I, mA, mB, mO, a, s);
     if (err != cudaSuccess) return err;
   }
   // wgrad1: dW1[e] = G_gu^T x_disp   (M = 2I, N = H)
   {
-    CUtensorMap mA, mB;
+    CUtensorMap mA, mB, mO;
     const uint64_t rows = C > 0 ? static_cast<uint64_t>(C) : 1;
     if (!make_tma_2d_bf16(&mA, C > 0 ? static_cast<const void*>(g_gu) : static_cast<const void*>(dW1), rows, 2 * I, 64) ||
-        !make_tma_2d_bf16(&mB, C > 0 ? static_cast<const void*>(x_disp) : static_cast<const void*>(dW1), rows, H, 64))
+        !make_tma_2d_bf16(&mB, C > 0 ? static_cast<const void*>(x_disp) : static_cast<const void*>(dW1), rows, H, 64) ||
+        !make_tma_store_2d_f32(&mO, dW1, static_cast<uint64_t>(E) * 2 * I, H))
       return cudaErrorInvalidValue;
     BwdArgs a = base;
     a.m_tiles = 2 * I / BM;
+    // With groups padded to a multiple of 64 rows, an expert's last K block
+    // holds only its own pad rows, which are zero in every operand (x_disp by
+    // the dispatch, h and the gate/up values by the forward, G_o and G_gu
+    // here); otherwise the lines past the count are zeroed in shared memory.
+    a.zero_tail = (L.pad_multiple % BK) != 0;
     a.m_total = 2 * I;
     a.n_total = H;
     a.out_f32 = dW1;
-    err = launch_bwd_bn<true, EPI_F32>(H, mA, mB, a, s);
+    err = launch_bwd_bn<true, EPI_F32>(H, mA, mB, mO, a, s);
   }
   return err;
 }

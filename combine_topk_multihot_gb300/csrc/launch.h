@@ -22,6 +22,8 @@ bool make_tma_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_
 // Tensor map for TMA stores of 32-row x 32-column bf16 boxes (64-byte rows,
 // no swizzle) into a row-major [rows, cols] matrix.
 bool make_tma_store_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols);
+// The same for fp32: 32-row x 16-column boxes (64-byte rows).
+bool make_tma_store_2d_f32(CUtensorMap* map, void* base, uint64_t rows, uint64_t cols);
 
 // Records `text` as this thread's moe_last_error() and returns `st`.
 moe_status set_last_error(moe_status st, const char* text);

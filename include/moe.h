@@ -205,10 +205,13 @@ MOE_API moe_status moe_dispatch_static_scratch(const moe_bf16* x, const uint8_t*
  *           the routing-weight gradient needs.
  *   gu_save [C, 2I] bf16 (out, nullable): bf16 of the gate and up
  *           pre-activations, which the expert backward needs.
- * Only the N valid rows are computed and written; pad and spare rows
- * (sentinel expert) are skipped and their output rows are left untouched.
- * The row counts are read on the device, so the call never synchronises and
- * can be captured.
+ * Each expert's rows are computed in 128-row tiles (ceil(count / 128) of
+ * them).  The valid rows are written.  When gu_save is given (training), the
+ * pad rows of each expert's group that its tiles cover are written too, and
+ * come out as zeros in h, y, o_save and gu_save because moe_dispatch leaves
+ * x_disp's pad rows zero and their weight is 0; without gu_save they are not
+ * touched.  Spare rows (R..C-1) are never written.  The row counts are read on
+ * the device, so the call never synchronises and can be captured.
  */
 MOE_API moe_status moe_grouped_experts(const moe_bf16* x_disp, const moe_layout* L,
                                int32_t H, int32_t I,
@@ -278,7 +281,8 @@ MOE_API moe_status moe_route_to_multihot_backward(const float* grad_probs, const
  *   grad_y [C, H] bf16 (moe_combine_backward's output); x_disp [C, H], h [C, I]
  *     and gu_save [C, 2I] bf16 from the forward (gu_save is required here).
  *   W1, W2: as in moe_grouped_experts.
- *   grad_x_disp [C, H] bf16 (out): written on the valid rows only.
+ *   grad_x_disp [C, H] bf16 (out): written on the valid rows and the pad
+ *     rows inside each expert's tiles (zeros there).
  *   dW1 [E, 2I, H], dW2 [E, H, I] fp32 (out): fully overwritten, fp32
  *     accumulation; an expert with no rows gets zeros.
  *   workspace: moe_experts_backward_workspace_bytes(capacity, H, I) bytes,
@@ -286,7 +290,11 @@ MOE_API moe_status moe_route_to_multihot_backward(const float* grad_probs, const
  *     operands on the valid rows: G_o [C, H] from the workspace's first
  *     256-byte boundary, then [G_g | G_u] [C, 2I] from the next 256-byte
  *     boundary after C*H*2 bytes.
- * Row counts are read on the device: no host sync.
+ * Row counts are read on the device: no host sync.  When pad_multiple is a
+ * multiple of 64, the pad rows of x_disp, h and gu_save must be zero, as
+ * moe_dispatch and moe_grouped_experts (with gu_save) leave them: the weight
+ * gradients then read them instead of masking the last partial 64-row block
+ * of each expert.
  */
 MOE_API moe_status moe_experts_backward_workspace_bytes(int64_t capacity, int32_t H, int32_t I,
                                                         size_t* bytes);

@@ -202,9 +202,13 @@ def test_experts_match_oracle(moe, T, H, E, K, I, P):
     assert_gemm_close(bits(fwd.out), O.combine(y, Lr["token_row"]), "out")
 
 
-def test_experts_skip_sentinel_rows(moe):
-    """Pad / spare rows are never written by the experts, and the combine never
-    reads them: poisoning them with NaN changes nothing."""
+@pytest.mark.parametrize("save", [False, True])
+def test_experts_sentinel_rows(moe, save):
+    """Spare rows (R..C-1) are never written by the experts.  Pad rows inside
+    an expert's group are left untouched in inference and written as zeros
+    when the gate/up values are saved for the backward.  The combine reads
+    neither: with every sentinel row poisoned with NaN beforehand its output
+    is unchanged."""
     T, H, E, K, I, P = 90, 256, 8, 2, 128, 16
     idx, p = random_routing(T, E, K, seed=9, drop=0.3)
     x = torch.randn(T, H).to(torch.bfloat16).to(DEV)
@@ -213,10 +217,20 @@ def test_experts_skip_sentinel_rows(moe):
     C = O.worst_case_capacity(T, E, K, P)
     fwd = moe.moe_layer_forward(x, idx.to(DEV), p.to(DEV), W1, W2, P, capacity=C)
     nan = torch.full((C, H), float("nan"), dtype=torch.bfloat16, device=DEV)
-    ex = moe.moe_grouped_experts(fwd.x_disp, fwd.layout, W1, W2, out={"y": nan.clone()})
-    sentinel = (fwd.layout.row_expert == E)
-    assert torch.isnan(ex["y"][sentinel]).all()
-    assert not torch.isnan(ex["y"][~sentinel]).any()
+    nan_h = torch.full((C, I), float("nan"), dtype=torch.bfloat16, device=DEV)
+    ex = moe.moe_grouped_experts(fwd.x_disp, fwd.layout, W1, W2, out={"y": nan.clone(), "h": nan_h},
+                                 save_o=save, save_gu=save)
+    R = int(fwd.layout.totals[0].item())
+    pad = fwd.layout.row_expert == E
+    pad[R:] = False
+    assert torch.isnan(ex["y"][R:]).all() and torch.isnan(ex["h"][R:]).all()
+    if save:
+        assert (ex["y"][pad] == 0).all() and (ex["h"][pad] == 0).all()
+        assert (ex["o"][pad] == 0).all() and (ex["gu"][pad] == 0).all()
+    else:
+        assert torch.isnan(ex["y"][pad]).all() and torch.isnan(ex["h"][pad]).all()
+    valid = fwd.layout.row_token >= 0
+    assert not torch.isnan(ex["y"][valid]).any()
     out = moe.moe_combine(ex["y"], fwd.layout)
     assert torch.equal(out.view(torch.int16), fwd.out.view(torch.int16))
 
