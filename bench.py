@@ -261,12 +261,32 @@ def run_ours(args, world, rank, local):
 
     step_events = [[ev() for _ in range(len(stages) + 1)] for _ in range(args.steps)]
     t0, t1 = ev(), ev()
+    # Sync-free workloads (decode) run as CUDA graphs, one per cycled layer,
+    # captured after the eager warm-up and replayed in the timed loop; their
+    # per-stage split comes from an eager pass of the same steps.
+    graphs = None
+    if cfg.sync_free:
+        for i in range(args.steps):
+            step(layers[i % n_layers], step_events[i])
+        torch.cuda.synchronize()
+        graphs = []
+        for L in layers:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step(L)
+            graphs.append(g)
+        for i in range(args.warmup):
+            graphs[i % n_layers].replay()
+        torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
         barrier(world)
         t0.record(stream)
         for i in range(args.steps):
-            step(layers[i % n_layers], step_events[i])
+            if graphs is not None:
+                graphs[i % n_layers].replay()
+            else:
+                step(layers[i % n_layers], step_events[i])
         t1.record(stream)
         torch.cuda.synchronize()
     barrier(world)
@@ -309,6 +329,12 @@ def run_ours(args, world, rank, local):
 
     def e2e_step(i):
         hs = host[i % n_layers]
+        if graphs is not None:  # the graphs read their layer's own input buffers
+            for k in in_keys:
+                layers[i % n_layers][k].copy_(hs[k], non_blocking=True)
+            graphs[i % n_layers].replay()
+            out_host.copy_(out, non_blocking=True)
+            return
         for k in d_in:
             d_in[k].copy_(hs[k], non_blocking=True)
         L = dict(layers[i % n_layers])
@@ -391,7 +417,8 @@ def run_ours(args, world, rank, local):
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) tokens, softmax top-k routing, N(0,0.02) weights)",
         "config": {"workload": cfg.name, "T": T, "H": H, "E": E, "top_k": K, "I": I,
-                   "pad_multiple": P, "mode": "host-synced" if host_sync else "sync-free",
+                   "pad_multiple": P,
+                   "mode": "host-synced" if host_sync else "sync-free, CUDA graph replay",
                    "layers_cycled": n_layers, "l2": "inputs larger than L2 (4 distinct layers cycled, >1.2 GB weights each)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
