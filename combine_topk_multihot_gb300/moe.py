@@ -85,6 +85,38 @@ class Layout:
     def ref(self):
         return ctypes.byref(self.c)
 
+    # The buffers that later steps read.  The workspace is scratch for the
+    # dispatch alone and is not part of this list.
+    TENSOR_FIELDS = ("tokens_per_expert", "offsets", "totals", "row_token", "row_expert",
+                     "row_weight", "token_row", "status")
+
+    def tensors(self):
+        """The layout's buffers in TENSOR_FIELDS order, to pass it between ops."""
+        return tuple(getattr(self, f) for f in self.TENSOR_FIELDS)
+
+    @classmethod
+    def from_tensors(cls, T: int, E: int, K: int, pad_multiple: int, tensors,
+                     workspace: Optional[torch.Tensor] = None) -> "Layout":
+        """Rebuild a layout around the buffers of ``tensors()``.  Without a
+        ``workspace`` it gets a 256-byte placeholder: enough for every call
+        except moe_dispatch, which needs ``moe_layout_workspace_bytes``."""
+        self = cls.__new__(cls)
+        for f, t in zip(cls.TENSOR_FIELDS, tensors):
+            setattr(self, f, t)
+        self.workspace = (workspace if workspace is not None else
+                          torch.empty(256, dtype=torch.uint8, device=self.status.device))
+        self.T, self.E, self.K, self.pad_multiple = T, E, K, pad_multiple
+        self.capacity = self.row_token.numel()
+        C = self.capacity
+        self.c = N.MoeLayout(
+            T, E, K, pad_multiple, C,
+            self.tokens_per_expert.data_ptr(), self.offsets.data_ptr(), self.totals.data_ptr(),
+            self.row_token.data_ptr() if C else None, self.row_expert.data_ptr() if C else None,
+            self.row_weight.data_ptr() if C else None,
+            self.token_row.data_ptr() if T * K else None,
+            self.status.data_ptr(), self.workspace.data_ptr())
+        return self
+
 
 def moe_route_to_multihot(topk_idx: torch.Tensor, topk_probs: torch.Tensor, E: int,
                           status: torch.Tensor, stream=None):

@@ -1,0 +1,212 @@
+"""The custom-operator layer on the GPU.
+
+Page: "Add the deepep expert-parallel implementation (huggingface/transformers
+#49638)", What this adds, Custom ops, and its test list (the capture-and-compile
+test): the layer trains through autograd, a CUDA graph captured after an eager
+warm-up replays like eager, and torch.compile(fullgraph=True) matches eager.
+
+* the operators' forward and backward equal, bit for bit, the same steps called
+  through the binding directly (sync-free, worst-case rows);
+* end to end against the fp64 oracle's layer forward and backward;
+* torch.library.opcheck of every operator (schema, fake tensors, autograd
+  registration);
+* CUDA graph replay of forward + backward == eager, bit for bit;
+* torch.compile(fullgraph=True) of the layer (the aot_eager backend: the
+  trace and the autograd split, with no generated kernels) == eager, bit for bit;
+* a bad expert index is reported in the returned device status word.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synthetic
+from tests._util import GEMM_REL_L2, assert_gemm_close, bits, random_routing
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+BF = torch.bfloat16
+
+
+@pytest.fixture(scope="module")
+def moe():
+    assert torch.cuda.is_available(), "GPU tests need a GPU"
+    import combine_topk_multihot_gb300 as m
+    return m
+
+
+def _inputs(T, H, E, K, I, seed, drop=0.0, dup=0.0):
+    idx, p = random_routing(T, E, K, seed=seed, drop=drop, dup=dup)
+    gen = torch.Generator().manual_seed(seed)
+    x = torch.randn(T, H, generator=gen).to(BF)
+    W1 = (torch.randn(E, 2 * I, H, generator=gen) * 0.02).to(BF)
+    W2 = (torch.randn(E, H, I, generator=gen) * 0.02).to(BF)
+    g = torch.randn(T, H, generator=gen).to(BF)
+    return [t.to(DEV) for t in (x, idx, p, W1, W2, g)]
+
+
+def _layer(fn, x, idx, p, W1, W2, g):
+    """Forward + backward through autograd; returns (out, dx, dp, dW1, dW2)."""
+    leaves = [t.detach().clone().requires_grad_(True) for t in (x, p, W1, W2)]
+    xs, ps, W1s, W2s = leaves
+    out = fn(xs, idx, ps, W1s, W2s)
+    out.backward(g)
+    return [out.detach()] + [t.grad for t in leaves]
+
+
+def _direct(moe, x, idx, p, W1, W2, g, P):
+    """The same steps called through the binding (no operators, no autograd)."""
+    fwd = moe.moe_layer_forward(x, idx, p, W1, W2, P, host_sync=False, save_for_backward=True)
+    grad_y, grad_w = moe.moe_combine_backward(g, fwd.layout, o_save=fwd.o)
+    gxd, dW1, dW2 = moe.moe_grouped_experts_backward(grad_y, fwd.x_disp, fwd.h, fwd.gu, fwd.layout,
+                                                     W1, W2)
+    grad_x, grad_probs = moe.moe_dispatch_backward(gxd, fwd.layout, grad_w=grad_w)
+    g_topk = moe.moe_route_to_multihot_backward(grad_probs, idx, fwd.winner_slot)
+    return [fwd.out, grad_x, g_topk, dW1.to(BF), dW2.to(BF)]
+
+
+def _same(a, b, what):
+    for name, u, v in zip(("out", "grad_x", "grad_topk_probs", "dW1", "dW2"), a, b):
+        assert u.dtype == v.dtype and u.shape == v.shape, f"{what} {name}"
+        assert torch.equal(u.view(torch.int8), v.view(torch.int8)) if u.dtype != torch.float32 \
+            else torch.equal(u, v), f"{what} {name} differs"
+
+
+CASES = [  # T, H, E, K, I, P, drop, dup
+    (64, 256, 8, 2, 128, 16, 0.0, 0.0),
+    (300, 512, 8, 2, 256, 16, 0.1, 0.1),
+    (20, 512, 12, 1, 384, 1, 0.0, 0.0),
+    (260, 768, 12, 3, 256, 128, 0.2, 0.0),
+]
+
+
+@pytest.mark.parametrize("T,H,E,K,I,P,drop,dup", CASES)
+def test_ops_equal_the_direct_calls(moe, T, H, E, K, I, P, drop, dup):
+    x, idx, p, W1, W2, g = _inputs(T, H, E, K, I, seed=T + H, drop=drop, dup=dup)
+    got = _layer(lambda *a: moe.moe_layer(*a, pad_multiple=P), x, idx, p, W1, W2, g)
+    ref = _direct(moe, x, idx, p, W1, W2, g, P)
+    torch.cuda.synchronize()
+    _same(got, ref, "ops vs direct")
+
+
+@pytest.mark.parametrize("T,H,E,K,I,P,drop,dup", CASES[:2])
+def test_ops_match_the_oracle_end_to_end(moe, T, H, E, K, I, P, drop, dup):
+    """Forward output within the GEMM tolerance; every gradient within
+    rel L2 5e-3 of the oracle's fp64 chain rule with bf16 operands."""
+    x, idx, p, W1, W2, g = _inputs(T, H, E, K, I, seed=7 * T + H, drop=drop, dup=dup)
+    out, dx, dp, dW1, dW2 = _layer(lambda *a: moe.moe_layer(*a, pad_multiple=P), x, idx, p, W1, W2, g)
+    torch.cuda.synchronize()
+    idx_np = idx.cpu().numpy()
+    W1b, W2b = bits(W1), bits(W2)
+    C = O.worst_case_capacity(T, E, K, P)
+    fwd = O.layer_forward(bits(x), idx_np, p.cpu().numpy(), W1b, W2b, I, P, capacity=C)
+    bwd = O.layer_backward(fwd, bits(g), W1b, W2b, idx_np, I)
+    assert_gemm_close(bits(out), fwd["out"], "out")
+
+    def rel(gpu, ref, what):
+        gpu, ref = np.asarray(gpu, np.float64), np.asarray(ref, np.float64)
+        r = np.linalg.norm(gpu - ref) / max(np.linalg.norm(ref), 1e-30)
+        assert np.isfinite(gpu).all() and r <= GEMM_REL_L2, f"{what}: rel_l2={r:.3g}"
+
+    rel(O.bf16_bits_to_f64(bits(dx)), O.bf16_bits_to_f64(bwd["grad_x"]), "grad_x")
+    rel(dp.cpu().numpy(), bwd["grad_topk_probs"], "grad_topk_probs")
+    rel(dW1.float().cpu().numpy(), bwd["dW1"], "dW1")
+    rel(dW2.float().cpu().numpy(), bwd["dW2"], "dW2")
+
+
+def test_opcheck_every_operator(moe):
+    T, H, E, K, I, P = 64, 256, 8, 2, 128, 16
+    x, idx, p, W1, W2, g = _inputs(T, H, E, K, I, seed=11, drop=0.1)
+    ops = torch.ops.moe_gb300
+    utils = ("test_schema", "test_autograd_registration", "test_faketensor")
+    rmap, probs, win, status = ops.route_to_multihot(idx, p, E)
+    x_disp, *lay = ops.dispatch(x, rmap, probs, status, K, P)
+    y, h, o, gu = ops.grouped_experts(x_disp, W1, W2, lay, T, K, P, True)
+    grad_y, grad_w = ops.combine_backward(g, o, lay, T, K, P, E)
+    gxd, dW1, dW2 = ops.experts_backward(grad_y, x_disp, h, gu, W1, W2, lay, T, K, P)
+    grad_x, grad_probs = ops.dispatch_backward(gxd, grad_w, lay, T, K, P, E)
+    calls = [
+        (ops.route_to_multihot.default, (idx, p, E)),
+        (ops.dispatch.default, (x, rmap, probs, status, K, P)),
+        (ops.grouped_experts.default, (x_disp, W1, W2, lay, T, K, P, True)),
+        (ops.grouped_experts.default, (x_disp, W1, W2, lay, T, K, P, False)),
+        (ops.combine.default, (y, lay, T, K, P, E)),
+        (ops.combine_backward.default, (g, o, lay, T, K, P, E)),
+        (ops.experts_backward.default, (grad_y, x_disp, h, gu, W1, W2, lay, T, K, P)),
+        (ops.dispatch_backward.default, (gxd, grad_w, lay, T, K, P, E)),
+        (ops.route_to_multihot_backward.default, (grad_probs, idx, win)),
+    ]
+    for op, args in calls:
+        torch.library.opcheck(op, args, test_utils=utils)
+
+
+def test_cuda_graph_replay_equals_eager(moe):
+    """Forward + backward captured once after an eager warm-up, replayed on
+    new inputs copied into the static ones: replay == eager, bit for bit."""
+    T, H, E, K, I, P = 256, 512, 8, 2, 256, 16
+    W1, W2 = synthetic.make_weights(E, H, I, 4, device=DEV)
+    W1.requires_grad_(True)
+    W2.requires_grad_(True)
+    sx = torch.zeros(T, H, dtype=BF, device=DEV, requires_grad=True)
+    sp = torch.zeros(T, K, dtype=torch.float32, device=DEV, requires_grad=True)
+    sidx = torch.zeros(T, K, dtype=torch.int64, device=DEV)
+    sg = torch.zeros(T, H, dtype=BF, device=DEV)
+    sets = [_inputs(T, H, E, K, I, seed=100 + k, drop=0.05 * k) for k in range(3)]
+
+    def load(s):
+        with torch.no_grad():
+            sx.copy_(s[0]); sidx.copy_(s[1]); sp.copy_(s[2]); sg.copy_(s[5])
+
+    def step():
+        out = moe.moe_layer(sx, sidx, sp, W1, W2, pad_multiple=P)
+        return (out,) + torch.autograd.grad(out, (sx, sp, W1, W2), sg)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    eager = []
+    with torch.cuda.stream(side):
+        for s in sets:
+            load(s)
+            eager.append([t.clone() for t in step()])
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        static_out = step()
+    for s, ref in zip(reversed(sets), reversed(eager)):
+        load(s)
+        graph.replay()
+        torch.cuda.synchronize()
+        _same(list(static_out), ref, "graph replay vs eager")
+
+
+def test_compile_fullgraph_equals_eager(moe):
+    T, H, E, K, I, P = 300, 512, 8, 2, 256, 16
+    x, idx, p, W1, W2, g = _inputs(T, H, E, K, I, seed=23, drop=0.1)
+    fn = lambda *a: moe.moe_layer(*a, pad_multiple=P)
+    compiled = torch.compile(fn, fullgraph=True, backend="aot_eager")
+    ref = _layer(fn, x, idx, p, W1, W2, g)
+    for _ in range(2):
+        got = _layer(compiled, x, idx, p, W1, W2, g)
+        torch.cuda.synchronize()
+        _same(got, ref, "compiled vs eager")
+
+
+def test_bad_index_is_reported_in_the_status_word(moe):
+    T, H, E, K, I, P = 64, 256, 8, 2, 128, 16
+    x, idx, p, W1, W2, g = _inputs(T, H, E, K, I, seed=5)
+    idx = idx.clone()
+    idx[3, 1] = E          # outside [-1, E): dropped and flagged
+    out, status = moe.moe_layer(x, idx, p, W1, W2, pad_multiple=P, return_status=True)
+    torch.cuda.synchronize()
+    assert int(status.item()) & moe._native.MOE_DEVERR_BAD_INDEX
+    # through autograd too: the bad slot gets no gradient
+    ps = p.clone().requires_grad_(True)
+    out, status = moe.moe_layer(x, idx, ps, W1, W2, pad_multiple=P, return_status=True)
+    out.backward(g)
+    torch.cuda.synchronize()
+    assert int(status.item()) & moe._native.MOE_DEVERR_BAD_INDEX
+    assert float(ps.grad[3, 1]) == 0.0 and torch.isfinite(ps.grad).all()
+    out, status = moe.moe_layer(x, idx.clamp(max=E - 1), p, W1, W2, pad_multiple=P,
+                                return_status=True)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
