@@ -142,8 +142,7 @@ int64_t moe_worst_case_rows(int32_t T, int32_t E, int32_t K, int32_t pad_multipl
 moe_status moe_layout_workspace_bytes(int32_t T, int32_t E, size_t* bytes) {
   MOE_REQUIRE(bytes != nullptr, MOE_ERR_INVALID_ARG, "bytes is NULL");
   MOE_REQUIRE(T >= 0 && E >= 1, MOE_ERR_INVALID_ARG, "bad T/E");
-  const size_t b = static_cast<size_t>(layout_chunks(T)) * E * sizeof(int32_t);
-  *bytes = ((b + 255) / 256) * 256 + 256;
+  *bytes = layout_counter_bytes(T, E) + 256;  // the counters, then the grid barrier's counter
   return MOE_OK;
 }
 
@@ -180,10 +179,13 @@ moe_status moe_dispatch(const moe_bf16* x, const uint8_t* routing_map, const flo
                 static_cast<long long>(worst), static_cast<long long>(L->capacity));
   if ((st = check_device()) != MOE_OK) return st;
 
-  int* chunk_counts = static_cast<int*>(L->workspace);
-  cudaError_t err = launch_layout_counts(routing_map, *L, chunk_counts, stream);
-  if (err != cudaSuccess) return cuda_fail(err, "moe_dispatch: counts");
-  if (rows_host) {
+  cudaError_t err;
+  if (!rows_host) {
+    if ((err = launch_layout(routing_map, probs, *L, L->workspace, LayoutStep::kAll, stream)) != cudaSuccess)
+      return cuda_fail(err, "moe_dispatch: layout");
+  } else {
+    if ((err = launch_layout(routing_map, probs, *L, L->workspace, LayoutStep::kCounts, stream)) != cudaSuccess)
+      return cuda_fail(err, "moe_dispatch: counts");
     int32_t tot[2] = {0, 0}, dev_status = 0;
     if ((err = cudaMemcpyAsync(tot, L->totals, sizeof(tot), cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
         (err = cudaMemcpyAsync(&dev_status, L->status, sizeof(int32_t), cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
@@ -191,14 +193,16 @@ moe_status moe_dispatch(const moe_bf16* x, const uint8_t* routing_map, const flo
       return cuda_fail(err, "moe_dispatch: reading the row counts");
     rows_host[0] = tot[0];
     rows_host[1] = tot[1];
+    if (dev_status & MOE_DEVERR_TIMEOUT)
+      return fail(MOE_ERR_TIMEOUT, "the layout kernel's grid barrier timed out");
     if (dev_status & MOE_DEVERR_BAD_INDEX)
       return fail(MOE_ERR_BAD_INDEX, "an expert index outside [-1, E) was seen");
     if (tot[0] > L->capacity)
       return fail(MOE_ERR_CAPACITY, "the layout needs %d rows, capacity is %lld", tot[0],
                   static_cast<long long>(L->capacity));
+    if ((err = launch_layout(routing_map, probs, *L, L->workspace, LayoutStep::kPlace, stream)) != cudaSuccess)
+      return cuda_fail(err, "moe_dispatch: placement");
   }
-  if ((err = launch_layout_place(routing_map, probs, *L, chunk_counts, stream)) != cudaSuccess)
-    return cuda_fail(err, "moe_dispatch: placement");
   if ((err = launch_row_gather(x, *L, H, x_disp, true, nullptr, nullptr, stream)) != cudaSuccess)
     return cuda_fail(err, "moe_dispatch: gather");
   return MOE_OK;

@@ -2,7 +2,7 @@
 // device memory.
 //
 // moe_dispatch needs a small scratch buffer for its per-chunk expert counters
-// (moe_layout.workspace, E * ceil(T/32) int32).  Some callers have no way to
+// (moe_layout.workspace, E * ceil(T/32) int32, plus a grid-barrier counter).  Some callers have no way to
 // get one: a plugin inside an inference engine that owns every byte of the
 // device pool and hands a layer only its declared inputs and outputs, or a
 // serving loop that must never call cudaMalloc because it can synchronise the
@@ -10,7 +10,8 @@
 // fixed array that lives in the library's own device memory instead.
 //
 // The array below is a file-scope __device__ variable: every GPU on which
-// the library is loaded holds its 1 MiB from load until the process exits.
+// the library is loaded holds its 1 MiB (+ 256 bytes) from load until the
+// process exits.
 // Host code only knows the symbol, not its device address, so the address is
 // looked up once per device with cudaGetSymbolAddress and handed to the
 // kernels through the layout's workspace pointer.
@@ -27,7 +28,8 @@ namespace {
 
 constexpr long long STATIC_SCRATCH_INTS = MOE_STATIC_SCRATCH_INTS;  // 1 MiB of int32 counters
 
-static __device__ __align__(256) int g_dispatch_scratch[STATIC_SCRATCH_INTS];
+// The counters, then 256 bytes for the layout kernel's grid-barrier counter.
+static __device__ __align__(256) int g_dispatch_scratch[STATIC_SCRATCH_INTS + 64];
 
 constexpr int MAX_DEVICES = 64;
 std::mutex g_scratch_mu;
@@ -87,9 +89,9 @@ extern "C" moe_status moe_dispatch_static_scratch(const moe_bf16* x, const uint8
   int* scratch = nullptr;
   moe_status st = static_scratch(&scratch);
   if (st != MOE_OK) return st;
-  // Same call as moe_dispatch; only the counters' scratch differs.  Every
-  // counter the kernels read is written earlier in the same call, so nothing
-  // in the array has to start at zero.
+  // Same call as moe_dispatch; only the scratch differs.  Every counter the
+  // kernels read is written earlier in the same call (the barrier counter is
+  // zeroed by the launch itself), so nothing in the array has to start at zero.
   moe_layout with_scratch = *L;
   with_scratch.workspace = scratch;
   return moe_dispatch(x, routing_map, probs, H, &with_scratch, x_disp, rows_host, stream);

@@ -40,12 +40,23 @@ cudaError_t launch_multihot_backward(const float* grad_probs, const int64_t* top
                                      const int8_t* winner, int T, int K, int E, float* grad_topk,
                                      cudaStream_t s);
 
-// Counts and offsets (a2).  chunk_counts is [E][chunks] int32 scratch.
-cudaError_t launch_layout_counts(const uint8_t* routing_map, const moe_layout& L,
-                                 int* chunk_counts, cudaStream_t s);
-// Stable placement of every (token, expert) pair (a3).
-cudaError_t launch_layout_place(const uint8_t* routing_map, const float* probs,
-                                const moe_layout& L, const int* chunk_base, cudaStream_t s);
+// Bytes of per-chunk expert counters at the start of the layout workspace
+// (E * chunks int32, rounded up to 256); the grid barrier's counter follows.
+inline size_t layout_counter_bytes(int32_t T, int32_t E) {
+  const size_t b = static_cast<size_t>(layout_chunks(T)) * E * sizeof(int32_t);
+  return (b + 255) / 256 * 256;
+}
+
+enum class LayoutStep {
+  kAll,     // a2 + a3 in one cooperative launch (the sync-free path)
+  kCounts,  // a2 only: counts, per-chunk starts, offsets and totals
+  kPlace,   // a3 only, after kCounts (the host-synced path reads the totals in between)
+};
+
+// Counts, padded offsets and the stable placement of every (token, expert)
+// pair.  workspace: layout_counter_bytes(T, E) + 256 bytes.
+cudaError_t launch_layout(const uint8_t* routing_map, const float* probs, const moe_layout& L,
+                          void* workspace, LayoutStep step, cudaStream_t s);
 // Rows of the expanded layout from token rows (a4: x -> x_disp, plus the pad /
 // spare rows' metadata when from_offsets); also the combine backward (a7)
 // with the optional routing-weight gradient (a8).  Each token row is read

@@ -24,34 +24,6 @@ namespace moe {
 
 namespace {
 
-// Per-chunk, per-expert counts.  The chunk's routing_map bytes are read as
-// coalesced 32-bit words; only set bytes touch the shared counters.
-__global__ void __launch_bounds__(256) layout_count_kernel(const uint8_t* __restrict__ map, int T,
-                                                           int E, int chunks,
-                                                           int* __restrict__ chunk_counts) {
-  extern __shared__ int s_cnt[];  // [E]
-  const int c = blockIdx.x;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
-  __syncthreads();
-  const long long t0 = static_cast<long long>(c) * LAYOUT_CHUNK;
-  const int nt = static_cast<int>(min(static_cast<long long>(LAYOUT_CHUNK), T - t0));
-  const int E4 = E >> 2;
-  const uint32_t* words = reinterpret_cast<const uint32_t*>(map + t0 * E);
-  const int nw = nt * E4;
-  for (int i = threadIdx.x; i < nw; i += blockDim.x) {
-    const uint32_t v = words[i];
-    if (v) {
-      const int eb = (i % E4) * 4;
-#pragma unroll
-      for (int d = 0; d < 4; ++d)
-        if ((v >> (8 * d)) & 0xffu) atomicAdd(&s_cnt[eb + d], 1);
-    }
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x)
-    chunk_counts[static_cast<long long>(e) * chunks + c] = s_cnt[e];
-}
-
 __device__ __forceinline__ int warp_inclusive_scan(int v, int lane) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -80,134 +52,223 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
   return excl;
 }
 
-// One CTA per expert: the expert's per-chunk counts become each chunk's
-// exclusive start inside the expert's group (in place), and the total is the
-// expert's token count.  Thread i owns a contiguous run of chunks.
-__global__ void __launch_bounds__(256) layout_expert_scan_kernel(int* __restrict__ chunk_counts,
-                                                                 int chunks,
-                                                                 int* __restrict__ tokens_per_expert) {
-  __shared__ int s_warp[33];
-  const int e = blockIdx.x;
-  int* row = chunk_counts + static_cast<long long>(e) * chunks;
-  const int per = (chunks + blockDim.x - 1) / blockDim.x;
-  const int c0 = min(chunks, static_cast<int>(threadIdx.x) * per), c1 = min(chunks, c0 + per);
-  int sum = 0;
-  for (int c = c0; c < c1; c += 8) {
-    int v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = c + i < c1 ? row[c + i] : 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) sum += v[i];
-  }
-  int total;
-  int run = block_exclusive_scan(sum, s_warp, &total);
-  for (int c = c0; c < c1; c += 8) {
-    int v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = c + i < c1 ? row[c + i] : 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (c + i < c1) row[c + i] = run;
-      run += v[i];
-    }
-  }
-  if (threadIdx.x == 0) tokens_per_expert[e] = total;
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
-// One CTA of 1024 threads: offsets[e] = exclusive prefix of the counts padded
-// to multiples of P; offsets[E] = R = totals[0]; totals[1] = N.
-__global__ void __launch_bounds__(1024) layout_offsets_kernel(const int* __restrict__ tokens_per_expert,
-                                                              int E, int P, long long capacity,
-                                                              int* __restrict__ offsets,
-                                                              int* __restrict__ totals,
-                                                              int* __restrict__ status) {
-  __shared__ int s_warp[33];
-  const int e = threadIdx.x;
-  const int cnt = e < E ? tokens_per_expert[e] : 0;
-  const int padded = e < E ? ((cnt + P - 1) / P) * P : 0;
-  int R, N;
-  const int excl = block_exclusive_scan(padded, s_warp, &R);
+// Grid-wide barrier of a cooperative launch (every CTA is resident).  The
+// counter is zeroed before the launch and each CTA adds one per barrier, so
+// barrier n is passed once it reads n * gridDim.x.  The wait is bounded: after
+// WAIT_LIMIT_NS it reports MOE_DEVERR_TIMEOUT and returns false, and the
+// caller's CTA stops.  Data written before the barrier by other CTAs is read
+// after it with ld.global.cg (L2), never through this SM's L1.
+__device__ bool grid_barrier(unsigned* ctr, unsigned target, int* status, int* s_ok) {
   __syncthreads();
-  block_exclusive_scan(cnt, s_warp, &N);
-  if (e < E) offsets[e] = excl;
-  if (e == 0) {
-    offsets[E] = R;
-    totals[0] = R;
-    totals[1] = N;
-    if (R > capacity) report(status, MOE_DEVERR_CAPACITY);
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(ctr, 1u);
+    int ok = 1;
+    const unsigned long long t0 = global_timer_ns();
+    while (ld_acquire_gpu(ctr) < target) {
+      if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+        report(status, MOE_DEVERR_TIMEOUT);
+        ok = 0;
+        break;
+      }
+      __nanosleep(64);
+    }
+    __threadfence();
+    *s_ok = ok;
   }
+  __syncthreads();
+  return *s_ok != 0;
 }
 
-// Stable placement.  A chunk is 32 tokens, so the tokens of the chunk that go
-// to expert e form one 32-bit mask, and a pair's rank inside its expert's
-// group is (the chunk's start in the group) + popcount(mask below the token).
-// The chunk's map is staged in shared memory and turned into both bit
-// matrices: experts per token (ballots) and tokens per expert (a transpose of
-// it); then one warp per token places the token's pairs, lane l taking the
-// experts l, l+32, ...  A pair's position j in token_row is the popcount of the
-// token's expert mask below it.
-__global__ void __launch_bounds__(256) layout_place_kernel(
-    const uint8_t* __restrict__ map, const float* __restrict__ probs, int T, int E, int K,
-    int chunks, const int* __restrict__ chunk_base, const int* __restrict__ offsets,
-    long long capacity, int* __restrict__ row_token, int* __restrict__ row_expert,
-    float* __restrict__ row_weight, int* __restrict__ token_row, int* __restrict__ status) {
+enum LayoutMode : int {
+  LAYOUT_ALL = 0,    // counts, scans, offsets and placement: one cooperative launch
+  LAYOUT_COUNT = 1,  // counts, scans and offsets only (cooperative), for the host-synced path
+  LAYOUT_PLACE = 2,  // placement only, after LAYOUT_COUNT (ordinary launch)
+};
+
+struct LayoutArgs {
+  const uint8_t* map;
+  const float* probs;
+  int T, E, K, P, chunks;
+  long long capacity;
+  int* chunk_counts;  // [E][chunks]: counts, then in place each chunk's start in its expert's group
+  unsigned* barrier;  // zeroed before a cooperative launch
+  int* tokens_per_expert;
+  int* offsets;
+  int* totals;
+  int* row_token;
+  int* row_expert;
+  float* row_weight;
+  int* token_row;
+  int* status;
+};
+
+// a2 + a3 in one kernel.  A chunk is 32 tokens.
+//   1. Per chunk, each expert's token count (the chunk's routing_map bytes are
+//      staged in shared memory; thread e counts column e).
+//   -- grid barrier --
+//   2. One warp per expert turns the expert's per-chunk counts into each
+//      chunk's exclusive start inside the expert's group (in place, 32 chunks
+//      per coalesced step); the total is tokens_per_expert[e].
+//   -- grid barrier --
+//   3. Every CTA forms the padded offsets itself (a block scan over E);
+//      CTA 0 also writes offsets, totals and the capacity check.
+//   4. Stable placement per chunk: the tokens of the chunk that go to expert
+//      e form one 32-bit mask, so a pair's rank in its group is (the chunk's
+//      start) + popcount(mask below the token).  Ballots turn the staged map
+//      into experts-per-token masks, a transpose gives tokens-per-expert, and
+//      one thread per (token, slot j) places the token's j-th expert (the
+//      j-th set bit of its expert mask), so all of a chunk's loads and
+//      stores are in flight together.
+// Rows inside a group come out in ascending token order and nothing depends
+// on scheduling: no atomics decide a position.
+template <int MODE>
+__global__ void __launch_bounds__(256) layout_kernel(LayoutArgs a) {
   static_assert(LAYOUT_CHUNK == 32, "one 32-bit token mask per expert");
   extern __shared__ __align__(16) uint8_t smem[];
-  const int c = blockIdx.x;
-  const long long t0 = static_cast<long long>(c) * LAYOUT_CHUNK;
-  const int nt = static_cast<int>(min(static_cast<long long>(LAYOUT_CHUNK), T - t0));
-  const int E4 = E >> 2, EW = (E + 31) >> 5;
-  uint32_t* s_map32 = reinterpret_cast<uint32_t*>(smem);     // [32][E] bytes
-  uint32_t* s_emask = s_map32 + LAYOUT_CHUNK * E4;             // [32][EW]: experts of each token
-  uint32_t* s_tmask = s_emask + LAYOUT_CHUNK * EW;             // [E]: tokens of each expert
-  int* s_base = reinterpret_cast<int*>(s_tmask + E);           // [E]: first row of this chunk's pairs
+  __shared__ int s_warp[33];
+  __shared__ int s_ok;
+  const int E = a.E, E4 = E >> 2, EW = (E + 31) >> 5;
+  uint32_t* s_map32 = reinterpret_cast<uint32_t*>(smem);             // [32][E] bytes
   const uint8_t* s_map = smem;
-  const uint32_t* words = reinterpret_cast<const uint32_t*>(map + t0 * E);
-  for (int i = threadIdx.x; i < nt * E4; i += blockDim.x) s_map32[i] = words[i];
-  for (int e = threadIdx.x; e < E; e += blockDim.x)
-    s_base[e] = offsets[e] + chunk_base[static_cast<long long>(e) * chunks + c];
-  __syncthreads();
+  uint32_t* s_tmask = s_map32;                                         // [E], over the map once read
+  int* s_base = reinterpret_cast<int*>(s_map32 + E);                   // [E], likewise
+  uint32_t* s_emask = s_map32 + LAYOUT_CHUNK * E4;                     // [32][EW]
+  int* s_off = reinterpret_cast<int*>(s_emask + LAYOUT_CHUNK * EW);    // [E + 1]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  for (int tl = warp; tl < LAYOUT_CHUNK; tl += nwarps) {
-    for (int seg = 0; seg < EW; ++seg) {
-      const int e = seg * 32 + lane;
-      const bool b = tl < nt && e < E && s_map[tl * E + e] != 0;
-      const uint32_t m = __ballot_sync(FULL_MASK, b);
-      if (lane == 0) s_emask[tl * EW + seg] = m;
+
+  if (MODE != LAYOUT_PLACE) {
+    for (int c = blockIdx.x; c < a.chunks; c += gridDim.x) {
+      const long long t0 = static_cast<long long>(c) * LAYOUT_CHUNK;
+      const int nt = static_cast<int>(min(static_cast<long long>(LAYOUT_CHUNK), a.T - t0));
+      const uint32_t* words = reinterpret_cast<const uint32_t*>(a.map + t0 * E);
+      for (int i = threadIdx.x; i < nt * E4; i += blockDim.x) s_map32[i] = words[i];
+      __syncthreads();
+      for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int n = 0;
+        for (int tl = 0; tl < nt; ++tl) n += s_map[tl * E + e] != 0;
+        a.chunk_counts[static_cast<long long>(e) * a.chunks + c] = n;
+      }
+      __syncthreads();
+    }
+    if (!grid_barrier(a.barrier, gridDim.x, a.status, &s_ok)) return;
+    for (int e = blockIdx.x * nwarps + warp; e < E; e += gridDim.x * nwarps) {
+      int* row = a.chunk_counts + static_cast<long long>(e) * a.chunks;
+      int run = 0;
+      for (int c0 = 0; c0 < a.chunks; c0 += 32) {
+        const int c = c0 + lane;
+        const int v = c < a.chunks ? __ldcg(row + c) : 0;
+        const int incl = warp_inclusive_scan(v, lane);
+        if (c < a.chunks) row[c] = run + incl - v;
+        run += __shfl_sync(FULL_MASK, incl, 31);
+      }
+      if (lane == 0) a.tokens_per_expert[e] = run;
+    }
+    if (!grid_barrier(a.barrier, 2 * gridDim.x, a.status, &s_ok)) return;
+    if constexpr (MODE == LAYOUT_COUNT) {
+      if (blockIdx.x != 0) return;
     }
   }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int seg = e >> 5, bit = e & 31;
-    uint32_t m = 0;
-#pragma unroll 8
-    for (int tl = 0; tl < LAYOUT_CHUNK; ++tl) m |= ((s_emask[tl * EW + seg] >> bit) & 1u) << tl;
-    s_tmask[e] = m;
+
+  // Padded offsets; thread i owns experts 4i .. 4i + 3 (E <= 4 * blockDim.x).
+  {
+    int cnt[4], pad[4], psum = 0, nsum = 0;
+#pragma unroll
+    for (int d = 0; d < 4; ++d) {
+      const int e = 4 * threadIdx.x + d;
+      cnt[d] = e < E ? __ldcg(a.tokens_per_expert + e) : 0;
+      pad[d] = ((cnt[d] + a.P - 1) / a.P) * a.P;
+      psum += pad[d];
+      nsum += cnt[d];
+    }
+    int R;
+    int excl = block_exclusive_scan(psum, s_warp, &R);
+#pragma unroll
+    for (int d = 0; d < 4; ++d) {
+      const int e = 4 * threadIdx.x + d;
+      if (e < E) s_off[e] = excl;
+      excl += pad[d];
+    }
+    if (threadIdx.x == 0) s_off[E] = R;
+    if (MODE != LAYOUT_PLACE && blockIdx.x == 0) {
+      __syncthreads();
+      int N;
+      block_exclusive_scan(nsum, s_warp, &N);
+      for (int e = threadIdx.x; e <= E; e += blockDim.x) a.offsets[e] = s_off[e];
+      if (threadIdx.x == 0) {
+        a.totals[0] = R;
+        a.totals[1] = N;
+        if (R > a.capacity) report(a.status, MOE_DEVERR_CAPACITY);
+      }
+    }
+    __syncthreads();
   }
-  __syncthreads();
-  const uint32_t lt = (1u << lane) - 1u;
-  for (int tl = warp; tl < nt; tl += nwarps) {
-    const long long t = t0 + tl;
-    const uint32_t below_t = (1u << tl) - 1u;
-    int j_base = 0;
-    for (int seg = 0; seg < EW; ++seg) {
-      const uint32_t em = s_emask[tl * EW + seg];
-      const int e = seg * 32 + lane;
-      if ((em >> lane) & 1u) {
-        const long long row = static_cast<long long>(s_base[e]) + __popc(s_tmask[e] & below_t);
-        const int j = j_base + __popc(em & lt);
-        if (row < capacity && j < K) {
-          row_token[row] = static_cast<int>(t);
-          row_expert[row] = e;
-          row_weight[row] = probs[t * E + e];
-          token_row[t * K + j] = static_cast<int>(row);
-        } else {
-          report(status, row < capacity ? MOE_DEVERR_BAD_INDEX : MOE_DEVERR_CAPACITY);
+  if constexpr (MODE != LAYOUT_COUNT) {
+    for (int c = blockIdx.x; c < a.chunks; c += gridDim.x) {
+      const long long t0 = static_cast<long long>(c) * LAYOUT_CHUNK;
+      const int nt = static_cast<int>(min(static_cast<long long>(LAYOUT_CHUNK), a.T - t0));
+      const uint32_t* words = reinterpret_cast<const uint32_t*>(a.map + t0 * E);
+      for (int i = threadIdx.x; i < nt * E4; i += blockDim.x) s_map32[i] = words[i];
+      __syncthreads();
+      for (int tl = warp; tl < LAYOUT_CHUNK; tl += nwarps) {
+        for (int seg = 0; seg < EW; ++seg) {
+          const int e = seg * 32 + lane;
+          const bool b = tl < nt && e < E && s_map[tl * E + e] != 0;
+          const uint32_t m = __ballot_sync(FULL_MASK, b);
+          if (lane == 0) s_emask[tl * EW + seg] = m;
         }
       }
-      j_base += __popc(em);
+      __syncthreads();  // the map's space now holds s_tmask and s_base
+      for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int seg = e >> 5, bit = e & 31;
+        uint32_t m = 0;
+  #pragma unroll 8
+        for (int tl = 0; tl < LAYOUT_CHUNK; ++tl) m |= ((s_emask[tl * EW + seg] >> bit) & 1u) << tl;
+        s_tmask[e] = m;
+        s_base[e] = s_off[e] + __ldcg(a.chunk_counts + static_cast<long long>(e) * a.chunks + c);
+      }
+      __syncthreads();
+      // One thread per (token, slot j): slot j of a token is the token's j-th
+      // expert in ascending order.  Every load of the chunk is issued at once.
+      for (int i = threadIdx.x; i < nt * a.K; i += blockDim.x) {
+        const int tl = i / a.K, j = i - tl * a.K;
+        const long long t = t0 + tl;
+        const uint32_t* em = s_emask + tl * EW;
+        int seg = 0, below = 0, n = __popc(em[0]);
+        while (below + n <= j && seg + 1 < EW) {
+          below += n;
+          n = __popc(em[++seg]);
+        }
+        int row_out = -1;
+        if (below + n > j) {
+          uint32_t m = em[seg];
+          for (int k = j - below; k > 0; --k) m &= m - 1u;  // drop the lower set bits
+          const int e = seg * 32 + __ffs(m) - 1;
+          const long long row = static_cast<long long>(s_base[e]) + __popc(s_tmask[e] & ((1u << tl) - 1u));
+          if (row < a.capacity) {
+            a.row_token[row] = static_cast<int>(t);
+            a.row_expert[row] = e;
+            a.row_weight[row] = __ldg(a.probs + t * E + e);
+            row_out = static_cast<int>(row);
+          } else {
+            report(a.status, MOE_DEVERR_CAPACITY);
+          }
+        }
+        a.token_row[t * a.K + j] = row_out;
+        if (j == 0) {  // more experts than slots: a routing_map that no top-k could make
+          int total = 0;
+          for (int w = 0; w < EW; ++w) total += __popc(em[w]);
+          if (total > a.K) report(a.status, MOE_DEVERR_BAD_INDEX);
+        }
+      }
+      __syncthreads();  // before the next chunk overwrites the shared arrays
     }
-    for (int j = j_base + lane; j < K; j += 32) token_row[t * K + j] = -1;
   }
 }
 
@@ -246,8 +307,11 @@ __global__ void __launch_bounds__(256) row_scatter_kernel(
     if (it < T) {
       const long long t = it;
       const uint4* s = reinterpret_cast<const uint4*>(src + t * H);
+      // The token's rows, 32 slots per load (a token's valid slots come first).
+      int r_lane = -1;
       for (int j = 0; j < K; ++j) {
-        const int r = __ldg(token_row + t * K + j);
+        if ((j & 31) == 0) r_lane = j + lane < K ? __ldg(token_row + t * K + j + lane) : -1;
+        const int r = __shfl_sync(FULL_MASK, r_lane, j & 31);
         if (r < 0) break;
         uint4* d = reinterpret_cast<uint4*>(dst + static_cast<long long>(r) * H);
         const uint4* o = DOT ? reinterpret_cast<const uint4*>(o_save + static_cast<long long>(r) * H) : nullptr;
@@ -317,31 +381,92 @@ __global__ void __launch_bounds__(256) row_scatter_kernel(
 
 }  // namespace
 
-cudaError_t launch_layout_counts(const uint8_t* routing_map, const moe_layout& L,
-                                 int* chunk_counts, cudaStream_t s) {
-  const int chunks = static_cast<int>(layout_chunks(L.T));
-  if (chunks > 0) {
-    layout_count_kernel<<<chunks, 256, L.E * sizeof(int), s>>>(routing_map, L.T, L.E, chunks,
-                                                                chunk_counts);
-  }
-  if (chunks > 0) layout_expert_scan_kernel<<<L.E, 256, 0, s>>>(chunk_counts, chunks, L.tokens_per_expert);
-  else cudaMemsetAsync(L.tokens_per_expert, 0, L.E * sizeof(int), s);
-  layout_offsets_kernel<<<1, 1024, 0, s>>>(L.tokens_per_expert, L.E, L.pad_multiple, L.capacity,
-                                           L.offsets, L.totals, L.status);
-  return cudaGetLastError();
+namespace {
+
+size_t layout_smem_bytes(int E) {
+  return static_cast<size_t>(LAYOUT_CHUNK) * E +
+         static_cast<size_t>(LAYOUT_CHUNK) * ((E + 31) / 32) * sizeof(uint32_t) +
+         static_cast<size_t>(E + 1) * sizeof(int);
 }
 
-cudaError_t launch_layout_place(const uint8_t* routing_map, const float* probs,
-                                const moe_layout& L, const int* chunk_base, cudaStream_t s) {
-  const int chunks = static_cast<int>(layout_chunks(L.T));
-  if (chunks == 0) return cudaSuccess;
-  const size_t smem = static_cast<size_t>(LAYOUT_CHUNK) * L.E +
-                      static_cast<size_t>(LAYOUT_CHUNK) * ((L.E + 31) / 32) * sizeof(uint32_t) +
-                      static_cast<size_t>(L.E) * (sizeof(uint32_t) + sizeof(int));
-  layout_place_kernel<<<chunks, 256, smem, s>>>(routing_map, probs, L.T, L.E, L.K, chunks,
-                                                chunk_base, L.offsets, L.capacity, L.row_token,
-                                                L.row_expert, L.row_weight, L.token_row, L.status);
-  return cudaGetLastError();
+// CTAs of layout_kernel<MODE> resident at once on the current device with
+// `smem` bytes of dynamic shared memory (the last answer is kept per thread).
+template <int MODE>
+int layout_resident_ctas(size_t smem) {
+  static thread_local int last_dev = -1;
+  static thread_local size_t last_smem = 0;
+  static thread_local int last_ctas = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev == last_dev && smem == last_smem) return last_ctas;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layout_kernel<MODE>, 256, smem) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  last_dev = dev;
+  last_smem = smem;
+  last_ctas = per_sm * sm_count();
+  return last_ctas;
+}
+
+template <int MODE>
+cudaError_t launch_layout_mode(const LayoutArgs& a, size_t smem, cudaStream_t s) {
+  if (MODE == LAYOUT_PLACE) {
+    if (a.chunks == 0) return cudaSuccess;
+    layout_kernel<MODE><<<a.chunks, 256, smem, s>>>(a);
+    return cudaGetLastError();
+  }
+  cudaError_t err = cudaMemsetAsync(a.barrier, 0, sizeof(unsigned), s);
+  if (err != cudaSuccess) return err;
+  // Enough CTAs for one chunk each (phases 1 and 4) and one warp per expert
+  // (phase 2), but never more than can be resident at once.
+  const int want = a.chunks > (a.E + 7) / 8 ? a.chunks : (a.E + 7) / 8;
+  const int resident = layout_resident_ctas<MODE>(smem);
+  const int grid = want < resident ? want : resident;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid > 0 ? grid : 1);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, layout_kernel<MODE>, a);
+}
+
+}  // namespace
+
+cudaError_t launch_layout(const uint8_t* routing_map, const float* probs, const moe_layout& L,
+                          void* workspace, LayoutStep step, cudaStream_t s) {
+  LayoutArgs a;
+  a.map = routing_map;
+  a.probs = probs;
+  a.T = L.T;
+  a.E = L.E;
+  a.K = L.K;
+  a.P = L.pad_multiple;
+  a.chunks = static_cast<int>(layout_chunks(L.T));
+  a.capacity = L.capacity;
+  a.chunk_counts = static_cast<int*>(workspace);
+  a.barrier = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) +
+                                          layout_counter_bytes(L.T, L.E));
+  a.tokens_per_expert = L.tokens_per_expert;
+  a.offsets = L.offsets;
+  a.totals = L.totals;
+  a.row_token = L.row_token;
+  a.row_expert = L.row_expert;
+  a.row_weight = L.row_weight;
+  a.token_row = L.token_row;
+  a.status = L.status;
+  const size_t smem = layout_smem_bytes(L.E);
+  switch (step) {
+    case LayoutStep::kAll: return launch_layout_mode<LAYOUT_ALL>(a, smem, s);
+    case LayoutStep::kCounts: return launch_layout_mode<LAYOUT_COUNT>(a, smem, s);
+    case LayoutStep::kPlace: return launch_layout_mode<LAYOUT_PLACE>(a, smem, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_row_gather(const uint16_t* src, const moe_layout& L, int H, uint16_t* dst,

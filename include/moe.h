@@ -174,7 +174,8 @@ MOE_API moe_status moe_dispatch(const moe_bf16* x, const uint8_t* routing_map, c
  * Arguments, results and errors are those of moe_dispatch, except that
  * L->workspace is ignored (it may be NULL): the per-chunk expert counters
  * live in a static device array inside the library, MOE_STATIC_SCRATCH_INTS
- * int32 (1 MiB) per GPU, held from library load until the process exits.
+ * int32 (1 MiB, plus 256 bytes for a barrier counter) per GPU, held from
+ * library load until the process exits.
  *   - Limit: E * ceil(T / 32) <= MOE_STATIC_SCRATCH_INTS (E = 128 allows
  *     T <= 65536); larger sizes return MOE_ERR_UNSUPPORTED_SHAPE before any
  *     work is queued.

@@ -72,6 +72,8 @@ def _check_layout(g, idx, p, E, P, capacity):
     (300, 1024, 4, 1, 0.0, 0.0),    # the largest E
     (40, 8, 1, 3, 0.0, 0.0),        # topk = 1
     (33, 4, 4, 2, 0.0, 0.0),        # K = E
+    (0, 8, 2, 16, 0.0, 0.0),        # no tokens
+    (40000, 128, 8, 4, 0.05, 0.0),  # 1250 chunks: more than the layout kernel's resident CTAs
 ])
 @pytest.mark.parametrize("host_sync", [True, False])
 def test_multihot_and_layout(moe, T, E, K, P, drop, dup, host_sync):
@@ -302,9 +304,13 @@ def test_backward_gathers(moe, T, H, E, K, I, P, drop):
     # a8 against the fp64 oracle on the same o_save
     gw_ref = O.routing_weight_grad(bits(grad_y), bits(fwd.o), re, E).astype(np.float64)
     gw = grad_w.cpu().numpy().astype(np.float64)
-    scale = np.abs(O.bf16_bits_to_f64(bits(grad_y)) * O.bf16_bits_to_f64(bits(fwd.o))).sum(axis=1)
-    assert np.all(np.abs(gw - gw_ref) <= 1e-5 * scale + 1e-30)
-    assert np.all(gw[rt < 0] == 0)
+    # valid rows within the fp32 bound; on pad and spare rows the weight
+    # gradient is exactly 0 (the experts never write o there, so o may hold
+    # anything and is not read)
+    v = rt >= 0
+    scale = np.abs(O.bf16_bits_to_f64(bits(grad_y)[v]) * O.bf16_bits_to_f64(bits(fwd.o)[v])).sum(axis=1)
+    assert np.all(np.abs(gw[v] - gw_ref[v]) <= 1e-5 * scale + 1e-30)
+    assert np.all(gw[~v] == 0)
     # a10 (+scatter) bit-exact given the same grad_x_disp and grad_w
     gxd = torch.randn(C, H, generator=torch.Generator().manual_seed(2)).to(torch.bfloat16)
     gxd_np = bits(gxd)
