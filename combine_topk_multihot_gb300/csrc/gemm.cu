@@ -40,18 +40,31 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128;          // rows per tile (tensor-memory lanes)
-constexpr int BN = 256;          // accumulator columns per tile
 constexpr int BK = 64;           // bf16 elements per 128-byte swizzled row
 constexpr int UMMA_K = 16;       // K per tcgen05.mma for 16-bit inputs
-constexpr int A_BYTES = BM * BK * 2;           // 16 KiB
-constexpr int B_BYTES = BN * BK * 2;           // 32 KiB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES; // 48 KiB
 constexpr int EPI_WARPS = 8;                   // two per TMEM lane quarter
 constexpr int NUM_THREADS = 32 * (2 + EPI_WARPS);
-constexpr int TMEM_COLS = 2 * BN;              // double-buffered accumulator
-constexpr int MAX_STAGES = 4;
+constexpr int MAX_STAGES = 16;                 // barrier slots (the ring uses up to this many)
 constexpr int SMEM_LIMIT = 232448;             // dynamic shared memory per CTA
-constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+
+// Tile shape.  BN (accumulator columns) is 256 in general, and 64 when the
+// layer has too few rows to give every SM a 256-column tile (decode), so
+// that four times as many CTAs stream the weights.  A_ROWS is how many rows
+// of A a stage loads: 128, or 32 when no tile can have more than 32 rows to
+// store.  The MMA always reads 128 rows; with A_ROWS = 32 the other 96 are
+// whatever bytes follow in shared memory and only feed accumulator rows that
+// are never stored.  The smaller A slot leaves room for more stages, i.e.
+// more weight bytes in flight per SM, which is what bounds a decode step.
+template <int BN, int A_ROWS>
+struct Fwd {
+  static constexpr int A_BYTES = A_ROWS * BK * 2;        // 16 KiB at A_ROWS = 128
+  static constexpr int B_BYTES = BN * BK * 2;            // 32 KiB at BN = 256
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KiB at BN = 256, A_ROWS = 128
+  static constexpr int TMEM_COLS = 2 * BN;               // double-buffered accumulator
+  // ring depth (one less when the per-expert tables of a large E need the room)
+  static constexpr int STAGES = BN == 256 ? 4 : (A_ROWS == 128 ? 8 : 16);
+  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+};
 
 enum Epilogue { EPI_SWIGLU = 0, EPI_WEIGHTED = 1 };
 
@@ -90,8 +103,8 @@ struct Smem {
 // Epilogue staging for TMA stores: per epilogue warp, two 32 x 32 bf16 boxes.
 constexpr int STAGING_BYTES = EPI_WARPS * 2 * 32 * 64;
 
-constexpr size_t smem_bytes(int stages, int E) {
-  return 1024 /*alignment slack*/ + static_cast<size_t>(stages) * STAGE_BYTES + STAGING_BYTES +
+constexpr size_t smem_bytes(int stages, int stage_bytes, int E) {
+  return 1024 /*alignment slack*/ + static_cast<size_t>(stages) * stage_bytes + STAGING_BYTES +
          sizeof(Smem) + static_cast<size_t>(3 * E + 2) * sizeof(int);
 }
 
@@ -115,11 +128,16 @@ __device__ __forceinline__ Tile decode_tile(const int* tile_prefix, int E, int n
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
 
-template <int EPI, int STAGES>
+template <int EPI, int BN, int A_ROWS, int STAGES>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmOut, const GemmArgs args) {
+  static_assert(STAGES <= MAX_STAGES, "barrier slots");
+  using F = Fwd<BN, A_ROWS>;
+  constexpr int A_BYTES = F::A_BYTES, B_BYTES = F::B_BYTES, STAGE_BYTES = F::STAGE_BYTES;
+  constexpr int TMEM_COLS = F::TMEM_COLS;
+  constexpr uint32_t IDESC = F::IDESC;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* tiles = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -295,10 +313,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       warp_row0 = s_off[t.e] + t.mt * BM + q * 32;
       const uint32_t tb = tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
       if (EPI == EPI_SWIGLU) {
-        // columns [0,128) gate, [128,256) up, for h columns nt*128 + [0,128)
-        const int col0 = t.nt * (BN / 2);
+        // columns [0, BN/2) gate, [BN/2, BN) up, for h columns nt*BN/2 + [0, BN/2);
+        // each column half of the epilogue takes half of them (at BN = 64
+        // there are only 32: the first half takes them)
+        constexpr int H_COLS = BN / 2;
+        constexpr int PER_HALF = H_COLS >= 64 ? H_COLS / 2 : H_COLS;
+        const int col0 = t.nt * H_COLS;
+        const int c_end = (half + 1) * PER_HALF < H_COLS ? (half + 1) * PER_HALF : H_COLS;
 #pragma unroll 1
-        for (int c = half * (BN / 4); c < (half + 1) * (BN / 4); c += 32) {
+        for (int c = half * PER_HALF; c < c_end; c += 32) {
           uint32_t g[32], u[32];
           __syncwarp();
           tmem_ld32(tb + c, g);
@@ -390,13 +413,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // ---------------------------------------------------------------- host side
 
-// A row-major bf16 matrix [rows, cols] read as 128-row x 64-column boxes with
-// the 128-byte swizzle; out-of-range rows read as zero.
-bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols) {
-  return make_tma_2d_bf16(map, base, rows, cols, 128);
-}
-
-template <int EPI, int STAGES>
+template <int EPI, int BN, int A_ROWS, int STAGES>
 cudaError_t launch_gemm_stages(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
                                const GemmArgs& args, cudaStream_t s) {
   static bool configured[64] = {};
@@ -404,37 +421,40 @@ cudaError_t launch_gemm_stages(const CUtensorMap& a, const CUtensorMap& b, const
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    err = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, STAGES>,
+    err = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, BN, A_ROWS, STAGES>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  grouped_gemm_kernel<EPI, STAGES><<<sm_count(), NUM_THREADS, smem_bytes(STAGES, args.E), s>>>(
-      a, b, out, args);
+  grouped_gemm_kernel<EPI, BN, A_ROWS, STAGES>
+      <<<sm_count(), NUM_THREADS, smem_bytes(STAGES, Fwd<BN, A_ROWS>::STAGE_BYTES, args.E), s>>>(
+          a, b, out, args);
   return cudaGetLastError();
 }
 
-// Four pipeline stages when they fit beside the staging and the per-expert
-// tables (E up to about 200), else three.
-template <int EPI>
+// The ring depth of Fwd when it fits beside the staging and the per-expert
+// tables, else one stage less (E above about 200).
+template <int EPI, int BN, int A_ROWS>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
                         const GemmArgs& args, cudaStream_t s) {
-  if (smem_bytes(4, args.E) <= static_cast<size_t>(SMEM_LIMIT))
-    return launch_gemm_stages<EPI, 4>(a, b, out, args, s);
-  return launch_gemm_stages<EPI, 3>(a, b, out, args, s);
+  using F = Fwd<BN, A_ROWS>;
+  if (smem_bytes(F::STAGES, F::STAGE_BYTES, args.E) <= static_cast<size_t>(SMEM_LIMIT))
+    return launch_gemm_stages<EPI, BN, A_ROWS, F::STAGES>(a, b, out, args, s);
+  return launch_gemm_stages<EPI, BN, A_ROWS, F::STAGES - 1>(a, b, out, args, s);
 }
 
-}  // namespace
-
-cudaError_t launch_experts_forward(const uint16_t* x_disp, const moe_layout& L, int H, int I,
-                                   const uint16_t* W1, const uint16_t* W2, uint16_t* h,
-                                   uint16_t* y, uint16_t* o_save, uint16_t* gu_save,
-                                   cudaStream_t s) {
-  if (L.capacity == 0) return cudaSuccess;
+template <int BN, int A_ROWS>
+cudaError_t experts_forward(const uint16_t* x_disp, const moe_layout& L, int H, int I,
+                            const uint16_t* W1, const uint16_t* W2, uint16_t* h, uint16_t* y,
+                            uint16_t* o_save, uint16_t* gu_save, cudaStream_t s) {
   const uint64_t C = static_cast<uint64_t>(L.capacity);
+  // B is loaded as two boxes of BN/2 rows: the gate and up rows (GEMM1) or
+  // the two halves of the tile's output columns (GEMM2).
   CUtensorMap mA1, mB1, mA2, mB2, mH, mY;
-  if (!make_map(&mA1, x_disp, C, H) || !make_map(&mB1, W1, static_cast<uint64_t>(L.E) * 2 * I, H) ||
-      !make_map(&mA2, h, C, I) || !make_map(&mB2, W2, static_cast<uint64_t>(L.E) * H, I) ||
+  if (!make_tma_2d_bf16(&mA1, x_disp, C, H, A_ROWS) ||
+      !make_tma_2d_bf16(&mB1, W1, static_cast<uint64_t>(L.E) * 2 * I, H, BN / 2) ||
+      !make_tma_2d_bf16(&mA2, h, C, I, A_ROWS) ||
+      !make_tma_2d_bf16(&mB2, W2, static_cast<uint64_t>(L.E) * H, I, BN / 2) ||
       !make_tma_store_2d_bf16(&mH, h, C, I) || !make_tma_store_2d_bf16(&mY, y, C, H))
     return cudaErrorInvalidValue;
 
@@ -455,7 +475,7 @@ cudaError_t launch_experts_forward(const uint16_t* x_disp, const moe_layout& L, 
   g1.I = I;
   g1.write_pad = gu_save != nullptr;  // training: the backward reads the pad rows
   g1.status = L.status;
-  cudaError_t err = launch_gemm<EPI_SWIGLU>(mA1, mB1, mH, g1, s);
+  cudaError_t err = launch_gemm<EPI_SWIGLU, BN, A_ROWS>(mA1, mB1, mH, g1, s);
   if (err != cudaSuccess) return err;
 
   GemmArgs g2 = g1;
@@ -468,7 +488,29 @@ cudaError_t launch_experts_forward(const uint16_t* x_disp, const moe_layout& L, 
   g2.ld0 = H;
   g2.out1 = o_save;
   g2.ld1 = H;
-  return launch_gemm<EPI_WEIGHTED>(mA2, mB2, mY, g2, s);
+  return launch_gemm<EPI_WEIGHTED, BN, A_ROWS>(mA2, mB2, mY, g2, s);
+}
+
+}  // namespace
+
+cudaError_t launch_experts_forward(const uint16_t* x_disp, const moe_layout& L, int H, int I,
+                                   const uint16_t* W1, const uint16_t* W2, uint16_t* h,
+                                   uint16_t* y, uint16_t* o_save, uint16_t* gu_save,
+                                   cudaStream_t s) {
+  if (L.capacity == 0) return cudaSuccess;
+  // At most min(E, T*K) experts have rows.  When even one 128-row tile per
+  // such expert at BN = 256 leaves SMs idle, take 64-column tiles.
+  const long long pairs = static_cast<long long>(L.T) * L.K;
+  const long long active = pairs < L.E ? pairs : L.E;
+  if (active * (I / 128) >= sm_count())
+    return experts_forward<256, 128>(x_disp, L, H, I, W1, W2, h, y, o_save, gu_save, s);
+  // An expert has at most T rows (one per token); with the pad rows written
+  // (training) its group is T rounded up to pad_multiple.
+  const long long P = L.pad_multiple;
+  const long long stored = gu_save ? (L.T + P - 1) / P * P : L.T;
+  if (stored <= 32)
+    return experts_forward<64, 32>(x_disp, L, H, I, W1, W2, h, y, o_save, gu_save, s);
+  return experts_forward<64, 128>(x_disp, L, H, I, W1, W2, h, y, o_save, gu_save, s);
 }
 
 }  // namespace moe

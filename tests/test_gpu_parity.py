@@ -178,6 +178,10 @@ def _experts_case(moe, T, H, E, K, I, P, seed, drop=0.0, save=True):
     (1000, 256, 4, 2, 128, 1),     # several 128-row tiles per expert, unaligned groups
     (5, 1024, 8, 4, 384, 1),       # decode-like: a few rows, long K
     (260, 768, 12, 3, 128, 128),   # padded groups, 3 N tiles in GEMM2
+    # the cases above have few experts with rows, so the GEMMs take 64-column
+    # tiles; these have enough for 256-column tiles on every SM
+    (64, 256, 64, 4, 384, 16),     # 256-column tiles, a few rows per expert
+    (2000, 512, 40, 4, 512, 1),    # 256-column tiles, two 128-row tiles per expert
 ])
 def test_experts_match_oracle(moe, T, H, E, K, I, P):
     idx, p, x, W1, W2, C, fwd = _experts_case(moe, T, H, E, K, I, P, seed=T + H)
