@@ -7,7 +7,8 @@ no code with the CUDA library (no kernels, headers, helpers, tables or
 constants); the only thing both sides share is the seeded input generator in
 ``synthetic``, which holds none of the method's arithmetic.
 
-It is a plain, slow, obviously-correct restatement of what the pages define:
+It is a plain, slow, obviously-correct restatement of what the pages define
+(and, in ``router.py``, of the router step in front of the path):
 
 * "feat: add hybridep (NVIDIA-NeMo/Automodel #1333)" -- the preprocessing
   that maps top-k indices to a multihot ``routing_map`` with fp32 ``probs``
@@ -44,6 +45,7 @@ from .moe_oracle import (OracleIndexError, OracleCapacityError, sentinel_expert,
                          backward_gemms,
                          dispatch_backward, route_to_multihot_backward,
                          layer_forward, layer_backward, worst_case_capacity)
+from .router import router_topk, router_topk_f64, router_topk_backward
 
 __all__ = [
     "bf16_bits_to_f64", "bf16_bits_to_f32", "f64_to_bf16_bits", "f32_to_bf16_bits",
@@ -53,5 +55,6 @@ __all__ = [
     "routing_weight_grad", "expert_backward_f64", "grouped_experts_backward",
     "backward_scale", "backward_gate_up", "backward_swiglu", "backward_gemms",
     "dispatch_backward", "route_to_multihot_backward", "layer_forward",
-    "layer_backward", "worst_case_capacity",
+    "layer_backward", "worst_case_capacity", "router_topk", "router_topk_f64",
+    "router_topk_backward",
 ]
