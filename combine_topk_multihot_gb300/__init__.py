@@ -6,7 +6,8 @@ loudly if the library has not been built -- there is no CPU fallback.
 ``ops`` registers every step as a PyTorch custom operator (``torch.ops.moe_gb300``)
 and ``moe_layer`` is the differentiable layer built from them.
 """
-from .moe import (Layout, MoEError, ForwardResult, worst_case_rows, moe_route_to_multihot,
+from .moe import (Layout, MoEError, ForwardResult, worst_case_rows, moe_router_topk,
+                  moe_router_topk_backward, moe_route_to_multihot,
                   moe_dispatch, moe_grouped_experts, moe_combine, moe_combine_backward,
                   moe_dispatch_backward, moe_route_to_multihot_backward, moe_layer_forward,
                   moe_grouped_experts_backward)
@@ -15,7 +16,8 @@ from . import ops
 from .ops import moe_layer
 
 __all__ = [
-    "Layout", "MoEError", "ForwardResult", "worst_case_rows", "moe_route_to_multihot",
+    "Layout", "MoEError", "ForwardResult", "worst_case_rows", "moe_router_topk",
+    "moe_router_topk_backward", "moe_route_to_multihot",
     "moe_dispatch", "moe_grouped_experts", "moe_combine", "moe_combine_backward",
     "moe_dispatch_backward", "moe_route_to_multihot_backward", "moe_layer_forward",
     "moe_grouped_experts_backward", "_native", "ops", "moe_layer",

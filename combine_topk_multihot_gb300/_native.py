@@ -58,6 +58,8 @@ SIGNATURES = {
     "moe_device_check": (c_int32, []),
     "moe_worst_case_rows": (c_int64, [c_int32, c_int32, c_int32, c_int32]),
     "moe_layout_workspace_bytes": (c_int32, [c_int32, c_int32, ctypes.POINTER(c_size_t)]),
+    "moe_router_topk": (c_int32, [_P, c_int32, c_int32, c_int32, _P, _P, _P, _P, _P, _P]),
+    "moe_router_topk_backward": (c_int32, [_P, _P, _P, c_int32, c_int32, c_int32, _P, _P]),
     "moe_route_to_multihot": (c_int32, [_P, _P, c_int32, c_int32, c_int32, _P, _P, _P, _P, _P]),
     "moe_dispatch": (c_int32, [_P, _P, _P, c_int32, _LP, _P, ctypes.POINTER(c_int64), _P]),
     "moe_dispatch_static_scratch": (c_int32, [_P, _P, _P, c_int32, _LP, _P, ctypes.POINTER(c_int64), _P]),

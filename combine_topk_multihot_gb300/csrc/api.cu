@@ -272,6 +272,39 @@ moe_status moe_dispatch_backward(const moe_bf16* grad_x_disp, const float* grad_
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_dispatch_backward launch");
 }
 
+moe_status moe_router_topk(const float* logits, int32_t T, int32_t E, int32_t K, int64_t* topk_idx,
+                           float* topk_probs, uint8_t* routing_map, float* probs,
+                           int8_t* winner_slot, moe_stream_t stream) {
+  moe_status st = check_routing_shape(T, K, E);
+  if (st != MOE_OK) return st;
+  MOE_REQUIRE(T == 0 || (logits && topk_idx && topk_probs), MOE_ERR_INVALID_ARG,
+              "moe_router_topk: NULL logits or top-k output");
+  const bool mh = routing_map || probs || winner_slot;
+  MOE_REQUIRE(!mh || (routing_map && probs && winner_slot), MOE_ERR_INVALID_ARG,
+              "moe_router_topk: give all three multihot outputs or none");
+  MOE_REQUIRE(aligned16(routing_map) && aligned16(probs) && aligned16(winner_slot),
+              MOE_ERR_INVALID_ARG, "moe_router_topk: multihot outputs must be 16-byte aligned");
+  if ((st = check_device()) != MOE_OK) return st;
+  cudaError_t err = launch_router_topk(logits, T, K, E, topk_idx, topk_probs,
+                                       mh ? routing_map : nullptr, probs, winner_slot, stream);
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_router_topk launch");
+}
+
+moe_status moe_router_topk_backward(const float* grad_topk_probs, const float* topk_probs,
+                                    const int64_t* topk_idx, int32_t T, int32_t E, int32_t K,
+                                    float* grad_logits, moe_stream_t stream) {
+  moe_status st = check_routing_shape(T, K, E);
+  if (st != MOE_OK) return st;
+  MOE_REQUIRE(T == 0 || (grad_topk_probs && topk_probs && topk_idx && grad_logits),
+              MOE_ERR_INVALID_ARG, "moe_router_topk_backward: NULL pointer");
+  MOE_REQUIRE(aligned16(grad_logits), MOE_ERR_INVALID_ARG,
+              "moe_router_topk_backward: grad_logits must be 16-byte aligned");
+  if ((st = check_device()) != MOE_OK) return st;
+  cudaError_t err = launch_router_topk_backward(grad_topk_probs, topk_probs, topk_idx, T, K, E,
+                                                grad_logits, stream);
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_router_topk_backward launch");
+}
+
 moe_status moe_route_to_multihot_backward(const float* grad_probs, const int64_t* topk_idx,
                                           const int8_t* winner_slot, int32_t T, int32_t K,
                                           int32_t E, float* grad_topk_probs, moe_stream_t stream) {

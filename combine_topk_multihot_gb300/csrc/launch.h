@@ -36,6 +36,14 @@ inline int64_t layout_chunks(int32_t T) { return (T + LAYOUT_CHUNK - 1) / LAYOUT
 cudaError_t launch_multihot(const int64_t* topk_idx, const float* topk_probs, int T, int K, int E,
                             uint8_t* routing_map, float* probs, int8_t* winner, int* status,
                             cudaStream_t s);
+// Router: softmax -> top-K -> renormalise per token; with routing_map also
+// the multihot outputs (probs and winner then non-NULL too).
+cudaError_t launch_router_topk(const float* logits, int T, int K, int E, int64_t* topk_idx,
+                               float* topk_probs, uint8_t* routing_map, float* probs,
+                               int8_t* winner, cudaStream_t s);
+cudaError_t launch_router_topk_backward(const float* grad_w, const float* w,
+                                        const int64_t* topk_idx, int T, int K, int E,
+                                        float* grad_logits, cudaStream_t s);
 cudaError_t launch_multihot_backward(const float* grad_probs, const int64_t* topk_idx,
                                      const int8_t* winner, int T, int K, int E, float* grad_topk,
                                      cudaStream_t s);

@@ -118,6 +118,33 @@ class Layout:
         return self
 
 
+def moe_router_topk(logits: torch.Tensor, K: int, multihot: bool = False, stream=None):
+    """r0: softmax -> top-K -> renormalise.  Returns (topk_idx int64 [T, K],
+    topk_probs fp32 [T, K]), plus (routing_map, probs, winner_slot) of the
+    multihot step when ``multihot`` (written by the same kernel)."""
+    T, E = logits.shape
+    if logits.dtype != torch.float32:
+        raise TypeError("logits must be float32")
+    dev = logits.device
+    idx = torch.empty(T, K, dtype=torch.int64, device=dev)
+    w = torch.empty(T, K, dtype=torch.float32, device=dev)
+    mh = (torch.empty(T, E, dtype=torch.uint8, device=dev), torch.empty(T, E, dtype=torch.float32, device=dev),
+          torch.empty(T, E, dtype=torch.int8, device=dev)) if multihot else (None, None, None)
+    _check(N.lib.moe_router_topk(_ptr(logits), T, E, K, _ptr(idx), _ptr(w), _ptr(mh[0]), _ptr(mh[1]),
+                                 _ptr(mh[2]), _stream(stream)), "moe_router_topk")
+    return (idx, w) + (mh if multihot else ())
+
+
+def moe_router_topk_backward(grad_topk_probs: torch.Tensor, topk_probs: torch.Tensor,
+                             topk_idx: torch.Tensor, E: int, stream=None):
+    """r0 backward: grad_logits fp32 [T, E]."""
+    T, K = topk_idx.shape
+    g = torch.empty(T, E, dtype=torch.float32, device=topk_idx.device)
+    _check(N.lib.moe_router_topk_backward(_ptr(grad_topk_probs), _ptr(topk_probs), _ptr(topk_idx), T, E, K,
+                                          _ptr(g), _stream(stream)), "moe_router_topk_backward")
+    return g
+
+
 def moe_route_to_multihot(topk_idx: torch.Tensor, topk_probs: torch.Tensor, E: int,
                           status: torch.Tensor, stream=None):
     """a1: returns (routing_map uint8 [T,E], probs fp32 [T,E], winner_slot int8 [T,E])."""

@@ -120,6 +120,40 @@ typedef struct moe_layout {
 MOE_API moe_status moe_layout_workspace_bytes(int32_t T, int32_t E, size_t* bytes);
 
 /*
+ * r0. The router in front of the path: per token, a softmax over the E
+ * logits, the K most probable experts, and their probabilities renormalised
+ * to sum to one.  The pages begin the path at its output (top-k indices and
+ * fp32 weights; [HEP] Changelog); the three steps are the workload's router
+ * recipe.
+ *   logits       [T, E] fp32, finite (a NaN counts as -inf; a token whose
+ *                chosen logits are all -inf gets NaN weights).
+ *   topk_idx     [T, K] int64 (out): experts in descending probability; equal
+ *                logits are ordered by ascending expert index.
+ *   topk_probs   [T, K] fp32  (out): the renormalised weights, which equal the
+ *                softmax of the K chosen logits.
+ *   routing_map, probs, winner_slot: NULL, or all three given: then the call
+ *                also writes the multihot outputs of moe_route_to_multihot
+ *                for these top-k choices (16-byte aligned), in the same
+ *                kernel.
+ * Errors: MOE_ERR_UNSUPPORTED_SHAPE unless E % 4 == 0, E <= 1024 and
+ * 1 <= K <= min(E, 127); MOE_ERR_INVALID_ARG for NULL or misaligned buffers.
+ * Every output is caller-owned device memory; nothing is allocated.
+ */
+MOE_API moe_status moe_router_topk(const float* logits, int32_t T, int32_t E, int32_t K,
+                                   int64_t* topk_idx, float* topk_probs, uint8_t* routing_map,
+                                   float* probs, int8_t* winner_slot, moe_stream_t stream);
+
+/*
+ * r0 backward.  grad_logits [T, E] fp32 (out, 16-byte aligned):
+ *   w_j * (g_j - sum_k w_k g_k) at each chosen expert j (w = topk_probs,
+ *   g = grad_topk_probs), 0 at the others -- the chain rule through the
+ *   softmax of the chosen logits; the selection passes no gradient.
+ */
+MOE_API moe_status moe_router_topk_backward(const float* grad_topk_probs, const float* topk_probs,
+                                            const int64_t* topk_idx, int32_t T, int32_t E,
+                                            int32_t K, float* grad_logits, moe_stream_t stream);
+
+/*
  * a1. Top-k -> multihot.  [HEP] Changelog (the HybridEP preprocessing turns
  * top-k indices into multihot routing metadata) and the review of dispatch()
  * (probs are fp32).

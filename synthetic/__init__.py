@@ -8,7 +8,10 @@ CPU oracle can take their inputs from here without sharing any of the method.
 The router that produces top-k choices is the step *before* the path
 (softmax over router logits, top-k, renormalise), as in the MoE layers that
 "feat: add hybridep (NVIDIA-NeMo/Automodel #1333)" wires up: the path starts at
-the top-k expert indices and their fp32 probabilities.
+the top-k expert indices and their fp32 probabilities.  make_routing applies
+that recipe with torch's CPU softmax and top-k to draw the inputs of the path
+itself.  The library's own router kernel is checked against the separate
+router oracle on logits from make_logits, never against make_routing.
 
 Shapes follow the layer shapes of "Add the deepep expert-parallel
 implementation (huggingface/transformers #49638)", Benchmarks: "30b" is the
@@ -64,6 +67,20 @@ def make_tokens(T: int, H: int, seed: int, device="cpu") -> torch.Tensor:
     return torch.randn(T, H, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
 
 
+def _draw_logits(g, T: int, E: int, zipf_s: float):
+    logits = torch.randn(T, E, generator=g, dtype=torch.float32)
+    if zipf_s:
+        bias = -zipf_s * torch.log(torch.arange(1, E + 1, dtype=torch.float32))
+        logits = logits + bias
+    return logits
+
+
+def make_logits(T: int, E: int, seed: int, zipf_s: float = 0.0) -> torch.Tensor:
+    """Router logits fp32 [T, E] ~ N(0,1) [+ log-Zipf bias], on the CPU: the
+    same draw make_routing starts from, as input for the router step."""
+    return _draw_logits(_gen(seed * 1000 + 2), T, E, zipf_s).contiguous()
+
+
 def make_routing(T: int, E: int, K: int, seed: int, zipf_s: float = 0.0, drop: float = 0.0):
     """Router choices: fp32 logits ~ N(0,1) [+ log-Zipf bias], softmax, top-k, renormalise.
 
@@ -74,10 +91,7 @@ def make_routing(T: int, E: int, K: int, seed: int, zipf_s: float = 0.0, drop: f
     topk_probs fp32 [T, K]), on the CPU.
     """
     g = _gen(seed * 1000 + 2)
-    logits = torch.randn(T, E, generator=g, dtype=torch.float32)
-    if zipf_s:
-        bias = -zipf_s * torch.log(torch.arange(1, E + 1, dtype=torch.float32))
-        logits = logits + bias
+    logits = _draw_logits(g, T, E, zipf_s)
     p = torch.softmax(logits, dim=-1)
     vals, idx = torch.topk(p, K, dim=-1)
     vals = vals / vals.sum(dim=-1, keepdim=True)

@@ -62,3 +62,26 @@ def test_validation_rejects_bad_shapes_without_a_gpu(lib):
     st = N.lib.moe_combine(None, ctypes.byref(L), 100, None, None)  # layout pointers NULL
     assert st == N.MOE_ERR_INVALID_ARG
     assert b"NULL" in N.lib.moe_last_error()
+
+
+def test_router_validation_without_a_gpu(lib):
+    """The router entry points check shapes, NULLs and the all-or-none rule
+    for the fused multihot outputs on the host."""
+    from combine_topk_multihot_gb300 import _native as N
+    fake = ctypes.c_void_p(16)        # never dereferenced: validation fails first
+    odd = ctypes.c_void_p(16 + 4)     # not 16-byte aligned
+    # K > E
+    assert N.lib.moe_router_topk(fake, 4, 8, 9, fake, fake, None, None, None, None) == N.MOE_ERR_UNSUPPORTED_SHAPE
+    # E not a multiple of 4, E above 1024
+    assert N.lib.moe_router_topk(fake, 4, 6, 2, fake, fake, None, None, None, None) == N.MOE_ERR_UNSUPPORTED_SHAPE
+    assert N.lib.moe_router_topk(fake, 4, 1028, 2, fake, fake, None, None, None, None) == N.MOE_ERR_UNSUPPORTED_SHAPE
+    # NULL logits with tokens
+    assert N.lib.moe_router_topk(None, 4, 8, 2, fake, fake, None, None, None, None) == N.MOE_ERR_INVALID_ARG
+    # only some of the multihot outputs
+    assert N.lib.moe_router_topk(fake, 4, 8, 2, fake, fake, fake, None, fake, None) == N.MOE_ERR_INVALID_ARG
+    assert b"all three" in N.lib.moe_last_error()
+    # misaligned multihot output
+    assert N.lib.moe_router_topk(fake, 4, 8, 2, fake, fake, odd, fake, fake, None) == N.MOE_ERR_INVALID_ARG
+    # backward: misaligned grad_logits, bad K
+    assert N.lib.moe_router_topk_backward(fake, fake, fake, 4, 8, 2, odd, None) == N.MOE_ERR_INVALID_ARG
+    assert N.lib.moe_router_topk_backward(fake, fake, fake, 4, 8, 0, fake, None) == N.MOE_ERR_UNSUPPORTED_SHAPE
