@@ -13,12 +13,12 @@ from .moe import (Layout, MoEError, ForwardResult, worst_case_rows, moe_router_t
                   moe_grouped_experts_backward)
 from . import _native
 from . import ops
-from .ops import moe_layer
+from .ops import moe_layer, moe_layer_from_logits
 
 __all__ = [
     "Layout", "MoEError", "ForwardResult", "worst_case_rows", "moe_router_topk",
     "moe_router_topk_backward", "moe_route_to_multihot",
     "moe_dispatch", "moe_grouped_experts", "moe_combine", "moe_combine_backward",
     "moe_dispatch_backward", "moe_route_to_multihot_backward", "moe_layer_forward",
-    "moe_grouped_experts_backward", "_native", "ops", "moe_layer",
+    "moe_grouped_experts_backward", "_native", "ops", "moe_layer", "moe_layer_from_logits",
 ]

@@ -6,8 +6,9 @@ dispatch, the combine and the combine's backward become torch.library
 operators, each with a shape-only ("fake") implementation for tracing and an
 autograd rule, and the dispatch handle, which no operator can carry, travels
 between them as its component tensors and is put back together on the far
-side.  Here every step of the layer is such an operator: multihot, dispatch,
-grouped experts, combine, and the four backward steps.
+side.  Here every step of the layer is such an operator: the router (with
+its gradient registered on the operator), multihot, dispatch, grouped
+experts, combine, and the four backward steps.
 
 Every operator takes the sync-free route: the expanded buffers are sized for
 the worst case (T*K + E*(pad_multiple - 1) rows), nothing is read back to the
@@ -45,6 +46,50 @@ def _layout_fake(T, E, K, P, device) -> Tuple[Tensor, ...]:
             torch.empty(C, **i32), torch.empty(C, **i32),
             torch.empty(C, dtype=torch.float32, device=device), torch.empty(T * K, **i32),
             torch.empty(1, **i32))
+
+
+# ------------------------------------------------------------------ router
+@torch.library.custom_op(f"{NS}::router_topk", mutates_args=(), device_types="cuda")
+def router_topk(logits: Tensor, top_k: int) -> Tuple[Tensor, Tensor]:
+    """(topk_idx int64 [T, K], topk_probs fp32 [T, K]): softmax, top-k, renormalise."""
+    return _m.moe_router_topk(logits.contiguous(), top_k)
+
+
+@router_topk.register_fake
+def _(logits, top_k):
+    T = logits.shape[0]
+    return (torch.empty(T, top_k, dtype=torch.int64, device=logits.device),
+            torch.empty(T, top_k, dtype=torch.float32, device=logits.device))
+
+
+@torch.library.custom_op(f"{NS}::router_topk_backward", mutates_args=(), device_types="cuda")
+def router_topk_backward(grad_topk_probs: Tensor, topk_probs: Tensor, topk_idx: Tensor,
+                         num_experts: int) -> Tensor:
+    """grad_logits fp32 [T, E]."""
+    return _m.moe_router_topk_backward(grad_topk_probs.contiguous(), topk_probs, topk_idx, num_experts)
+
+
+@router_topk_backward.register_fake
+def _(grad_topk_probs, topk_probs, topk_idx, num_experts):
+    return torch.empty(topk_idx.shape[0], num_experts, dtype=torch.float32, device=topk_idx.device)
+
+
+def _router_setup(ctx, inputs, output):
+    logits, _ = inputs
+    idx, w = output
+    ctx.save_for_backward(idx, w)
+    ctx.num_experts = logits.shape[1]
+    ctx.mark_non_differentiable(idx)
+
+
+def _router_backward(ctx, grad_idx, grad_w):
+    idx, w = ctx.saved_tensors
+    if grad_w is None:
+        return None, None
+    return torch.ops.moe_gb300.router_topk_backward(grad_w, w, idx, ctx.num_experts), None
+
+
+torch.library.register_autograd(f"{NS}::router_topk", _router_backward, setup_context=_router_setup)
 
 
 # ------------------------------------------------------------------ forward
@@ -238,3 +283,11 @@ def moe_layer(x: Tensor, topk_idx: Tensor, topk_probs: Tensor, W1: Tensor, W2: T
         out = _ops.combine(y, lay, T, K, pad_multiple, E)
         status = lay[-1]
     return (out, status) if return_status else out
+
+
+def moe_layer_from_logits(x: Tensor, router_logits: Tensor, top_k: int, W1: Tensor, W2: Tensor,
+                          pad_multiple: int = 1, return_status: bool = False):
+    """The router (softmax, top-k, renormalise) and the layer; gradients also
+    reach the router logits."""
+    topk_idx, topk_probs = torch.ops.moe_gb300.router_topk(router_logits, top_k)
+    return moe_layer(x, topk_idx, topk_probs, W1, W2, pad_multiple, return_status)

@@ -13,7 +13,9 @@ warm-up replays like eager, and torch.compile(fullgraph=True) matches eager.
 * CUDA graph replay of forward + backward == eager, bit for bit;
 * torch.compile(fullgraph=True) of the layer (the aot_eager backend: the
   trace and the autograd split, with no generated kernels) == eager, bit for bit;
-* a bad expert index is reported in the returned device status word.
+* a bad expert index is reported in the returned device status word;
+* the router in front (moe_layer_from_logits) == router then layer, with the
+  logits' gradient from the router backward.
 """
 import numpy as np
 import pytest
@@ -210,3 +212,42 @@ def test_bad_index_is_reported_in_the_status_word(moe):
                                 return_status=True)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
+
+
+def test_layer_from_logits_equals_router_then_layer(moe):
+    """moe_layer_from_logits == the router's top-k fed to moe_layer, forward
+    and backward, bit for bit; the logits' gradient is the router backward of
+    the layer's top-k gradient; the router op passes opcheck; compiled == eager."""
+    T, H, E, K, I, P = 300, 512, 8, 2, 256, 16
+    x, _, _, W1, W2, g = _inputs(T, H, E, K, I, seed=31)
+    logits = synthetic.make_logits(T, E, seed=31).to(DEV)
+
+    def run(fn):
+        xs = x.detach().clone().requires_grad_(True)
+        ls = logits.detach().clone().requires_grad_(True)
+        W1s = W1.detach().clone().requires_grad_(True)
+        W2s = W2.detach().clone().requires_grad_(True)
+        out = fn(xs, ls, W1s, W2s)
+        out.backward(g)
+        return out.detach(), xs.grad, ls.grad, W1s.grad, W2s.grad
+
+    fused = lambda xs, ls, a, b: moe.moe_layer_from_logits(xs, ls, K, a, b, pad_multiple=P)
+    got = run(fused)
+    idx, w = moe.moe_router_topk(logits, K)
+    ref = _layer(lambda *a: moe.moe_layer(*a, pad_multiple=P), x, idx, w, W1, W2, g)
+    torch.cuda.synchronize()
+    assert torch.equal(got[0].view(torch.int16), ref[0].view(torch.int16))
+    assert torch.equal(got[1].view(torch.int16), ref[1].view(torch.int16))
+    assert torch.equal(got[3].view(torch.int16), ref[3].view(torch.int16))
+    assert torch.equal(got[4].view(torch.int16), ref[4].view(torch.int16))
+    assert torch.equal(got[2], moe.moe_router_topk_backward(ref[2], w, idx, E))
+    torch.library.opcheck(torch.ops.moe_gb300.router_topk.default, (logits, K),
+                          test_utils=("test_schema", "test_faketensor"))
+    torch.library.opcheck(torch.ops.moe_gb300.router_topk_backward.default, (ref[2], w, idx, E),
+                          test_utils=("test_schema", "test_autograd_registration", "test_faketensor"))
+    compiled = torch.compile(fused, fullgraph=True, backend="aot_eager")
+    for _ in range(2):
+        c = run(compiled)
+        torch.cuda.synchronize()
+        for u, v in zip(c, got):
+            assert torch.equal(u.view(torch.int8), v.view(torch.int8))

@@ -15,6 +15,7 @@ T, H, E, K, I, P = 64, 256, 8, 2, 128, 16
 C = T * K + E * (P - 1)
 ALL_OPS = {"route_to_multihot", "dispatch", "grouped_experts", "combine", "combine_backward",
            "experts_backward", "dispatch_backward", "route_to_multihot_backward"}
+ROUTER_OPS = {"router_topk", "router_topk_backward"}
 
 
 def _inputs(device, grad=True):
@@ -94,3 +95,22 @@ def test_cpu_tensors_fail_loudly():
     x, idx, p, W1, W2 = _inputs("cpu", grad=False)
     with pytest.raises(NotImplementedError, match="CPU"):
         ops.moe_layer(x, idx, p, W1, W2, P)
+
+
+def test_layer_from_logits_fake_shapes_and_trace():
+    """The router in front of the layer: gradients reach the logits, and the
+    traced forward + backward consists of the library's operators."""
+    x, idx, p, W1, W2 = _inputs("meta")
+    lg = torch.zeros(T, E, dtype=torch.float32, device="meta", requires_grad=True)
+    out = ops.moe_layer_from_logits(x, lg, K, W1, W2, P)
+    out.float().sum().backward()
+    assert lg.grad.shape == (T, E) and lg.grad.dtype == torch.float32
+
+    def step(x, lg, W1, W2, g):
+        out = ops.moe_layer_from_logits(x, lg, K, W1, W2, P)
+        return (out,) + torch.autograd.grad(out, (x, lg, W1, W2), g)
+
+    x, _, _, W1, W2 = _inputs("cpu")
+    lg = torch.zeros(T, E, dtype=torch.float32, requires_grad=True)
+    gm = make_fx(step, tracing_mode="symbolic")(x, lg, W1, W2, torch.zeros(T, H, dtype=torch.bfloat16))
+    assert _ops_in(gm) == ALL_OPS | ROUTER_OPS
