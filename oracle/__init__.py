@@ -8,7 +8,8 @@ constants); the only thing both sides share is the seeded input generator in
 ``synthetic``, which holds none of the method's arithmetic.
 
 It is a plain, slow, obviously-correct restatement of what the pages define
-(and, in ``router.py``, of the router step in front of the path):
+(and, in ``router.py``, of the router step in front of the path; in ``fp8.py``,
+of the FP8 dispatch and gate/up GEMM):
 
 * "feat: add hybridep (NVIDIA-NeMo/Automodel #1333)" -- the preprocessing
   that maps top-k indices to a multihot ``routing_map`` with fp32 ``probs``
@@ -46,6 +47,8 @@ from .moe_oracle import (OracleIndexError, OracleCapacityError, sentinel_expert,
                          dispatch_backward, route_to_multihot_backward,
                          layer_forward, layer_backward, worst_case_capacity)
 from .router import router_topk, router_topk_f64, router_topk_backward
+from .fp8 import (e4m3_round, e4m3_to_bits, e4m3_bits_to_f64, quantize_rows, dispatch_fp8,
+                  expert_gate_up_fp8, grouped_experts_fp8)
 
 __all__ = [
     "bf16_bits_to_f64", "bf16_bits_to_f32", "f64_to_bf16_bits", "f32_to_bf16_bits",
@@ -56,5 +59,6 @@ __all__ = [
     "backward_scale", "backward_gate_up", "backward_swiglu", "backward_gemms",
     "dispatch_backward", "route_to_multihot_backward", "layer_forward",
     "layer_backward", "worst_case_capacity", "router_topk", "router_topk_f64",
-    "router_topk_backward",
+    "router_topk_backward", "e4m3_round", "e4m3_to_bits", "e4m3_bits_to_f64", "quantize_rows",
+    "dispatch_fp8", "expert_gate_up_fp8", "grouped_experts_fp8",
 ]
