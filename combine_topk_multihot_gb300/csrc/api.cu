@@ -161,17 +161,24 @@ moe_status moe_route_to_multihot(const int64_t* topk_idx, const float* topk_prob
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_route_to_multihot launch");
 }
 
-moe_status moe_dispatch(const moe_bf16* x, const uint8_t* routing_map, const float* probs,
-                        int32_t H, const moe_layout* L, moe_bf16* x_disp, int64_t* rows_host,
-                        moe_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// moe_dispatch and moe_dispatch_fp8: the layout (host-synced or sync-free),
+// then the rows, in bf16 (x_disp) or as e4m3 codes with per-row scales.
+moe_status dispatch_impl(const char* who, const moe_bf16* x, const uint8_t* routing_map,
+                         const float* probs, int32_t H, const moe_layout* L, moe_bf16* x_disp,
+                         uint8_t* x_q, float* x_scale, int64_t* rows_host, moe_stream_t stream) {
   moe_status st = check_layout(L);
   if (st != MOE_OK) return st;
   if ((st = check_hidden(H)) != MOE_OK) return st;
-  MOE_REQUIRE(L->T == 0 || (x && routing_map && probs), MOE_ERR_INVALID_ARG,
-              "moe_dispatch: NULL input");
-  MOE_REQUIRE(L->capacity == 0 || x_disp, MOE_ERR_INVALID_ARG, "moe_dispatch: NULL x_disp");
-  MOE_REQUIRE(aligned16(x) && aligned16(x_disp) && aligned16(routing_map), MOE_ERR_INVALID_ARG,
-              "moe_dispatch: x, x_disp and routing_map must be 16-byte aligned");
+  MOE_REQUIRE(L->T == 0 || (x && routing_map && probs), MOE_ERR_INVALID_ARG, "%s: NULL input", who);
+  MOE_REQUIRE(L->capacity == 0 || x_disp || (x_q && x_scale), MOE_ERR_INVALID_ARG,
+              "%s: NULL output rows", who);
+  MOE_REQUIRE(aligned16(x) && aligned16(x_disp) && aligned16(x_q) && aligned16(routing_map),
+              MOE_ERR_INVALID_ARG, "%s: x, the output rows and routing_map must be 16-byte aligned",
+              who);
   const int64_t worst = moe_worst_case_rows(L->T, L->E, L->K, L->pad_multiple);
   if (!rows_host && L->capacity < worst)
     return fail(MOE_ERR_CAPACITY,
@@ -182,15 +189,15 @@ moe_status moe_dispatch(const moe_bf16* x, const uint8_t* routing_map, const flo
   cudaError_t err;
   if (!rows_host) {
     if ((err = launch_layout(routing_map, probs, *L, L->workspace, LayoutStep::kAll, stream)) != cudaSuccess)
-      return cuda_fail(err, "moe_dispatch: layout");
+      return cuda_fail(err, "dispatch: layout");
   } else {
     if ((err = launch_layout(routing_map, probs, *L, L->workspace, LayoutStep::kCounts, stream)) != cudaSuccess)
-      return cuda_fail(err, "moe_dispatch: counts");
+      return cuda_fail(err, "dispatch: counts");
     int32_t tot[2] = {0, 0}, dev_status = 0;
     if ((err = cudaMemcpyAsync(tot, L->totals, sizeof(tot), cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
         (err = cudaMemcpyAsync(&dev_status, L->status, sizeof(int32_t), cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
         (err = cudaStreamSynchronize(stream)) != cudaSuccess)
-      return cuda_fail(err, "moe_dispatch: reading the row counts");
+      return cuda_fail(err, "dispatch: reading the row counts");
     rows_host[0] = tot[0];
     rows_host[1] = tot[1];
     if (dev_status & MOE_DEVERR_TIMEOUT)
@@ -201,11 +208,69 @@ moe_status moe_dispatch(const moe_bf16* x, const uint8_t* routing_map, const flo
       return fail(MOE_ERR_CAPACITY, "the layout needs %d rows, capacity is %lld", tot[0],
                   static_cast<long long>(L->capacity));
     if ((err = launch_layout(routing_map, probs, *L, L->workspace, LayoutStep::kPlace, stream)) != cudaSuccess)
-      return cuda_fail(err, "moe_dispatch: placement");
+      return cuda_fail(err, "dispatch: placement");
   }
-  if ((err = launch_row_gather(x, *L, H, x_disp, true, nullptr, nullptr, stream)) != cudaSuccess)
-    return cuda_fail(err, "moe_dispatch: gather");
+  err = x_disp ? launch_row_gather(x, *L, H, x_disp, true, nullptr, nullptr, stream)
+               : launch_row_gather_fp8(x, *L, H, x_q, x_scale, stream);
+  if (err != cudaSuccess) return cuda_fail(err, "dispatch: rows");
   return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_dispatch(const moe_bf16* x, const uint8_t* routing_map, const float* probs,
+                        int32_t H, const moe_layout* L, moe_bf16* x_disp, int64_t* rows_host,
+                        moe_stream_t stream) {
+  MOE_REQUIRE(L == nullptr || L->capacity == 0 || x_disp, MOE_ERR_INVALID_ARG,
+              "moe_dispatch: NULL x_disp");
+  return dispatch_impl("moe_dispatch", x, routing_map, probs, H, L, x_disp, nullptr, nullptr,
+                       rows_host, stream);
+}
+
+moe_status moe_dispatch_fp8(const moe_bf16* x, const uint8_t* routing_map, const float* probs,
+                            int32_t H, const moe_layout* L, uint8_t* x_disp_q, float* x_disp_scale,
+                            int64_t* rows_host, moe_stream_t stream) {
+  MOE_REQUIRE(L == nullptr || L->capacity == 0 || (x_disp_q && x_disp_scale), MOE_ERR_INVALID_ARG,
+              "moe_dispatch_fp8: NULL x_disp_q or x_disp_scale");
+  return dispatch_impl("moe_dispatch_fp8", x, routing_map, probs, H, L, nullptr, x_disp_q,
+                       x_disp_scale, rows_host, stream);
+}
+
+moe_status moe_quantize_fp8(const moe_bf16* src, int64_t rows, int32_t cols, uint8_t* codes,
+                            float* scales, moe_stream_t stream) {
+  MOE_REQUIRE(rows >= 0, MOE_ERR_INVALID_ARG, "moe_quantize_fp8: rows must be >= 0");
+  MOE_REQUIRE(cols > 0 && cols % 256 == 0, MOE_ERR_UNSUPPORTED_SHAPE,
+              "moe_quantize_fp8: cols must be a positive multiple of 256 (got %d)", cols);
+  MOE_REQUIRE(rows == 0 || (src && codes && scales), MOE_ERR_INVALID_ARG,
+              "moe_quantize_fp8: NULL pointer");
+  MOE_REQUIRE(aligned16(src) && aligned16(codes), MOE_ERR_INVALID_ARG,
+              "moe_quantize_fp8: src and codes must be 16-byte aligned");
+  moe_status st = check_device();
+  if (st != MOE_OK) return st;
+  cudaError_t err = launch_quantize_rows_fp8(src, rows, cols, codes, scales, stream);
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_quantize_fp8 launch");
+}
+
+moe_status moe_grouped_experts_fp8(const uint8_t* x_disp_q, const float* x_disp_scale,
+                                   const moe_layout* L, int32_t H, int32_t I, const uint8_t* W1_q,
+                                   const float* W1_scale, const moe_bf16* W2, moe_bf16* h,
+                                   moe_bf16* y_disp, moe_stream_t stream) {
+  moe_status st = check_layout(L);
+  if (st != MOE_OK) return st;
+  if ((st = check_hidden(H)) != MOE_OK) return st;
+  MOE_REQUIRE(I > 0 && I % 128 == 0, MOE_ERR_UNSUPPORTED_SHAPE,
+              "the intermediate size must be a positive multiple of 128 (got %d)", I);
+  MOE_REQUIRE(L->capacity == 0 || (x_disp_q && x_disp_scale && W1_q && W1_scale && W2 && h && y_disp),
+              MOE_ERR_INVALID_ARG, "moe_grouped_experts_fp8: NULL pointer");
+  MOE_REQUIRE(aligned16(x_disp_q) && aligned16(W1_q) && aligned16(W2) && aligned16(h) &&
+                  aligned16(y_disp),
+              MOE_ERR_INVALID_ARG, "moe_grouped_experts_fp8: pointers must be 16-byte aligned");
+  if ((st = check_device()) != MOE_OK) return st;
+  cudaError_t err = launch_experts_forward_fp8(x_disp_q, x_disp_scale, *L, H, I, W1_q, W1_scale, W2,
+                                               h, y_disp, stream);
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_grouped_experts_fp8 launch");
 }
 
 moe_status moe_grouped_experts(const moe_bf16* x_disp, const moe_layout* L, int32_t H, int32_t I,

@@ -1,0 +1,163 @@
+// FP8 dispatch (a4 with e4m3 rows) and rowwise e4m3 quantization.
+//
+// "Add the deepep expert-parallel implementation (huggingface/transformers
+// #49638)", What this adds, scope note: FP8 dispatch -- half the dispatch bytes
+// for FP8 recipes -- is the named follow-up.  Format: e4m3 values with one
+// fp32 scale per row, scale = amax(|row|) / 448 (1 for an all-zero row), code
+// = e4m3(v / scale) rounded to nearest even and saturated at +-448.  The
+// division is an IEEE fp32 division, so a code is the same on any machine.
+//
+// A warp owns a row of H values: lane l holds the 8-value vectors l, l + 32,
+// ...  A first pass finds the row's amax (warp max), a second re-reads the
+// row (now in L1), converts it and stores 8 codes per vector.
+
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+
+namespace {
+
+constexpr float E4M3_MAX = 448.0f;
+
+__device__ __forceinline__ float bf16_abs_max8(uint4 q) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+  return m;
+}
+
+__device__ __forceinline__ uint32_t e4m3_of(float v) {
+  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+}
+
+// 8 bf16 values / scale -> 8 e4m3 codes, in element order (lowest byte first).
+__device__ __forceinline__ uint2 quantize8(uint4 q, float scale) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  uint32_t c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    c[i] = e4m3_of(bf16_lo(w[i]) / scale) | (e4m3_of(bf16_hi(w[i]) / scale) << 8);
+  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
+// The scale of a warp-owned row (V vectors per lane).
+__device__ __forceinline__ float row_scale(const uint4* src, int V, int lane) {
+  float amax = 0.f;
+  for (int v = 0; v < V; ++v) amax = fmaxf(amax, bf16_abs_max8(__ldg(src + lane + 32 * v)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(FULL_MASK, amax, o));
+  return amax > 0.f ? amax / E4M3_MAX : 1.0f;
+}
+
+// a4 in e4m3.  Items [0, T): tokens -- the token's row is quantized once and
+// its codes and scale written to each of its rows.  Items [T, T + C): rows --
+// a pad or spare row (found from offsets and counts) gets zero codes, scale
+// 0 and the sentinel metadata (token -1, expert E, weight 0).
+__global__ void __launch_bounds__(256) row_scatter_fp8_kernel(
+    const uint16_t* __restrict__ x, int T, int K, int H, int E, long long C,
+    const int* __restrict__ token_row, const int* __restrict__ offsets,
+    const int* __restrict__ counts, int* __restrict__ row_token, int* __restrict__ row_expert,
+    float* __restrict__ row_weight, uint8_t* __restrict__ x_q, float* __restrict__ x_scale) {
+  extern __shared__ int s_meta[];  // offsets [E + 1], counts [E]
+  int* s_off = s_meta;
+  int* s_cnt = s_meta + E + 1;
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = offsets[i];
+  for (int i = threadIdx.x; i < E; i += blockDim.x) s_cnt[i] = counts[i];
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int V = H >> 8;
+  const long long items = T + C;
+  const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  const int R = s_off[E];
+  for (long long it = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       it < items; it += nwarps) {
+    if (it < T) {
+      const long long t = it;
+      const uint4* src = reinterpret_cast<const uint4*>(x + t * H);
+      const float scale = row_scale(src, V, lane);
+      for (int j0 = 0; j0 < K; j0 += 32) {
+        const int r_lane = j0 + lane < K ? __ldg(token_row + t * K + j0 + lane) : -1;
+        const uint32_t rows = __ballot_sync(FULL_MASK, r_lane >= 0);
+        if (r_lane >= 0) x_scale[r_lane] = scale;
+        for (int v = 0; v < V; ++v) {
+          const uint2 c = quantize8(__ldg(src + lane + 32 * v), scale);
+          for (uint32_t m = rows; m; m &= m - 1u) {
+            const int r = __shfl_sync(FULL_MASK, r_lane, __ffs(m) - 1);
+            reinterpret_cast<uint2*>(x_q + static_cast<long long>(r) * H)[lane + 32 * v] = c;
+          }
+        }
+      }
+    } else {
+      const long long r = it - T;
+      bool pad = true;
+      if (r < R) {
+        int lo = 0, hi = E;  // s_off[lo] <= r < s_off[hi]
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (s_off[mid] <= r) lo = mid; else hi = mid;
+        }
+        pad = r - s_off[lo] >= s_cnt[lo];
+      }
+      if (!pad) continue;
+      if (lane == 0) {
+        row_token[r] = -1;
+        row_expert[r] = E;
+        row_weight[r] = 0.f;
+        x_scale[r] = 0.f;
+      }
+      uint2* d = reinterpret_cast<uint2*>(x_q + r * H);
+      for (int v = 0; v < V; ++v) d[lane + 32 * v] = make_uint2(0, 0);
+    }
+  }
+}
+
+// Rowwise e4m3 of a bf16 matrix [rows, cols], one warp per row.
+__global__ void __launch_bounds__(256) quantize_rows_fp8_kernel(const uint16_t* __restrict__ src,
+                                                                long long rows, int cols,
+                                                                uint8_t* __restrict__ codes,
+                                                                float* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int V = cols >> 8;
+  const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       r < rows; r += nwarps) {
+    const uint4* s = reinterpret_cast<const uint4*>(src + r * cols);
+    const float scale = row_scale(s, V, lane);
+    uint2* d = reinterpret_cast<uint2*>(codes + r * cols);
+    for (int v = 0; v < V; ++v) d[lane + 32 * v] = quantize8(__ldg(s + lane + 32 * v), scale);
+    if (lane == 0) scales[r] = scale;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_row_gather_fp8(const uint16_t* x, const moe_layout& L, int H, uint8_t* x_q,
+                                  float* x_scale, cudaStream_t s) {
+  const long long C = L.capacity;
+  const long long items = static_cast<long long>(L.T) + C;
+  if (items == 0) return cudaSuccess;
+  const int threads = 256;
+  const long long need = (items + 7) / 8;
+  const int blocks = static_cast<int>(need < 8LL * sm_count() ? need : 8LL * sm_count());
+  const size_t smem = (2 * L.E + 1) * sizeof(int);
+  row_scatter_fp8_kernel<<<blocks, threads, smem, s>>>(x, L.T, L.K, H, L.E, C, L.token_row,
+                                                       L.offsets, L.tokens_per_expert, L.row_token,
+                                                       L.row_expert, L.row_weight, x_q, x_scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_rows_fp8(const uint16_t* src, long long rows, int cols, uint8_t* codes,
+                                     float* scales, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  const int threads = 256;
+  const long long need = (rows + 7) / 8;
+  const int blocks = static_cast<int>(need < 8LL * sm_count() ? need : 8LL * sm_count());
+  quantize_rows_fp8_kernel<<<blocks, threads, 0, s>>>(src, rows, cols, codes, scales);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

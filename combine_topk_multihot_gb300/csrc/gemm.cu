@@ -40,7 +40,7 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128;          // rows per tile (tensor-memory lanes)
-constexpr int BK = 64;           // bf16 elements per 128-byte swizzled row
+constexpr int BK = 64;           // bf16 elements per 128-byte swizzled row (128 for e4m3)
 constexpr int UMMA_K = 16;       // K per tcgen05.mma for 16-bit inputs
 constexpr int EPI_WARPS = 8;                   // two per TMEM lane quarter
 constexpr int NUM_THREADS = 32 * (2 + EPI_WARPS);
@@ -55,6 +55,8 @@ constexpr int SMEM_LIMIT = 232448;             // dynamic shared memory per CTA
 // whatever bytes follow in shared memory and only feed accumulator rows that
 // are never stored.  The smaller A slot leaves room for more stages, i.e.
 // more weight bytes in flight per SM, which is what bounds a decode step.
+enum OperandKind { OPS_BF16 = 0, OPS_E4M3 = 1 };
+
 template <int BN, int A_ROWS>
 struct Fwd {
   static constexpr int A_BYTES = A_ROWS * BK * 2;        // 16 KiB at A_ROWS = 128
@@ -64,6 +66,7 @@ struct Fwd {
   // ring depth (one less when the per-expert tables of a large E need the room)
   static constexpr int STAGES = BN == 256 ? 4 : (A_ROWS == 128 ? 8 : 16);
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+  static constexpr uint32_t IDESC_E4M3 = idesc_e4m3_f32(BM, BN);
 };
 
 enum Epilogue { EPI_SWIGLU = 0, EPI_WEIGHTED = 1 };
@@ -85,6 +88,8 @@ struct GemmArgs {
   int I;                   // GEMM1: offset of the up half in gu_save
   int write_pad;           // also write the pad rows of each expert's group (zeros)
   int* status;
+  const float* a_scale;    // e4m3 GEMM1: [C] scale of each A row
+  const float* b_scale;    // e4m3 GEMM1: [E * 2I] scale of each W1 row (output channel)
 };
 
 // Barriers and scalars; the per-expert tables (offsets [E+1], counts [E],
@@ -128,7 +133,7 @@ __device__ __forceinline__ Tile decode_tile(const int* tile_prefix, int E, int n
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
 
-template <int EPI, int BN, int A_ROWS, int STAGES>
+template <int EPI, int BN, int A_ROWS, int STAGES, int OPS>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
@@ -137,7 +142,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   using F = Fwd<BN, A_ROWS>;
   constexpr int A_BYTES = F::A_BYTES, B_BYTES = F::B_BYTES, STAGE_BYTES = F::STAGE_BYTES;
   constexpr int TMEM_COLS = F::TMEM_COLS;
-  constexpr uint32_t IDESC = F::IDESC;
+  constexpr uint32_t IDESC = OPS == OPS_E4M3 ? F::IDESC_E4M3 : F::IDESC;
+  constexpr int BKE = OPS == OPS_E4M3 ? 128 : BK;   // K elements per 128-byte row of a stage
+  static_assert(OPS == OPS_BF16 || EPI == EPI_SWIGLU, "e4m3 operands only in the gate/up GEMM");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* tiles = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -216,9 +223,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t a_dst = tiles_u32 + stage * STAGE_BYTES;
           const uint32_t b_dst = a_dst + A_BYTES;
           mbar_arrive_expect_tx(full, STAGE_BYTES);
-          tma_load_2d(a_dst, &tmA, kb * BK, a_row, full);
-          tma_load_2d(b_dst, &tmB, kb * BK, b_row, full);
-          tma_load_2d(b_dst + B_BYTES / 2, &tmB, kb * BK, b_row + args.b_second_off, full);
+          tma_load_2d(a_dst, &tmA, kb * BKE, a_row, full);
+          tma_load_2d(b_dst, &tmB, kb * BKE, b_row, full);
+          tma_load_2d(b_dst + B_BYTES / 2, &tmB, kb * BKE, b_row + args.b_second_off, full);
           ++issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -254,7 +261,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
             // advance along K inside the 128-byte swizzled row: 32 bytes per step
-            tc_mma_bf16(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, IDESC, (kb | kk) != 0);
+            // (16 bf16 or 32 e4m3 elements)
+            if constexpr (OPS == OPS_E4M3)
+              tc_mma_e4m3(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, IDESC, (kb | kk) != 0);
+            else
+              tc_mma_bf16(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, IDESC, (kb | kk) != 0);
           }
           tc_commit(smem_u32(&s.empty[stage]));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -327,6 +338,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld32(tb + c, g);
           tmem_ld32(tb + BN / 2 + c, u);
           tmem_ld_wait();
+          if constexpr (OPS == OPS_E4M3) {
+            // acc * scale(row) * scale(channel); lane i holds channel i's scales
+            const long long bs = static_cast<long long>(t.e) * args.b_rows_per_expert + col0 + c + lane;
+            const float sg = __ldg(args.b_scale + bs);
+            const float su = __ldg(args.b_scale + bs + args.b_second_off);
+            const float sa = valid ? __ldg(args.a_scale + row) : 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              g[i] = __float_as_uint(__uint_as_float(g[i]) * (sa * __shfl_sync(FULL_MASK, sg, i)));
+              u[i] = __float_as_uint(__uint_as_float(u[i]) * (sa * __shfl_sync(FULL_MASK, su, i)));
+            }
+          }
           if (valid) {
             uint32_t hv[16];
 #pragma unroll
@@ -413,7 +436,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // ---------------------------------------------------------------- host side
 
-template <int EPI, int BN, int A_ROWS, int STAGES>
+template <int EPI, int BN, int A_ROWS, int STAGES, int OPS>
 cudaError_t launch_gemm_stages(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
                                const GemmArgs& args, cudaStream_t s) {
   static bool configured[64] = {};
@@ -421,12 +444,12 @@ cudaError_t launch_gemm_stages(const CUtensorMap& a, const CUtensorMap& b, const
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    err = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, BN, A_ROWS, STAGES>,
+    err = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, BN, A_ROWS, STAGES, OPS>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  grouped_gemm_kernel<EPI, BN, A_ROWS, STAGES>
+  grouped_gemm_kernel<EPI, BN, A_ROWS, STAGES, OPS>
       <<<sm_count(), NUM_THREADS, smem_bytes(STAGES, Fwd<BN, A_ROWS>::STAGE_BYTES, args.E), s>>>(
           a, b, out, args);
   return cudaGetLastError();
@@ -434,26 +457,33 @@ cudaError_t launch_gemm_stages(const CUtensorMap& a, const CUtensorMap& b, const
 
 // The ring depth of Fwd when it fits beside the staging and the per-expert
 // tables, else one stage less (E above about 200).
-template <int EPI, int BN, int A_ROWS>
+template <int EPI, int BN, int A_ROWS, int OPS = OPS_BF16>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
                         const GemmArgs& args, cudaStream_t s) {
   using F = Fwd<BN, A_ROWS>;
   if (smem_bytes(F::STAGES, F::STAGE_BYTES, args.E) <= static_cast<size_t>(SMEM_LIMIT))
-    return launch_gemm_stages<EPI, BN, A_ROWS, F::STAGES>(a, b, out, args, s);
-  return launch_gemm_stages<EPI, BN, A_ROWS, F::STAGES - 1>(a, b, out, args, s);
+    return launch_gemm_stages<EPI, BN, A_ROWS, F::STAGES, OPS>(a, b, out, args, s);
+  return launch_gemm_stages<EPI, BN, A_ROWS, F::STAGES - 1, OPS>(a, b, out, args, s);
 }
 
-template <int BN, int A_ROWS>
-cudaError_t experts_forward(const uint16_t* x_disp, const moe_layout& L, int H, int I,
-                            const uint16_t* W1, const uint16_t* W2, uint16_t* h, uint16_t* y,
-                            uint16_t* o_save, uint16_t* gu_save, cudaStream_t s) {
+// GEMM1 reads A (x_disp rows) and B (W1) as bf16, or as e4m3 codes with
+// fp32 scales per A row and per W1 row; GEMM2 is bf16.
+template <int BN, int A_ROWS, int OPS>
+cudaError_t experts_forward(const void* x_disp, const float* x_scale, const moe_layout& L, int H,
+                            int I, const void* W1, const float* W1_scale, const uint16_t* W2,
+                            uint16_t* h, uint16_t* y, uint16_t* o_save, uint16_t* gu_save,
+                            cudaStream_t s) {
   const uint64_t C = static_cast<uint64_t>(L.capacity);
+  const uint64_t w1_rows = static_cast<uint64_t>(L.E) * 2 * I;
   // B is loaded as two boxes of BN/2 rows: the gate and up rows (GEMM1) or
   // the two halves of the tile's output columns (GEMM2).
   CUtensorMap mA1, mB1, mA2, mB2, mH, mY;
-  if (!make_tma_2d_bf16(&mA1, x_disp, C, H, A_ROWS) ||
-      !make_tma_2d_bf16(&mB1, W1, static_cast<uint64_t>(L.E) * 2 * I, H, BN / 2) ||
-      !make_tma_2d_bf16(&mA2, h, C, I, A_ROWS) ||
+  const bool maps1 = OPS == OPS_E4M3
+                         ? make_tma_2d_u8(&mA1, x_disp, C, H, A_ROWS) &&
+                               make_tma_2d_u8(&mB1, W1, w1_rows, H, BN / 2)
+                         : make_tma_2d_bf16(&mA1, x_disp, C, H, A_ROWS) &&
+                               make_tma_2d_bf16(&mB1, W1, w1_rows, H, BN / 2);
+  if (!maps1 || !make_tma_2d_bf16(&mA2, h, C, I, A_ROWS) ||
       !make_tma_2d_bf16(&mB2, W2, static_cast<uint64_t>(L.E) * H, I, BN / 2) ||
       !make_tma_store_2d_bf16(&mH, h, C, I) || !make_tma_store_2d_bf16(&mY, y, C, H))
     return cudaErrorInvalidValue;
@@ -463,7 +493,7 @@ cudaError_t experts_forward(const uint16_t* x_disp, const moe_layout& L, int H, 
   g1.offsets = L.offsets;
   g1.row_weight = L.row_weight;
   g1.E = L.E;
-  g1.k_blocks = H / BK;
+  g1.k_blocks = H / (OPS == OPS_E4M3 ? 128 : BK);
   g1.n_tiles = I / (BN / 2);
   g1.b_rows_per_expert = 2 * I;
   g1.b_tile_step = BN / 2;
@@ -475,7 +505,9 @@ cudaError_t experts_forward(const uint16_t* x_disp, const moe_layout& L, int H, 
   g1.I = I;
   g1.write_pad = gu_save != nullptr;  // training: the backward reads the pad rows
   g1.status = L.status;
-  cudaError_t err = launch_gemm<EPI_SWIGLU, BN, A_ROWS>(mA1, mB1, mH, g1, s);
+  g1.a_scale = x_scale;
+  g1.b_scale = W1_scale;
+  cudaError_t err = launch_gemm<EPI_SWIGLU, BN, A_ROWS, OPS>(mA1, mB1, mH, g1, s);
   if (err != cudaSuccess) return err;
 
   GemmArgs g2 = g1;
@@ -488,7 +520,44 @@ cudaError_t experts_forward(const uint16_t* x_disp, const moe_layout& L, int H, 
   g2.ld0 = H;
   g2.out1 = o_save;
   g2.ld1 = H;
+  g2.a_scale = nullptr;
+  g2.b_scale = nullptr;
   return launch_gemm<EPI_WEIGHTED, BN, A_ROWS>(mA2, mB2, mY, g2, s);
+}
+
+// The tile shape for a layer (all from host-known sizes, so the sync-free
+// path needs no row counts).  At most min(E, T*K) experts have rows; when
+// even one 128-row tile per such expert at BN = 256 leaves SMs idle, take
+// 64-column tiles.  An expert has at most T rows (one per token); with the
+// pad rows written (training) its group is T rounded up to pad_multiple.
+enum class Shape { kWide, kNarrow, kNarrowShortA };
+
+Shape pick_shape(const moe_layout& L, int I, bool write_pad) {
+  const long long pairs = static_cast<long long>(L.T) * L.K;
+  const long long active = pairs < L.E ? pairs : L.E;
+  if (active * (I / 128) >= sm_count()) return Shape::kWide;
+  const long long P = L.pad_multiple;
+  const long long stored = write_pad ? (L.T + P - 1) / P * P : L.T;
+  return stored <= 32 ? Shape::kNarrowShortA : Shape::kNarrow;
+}
+
+template <int OPS>
+cudaError_t experts_forward_any(const void* x_disp, const float* x_scale, const moe_layout& L,
+                                int H, int I, const void* W1, const float* W1_scale,
+                                const uint16_t* W2, uint16_t* h, uint16_t* y, uint16_t* o_save,
+                                uint16_t* gu_save, cudaStream_t s) {
+  switch (pick_shape(L, I, gu_save != nullptr)) {
+    case Shape::kWide:
+      return experts_forward<256, 128, OPS>(x_disp, x_scale, L, H, I, W1, W1_scale, W2, h, y,
+                                            o_save, gu_save, s);
+    case Shape::kNarrow:
+      return experts_forward<64, 128, OPS>(x_disp, x_scale, L, H, I, W1, W1_scale, W2, h, y,
+                                           o_save, gu_save, s);
+    case Shape::kNarrowShortA:
+      return experts_forward<64, 32, OPS>(x_disp, x_scale, L, H, I, W1, W1_scale, W2, h, y,
+                                          o_save, gu_save, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -498,19 +567,17 @@ cudaError_t launch_experts_forward(const uint16_t* x_disp, const moe_layout& L, 
                                    uint16_t* y, uint16_t* o_save, uint16_t* gu_save,
                                    cudaStream_t s) {
   if (L.capacity == 0) return cudaSuccess;
-  // At most min(E, T*K) experts have rows.  When even one 128-row tile per
-  // such expert at BN = 256 leaves SMs idle, take 64-column tiles.
-  const long long pairs = static_cast<long long>(L.T) * L.K;
-  const long long active = pairs < L.E ? pairs : L.E;
-  if (active * (I / 128) >= sm_count())
-    return experts_forward<256, 128>(x_disp, L, H, I, W1, W2, h, y, o_save, gu_save, s);
-  // An expert has at most T rows (one per token); with the pad rows written
-  // (training) its group is T rounded up to pad_multiple.
-  const long long P = L.pad_multiple;
-  const long long stored = gu_save ? (L.T + P - 1) / P * P : L.T;
-  if (stored <= 32)
-    return experts_forward<64, 32>(x_disp, L, H, I, W1, W2, h, y, o_save, gu_save, s);
-  return experts_forward<64, 128>(x_disp, L, H, I, W1, W2, h, y, o_save, gu_save, s);
+  return experts_forward_any<OPS_BF16>(x_disp, nullptr, L, H, I, W1, nullptr, W2, h, y, o_save,
+                                       gu_save, s);
+}
+
+cudaError_t launch_experts_forward_fp8(const uint8_t* x_q, const float* x_scale,
+                                       const moe_layout& L, int H, int I, const uint8_t* W1_q,
+                                       const float* W1_scale, const uint16_t* W2, uint16_t* h,
+                                       uint16_t* y, cudaStream_t s) {
+  if (L.capacity == 0) return cudaSuccess;
+  return experts_forward_any<OPS_E4M3>(x_q, x_scale, L, H, I, W1_q, W1_scale, W2, h, y, nullptr,
+                                       nullptr, s);
 }
 
 }  // namespace moe

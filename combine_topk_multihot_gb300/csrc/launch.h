@@ -19,6 +19,11 @@ int sm_count();  // SMs of the current device (cached)
 bool make_tma_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                       uint32_t box_rows);
 
+// The same for a row-major 8-bit matrix, read as boxes of box_rows x 128
+// columns (128 bytes) with the 128-byte swizzle.
+bool make_tma_2d_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows);
+
 // Tensor map for TMA stores of 32-row x 32-column bf16 boxes (64-byte rows,
 // no swizzle) into a row-major [rows, cols] matrix.
 bool make_tma_store_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols);
@@ -81,6 +86,20 @@ cudaError_t launch_experts_forward(const uint16_t* x_disp, const moe_layout& L, 
                                    const uint16_t* W1, const uint16_t* W2, uint16_t* h,
                                    uint16_t* y, uint16_t* o_save, uint16_t* gu_save,
                                    cudaStream_t s);
+
+// FP8: a4 with e4m3 rows (one fp32 scale per row; pad and spare rows zero
+// codes, scale 0, sentinel metadata), and rowwise e4m3 quantization of a
+// bf16 matrix (cols % 256 == 0).
+cudaError_t launch_row_gather_fp8(const uint16_t* x, const moe_layout& L, int H, uint8_t* x_q,
+                                  float* x_scale, cudaStream_t s);
+cudaError_t launch_quantize_rows_fp8(const uint16_t* src, long long rows, int cols, uint8_t* codes,
+                                     float* scales, cudaStream_t s);
+// a5 with the gate/up GEMM on e4m3 operands (scales applied in its epilogue);
+// the down projection stays bf16.
+cudaError_t launch_experts_forward_fp8(const uint8_t* x_q, const float* x_scale,
+                                       const moe_layout& L, int H, int I, const uint8_t* W1_q,
+                                       const float* W1_scale, const uint16_t* W2, uint16_t* h,
+                                       uint16_t* y, cudaStream_t s);
 
 // tcgen05 grouped GEMMs of the expert backward (a9); workspace holds G_o [C, H]
 // and G_gu [C, 2I] (bf16).

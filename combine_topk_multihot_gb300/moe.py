@@ -173,6 +173,51 @@ def moe_dispatch(x: torch.Tensor, routing_map: torch.Tensor, probs: torch.Tensor
     return x_disp, ((int(rows[0]), int(rows[1])) if host_sync else None)
 
 
+def moe_dispatch_fp8(x: torch.Tensor, routing_map: torch.Tensor, probs: torch.Tensor, layout: Layout,
+                     host_sync: bool = True, out=None, stream=None):
+    """a4 in e4m3: fills ``layout`` and returns (x_disp_q uint8 [C, H],
+    x_disp_scale fp32 [C], (R, N) or None)."""
+    _bf16(x, "x")
+    H = x.shape[1]
+    C = layout.capacity
+    q = out[0] if out is not None else torch.empty(C, H, dtype=torch.uint8, device=x.device)
+    sc = out[1] if out is not None else torch.empty(C, dtype=torch.float32, device=x.device)
+    rows = (ctypes.c_int64 * 2)() if host_sync else None
+    _check(N.lib.moe_dispatch_fp8(_ptr(x), _ptr(routing_map), _ptr(probs), H, layout.ref, _ptr(q), _ptr(sc),
+                                  rows, _stream(stream)), "moe_dispatch_fp8")
+    return q, sc, ((int(rows[0]), int(rows[1])) if host_sync else None)
+
+
+def moe_quantize_fp8(src: torch.Tensor, stream=None):
+    """Rowwise e4m3 of a bf16 tensor whose last dimension is the row: returns
+    (codes uint8, same shape; scales fp32, shape[:-1])."""
+    _bf16(src, "src")
+    cols = src.shape[-1]
+    rows = src.numel() // cols
+    codes = torch.empty(src.shape, dtype=torch.uint8, device=src.device)
+    scales = torch.empty(src.shape[:-1], dtype=torch.float32, device=src.device)
+    _check(N.lib.moe_quantize_fp8(_ptr(src), rows, cols, _ptr(codes), _ptr(scales), _stream(stream)),
+           "moe_quantize_fp8")
+    return codes, scales
+
+
+def moe_grouped_experts_fp8(x_disp_q: torch.Tensor, x_disp_scale: torch.Tensor, layout: Layout,
+                            W1_q: torch.Tensor, W1_scale: torch.Tensor, W2: torch.Tensor, out=None,
+                            stream=None):
+    """a5 with the e4m3 gate/up GEMM: returns dict(h, y), bf16 [C, *]."""
+    E, twoI, H = W1_q.shape
+    I = twoI // 2
+    C = layout.capacity
+    dev = x_disp_q.device
+    o = out or {}
+    h = o.get("h") if o.get("h") is not None else torch.empty(C, I, dtype=torch.bfloat16, device=dev)
+    y = o.get("y") if o.get("y") is not None else torch.empty(C, H, dtype=torch.bfloat16, device=dev)
+    _check(N.lib.moe_grouped_experts_fp8(_ptr(x_disp_q), _ptr(x_disp_scale), layout.ref, H, I, _ptr(W1_q),
+                                         _ptr(W1_scale), _ptr(W2), _ptr(h), _ptr(y), _stream(stream)),
+           "moe_grouped_experts_fp8")
+    return {"h": h, "y": y}
+
+
 def moe_grouped_experts(x_disp: torch.Tensor, layout: Layout, W1: torch.Tensor, W2: torch.Tensor,
                         save_o: bool = False, save_gu: bool = False, out=None, stream=None):
     """a5: returns dict(h, y, o (or None), gu (or None)), each [C, *] bf16."""

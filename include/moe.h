@@ -198,6 +198,31 @@ MOE_API moe_status moe_dispatch(const moe_bf16* x, const uint8_t* routing_map, c
                         int64_t* rows_host, moe_stream_t stream);
 
 /*
+ * a4 in FP8 ([DEP] What this adds, scope note: FP8 dispatch, half the
+ * dispatch bytes, is the named follow-up).  As moe_dispatch, but the rows are
+ * float8 e4m3 codes with one fp32 scale per row:
+ *   x_disp_q     [C, H] uint8 (out): e4m3(x[t] / s_t) for row r of token t,
+ *                rounded to nearest even, saturated at +-448.
+ *   x_disp_scale [C] fp32 (out): s_t = amax(|x[t]|) / 448 (1 for a zero row);
+ *                pad and spare rows get zero codes and scale 0.
+ * The division and the amax are fp32, so the codes are exact functions of x.
+ * Arguments, modes and errors are otherwise those of moe_dispatch.
+ */
+MOE_API moe_status moe_dispatch_fp8(const moe_bf16* x, const uint8_t* routing_map,
+                                    const float* probs, int32_t H, const moe_layout* L,
+                                    uint8_t* x_disp_q, float* x_disp_scale, int64_t* rows_host,
+                                    moe_stream_t stream);
+
+/*
+ * Rowwise e4m3 quantization of a bf16 matrix [rows, cols] (cols a multiple
+ * of 256, src and codes 16-byte aligned), with the rule of moe_dispatch_fp8:
+ * codes [rows, cols] uint8 and scales [rows] fp32 (out).  For the gate/up
+ * weight W1 [E, 2I, H] this is one scale per output channel (rows = E * 2I).
+ */
+MOE_API moe_status moe_quantize_fp8(const moe_bf16* src, int64_t rows, int32_t cols,
+                                    uint8_t* codes, float* scales, moe_stream_t stream);
+
+/*
  * moe_dispatch without caller-provided scratch.  The pages have no
  * counterpart to this entry point; it exists for callers that cannot
  * allocate device memory -- for example a plugin inside an inference engine
@@ -254,6 +279,22 @@ MOE_API moe_status moe_grouped_experts(const moe_bf16* x_disp, const moe_layout*
                                moe_bf16* h, moe_bf16* y_disp,
                                moe_bf16* o_save, moe_bf16* gu_save,
                                moe_stream_t stream);
+
+/*
+ * a5 with the gate/up GEMM on e4m3 operands: x_disp_q / x_disp_scale from
+ * moe_dispatch_fp8 and W1_q [E, 2I, H] uint8 / W1_scale [E * 2I] fp32 from
+ * moe_quantize_fp8.  The tensor cores multiply the codes exactly
+ * (tcgen05.mma kind::f8f6f4, fp32 accumulation); the epilogue multiplies by
+ * row scale x channel scale, then applies the SwiGLU.  The down projection,
+ * W2 and the outputs h and y are bf16, as in moe_grouped_experts.  Inference
+ * only (no saved operands for the backward).  Shapes and errors as in
+ * moe_grouped_experts.
+ */
+MOE_API moe_status moe_grouped_experts_fp8(const uint8_t* x_disp_q, const float* x_disp_scale,
+                                           const moe_layout* L, int32_t H, int32_t I,
+                                           const uint8_t* W1_q, const float* W1_scale,
+                                           const moe_bf16* W2, moe_bf16* h, moe_bf16* y_disp,
+                                           moe_stream_t stream);
 
 /*
  * a6. Combine: out[t] = bf16(sum over t's rows of fp32(y_disp[row])), adding

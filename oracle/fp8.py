@@ -112,16 +112,19 @@ def expert_gate_up_fp8(qx, sx, qw1e, sw1e, I, rnd=bf16_round_f64):
     return rnd(_silu(g) * u)
 
 
-def grouped_experts_fp8(qx_disp, sx_disp, row_expert, row_weight, qW1, sW1, W2_bits, I):
+def grouped_experts_fp8(qx_disp, sx_disp, row_expert, row_weight, qW1, sW1, W2_bits, I,
+                        experts=None):
     """The experts with the FP8 gate/up GEMM.  Returns (y bits [C, H], h bits
     [C, I]); h from expert_gate_up_fp8, o = h W2^T and y = bf16(w o) as in the
-    bf16 experts; sentinel rows stay zero."""
+    bf16 experts; sentinel rows stay zero.  qW1[e], sW1[e], W2_bits[e] are read
+    only for the experts computed: all that have rows, or those in ``experts``."""
     re = np.asarray(row_expert)
     C, H = np.asarray(qx_disp).shape
-    E = np.asarray(qW1).shape[0]
+    todo = sorted(set(int(e) for e in np.unique(re) if 0 <= e < len(W2_bits)) if experts is None
+                  else set(experts))
     h_bits = np.zeros((C, I), dtype=np.uint16)
     y_bits = np.zeros((C, H), dtype=np.uint16)
-    for e in range(E):
+    for e in todo:
         R = np.flatnonzero(re == e)
         if R.size == 0:
             continue

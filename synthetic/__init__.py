@@ -138,6 +138,6 @@ def make_grad_out(T: int, H: int, seed: int, device="cpu") -> torch.Tensor:
 
 
 __all__ = [
-    "LayerConfig", "CONFIGS", "make_tokens", "make_routing", "make_weights",
+    "LayerConfig", "CONFIGS", "make_tokens", "make_logits", "make_routing", "make_weights",
     "make_layer_inputs", "make_grad_out",
 ]
