@@ -151,15 +151,17 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- algorithmic work
 
-def algorithmic(cfg, counts: np.ndarray, R: int, N: int, C: int, backward: bool):
-    """Bytes / flops the layer's steps must move, per call (definitions in the design doc)."""
+def algorithmic(cfg, counts: np.ndarray, R: int, N: int, C: int, backward: bool, fp8: bool = False):
+    """Bytes / flops the layer's steps must move, per call (definitions in the design doc).
+    With fp8 the dispatched rows and W1 are e4m3 (1 byte) with fp32 per-row scales."""
     T, H, E, K, I = cfg.T, cfg.H, cfg.E, cfg.K, cfg.I
     active = int((counts > 0).sum())
     meta_disp = T * E * 1 + 4 * N + 12 * C + 4 * T * K + 8 * (E + 1)
-    disp = T * H * 2 + C * H * 2 + meta_disp
+    row_b = 1 if fp8 else 2
+    disp = T * H * 2 + C * H * row_b + meta_disp + (4 * C if fp8 else 0)
     comb = N * H * 2 + T * H * 2 + 4 * T * K
-    w_bytes = active * (2 * I * H + H * I) * 2
-    ex_bytes = w_bytes + N * H * 2 + 2 * N * I * 2 + N * H * 2
+    w_bytes = active * (2 * I * H * row_b + H * I * 2) + (active * 2 * I * 4 if fp8 else 0)
+    ex_bytes = w_bytes + N * H * row_b + 2 * N * I * 2 + N * H * 2
     ex_flops = 6.0 * N * H * I
     out = {"dispatch_bytes": disp, "combine_bytes": comb, "experts_bytes": ex_bytes,
            "experts_flops": ex_flops, "multihot_bytes": T * K * 12 + T * E * 6}
@@ -186,6 +188,9 @@ def run_ours(args, world, rank, local):
     T, H, E, K, I, P = cfg.T, cfg.H, cfg.E, cfg.K, cfg.I, cfg.P
     host_sync = not cfg.sync_free
     n_layers = args.layers
+    fp8 = args.fp8
+    if fp8 and cfg.backward:
+        raise SystemExit("--fp8 is the inference path (the e4m3 gate/up GEMM saves nothing for a backward)")
 
     layers = []
     for l in range(n_layers):
@@ -194,6 +199,8 @@ def run_ours(args, world, rank, local):
         idx, p = synthetic.make_routing(T, E, K, s, cfg.zipf_s, cfg.drop)
         W1, W2 = synthetic.make_weights(E, H, I, s, device=dev)
         layers.append({"x": x, "topk_idx": idx.to(dev), "topk_probs": p.to(dev), "W1": W1, "W2": W2})
+        if fp8:  # weights are quantized once, like a checkpoint converted at load time
+            layers[-1]["W1q"], layers[-1]["W1s"] = moe.moe_quantize_fp8(W1)
     worst = moe.worst_case_rows(T, E, K, P)
     # host-synced mode: buffers sized once to the largest R over the layers, as
     # a caching allocator would hold them; sync-free: the worst case
@@ -217,11 +224,15 @@ def run_ours(args, world, rank, local):
         bufs = {"h": torch.empty(C, I, dtype=torch.bfloat16, device=dev),
                 "y": torch.empty(C, H, dtype=torch.bfloat16, device=dev)}
 
+    if fp8:
+        x_q = (torch.empty(C, H, dtype=torch.uint8, device=dev), torch.empty(C, dtype=torch.float32, device=dev))
     stream = torch.cuda.current_stream()
     ev = lambda: torch.cuda.Event(enable_timing=True)
     bwd = cfg.backward
     stages = ["multihot", "dispatch", "experts", "combine"]
-    launches_per_step = 1 + 4 + 2 + 1
+    # our kernels per step: multihot; the layout kernel (two launches when
+    # host-synced) and the row copy; the two expert GEMMs; the combine
+    launches_per_step = 1 + (3 if host_sync else 2) + 2 + 1
     if bwd:
         stages += ["combine_bwd", "experts_bwd", "dispatch_bwd", "multihot_bwd"]
         launches_per_step += 1 + 5 + 1 + 1
@@ -235,10 +246,16 @@ def run_ours(args, world, rank, local):
         rec(0)
         rmap, probs, win = moe.moe_route_to_multihot(L["topk_idx"], L["topk_probs"], E, lay.status)
         rec(1)
-        moe.moe_dispatch(L["x"], rmap, probs, lay, host_sync=host_sync, x_disp=x_disp)
-        rec(2)
-        moe.moe_grouped_experts(x_disp, lay, L["W1"], L["W2"], out=bufs, save_o=bwd, save_gu=bwd)
-        rec(3)
+        if fp8:
+            moe.moe_dispatch_fp8(L["x"], rmap, probs, lay, host_sync=host_sync, out=x_q)
+            rec(2)
+            moe.moe_grouped_experts_fp8(x_q[0], x_q[1], lay, L["W1q"], L["W1s"], L["W2"], out=bufs)
+            rec(3)
+        else:
+            moe.moe_dispatch(L["x"], rmap, probs, lay, host_sync=host_sync, x_disp=x_disp)
+            rec(2)
+            moe.moe_grouped_experts(x_disp, lay, L["W1"], L["W2"], out=bufs, save_o=bwd, save_gu=bwd)
+            rec(3)
         moe.moe_combine(bufs["y"], lay, out=out)
         rec(4)
         if bwd:
@@ -304,18 +321,23 @@ def run_ours(args, world, rank, local):
     # sync-free mode (worst-case capacity), outside the timed region
     lay_sf = moe.Layout(T, E, K, P, worst, device=dev)
     xd_sf = torch.empty(worst, H, dtype=torch.bfloat16, device=dev)
+    xq_sf = (torch.empty(worst, H, dtype=torch.uint8, device=dev),
+             torch.empty(worst, dtype=torch.float32, device=dev)) if fp8 else None
     sf_us = []
     for i in range(args.warmup + args.steps):
         L = layers[i % n_layers]
         rmap, probs, _ = moe.moe_route_to_multihot(L["topk_idx"], L["topk_probs"], E, lay_sf.status)
         a, b = ev(), ev()
         a.record(stream)
-        moe.moe_dispatch(L["x"], rmap, probs, lay_sf, host_sync=False, x_disp=xd_sf)
+        if fp8:
+            moe.moe_dispatch_fp8(L["x"], rmap, probs, lay_sf, host_sync=False, out=xq_sf)
+        else:
+            moe.moe_dispatch(L["x"], rmap, probs, lay_sf, host_sync=False, x_disp=xd_sf)
         b.record(stream)
         torch.cuda.synchronize()
         if i >= args.warmup:
             sf_us.append(1e3 * a.elapsed_time(b))
-    del lay_sf, xd_sf
+    del lay_sf, xd_sf, xq_sf
 
     # ---- end to end through the public API with host buffers
     pin = lambda t: t.cpu().pin_memory()
@@ -358,7 +380,7 @@ def run_ours(args, world, rank, local):
 
     # ---- roofline of the dominant step (the experts' two grouped GEMM launches)
     hbm, bf16_burst, bf16_sust, src = peaks()
-    work = [algorithmic(cfg, L["counts"], r[0], r[1], C, cfg.backward) for L, r in zip(layers, rows)]
+    work = [algorithmic(cfg, L["counts"], r[0], r[1], C, cfg.backward, fp8) for L, r in zip(layers, rows)]
     mean = lambda key: float(np.mean([w[key] for w in work]))
     # per-step averages over the timed steps (layer i % n_layers)
     steps_w = [work[i % n_layers] for i in range(args.steps)]
@@ -370,15 +392,19 @@ def run_ours(args, world, rank, local):
         ex_bytes += float(np.mean([w["experts_bwd_bytes"] for w in steps_w]))
         ex_flops += float(np.mean([w["experts_bwd_flops"] for w in steps_w]))
     t_hbm = ex_bytes / (hbm * 1e9)
-    t_tc = ex_flops / (bf16_burst * 1e12)
+    # with fp8, the gate/up GEMM (2/3 of the flops) runs at twice the bf16 rate
+    # (the nominal 4.5 : 2.25 PFLOP/s ratio applied to the measured bf16 peak)
+    tc_peak = bf16_burst * (1.0 / (2.0 / 3.0 / 2.0 + 1.0 / 3.0)) if fp8 else bf16_burst
+    t_tc = ex_flops / (tc_peak * 1e12)
     if t_hbm >= t_tc:
         roof = {"bound": "hbm", "achieved": ex_bytes / (ex_us * 1e-6) / 1e9, "peak": hbm, "unit": "GB/s"}
     else:
-        roof = {"bound": "tensor", "achieved": ex_flops / (ex_us * 1e-6) / 1e12, "peak": bf16_burst, "unit": "TFLOP/s"}
+        roof = {"bound": "tensor", "achieved": ex_flops / (ex_us * 1e-6) / 1e12, "peak": tc_peak, "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None if bwd else profiled_traffic(cfg.name)
+    roof["traffic"] = None if (bwd or fp8) else profiled_traffic(cfg.name)
     roof["algorithmic_bytes"] = ex_bytes
-    roof["kernel"] = ("experts: grouped_gemm_kernel<0> (gate/up + SwiGLU) + grouped_gemm_kernel<1> (down x weight)"
+    roof["kernel"] = ("experts: grouped_gemm_kernel<0> (gate/up + SwiGLU" + (", e4m3 operands" if fp8 else "")
+                      + ") + grouped_gemm_kernel<1> (down x weight)"
                       + (" + the backward's scale_rows + 4 bwd_gemm_kernel launches" if bwd else ""))
     roof["peak_source"] = src
     roof["tensor_frac_of_burst"] = ex_flops / (ex_us * 1e-6) / 1e12 / bf16_burst
@@ -397,7 +423,7 @@ def run_ours(args, world, rank, local):
         "rows_used": [r[0] for r in rows], "rows_valid": [r[1] for r in rows], "capacity": C,
     }
     kernels["dispatch_frac_hbm"] = kernels["dispatch_GBs"] / hbm
-    sf_bytes = float(np.mean([algorithmic(cfg, w_l["counts"], r[0], r[1], worst, False)["dispatch_bytes"]
+    sf_bytes = float(np.mean([algorithmic(cfg, w_l["counts"], r[0], r[1], worst, False, fp8)["dispatch_bytes"]
                               for w_l, r in zip(layers, rows)]))
     kernels["dispatch_sync_free_us"] = float(np.mean(sf_us))
     kernels["dispatch_sync_free_GBs"] = sf_bytes / (kernels["dispatch_sync_free_us"] * 1e-6) / 1e9
@@ -406,7 +432,8 @@ def run_ours(args, world, rank, local):
 
     tokens = T * world * args.steps
     res = {
-        "metric": "MoE layer tokens/sec (dispatch+experts+combine)" + (", forward + backward" if bwd else ""),
+        "metric": "MoE layer tokens/sec (dispatch+experts+combine)" + (", forward + backward" if bwd else "")
+                  + (", FP8 dispatch and gate/up GEMM" if fp8 else ""),
         "value": tokens / (ms_max * 1e-3),
         "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -414,10 +441,10 @@ def run_ours(args, world, rank, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "e4m3 dispatch + gate/up, bf16 down" if fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) tokens, softmax top-k routing, N(0,0.02) weights)",
         "config": {"workload": cfg.name, "T": T, "H": H, "E": E, "top_k": K, "I": I,
-                   "pad_multiple": P,
+                   "pad_multiple": P, **({"fp8": "e4m3, one fp32 scale per row (tokens, W1 channels)"} if fp8 else {}),
                    "mode": "host-synced" if host_sync else "sync-free, CUDA graph replay",
                    "layers_cycled": n_layers, "l2": "inputs larger than L2 (4 distinct layers cycled, >1.2 GB weights each)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -502,6 +529,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="qwen3_30b_a3b", choices=sorted(synthetic.CONFIGS))
     ap.add_argument("--layers", type=int, default=4)
+    ap.add_argument("--fp8", action="store_true",
+                    help="run the FP8 dispatch and e4m3 gate/up GEMM instead of the bf16 ones")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=8.0, help="seconds of oracle work per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
