@@ -567,6 +567,8 @@ cudaError_t launch_experts_forward(const uint16_t* x_disp, const moe_layout& L, 
                                    uint16_t* y, uint16_t* o_save, uint16_t* gu_save,
                                    cudaStream_t s) {
   if (L.capacity == 0) return cudaSuccess;
+  if (gemv_experts_fits(L, H, I, o_save || gu_save))
+    return launch_experts_forward_gemv(x_disp, L, H, I, W1, W2, h, y, s);
   return experts_forward_any<OPS_BF16>(x_disp, nullptr, L, H, I, W1, nullptr, W2, h, y, o_save,
                                        gu_save, s);
 }

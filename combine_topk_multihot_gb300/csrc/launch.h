@@ -87,6 +87,13 @@ cudaError_t launch_experts_forward(const uint16_t* x_disp, const moe_layout& L, 
                                    uint16_t* y, uint16_t* o_save, uint16_t* gu_save,
                                    cudaStream_t s);
 
+// a5 on the CUDA cores for layers with at most 4 rows per expert (T <= 4)
+// and nothing saved for a backward: weight streaming with warp dot products.
+bool gemv_experts_fits(const moe_layout& L, int H, int I, bool saves);
+cudaError_t launch_experts_forward_gemv(const uint16_t* x_disp, const moe_layout& L, int H, int I,
+                                        const uint16_t* W1, const uint16_t* W2, uint16_t* h,
+                                        uint16_t* y, cudaStream_t s);
+
 // FP8: a4 with e4m3 rows (one fp32 scale per row; pad and spare rows zero
 // codes, scale 0, sentinel metadata), and rowwise e4m3 quantization of a
 // bf16 matrix (cols % 256 == 0).

@@ -208,6 +208,26 @@ def test_experts_match_oracle(moe, T, H, E, K, I, P):
     assert_gemm_close(bits(fwd.out), O.combine(y, Lr["token_row"]), "out")
 
 
+@pytest.mark.parametrize("T,H,E,K,I,P", [
+    (1, 2048, 128, 8, 768, 1),     # the decode T = 1 layer: CUDA-core path
+    (4, 512, 16, 4, 256, 1),       # four tokens: up to four rows per expert
+    (3, 256, 8, 2, 128, 16),       # padded groups (pad rows not written)
+    (2, 4096, 8, 2, 1536, 1),      # the h4096 expert shape
+    (64, 256, 8, 2, 128, 16),      # tensor-core path without saved operands
+])
+def test_experts_inference_match_oracle(moe, T, H, E, K, I, P):
+    """Inference (nothing saved for a backward): layers with at most four rows
+    per expert take the CUDA-core path, larger ones the tensor cores."""
+    idx, p, x, W1, W2, C, fwd = _experts_case(moe, T, H, E, K, I, P, seed=3 * T + H, save=False)
+    Lr = O.build_layout(*O.route_to_multihot(idx.numpy(), p.numpy(), E)[:2], K, P, C)
+    xd = bits(fwd.x_disp)
+    y, h, _ = O.grouped_experts(xd, Lr["row_expert"], Lr["row_weight"], bits(W1), bits(W2), I)
+    valid = Lr["row_token"] >= 0
+    assert_gemm_close(bits(fwd.h)[valid], h[valid], "h", intermediate=True)
+    assert_gemm_close(bits(fwd.y)[valid], y[valid], "y")
+    assert_gemm_close(bits(fwd.out), O.combine(y, Lr["token_row"]), "out")
+
+
 @pytest.mark.parametrize("save", [False, True])
 def test_experts_sentinel_rows(moe, save):
     """Spare rows (R..C-1) are never written by the experts.  Pad rows inside
