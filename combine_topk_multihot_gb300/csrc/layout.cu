@@ -90,6 +90,7 @@ enum LayoutMode : int {
   LAYOUT_ALL = 0,    // counts, scans, offsets and placement: one cooperative launch
   LAYOUT_COUNT = 1,  // counts, scans and offsets only (cooperative), for the host-synced path
   LAYOUT_PLACE = 2,  // placement only, after LAYOUT_COUNT (ordinary launch)
+  LAYOUT_SINGLE = 3, // all four phases in one CTA, for layers of one or two chunks (no barrier)
 };
 
 struct LayoutArgs {
@@ -141,6 +142,7 @@ __global__ void __launch_bounds__(256) layout_kernel(LayoutArgs a) {
   int* s_base = reinterpret_cast<int*>(s_map32 + E);                   // [E], likewise
   uint32_t* s_emask = s_map32 + LAYOUT_CHUNK * E4;                     // [32][EW]
   int* s_off = reinterpret_cast<int*>(s_emask + LAYOUT_CHUNK * EW);    // [E + 1]
+  int* s_cc = s_off + E + 1;  // LAYOUT_SINGLE: [chunks][E] counts, then each chunk's start
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
 
   if (MODE != LAYOUT_PLACE) {
@@ -153,10 +155,27 @@ __global__ void __launch_bounds__(256) layout_kernel(LayoutArgs a) {
       for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int n = 0;
         for (int tl = 0; tl < nt; ++tl) n += s_map[tl * E + e] != 0;
-        a.chunk_counts[static_cast<long long>(e) * a.chunks + c] = n;
+        if constexpr (MODE == LAYOUT_SINGLE)
+          s_cc[c * E + e] = n;
+        else
+          a.chunk_counts[static_cast<long long>(e) * a.chunks + c] = n;
       }
       __syncthreads();
     }
+  }
+  if constexpr (MODE == LAYOUT_SINGLE) {
+    // one CTA: each expert's per-chunk starts and total, in shared memory
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      int run = 0;
+      for (int c = 0; c < a.chunks; ++c) {
+        const int v = s_cc[c * E + e];
+        s_cc[c * E + e] = run;
+        run += v;
+      }
+      a.tokens_per_expert[e] = run;
+    }
+    __syncthreads();
+  } else if constexpr (MODE != LAYOUT_PLACE) {
     if (!grid_barrier(a.barrier, gridDim.x, a.status, &s_ok)) return;
     for (int e = blockIdx.x * nwarps + warp; e < E; e += gridDim.x * nwarps) {
       int* row = a.chunk_counts + static_cast<long long>(e) * a.chunks;
@@ -231,7 +250,10 @@ __global__ void __launch_bounds__(256) layout_kernel(LayoutArgs a) {
   #pragma unroll 8
         for (int tl = 0; tl < LAYOUT_CHUNK; ++tl) m |= ((s_emask[tl * EW + seg] >> bit) & 1u) << tl;
         s_tmask[e] = m;
-        s_base[e] = s_off[e] + __ldcg(a.chunk_counts + static_cast<long long>(e) * a.chunks + c);
+        if constexpr (MODE == LAYOUT_SINGLE)
+          s_base[e] = s_off[e] + s_cc[c * E + e];
+        else
+          s_base[e] = s_off[e] + __ldcg(a.chunk_counts + static_cast<long long>(e) * a.chunks + c);
       }
       __syncthreads();
       // One thread per (token, slot j): slot j of a token is the token's j-th
@@ -411,6 +433,10 @@ int layout_resident_ctas(size_t smem) {
 
 template <int MODE>
 cudaError_t launch_layout_mode(const LayoutArgs& a, size_t smem, cudaStream_t s) {
+  if (MODE == LAYOUT_SINGLE) {
+    layout_kernel<MODE><<<1, 256, smem + static_cast<size_t>(a.chunks) * a.E * sizeof(int), s>>>(a);
+    return cudaGetLastError();
+  }
   if (MODE == LAYOUT_PLACE) {
     if (a.chunks == 0) return cudaSuccess;
     layout_kernel<MODE><<<a.chunks, 256, smem, s>>>(a);
@@ -462,7 +488,13 @@ cudaError_t launch_layout(const uint8_t* routing_map, const float* probs, const 
   a.status = L.status;
   const size_t smem = layout_smem_bytes(L.E);
   switch (step) {
-    case LayoutStep::kAll: return launch_layout_mode<LAYOUT_ALL>(a, smem, s);
+    case LayoutStep::kAll:
+      // one or two chunks (T <= 64): one CTA, no barrier, no memset.  It takes
+      // the chunks one after another, about 4 us each, so beyond two the
+      // cooperative launch (about 15 us at any small size) is faster.
+      if (a.chunks <= 2 && smem + static_cast<size_t>(a.chunks) * a.E * sizeof(int) <= 48 * 1024)
+        return launch_layout_mode<LAYOUT_SINGLE>(a, smem, s);
+      return launch_layout_mode<LAYOUT_ALL>(a, smem, s);
     case LayoutStep::kCounts: return launch_layout_mode<LAYOUT_COUNT>(a, smem, s);
     case LayoutStep::kPlace: return launch_layout_mode<LAYOUT_PLACE>(a, smem, s);
   }
