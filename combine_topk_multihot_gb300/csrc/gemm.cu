@@ -17,9 +17,10 @@
 //     so no host sync is needed and the launch can be graph-captured; an
 //     expert's rows are covered by ceil(count / 128) tiles; only the valid
 //     rows are written, plus -- when the gate/up values are saved for the
-//     backward -- the pad rows of the expert's group, which come out as zeros
-//     (x_disp's pad rows are zero) and let the backward skip masking them;
-//     spare rows are never written;
+//     backward -- the pad rows of the expert's group (the tiles then cover
+//     the whole padded group), which come out as zeros (x_disp's pad rows
+//     are zero) and let the backward skip masking them; spare rows are never
+//     written;
 //   * warp 0 issues TMA loads into a 4-stage (3 for large E) shared-memory
 //     ring (128-byte swizzle), warp 1 owns the tensor memory and issues
 //     tcgen05.mma (128 x 256 x 16 per instruction), warps 2-9 are the
@@ -183,7 +184,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int running = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
       const int e = e0 + lane;
-      const int n = e < E ? ((s_cnt[e] + BM - 1) / BM) * args.n_tiles : 0;
+      // rows an expert's tiles cover: its valid rows, or with the pad rows
+      // written (training) its whole padded group
+      const int rows_e = e < E ? (args.write_pad ? s_off[e + 1] - s_off[e] : s_cnt[e]) : 0;
+      const int n = ((rows_e + BM - 1) / BM) * args.n_tiles;
       int incl = n;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
