@@ -96,6 +96,7 @@ def _run(moe, T, H, E, K, I, P, seed, drop=0.0):
     (20, 512, 12, 1, 384, 1, 0.0),      # empty experts, I = 384 (BN 128 in dgrad1)
     (260, 768, 12, 3, 256, 128, 0.2),   # padded groups, drops, 3 N tiles in dgrad2
     (150, 512, 8, 2, 128, 256, 0.1),    # groups padded past one 128-row tile
+    (300, 256, 1024, 4, 128, 1, 0.0),   # the largest E (per-expert tables in shared memory)
 ])
 def test_expert_backward_matches_oracle(moe, T, H, E, K, I, P, drop):
     r = _run(moe, T, H, E, K, I, P, seed=T + 3 * H, drop=drop)

@@ -182,6 +182,7 @@ def _experts_case(moe, T, H, E, K, I, P, seed, drop=0.0, save=True):
     # tiles; these have enough for 256-column tiles on every SM
     (64, 256, 64, 4, 384, 16),     # 256-column tiles, a few rows per expert
     (2000, 512, 40, 4, 512, 1),    # 256-column tiles, two 128-row tiles per expert
+    (700, 256, 1024, 4, 128, 1),   # the largest E: per-expert tables take a pipeline stage
 ])
 def test_experts_match_oracle(moe, T, H, E, K, I, P):
     idx, p, x, W1, W2, C, fwd = _experts_case(moe, T, H, E, K, I, P, seed=T + H)
