@@ -48,6 +48,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
                                                       const int* __restrict__ row_expert,
                                                       const float* __restrict__ grad_w,
                                                       float* __restrict__ grad_probs, int E) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int lane = threadIdx.x & 31;
   const int V = H >> 8;  // 512-byte chunks per row
   const long long items = static_cast<long long>(T) * V;
@@ -106,8 +108,9 @@ cudaError_t launch_combine(const uint16_t* rows, const moe_layout& L, int H, uin
     combine_kernel<true><<<blocks, threads, 0, s>>>(rows, L.token_row, L.T, L.K, H, out,
                                                     L.row_expert, grad_w, grad_probs, L.E);
   } else {
-    combine_kernel<false><<<blocks, threads, 0, s>>>(rows, L.token_row, L.T, L.K, H, out,
-                                                     nullptr, nullptr, nullptr, L.E);
+    return launch_dependent(combine_kernel<false>, blocks, threads, 0, s, rows, L.token_row, L.T, L.K,
+                            H, out, static_cast<const int*>(nullptr), static_cast<const float*>(nullptr),
+                            static_cast<float*>(nullptr), L.E);
   }
   return cudaGetLastError();
 }

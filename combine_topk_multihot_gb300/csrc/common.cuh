@@ -25,6 +25,15 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
   return t;
 }
 
+// Programmatic dependent launch.  A kernel lets the next kernel in the
+// stream begin launching once all of its own CTAs have started, and waits for
+// the previous kernel to complete (memory visible) before reading anything it
+// wrote.  Both are no-ops when the launches carry no programmatic dependency.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void report(int* status, int bits) {
   if (status) atomicOr(status, bits);
 }

@@ -62,6 +62,8 @@ __global__ void __launch_bounds__(256) row_scatter_fp8_kernel(
     const int* __restrict__ token_row, const int* __restrict__ offsets,
     const int* __restrict__ counts, int* __restrict__ row_token, int* __restrict__ row_expert,
     float* __restrict__ row_weight, uint8_t* __restrict__ x_q, float* __restrict__ x_scale) {
+  griddep_launch_dependents();
+  griddep_wait();
   extern __shared__ int s_meta[];  // offsets [E + 1], counts [E]
   int* s_off = s_meta;
   int* s_cnt = s_meta + E + 1;
@@ -144,10 +146,9 @@ cudaError_t launch_row_gather_fp8(const uint16_t* x, const moe_layout& L, int H,
   const long long need = (items + 7) / 8;
   const int blocks = static_cast<int>(need < 8LL * sm_count() ? need : 8LL * sm_count());
   const size_t smem = (2 * L.E + 1) * sizeof(int);
-  row_scatter_fp8_kernel<<<blocks, threads, smem, s>>>(x, L.T, L.K, H, L.E, C, L.token_row,
-                                                       L.offsets, L.tokens_per_expert, L.row_token,
-                                                       L.row_expert, L.row_weight, x_q, x_scale);
-  return cudaGetLastError();
+  return launch_dependent(row_scatter_fp8_kernel, blocks, threads, smem, s, x, L.T, L.K, H, L.E, C,
+                          L.token_row, L.offsets, L.tokens_per_expert, L.row_token, L.row_expert,
+                          L.row_weight, x_q, x_scale);
 }
 
 cudaError_t launch_quantize_rows_fp8(const uint16_t* src, long long rows, int cols, uint8_t* codes,

@@ -158,6 +158,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = args.E;
+  griddep_launch_dependents();
 
   // ---- set-up: barriers, tensor memory, the device-side tile list
   if (threadIdx.x == 0) {
@@ -177,6 +178,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tmOut);
   }
   if (warp == 1) tmem_alloc(smem_u32(&s.tmem_base), TMEM_COLS);
+  griddep_wait();  // the layout, the dispatched rows (and h) come from earlier kernels
   for (int e = threadIdx.x; e <= E; e += NUM_THREADS) s_off[e] = args.offsets[e];
   for (int e = threadIdx.x; e < E; e += NUM_THREADS) s_cnt[e] = args.counts[e];
   __syncthreads();
@@ -453,10 +455,9 @@ cudaError_t launch_gemm_stages(const CUtensorMap& a, const CUtensorMap& b, const
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  grouped_gemm_kernel<EPI, BN, A_ROWS, STAGES, OPS>
-      <<<sm_count(), NUM_THREADS, smem_bytes(STAGES, Fwd<BN, A_ROWS>::STAGE_BYTES, args.E), s>>>(
-          a, b, out, args);
-  return cudaGetLastError();
+  return launch_dependent(grouped_gemm_kernel<EPI, BN, A_ROWS, STAGES, OPS>, sm_count(), NUM_THREADS,
+                          smem_bytes(STAGES, Fwd<BN, A_ROWS>::STAGE_BYTES, args.E), s, a, b, out,
+                          args);
 }
 
 // The ring depth of Fwd when it fits beside the staging and the per-expert

@@ -100,6 +100,8 @@ __device__ __forceinline__ uint16_t to_bf16_bits(float v) {
 
 template <int STEP>
 __global__ void __launch_bounds__(GEMV_THREADS) gemv_experts_kernel(GemvArgs args) {
+  griddep_launch_dependents();
+  griddep_wait();
   extern __shared__ __align__(16) uint8_t smem[];
   const int K = STEP == 1 ? args.H : args.I;
   uint4* s_a = reinterpret_cast<uint4*>(smem);                                  // [4][K] bf16
@@ -200,8 +202,7 @@ cudaError_t launch_experts_forward_gemv(const uint16_t* x_disp, const moe_layout
   long long items = active * (I / S1_COLS);
   int grid = static_cast<int>(items < cap ? (items > 0 ? items : 1) : cap);
   size_t smem = static_cast<size_t>(GEMV_ROWS) * H * 2 + static_cast<size_t>(L.E) * sizeof(int);
-  gemv_experts_kernel<1><<<grid, GEMV_THREADS, smem, s>>>(a);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_dependent(gemv_experts_kernel<1>, grid, GEMV_THREADS, smem, s, a);
   if (err != cudaSuccess) return err;
   a.a = h;
   a.w = W2;
@@ -209,8 +210,7 @@ cudaError_t launch_experts_forward_gemv(const uint16_t* x_disp, const moe_layout
   items = active * (H / S2_COLS);
   grid = static_cast<int>(items < cap ? (items > 0 ? items : 1) : cap);
   smem = static_cast<size_t>(GEMV_ROWS) * I * 2 + static_cast<size_t>(L.E) * sizeof(int);
-  gemv_experts_kernel<2><<<grid, GEMV_THREADS, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(gemv_experts_kernel<2>, grid, GEMV_THREADS, smem, s, a);
 }
 
 }  // namespace moe

@@ -12,6 +12,25 @@ namespace moe {
 
 int sm_count();  // SMs of the current device (cached)
 
+// Launches `kernel` so that it may start while the previous kernel in the
+// stream is still running (programmatic dependent launch); the kernel itself
+// waits for that kernel's results with griddep_wait().
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+
 // Tensor map of a row-major bf16 matrix [rows, cols] (cols contiguous) read as
 // boxes of box_rows x 64 columns with the 128-byte swizzle; reads past the
 // last row return zeros.  False if the driver entry point is missing or the

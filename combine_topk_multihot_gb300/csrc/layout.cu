@@ -132,6 +132,8 @@ struct LayoutArgs {
 template <int MODE>
 __global__ void __launch_bounds__(256) layout_kernel(LayoutArgs a) {
   static_assert(LAYOUT_CHUNK == 32, "one 32-bit token mask per expert");
+  griddep_launch_dependents();
+  griddep_wait();
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ int s_warp[33];
   __shared__ int s_ok;
@@ -311,6 +313,8 @@ __global__ void __launch_bounds__(256) row_scatter_kernel(
     const int* __restrict__ counts, int* __restrict__ row_token, int* __restrict__ row_expert,
     float* __restrict__ row_weight, uint16_t* __restrict__ dst, const uint16_t* __restrict__ o_save,
     float* __restrict__ grad_w) {
+  griddep_launch_dependents();
+  griddep_wait();
   extern __shared__ int s_meta[];  // META: offsets [E+1], counts [E]
   int* s_off = s_meta;
   int* s_cnt = s_meta + E + 1;
@@ -434,13 +438,12 @@ int layout_resident_ctas(size_t smem) {
 template <int MODE>
 cudaError_t launch_layout_mode(const LayoutArgs& a, size_t smem, cudaStream_t s) {
   if (MODE == LAYOUT_SINGLE) {
-    layout_kernel<MODE><<<1, 256, smem + static_cast<size_t>(a.chunks) * a.E * sizeof(int), s>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(layout_kernel<MODE>, 1, 256,
+                            smem + static_cast<size_t>(a.chunks) * a.E * sizeof(int), s, a);
   }
   if (MODE == LAYOUT_PLACE) {
     if (a.chunks == 0) return cudaSuccess;
-    layout_kernel<MODE><<<a.chunks, 256, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(layout_kernel<MODE>, a.chunks, 256, smem, s, a);
   }
   cudaError_t err = cudaMemsetAsync(a.barrier, 0, sizeof(unsigned), s);
   if (err != cudaSuccess) return err;
@@ -512,9 +515,10 @@ cudaError_t launch_row_gather(const uint16_t* src, const moe_layout& L, int H, u
   const int blocks = static_cast<int>(need < 8LL * sm_count() ? need : 8LL * sm_count());
   if (from_offsets) {
     const size_t smem = (2 * L.E + 1) * sizeof(int);
-    row_scatter_kernel<true, false><<<blocks, threads, smem, s>>>(
-        src, L.T, L.K, H, L.E, C, L.token_row, L.offsets, L.tokens_per_expert, L.row_token,
-        L.row_expert, L.row_weight, dst, nullptr, nullptr);
+    return launch_dependent(row_scatter_kernel<true, false>, blocks, threads, smem, s, src, L.T, L.K,
+                            H, L.E, C, L.token_row, L.offsets, L.tokens_per_expert, L.row_token,
+                            L.row_expert, L.row_weight, dst, static_cast<const uint16_t*>(nullptr),
+                            static_cast<float*>(nullptr));
   } else if (grad_w) {
     row_scatter_kernel<false, true><<<blocks, threads, 0, s>>>(
         src, L.T, L.K, H, L.E, C, L.token_row, nullptr, nullptr, L.row_token, nullptr, nullptr,

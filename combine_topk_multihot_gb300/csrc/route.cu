@@ -63,6 +63,8 @@ __global__ void __launch_bounds__(256) multihot_kernel(const int64_t* __restrict
                                                        float* __restrict__ probs,
                                                        int8_t* __restrict__ winner,
                                                        int* __restrict__ status) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int lane = threadIdx.x & 31;
   const int warps_per_block = blockDim.x >> 5;
   const long long nwarps = static_cast<long long>(gridDim.x) * warps_per_block;
@@ -107,6 +109,8 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
                                                           uint8_t* __restrict__ routing_map,
                                                           float* __restrict__ probs,
                                                           int8_t* __restrict__ winner) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int lane = threadIdx.x & 31;
   const int warps_per_block = blockDim.x >> 5;
   const long long nwarps = static_cast<long long>(gridDim.x) * warps_per_block;
@@ -243,9 +247,8 @@ cudaError_t launch_multihot(const int64_t* topk_idx, const float* topk_probs, in
   const int threads = 256;
   const long long blocks_needed = (static_cast<long long>(T) + 7) / 8;
   const int blocks = static_cast<int>(blocks_needed < 8LL * sm_count() ? blocks_needed : 8LL * sm_count());
-  multihot_kernel<<<blocks, threads, 0, s>>>(topk_idx, topk_probs, T, K, E, routing_map, probs,
-                                             winner, status);
-  return cudaGetLastError();
+  return launch_dependent(multihot_kernel, blocks, threads, 0, s, topk_idx, topk_probs, T, K, E,
+                          routing_map, probs, winner, status);
 }
 
 cudaError_t launch_router_topk(const float* logits, int T, int K, int E, int64_t* topk_idx,
@@ -256,12 +259,11 @@ cudaError_t launch_router_topk(const float* logits, int T, int K, int E, int64_t
   const long long blocks_needed = (static_cast<long long>(T) + 7) / 8;
   const int blocks = static_cast<int>(blocks_needed < 8LL * sm_count() ? blocks_needed : 8LL * sm_count());
   if (routing_map)
-    router_topk_kernel<true><<<blocks, threads, 0, s>>>(logits, T, K, E, topk_idx, topk_probs,
-                                                         routing_map, probs, winner);
-  else
-    router_topk_kernel<false><<<blocks, threads, 0, s>>>(logits, T, K, E, topk_idx, topk_probs,
-                                                          nullptr, nullptr, nullptr);
-  return cudaGetLastError();
+    return launch_dependent(router_topk_kernel<true>, blocks, threads, 0, s, logits, T, K, E,
+                            topk_idx, topk_probs, routing_map, probs, winner);
+  return launch_dependent(router_topk_kernel<false>, blocks, threads, 0, s, logits, T, K, E, topk_idx,
+                          topk_probs, static_cast<uint8_t*>(nullptr), static_cast<float*>(nullptr),
+                          static_cast<int8_t*>(nullptr));
 }
 
 cudaError_t launch_router_topk_backward(const float* grad_w, const float* w,
