@@ -151,17 +151,20 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- algorithmic work
 
-def algorithmic(cfg, counts: np.ndarray, R: int, N: int, C: int, backward: bool, fp8: bool = False):
+def algorithmic(cfg, counts: np.ndarray, R: int, N: int, C: int, backward: bool, fp8: bool = False,
+                gather: bool = False):
     """Bytes / flops the layer's steps must move, per call (definitions in the design doc).
-    With fp8 the dispatched rows and W1 are e4m3 (1 byte) with fp32 per-row scales."""
+    With fp8 the dispatched rows and W1 are e4m3 (1 byte) with fp32 per-row scales.
+    With gather no rows are dispatched: the gate/up GEMM reads the tokens x once."""
     T, H, E, K, I = cfg.T, cfg.H, cfg.E, cfg.K, cfg.I
     active = int((counts > 0).sum())
     meta_disp = T * E * 1 + 4 * N + 12 * C + 4 * T * K + 8 * (E + 1)
     row_b = 1 if fp8 else 2
-    disp = T * H * 2 + C * H * row_b + meta_disp + (4 * C if fp8 else 0)
+    disp = (meta_disp if gather else
+            T * H * 2 + C * H * row_b + meta_disp + (4 * C if fp8 else 0))
     comb = N * H * 2 + T * H * 2 + 4 * T * K
     w_bytes = active * (2 * I * H * row_b + H * I * 2) + (active * 2 * I * 4 if fp8 else 0)
-    ex_bytes = w_bytes + N * H * row_b + 2 * N * I * 2 + N * H * 2
+    ex_bytes = w_bytes + (T * H * 2 if gather else N * H * row_b) + 2 * N * I * 2 + N * H * 2
     ex_flops = 6.0 * N * H * I
     out = {"dispatch_bytes": disp, "combine_bytes": comb, "experts_bytes": ex_bytes,
            "experts_flops": ex_flops, "multihot_bytes": T * K * 12 + T * E * 6}
@@ -189,8 +192,11 @@ def run_ours(args, world, rank, local):
     host_sync = not cfg.sync_free
     n_layers = args.layers
     fp8 = args.fp8
-    if fp8 and cfg.backward:
-        raise SystemExit("--fp8 is the inference path (the e4m3 gate/up GEMM saves nothing for a backward)")
+    gather = args.gather
+    if (fp8 or gather) and cfg.backward:
+        raise SystemExit("--fp8 and --gather are inference paths (the backward reads x_disp)")
+    if fp8 and gather:
+        raise SystemExit("--fp8 and --gather are separate paths")
 
     layers = []
     for l in range(n_layers):
@@ -251,6 +257,11 @@ def run_ours(args, world, rank, local):
             moe.moe_dispatch_fp8(L["x"], rmap, probs, lay, host_sync=host_sync, out=x_q)
             rec(2)
             moe.moe_grouped_experts_fp8(x_q[0], x_q[1], lay, L["W1q"], L["W1s"], L["W2"], out=bufs)
+            rec(3)
+        elif gather:
+            moe.moe_dispatch_layout(rmap, probs, lay, host_sync=host_sync)
+            rec(2)
+            moe.moe_grouped_experts_gather(L["x"], lay, L["W1"], L["W2"], out=bufs)
             rec(3)
         else:
             moe.moe_dispatch(L["x"], rmap, probs, lay, host_sync=host_sync, x_disp=x_disp)
@@ -333,6 +344,8 @@ def run_ours(args, world, rank, local):
         a.record(stream)
         if fp8:
             moe.moe_dispatch_fp8(L["x"], rmap, probs, lay_sf, host_sync=False, out=xq_sf)
+        elif gather:
+            moe.moe_dispatch_layout(rmap, probs, lay_sf, host_sync=False)
         else:
             moe.moe_dispatch(L["x"], rmap, probs, lay_sf, host_sync=False, x_disp=xd_sf)
         b.record(stream)
@@ -442,7 +455,7 @@ def run_ours(args, world, rank, local):
 
     # ---- roofline of the dominant step (the experts' two grouped GEMM launches)
     hbm, bf16_burst, bf16_sust, src = peaks()
-    work = [algorithmic(cfg, L["counts"], r[0], r[1], C, cfg.backward, fp8) for L, r in zip(layers, rows)]
+    work = [algorithmic(cfg, L["counts"], r[0], r[1], C, cfg.backward, fp8, gather) for L, r in zip(layers, rows)]
     mean = lambda key: float(np.mean([w[key] for w in work]))
     # per-step averages over the timed steps (layer i % n_layers)
     steps_w = [work[i % n_layers] for i in range(args.steps)]
@@ -463,7 +476,7 @@ def run_ours(args, world, rank, local):
     else:
         roof = {"bound": "tensor", "achieved": ex_flops / (ex_us * 1e-6) / 1e12, "peak": tc_peak, "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None if (bwd or fp8) else profiled_traffic(cfg.name)
+    roof["traffic"] = None if (bwd or fp8 or gather) else profiled_traffic(cfg.name)
     roof["algorithmic_bytes"] = ex_bytes
     roof["kernel"] = ("experts: grouped_gemm_kernel<0> (gate/up + SwiGLU" + (", e4m3 operands" if fp8 else "")
                       + ") + grouped_gemm_kernel<1> (down x weight)"
@@ -485,7 +498,7 @@ def run_ours(args, world, rank, local):
         "rows_used": [r[0] for r in rows], "rows_valid": [r[1] for r in rows], "capacity": C,
     }
     kernels["dispatch_frac_hbm"] = kernels["dispatch_GBs"] / hbm
-    sf_bytes = float(np.mean([algorithmic(cfg, w_l["counts"], r[0], r[1], worst, False, fp8)["dispatch_bytes"]
+    sf_bytes = float(np.mean([algorithmic(cfg, w_l["counts"], r[0], r[1], worst, False, fp8, gather)["dispatch_bytes"]
                               for w_l, r in zip(layers, rows)]))
     kernels["dispatch_sync_free_us"] = float(np.mean(sf_us))
     kernels["dispatch_sync_free_GBs"] = sf_bytes / (kernels["dispatch_sync_free_us"] * 1e-6) / 1e9
@@ -495,7 +508,8 @@ def run_ours(args, world, rank, local):
     tokens = T * world * args.steps
     res = {
         "metric": "MoE layer tokens/sec (dispatch+experts+combine)" + (", forward + backward" if bwd else "")
-                  + (", FP8 dispatch and gate/up GEMM" if fp8 else ""),
+                  + (", FP8 dispatch and gate/up GEMM" if fp8 else "")
+                  + (", dispatch fused into the gate/up GEMM" if gather else ""),
         "value": tokens / (ms_max * 1e-3),
         "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -593,6 +607,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="qwen3_30b_a3b", choices=sorted(synthetic.CONFIGS))
     ap.add_argument("--layers", type=int, default=4)
+    ap.add_argument("--gather", action="store_true",
+                    help="fuse the dispatch copy into the gate/up GEMM (the layout alone, then "
+                         "A rows gathered from the tokens)")
     ap.add_argument("--fp8", action="store_true",
                     help="run the FP8 dispatch and e4m3 gate/up GEMM instead of the bf16 ones")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")

@@ -61,6 +61,8 @@ SIGNATURES = {
     "moe_router_topk": (c_int32, [_P, c_int32, c_int32, c_int32, _P, _P, _P, _P, _P, _P]),
     "moe_router_topk_backward": (c_int32, [_P, _P, _P, c_int32, c_int32, c_int32, _P, _P]),
     "moe_route_to_multihot": (c_int32, [_P, _P, c_int32, c_int32, c_int32, _P, _P, _P, _P, _P]),
+    "moe_dispatch_layout": (c_int32, [_P, _P, _LP, ctypes.POINTER(c_int64), _P]),
+    "moe_grouped_experts_gather": (c_int32, [_P, _LP, c_int32, c_int32, _P, _P, _P, _P, _P, _P, _P]),
     "moe_dispatch_fp8": (c_int32, [_P, _P, _P, c_int32, _LP, _P, _P, ctypes.POINTER(c_int64), _P]),
     "moe_quantize_fp8": (c_int32, [_P, c_int64, c_int32, _P, _P, _P]),
     "moe_grouped_experts_fp8": (c_int32, [_P, _P, _LP, c_int32, c_int32, _P, _P, _P, _P, _P, _P]),

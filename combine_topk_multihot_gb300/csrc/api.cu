@@ -169,12 +169,15 @@ namespace {
 // then the rows, in bf16 (x_disp) or as e4m3 codes with per-row scales.
 moe_status dispatch_impl(const char* who, const moe_bf16* x, const uint8_t* routing_map,
                          const float* probs, int32_t H, const moe_layout* L, moe_bf16* x_disp,
-                         uint8_t* x_q, float* x_scale, int64_t* rows_host, moe_stream_t stream) {
+                         uint8_t* x_q, float* x_scale, int64_t* rows_host, moe_stream_t stream,
+                         bool layout_only = false) {
   moe_status st = check_layout(L);
   if (st != MOE_OK) return st;
+  if (layout_only) H = 256;  // no rows are copied; any valid hidden size will do
   if ((st = check_hidden(H)) != MOE_OK) return st;
-  MOE_REQUIRE(L->T == 0 || (x && routing_map && probs), MOE_ERR_INVALID_ARG, "%s: NULL input", who);
-  MOE_REQUIRE(L->capacity == 0 || x_disp || (x_q && x_scale), MOE_ERR_INVALID_ARG,
+  MOE_REQUIRE(L->T == 0 || ((x || layout_only) && routing_map && probs), MOE_ERR_INVALID_ARG,
+              "%s: NULL input", who);
+  MOE_REQUIRE(L->capacity == 0 || layout_only || x_disp || (x_q && x_scale), MOE_ERR_INVALID_ARG,
               "%s: NULL output rows", who);
   MOE_REQUIRE(aligned16(x) && aligned16(x_disp) && aligned16(x_q) && aligned16(routing_map),
               MOE_ERR_INVALID_ARG, "%s: x, the output rows and routing_map must be 16-byte aligned",
@@ -210,8 +213,9 @@ moe_status dispatch_impl(const char* who, const moe_bf16* x, const uint8_t* rout
     if ((err = launch_layout(routing_map, probs, *L, L->workspace, LayoutStep::kPlace, stream)) != cudaSuccess)
       return cuda_fail(err, "dispatch: placement");
   }
-  err = x_disp ? launch_row_gather(x, *L, H, x_disp, true, nullptr, nullptr, stream)
-               : launch_row_gather_fp8(x, *L, H, x_q, x_scale, stream);
+  // the rows (or, for the layout alone, just the pad and spare rows' metadata)
+  err = (x_disp || layout_only) ? launch_row_gather(x, *L, H, x_disp, true, nullptr, nullptr, stream)
+                                : launch_row_gather_fp8(x, *L, H, x_q, x_scale, stream);
   if (err != cudaSuccess) return cuda_fail(err, "dispatch: rows");
   return MOE_OK;
 }
@@ -236,6 +240,31 @@ moe_status moe_dispatch_fp8(const moe_bf16* x, const uint8_t* routing_map, const
               "moe_dispatch_fp8: NULL x_disp_q or x_disp_scale");
   return dispatch_impl("moe_dispatch_fp8", x, routing_map, probs, H, L, nullptr, x_disp_q,
                        x_disp_scale, rows_host, stream);
+}
+
+moe_status moe_dispatch_layout(const uint8_t* routing_map, const float* probs, const moe_layout* L,
+                               int64_t* rows_host, moe_stream_t stream) {
+  return dispatch_impl("moe_dispatch_layout", nullptr, routing_map, probs, 256, L, nullptr, nullptr,
+                       nullptr, rows_host, stream, /*layout_only=*/true);
+}
+
+moe_status moe_grouped_experts_gather(const moe_bf16* x, const moe_layout* L, int32_t H, int32_t I,
+                                      const moe_bf16* W1, const moe_bf16* W2, moe_bf16* h,
+                                      moe_bf16* y_disp, moe_bf16* o_save, moe_bf16* gu_save,
+                                      moe_stream_t stream) {
+  moe_status st = check_layout(L);
+  if (st != MOE_OK) return st;
+  if ((st = check_hidden(H)) != MOE_OK) return st;
+  MOE_REQUIRE(I > 0 && I % 128 == 0, MOE_ERR_UNSUPPORTED_SHAPE,
+              "the intermediate size must be a positive multiple of 128 (got %d)", I);
+  MOE_REQUIRE(L->capacity == 0 || ((x || L->T == 0) && W1 && W2 && h && y_disp), MOE_ERR_INVALID_ARG,
+              "moe_grouped_experts_gather: NULL pointer");
+  MOE_REQUIRE(aligned16(x) && aligned16(W1) && aligned16(W2) && aligned16(h) && aligned16(y_disp) &&
+                  aligned16(o_save) && aligned16(gu_save),
+              MOE_ERR_INVALID_ARG, "moe_grouped_experts_gather: pointers must be 16-byte aligned");
+  if ((st = check_device()) != MOE_OK) return st;
+  cudaError_t err = launch_experts_forward_gather(x, *L, H, I, W1, W2, h, y_disp, o_save, gu_save, stream);
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_grouped_experts_gather launch");
 }
 
 moe_status moe_quantize_fp8(const moe_bf16* src, int64_t rows, int32_t cols, uint8_t* codes,

@@ -91,6 +91,10 @@ struct GemmArgs {
   int* status;
   const float* a_scale;    // e4m3 GEMM1: [C] scale of each A row
   const float* b_scale;    // e4m3 GEMM1: [E * 2I] scale of each W1 row (output channel)
+  const uint16_t* x;       // gathered GEMM1: the tokens [T, H]; A row r is x[row_token[r]]
+  const int* row_token;    //   (a zero row where row_token is -1)
+  long long capacity;
+  int H;
 };
 
 // Barriers and scalars; the per-expert tables (offsets [E+1], counts [E],
@@ -134,7 +138,7 @@ __device__ __forceinline__ Tile decode_tile(const int* tile_prefix, int E, int n
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
 
-template <int EPI, int BN, int A_ROWS, int STAGES, int OPS>
+template <int EPI, int BN, int A_ROWS, int STAGES, int OPS, bool GATHER>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
@@ -146,6 +150,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr uint32_t IDESC = OPS == OPS_E4M3 ? F::IDESC_E4M3 : F::IDESC;
   constexpr int BKE = OPS == OPS_E4M3 ? 128 : BK;   // K elements per 128-byte row of a stage
   static_assert(OPS == OPS_BF16 || EPI == EPI_SWIGLU, "e4m3 operands only in the gate/up GEMM");
+  static_assert(!GATHER || (OPS == OPS_BF16 && EPI == EPI_SWIGLU && A_ROWS == BM),
+                "the gathered A is the bf16 gate/up GEMM's, 128 rows per stage");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* tiles = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -163,7 +169,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // ---- set-up: barriers, tensor memory, the device-side tile list
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      mbar_init(smem_u32(&s.full[i]), 1);
+      // gathered A: 32 cp.async arrivals of the producer's lanes + the TMA expect_tx of B
+      mbar_init(smem_u32(&s.full[i]), GATHER ? 33 : 1);
       mbar_init(smem_u32(&s.empty[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -212,7 +219,60 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = s.tmem_base;
   volatile int* abort_flag = &s.abort;
 
-  if (warp == 0) {
+  if (GATHER && warp == 0) {
+    // ================= producer, A gathered from the tokens =================
+    // Lane l copies rows 4l .. 4l + 3 of the A tile with 16-byte cp.async,
+    // into the positions the 128-byte swizzle gives them (chunk c of row r
+    // at r * 128 + ((c ^ (r & 7)) * 16)); lane 0 also loads B by TMA.
+    int stage = 0;
+    uint32_t phase = 0;
+    long long issued = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      const Tile t = decode_tile(s_pre, E, args.n_tiles, tile);
+      const long long row0 = static_cast<long long>(s_off[t.e]) + t.mt * BM;
+      const int b_row = t.e * args.b_rows_per_expert + t.nt * args.b_tile_step;
+      long long src[4];  // element offset of each of this lane's rows in x, or -1
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const long long r = row0 + 4 * lane + q;
+        const int tk = r < args.capacity ? __ldg(args.row_token + r) : -1;
+        src[q] = tk >= 0 ? static_cast<long long>(tk) * args.H : -1;
+      }
+      for (int kb = 0; kb < args.k_blocks; ++kb) {
+        int wok = 1;
+        if (lane == 0) wok = mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, abort_flag);
+        if (!__shfl_sync(FULL_MASK, wok, 0)) { ok = false; break; }
+        const uint32_t full = smem_u32(&s.full[stage]);
+        const uint32_t a_dst = tiles_u32 + stage * STAGE_BYTES;
+        const uint32_t b_dst = a_dst + A_BYTES;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full, B_BYTES);
+          tma_load_2d(b_dst, &tmB, kb * BKE, b_row, full);
+          tma_load_2d(b_dst + B_BYTES / 2, &tmB, kb * BKE, b_row + args.b_second_off, full);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int row = 4 * lane + q;
+          const uint16_t* base = src[q] >= 0 ? args.x + src[q] + kb * BK : args.x;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            cp_async_16(a_dst + row * 128 + ((c ^ (row & 7)) << 4), base + (src[q] >= 0 ? c * 8 : 0),
+                        src[q] >= 0 ? 16u : 0u);
+        }
+        cp_async_mbar_arrive_noinc(full);
+        ++issued;
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (!ok && lane == 0) {
+      for (int i = 0; i < STAGES && i < issued; ++i) {
+        if (--stage < 0) { stage = STAGES - 1; phase ^= 1u; }
+        mbar_wait_drain(smem_u32(&s.full[stage]), phase);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 0) {
     // ================= TMA producer =================
     if (lane == 0) {
       int stage = 0;
@@ -260,6 +320,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t d_tmem = tmem_base + buf * BN;
         for (int kb = 0; kb < args.k_blocks; ++kb) {
           if (!mbar_wait(smem_u32(&s.full[stage]), phase, abort_flag)) { ok = false; break; }
+          if constexpr (GATHER) fence_proxy_async_shared();  // A arrived through cp.async
           tc_fence_after();
           const uint32_t a_addr = tiles_u32 + stage * STAGE_BYTES;
           const uint64_t a_desc = sdesc_k_sw128(a_addr);
@@ -442,7 +503,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // ---------------------------------------------------------------- host side
 
-template <int EPI, int BN, int A_ROWS, int STAGES, int OPS>
+template <int EPI, int BN, int A_ROWS, int STAGES, int OPS, bool GATHER>
 cudaError_t launch_gemm_stages(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
                                const GemmArgs& args, cudaStream_t s) {
   static bool configured[64] = {};
@@ -450,30 +511,32 @@ cudaError_t launch_gemm_stages(const CUtensorMap& a, const CUtensorMap& b, const
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    err = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, BN, A_ROWS, STAGES, OPS>,
+    err = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, BN, A_ROWS, STAGES, OPS, GATHER>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  return launch_dependent(grouped_gemm_kernel<EPI, BN, A_ROWS, STAGES, OPS>, sm_count(), NUM_THREADS,
+  return launch_dependent(grouped_gemm_kernel<EPI, BN, A_ROWS, STAGES, OPS, GATHER>, sm_count(),
+                          NUM_THREADS,
                           smem_bytes(STAGES, Fwd<BN, A_ROWS>::STAGE_BYTES, args.E), s, a, b, out,
                           args);
 }
 
 // The ring depth of Fwd when it fits beside the staging and the per-expert
 // tables, else one stage less (E above about 200).
-template <int EPI, int BN, int A_ROWS, int OPS = OPS_BF16>
+template <int EPI, int BN, int A_ROWS, int OPS = OPS_BF16, bool GATHER = false>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
                         const GemmArgs& args, cudaStream_t s) {
   using F = Fwd<BN, A_ROWS>;
   if (smem_bytes(F::STAGES, F::STAGE_BYTES, args.E) <= static_cast<size_t>(SMEM_LIMIT))
-    return launch_gemm_stages<EPI, BN, A_ROWS, F::STAGES, OPS>(a, b, out, args, s);
-  return launch_gemm_stages<EPI, BN, A_ROWS, F::STAGES - 1, OPS>(a, b, out, args, s);
+    return launch_gemm_stages<EPI, BN, A_ROWS, F::STAGES, OPS, GATHER>(a, b, out, args, s);
+  return launch_gemm_stages<EPI, BN, A_ROWS, F::STAGES - 1, OPS, GATHER>(a, b, out, args, s);
 }
 
 // GEMM1 reads A (x_disp rows) and B (W1) as bf16, or as e4m3 codes with
-// fp32 scales per A row and per W1 row; GEMM2 is bf16.
-template <int BN, int A_ROWS, int OPS>
+// fp32 scales per A row and per W1 row, or (GATHER) A straight from the
+// tokens x by row_token; GEMM2 is bf16.
+template <int BN, int A_ROWS, int OPS, bool GATHER = false>
 cudaError_t experts_forward(const void* x_disp, const float* x_scale, const moe_layout& L, int H,
                             int I, const void* W1, const float* W1_scale, const uint16_t* W2,
                             uint16_t* h, uint16_t* y, uint16_t* o_save, uint16_t* gu_save,
@@ -486,8 +549,9 @@ cudaError_t experts_forward(const void* x_disp, const float* x_scale, const moe_
   const bool maps1 = OPS == OPS_E4M3
                          ? make_tma_2d_u8(&mA1, x_disp, C, H, A_ROWS) &&
                                make_tma_2d_u8(&mB1, W1, w1_rows, H, BN / 2)
-                         : make_tma_2d_bf16(&mA1, x_disp, C, H, A_ROWS) &&
+                         : (GATHER || make_tma_2d_bf16(&mA1, x_disp, C, H, A_ROWS)) &&
                                make_tma_2d_bf16(&mB1, W1, w1_rows, H, BN / 2);
+  if (GATHER) mA1 = mB1;  // unused: the producer gathers A with cp.async
   if (!maps1 || !make_tma_2d_bf16(&mA2, h, C, I, A_ROWS) ||
       !make_tma_2d_bf16(&mB2, W2, static_cast<uint64_t>(L.E) * H, I, BN / 2) ||
       !make_tma_store_2d_bf16(&mH, h, C, I) || !make_tma_store_2d_bf16(&mY, y, C, H))
@@ -512,7 +576,11 @@ cudaError_t experts_forward(const void* x_disp, const float* x_scale, const moe_
   g1.status = L.status;
   g1.a_scale = x_scale;
   g1.b_scale = W1_scale;
-  cudaError_t err = launch_gemm<EPI_SWIGLU, BN, A_ROWS, OPS>(mA1, mB1, mH, g1, s);
+  g1.x = static_cast<const uint16_t*>(x_disp);  // GATHER: the tokens
+  g1.row_token = L.row_token;
+  g1.capacity = L.capacity;
+  g1.H = H;
+  cudaError_t err = launch_gemm<EPI_SWIGLU, BN, A_ROWS, OPS, GATHER>(mA1, mB1, mH, g1, s);
   if (err != cudaSuccess) return err;
 
   GemmArgs g2 = g1;
@@ -576,6 +644,20 @@ cudaError_t launch_experts_forward(const uint16_t* x_disp, const moe_layout& L, 
     return launch_experts_forward_gemv(x_disp, L, H, I, W1, W2, h, y, s);
   return experts_forward_any<OPS_BF16>(x_disp, nullptr, L, H, I, W1, nullptr, W2, h, y, o_save,
                                        gu_save, s);
+}
+
+cudaError_t launch_experts_forward_gather(const uint16_t* x, const moe_layout& L, int H, int I,
+                                          const uint16_t* W1, const uint16_t* W2, uint16_t* h,
+                                          uint16_t* y, uint16_t* o_save, uint16_t* gu_save,
+                                          cudaStream_t s) {
+  if (L.capacity == 0) return cudaSuccess;
+  if (gemv_experts_fits(L, H, I, o_save || gu_save))
+    return launch_experts_forward_gemv(x, L, H, I, W1, W2, h, y, s, /*gather=*/true);
+  if (pick_shape(L, I, gu_save != nullptr) == Shape::kWide)
+    return experts_forward<256, 128, OPS_BF16, true>(x, nullptr, L, H, I, W1, nullptr, W2, h, y,
+                                                     o_save, gu_save, s);
+  return experts_forward<64, 128, OPS_BF16, true>(x, nullptr, L, H, I, W1, nullptr, W2, h, y, o_save,
+                                                  gu_save, s);
 }
 
 cudaError_t launch_experts_forward_fp8(const uint8_t* x_q, const float* x_scale,

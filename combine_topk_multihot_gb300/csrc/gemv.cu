@@ -35,7 +35,8 @@ struct GemvArgs {
   const int* offsets;      // [E + 1]
   const float* row_weight; // [C]
   int E, H, I;
-  const uint16_t* a;       // step 1: x_disp [C, H]; step 2: h [C, I]
+  const uint16_t* a;       // step 1: x_disp [C, H] (or x [T, H], see row_token); step 2: h [C, I]
+  const int* row_token;    // step 1 with the dispatch fused: row r of A is x[row_token[r]]
   const uint16_t* w;       // step 1: W1 [E, 2I, H]; step 2: W2 [E, H, I]
   uint16_t* out;           // step 1: h [C, I];      step 2: y [C, H]
 };
@@ -130,8 +131,12 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_experts_kernel(GemvArgs arg
     const int n = min(args.counts[e], GEMV_ROWS);
     const long long r0 = args.offsets[e];
     // the expert's rows of A into shared memory
-    const uint4* a4 = reinterpret_cast<const uint4*>(args.a + r0 * K);
-    for (int i = threadIdx.x; i < n * (K >> 3); i += GEMV_THREADS) s_a[i] = __ldg(a4 + i);
+    const int NV = K >> 3;
+    for (int i = threadIdx.x; i < n * NV; i += GEMV_THREADS) {
+      const int r = i / NV;
+      const long long src_row = args.row_token ? __ldg(args.row_token + r0 + r) : r0 + r;
+      s_a[i] = __ldg(reinterpret_cast<const uint4*>(args.a + src_row * K) + (i - r * NV));
+    }
     __syncthreads();
     if (STEP == 1) {
       // warp: h column c -> W1 rows c (gate) and I + c (up), in one pass
@@ -184,7 +189,7 @@ bool gemv_experts_fits(const moe_layout& L, int H, int I, bool saves) {
 
 cudaError_t launch_experts_forward_gemv(const uint16_t* x_disp, const moe_layout& L, int H, int I,
                                         const uint16_t* W1, const uint16_t* W2, uint16_t* h,
-                                        uint16_t* y, cudaStream_t s) {
+                                        uint16_t* y, cudaStream_t s, bool gather) {
   GemvArgs a{};
   a.counts = L.tokens_per_expert;
   a.offsets = L.offsets;
@@ -197,6 +202,7 @@ cudaError_t launch_experts_forward_gemv(const uint16_t* x_disp, const moe_layout
   const long long active = pairs < L.E ? pairs : L.E;
   const long long cap = 8LL * sm_count();
   a.a = x_disp;
+  a.row_token = gather ? L.row_token : nullptr;
   a.w = W1;
   a.out = h;
   long long items = active * (I / S1_COLS);
@@ -205,6 +211,7 @@ cudaError_t launch_experts_forward_gemv(const uint16_t* x_disp, const moe_layout
   cudaError_t err = launch_dependent(gemv_experts_kernel<1>, grid, GEMV_THREADS, smem, s, a);
   if (err != cudaSuccess) return err;
   a.a = h;
+  a.row_token = nullptr;
   a.w = W2;
   a.out = y;
   items = active * (H / S2_COLS);

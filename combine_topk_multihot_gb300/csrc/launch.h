@@ -109,9 +109,16 @@ cudaError_t launch_experts_forward(const uint16_t* x_disp, const moe_layout& L, 
 // a5 on the CUDA cores for layers with at most 4 rows per expert (T <= 4)
 // and nothing saved for a backward: weight streaming with warp dot products.
 bool gemv_experts_fits(const moe_layout& L, int H, int I, bool saves);
+// With gather, x_disp is the tokens x and row r of A is x[row_token[r]].
 cudaError_t launch_experts_forward_gemv(const uint16_t* x_disp, const moe_layout& L, int H, int I,
                                         const uint16_t* W1, const uint16_t* W2, uint16_t* h,
-                                        uint16_t* y, cudaStream_t s);
+                                        uint16_t* y, cudaStream_t s, bool gather = false);
+// a4 fused into a5: GEMM1's producer gathers the A rows from x by row_token
+// (zero rows for pad and spare rows); no x_disp is written or read.
+cudaError_t launch_experts_forward_gather(const uint16_t* x, const moe_layout& L, int H, int I,
+                                          const uint16_t* W1, const uint16_t* W2, uint16_t* h,
+                                          uint16_t* y, uint16_t* o_save, uint16_t* gu_save,
+                                          cudaStream_t s);
 
 // FP8: a4 with e4m3 rows (one fp32 scale per row; pad and spare rows zero
 // codes, scale 0, sentinel metadata), and rowwise e4m3 quantization of a

@@ -331,6 +331,7 @@ __global__ void __launch_bounds__(256) row_scatter_kernel(
   for (long long it = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
        it < items; it += nwarps) {
     if (it < T) {
+      if (META && dst == nullptr) continue;  // the layout alone: no rows to copy
       const long long t = it;
       const uint4* s = reinterpret_cast<const uint4*>(src + t * H);
       // The token's rows, 32 slots per load (a token's valid slots come first).
@@ -398,6 +399,7 @@ __global__ void __launch_bounds__(256) row_scatter_kernel(
         }
         if (DOT) grad_w[r] = 0.f;
       }
+      if (dst == nullptr) continue;
       uint4* d = reinterpret_cast<uint4*>(dst + r * H);
       const uint4 z = make_uint4(0, 0, 0, 0);
       for (int v = 0; v < V; ++v) d[lane + 32 * v] = z;

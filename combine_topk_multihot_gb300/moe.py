@@ -173,6 +173,35 @@ def moe_dispatch(x: torch.Tensor, routing_map: torch.Tensor, probs: torch.Tensor
     return x_disp, ((int(rows[0]), int(rows[1])) if host_sync else None)
 
 
+def moe_dispatch_layout(routing_map: torch.Tensor, probs: torch.Tensor, layout: Layout,
+                        host_sync: bool = True, stream=None):
+    """a2-a3 alone (no rows copied): fills ``layout``; returns (R, N) or None."""
+    rows = (ctypes.c_int64 * 2)() if host_sync else None
+    _check(N.lib.moe_dispatch_layout(_ptr(routing_map), _ptr(probs), layout.ref, rows, _stream(stream)),
+           "moe_dispatch_layout")
+    return (int(rows[0]), int(rows[1])) if host_sync else None
+
+
+def moe_grouped_experts_gather(x: torch.Tensor, layout: Layout, W1: torch.Tensor, W2: torch.Tensor,
+                               save_o: bool = False, save_gu: bool = False, out=None, stream=None):
+    """a4 fused into a5: the gate/up GEMM reads its rows from the tokens ``x``
+    by the layout's row_token.  Returns dict(h, y, o, gu) as moe_grouped_experts."""
+    _bf16(x, "x")
+    E, twoI, H = W1.shape
+    I = twoI // 2
+    C = layout.capacity
+    dev = x.device
+    o = out or {}
+    h = o.get("h") if o.get("h") is not None else torch.empty(C, I, dtype=torch.bfloat16, device=dev)
+    y = o.get("y") if o.get("y") is not None else torch.empty(C, H, dtype=torch.bfloat16, device=dev)
+    o_save = (o.get("o") if o.get("o") is not None else torch.empty(C, H, dtype=torch.bfloat16, device=dev)) if save_o else None
+    gu = (o.get("gu") if o.get("gu") is not None else torch.empty(C, 2 * I, dtype=torch.bfloat16, device=dev)) if save_gu else None
+    _check(N.lib.moe_grouped_experts_gather(_ptr(x), layout.ref, H, I, _ptr(W1), _ptr(W2), _ptr(h), _ptr(y),
+                                            _ptr(o_save), _ptr(gu), _stream(stream)),
+           "moe_grouped_experts_gather")
+    return {"h": h, "y": y, "o": o_save, "gu": gu}
+
+
 def moe_dispatch_fp8(x: torch.Tensor, routing_map: torch.Tensor, probs: torch.Tensor, layout: Layout,
                      host_sync: bool = True, out=None, stream=None):
     """a4 in e4m3: fills ``layout`` and returns (x_disp_q uint8 [C, H],

@@ -198,6 +198,16 @@ MOE_API moe_status moe_dispatch(const moe_bf16* x, const uint8_t* routing_map, c
                         int64_t* rows_host, moe_stream_t stream);
 
 /*
+ * a2-a3 alone: the layout of moe_dispatch (counts, offsets, totals, row
+ * metadata, with the pad and spare rows' sentinel metadata) without copying
+ * any rows -- for moe_grouped_experts_gather, which reads the tokens itself.
+ * Modes, rows_host and errors as in moe_dispatch.
+ */
+MOE_API moe_status moe_dispatch_layout(const uint8_t* routing_map, const float* probs,
+                                       const moe_layout* L, int64_t* rows_host,
+                                       moe_stream_t stream);
+
+/*
  * a4 in FP8 ([DEP] What this adds, scope note: FP8 dispatch, half the
  * dispatch bytes, is the named follow-up).  As moe_dispatch, but the rows are
  * float8 e4m3 codes with one fp32 scale per row:
@@ -279,6 +289,19 @@ MOE_API moe_status moe_grouped_experts(const moe_bf16* x_disp, const moe_layout*
                                moe_bf16* h, moe_bf16* y_disp,
                                moe_bf16* o_save, moe_bf16* gu_save,
                                moe_stream_t stream);
+
+/*
+ * a4 fused into a5 ([DEP] Expanded layout: the experts see their own rows):
+ * as moe_grouped_experts, but the gate/up GEMM gathers its A rows straight
+ * from the tokens, row r being x[row_token[r]] (zeros where row_token is -1),
+ * so no x_disp is written or read.  x [T, H] bf16; L from moe_dispatch_layout
+ * (or moe_dispatch).  The outputs equal moe_grouped_experts' on the x_disp
+ * moe_dispatch would have written, bit for bit.
+ */
+MOE_API moe_status moe_grouped_experts_gather(const moe_bf16* x, const moe_layout* L, int32_t H,
+                                              int32_t I, const moe_bf16* W1, const moe_bf16* W2,
+                                              moe_bf16* h, moe_bf16* y_disp, moe_bf16* o_save,
+                                              moe_bf16* gu_save, moe_stream_t stream);
 
 /*
  * a5 with the gate/up GEMM on e4m3 operands: x_disp_q / x_disp_scale from
