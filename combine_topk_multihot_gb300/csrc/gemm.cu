@@ -45,6 +45,10 @@ constexpr int BK = 64;           // bf16 elements per 128-byte swizzled row (128
 constexpr int UMMA_K = 16;       // K per tcgen05.mma for 16-bit inputs
 constexpr int EPI_WARPS = 8;                   // two per TMEM lane quarter
 constexpr int NUM_THREADS = 32 * (2 + EPI_WARPS);
+// The gathered-A kernel adds three producer warps (10..12) to warp 0: each of
+// the four copies 32 rows of the A tile, one row per lane.
+constexpr int GATHER_WARPS = 4;
+constexpr int NUM_THREADS_GATHER = NUM_THREADS + 32 * (GATHER_WARPS - 1);
 constexpr int MAX_STAGES = 16;                 // barrier slots (the ring uses up to this many)
 constexpr int SMEM_LIMIT = 232448;             // dynamic shared memory per CTA
 
@@ -139,7 +143,7 @@ __device__ __forceinline__ Tile decode_tile(const int* tile_prefix, int E, int n
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
 
 template <int EPI, int BN, int A_ROWS, int STAGES, int OPS, bool GATHER>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmOut, const GemmArgs args) {
@@ -169,8 +173,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // ---- set-up: barriers, tensor memory, the device-side tile list
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      // gathered A: 32 cp.async arrivals of the producer's lanes + the TMA expect_tx of B
-      mbar_init(smem_u32(&s.full[i]), GATHER ? 33 : 1);
+      // gathered A: the cp.async arrivals of the producer lanes + the TMA expect_tx of B
+      mbar_init(smem_u32(&s.full[i]), GATHER ? 32 * GATHER_WARPS + 1 : 1);
       mbar_init(smem_u32(&s.empty[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -186,8 +190,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   if (warp == 1) tmem_alloc(smem_u32(&s.tmem_base), TMEM_COLS);
   griddep_wait();  // the layout, the dispatched rows (and h) come from earlier kernels
-  for (int e = threadIdx.x; e <= E; e += NUM_THREADS) s_off[e] = args.offsets[e];
-  for (int e = threadIdx.x; e < E; e += NUM_THREADS) s_cnt[e] = args.counts[e];
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) s_off[e] = args.offsets[e];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = args.counts[e];
   __syncthreads();
   if (warp == 0) {  // exclusive scan of per-expert tile counts
     int running = 0;
@@ -219,26 +223,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = s.tmem_base;
   volatile int* abort_flag = &s.abort;
 
-  if (GATHER && warp == 0) {
-    // ================= producer, A gathered from the tokens =================
-    // Lane l copies rows 4l .. 4l + 3 of the A tile with 16-byte cp.async,
-    // into the positions the 128-byte swizzle gives them (chunk c of row r
-    // at r * 128 + ((c ^ (r & 7)) * 16)); lane 0 also loads B by TMA.
+  if (GATHER && (warp == 0 || warp >= 2 + EPI_WARPS)) {
+    // ================= producers, A gathered from the tokens =================
+    // Producer warp pw (warp 0, then 10..12) copies rows 32 pw .. 32 pw + 31 of
+    // the A tile, lane l row 32 pw + l, with 16-byte cp.async into the
+    // positions the 128-byte swizzle gives them (chunk c of row r at r * 128 +
+    // ((c ^ (r & 7)) * 16)); warp 0's lane 0 also loads B by TMA.
+    const int pw = warp == 0 ? 0 : warp - (1 + EPI_WARPS);
+    const int row = 32 * pw + lane;
     int stage = 0;
     uint32_t phase = 0;
     long long issued = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       const Tile t = decode_tile(s_pre, E, args.n_tiles, tile);
-      const long long row0 = static_cast<long long>(s_off[t.e]) + t.mt * BM;
+      const long long r = static_cast<long long>(s_off[t.e]) + t.mt * BM + row;
       const int b_row = t.e * args.b_rows_per_expert + t.nt * args.b_tile_step;
-      long long src[4];  // element offset of each of this lane's rows in x, or -1
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const long long r = row0 + 4 * lane + q;
-        const int tk = r < args.capacity ? __ldg(args.row_token + r) : -1;
-        src[q] = tk >= 0 ? static_cast<long long>(tk) * args.H : -1;
-      }
+      const int tk = r < args.capacity ? __ldg(args.row_token + r) : -1;
+      const uint16_t* src = tk >= 0 ? args.x + static_cast<long long>(tk) * args.H : args.x;
+      const uint32_t nbytes = tk >= 0 ? 16u : 0u;  // a zero row where there is no token
       for (int kb = 0; kb < args.k_blocks; ++kb) {
         int wok = 1;
         if (lane == 0) wok = mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, abort_flag);
@@ -246,26 +249,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t full = smem_u32(&s.full[stage]);
         const uint32_t a_dst = tiles_u32 + stage * STAGE_BYTES;
         const uint32_t b_dst = a_dst + A_BYTES;
-        if (lane == 0) {
+        if (pw == 0 && lane == 0) {
           mbar_arrive_expect_tx(full, B_BYTES);
           tma_load_2d(b_dst, &tmB, kb * BKE, b_row, full);
           tma_load_2d(b_dst + B_BYTES / 2, &tmB, kb * BKE, b_row + args.b_second_off, full);
         }
+        const uint16_t* src_k = tk >= 0 ? src + kb * BK : src;
+        const uint32_t row_dst = a_dst + row * 128;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int row = 4 * lane + q;
-          const uint16_t* base = src[q] >= 0 ? args.x + src[q] + kb * BK : args.x;
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            cp_async_16(a_dst + row * 128 + ((c ^ (row & 7)) << 4), base + (src[q] >= 0 ? c * 8 : 0),
-                        src[q] >= 0 ? 16u : 0u);
-        }
+        for (int c = 0; c < 8; ++c)
+          cp_async_16(row_dst + ((c ^ (row & 7)) << 4), src_k + (tk >= 0 ? c * 8 : 0), nbytes);
         cp_async_mbar_arrive_noinc(full);
         ++issued;
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
     }
-    if (!ok && lane == 0) {
+    if (!ok && pw == 0 && lane == 0) {
       for (int i = 0; i < STAGES && i < issued; ++i) {
         if (--stage < 0) { stage = STAGES - 1; phase ^= 1u; }
         mbar_wait_drain(smem_u32(&s.full[stage]), phase);
@@ -517,7 +516,7 @@ cudaError_t launch_gemm_stages(const CUtensorMap& a, const CUtensorMap& b, const
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
   return launch_dependent(grouped_gemm_kernel<EPI, BN, A_ROWS, STAGES, OPS, GATHER>, sm_count(),
-                          NUM_THREADS,
+                          GATHER ? NUM_THREADS_GATHER : NUM_THREADS,
                           smem_bytes(STAGES, Fwd<BN, A_ROWS>::STAGE_BYTES, args.E), s, a, b, out,
                           args);
 }
