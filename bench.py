@@ -110,6 +110,8 @@ class ClockSampler:
         self.lines = []
 
     def __enter__(self):
+        import threading
+        self._first = threading.Event()
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
@@ -117,6 +119,20 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
+            return self
+
+        def read():
+            for line in self.proc.stdout:
+                if line.strip():
+                    self.lines.append(line)
+                    self._first.set()
+
+        self._reader = threading.Thread(target=read, daemon=True)
+        self._reader.start()
+        # nvidia-smi's start-up (NVML initialisation) can hold driver locks
+        # that stall the host's CUDA calls for tens of milliseconds: let it
+        # finish before the timed region starts.
+        self._first.wait(timeout=5.0)
         return self
 
     def __exit__(self, *a):
@@ -124,11 +140,10 @@ class ClockSampler:
             time.sleep(0.15)
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+            self._reader.join(timeout=5)
 
     def summary(self):
         sm, mx, reasons = [], None, set()

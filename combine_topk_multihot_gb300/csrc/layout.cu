@@ -182,12 +182,22 @@ __global__ void __launch_bounds__(256) layout_kernel(LayoutArgs a) {
     for (int e = blockIdx.x * nwarps + warp; e < E; e += gridDim.x * nwarps) {
       int* row = a.chunk_counts + static_cast<long long>(e) * a.chunks;
       int run = 0;
-      for (int c0 = 0; c0 < a.chunks; c0 += 32) {
-        const int c = c0 + lane;
-        const int v = c < a.chunks ? __ldcg(row + c) : 0;
-        const int incl = warp_inclusive_scan(v, lane);
-        if (c < a.chunks) row[c] = run + incl - v;
-        run += __shfl_sync(FULL_MASK, incl, 31);
+      // 8 coalesced steps of 32 chunks per batch: the loads of a batch are
+      // issued together, then scanned in order
+      for (int b0 = 0; b0 < a.chunks; b0 += 8 * 32) {
+        int v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int c = b0 + 32 * i + lane;
+          v[i] = c < a.chunks ? __ldcg(row + c) : 0;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int c = b0 + 32 * i + lane;
+          const int incl = warp_inclusive_scan(v[i], lane);
+          if (c < a.chunks) row[c] = run + incl - v[i];
+          run += __shfl_sync(FULL_MASK, incl, 31);
+        }
       }
       if (lane == 0) a.tokens_per_expert[e] = run;
     }
