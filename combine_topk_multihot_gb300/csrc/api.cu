@@ -5,6 +5,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "launch.h"
@@ -30,6 +31,33 @@ moe_status cuda_fail(cudaError_t err, const char* where) {
 constexpr int MAX_DEVICES = 64;
 int g_cc_ok[MAX_DEVICES];    // 0 unknown, 1 compute capability 10.3, -1 other
 int g_sms[MAX_DEVICES];
+
+// The host-synced dispatch reads R, N and the status word from 16 bytes of
+// mapped pinned host memory that the count kernel writes directly, so the
+// readback needs no copy engine and cannot queue behind bulk copies on other
+// streams.  One buffer per device, made on first use; the mutex is held from
+// the launch to the read, so concurrent host-synced calls take turns.
+std::mutex g_rb_mu;
+int* g_rb_host[MAX_DEVICES];
+int* g_rb_dev[MAX_DEVICES];
+
+bool readback_buffer(int dev, int** host, int** dev_ptr) {
+  if (dev < 0 || dev >= MAX_DEVICES) return false;
+  if (!g_rb_host[dev]) {
+    void* h = nullptr;
+    void* d = nullptr;
+    if (cudaHostAlloc(&h, 16, cudaHostAllocMapped) != cudaSuccess) return false;
+    if (cudaHostGetDevicePointer(&d, h, 0) != cudaSuccess) {
+      cudaFreeHost(h);
+      return false;
+    }
+    g_rb_host[dev] = static_cast<int*>(h);
+    g_rb_dev[dev] = static_cast<int*>(d);
+  }
+  *host = g_rb_host[dev];
+  *dev_ptr = g_rb_dev[dev];
+  return true;
+}
 
 moe_status check_device() {
   int dev = 0;
@@ -194,13 +222,32 @@ moe_status dispatch_impl(const char* who, const moe_bf16* x, const uint8_t* rout
     if ((err = launch_layout(routing_map, probs, *L, L->workspace, LayoutStep::kAll, stream)) != cudaSuccess)
       return cuda_fail(err, "dispatch: layout");
   } else {
-    if ((err = launch_layout(routing_map, probs, *L, L->workspace, LayoutStep::kCounts, stream)) != cudaSuccess)
-      return cuda_fail(err, "dispatch: counts");
     int32_t tot[2] = {0, 0}, dev_status = 0;
-    if ((err = cudaMemcpyAsync(tot, L->totals, sizeof(tot), cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
-        (err = cudaMemcpyAsync(&dev_status, L->status, sizeof(int32_t), cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
-        (err = cudaStreamSynchronize(stream)) != cudaSuccess)
+    int dev = 0;
+    int *rb_host = nullptr, *rb_dev = nullptr;
+    std::unique_lock<std::mutex> rb_lock(g_rb_mu);
+    const bool mapped = cudaGetDevice(&dev) == cudaSuccess && readback_buffer(dev, &rb_host, &rb_dev);
+    if (mapped) {
+      volatile int* rb = rb_host;
+      rb[0] = rb[1] = rb[2] = -1;  // overwritten by the count kernel when it completes
+    } else {
+      rb_lock.unlock();
+    }
+    if ((err = launch_layout(routing_map, probs, *L, L->workspace, LayoutStep::kCounts, stream,
+                             mapped ? rb_dev : nullptr)) != cudaSuccess)
+      return cuda_fail(err, "dispatch: counts");
+    if ((err = cudaStreamSynchronize(stream)) != cudaSuccess)
+      return cuda_fail(err, "dispatch: waiting for the row counts");
+    volatile int* rb = rb_host;
+    if (mapped && rb[0] >= 0) {
+      tot[0] = rb[0];
+      tot[1] = rb[1];
+      dev_status = rb[2];
+    } else if ((err = cudaMemcpy(tot, L->totals, sizeof(tot), cudaMemcpyDeviceToHost)) != cudaSuccess ||
+               (err = cudaMemcpy(&dev_status, L->status, sizeof(int32_t), cudaMemcpyDeviceToHost)) != cudaSuccess) {
       return cuda_fail(err, "dispatch: reading the row counts");
+    }
+    if (rb_lock.owns_lock()) rb_lock.unlock();
     rows_host[0] = tot[0];
     rows_host[1] = tot[1];
     if (dev_status & MOE_DEVERR_TIMEOUT)

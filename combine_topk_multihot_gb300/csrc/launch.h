@@ -87,8 +87,11 @@ enum class LayoutStep {
 
 // Counts, padded offsets and the stable placement of every (token, expert)
 // pair.  workspace: layout_counter_bytes(T, E) + 256 bytes.
+// readback (kCounts only, may be NULL): device address of 3 ints of
+// host-mapped memory that receive R, N and the status word.
 cudaError_t launch_layout(const uint8_t* routing_map, const float* probs, const moe_layout& L,
-                          void* workspace, LayoutStep step, cudaStream_t s);
+                          void* workspace, LayoutStep step, cudaStream_t s,
+                          int* readback = nullptr);
 // Rows of the expanded layout from token rows (a4: x -> x_disp, plus the pad /
 // spare rows' metadata when from_offsets); also the combine backward (a7)
 // with the optional routing-weight gradient (a8).  Each token row is read

@@ -108,6 +108,7 @@ struct LayoutArgs {
   float* row_weight;
   int* token_row;
   int* status;
+  int* readback;  // LAYOUT_COUNT: {R, N, status} in host-mapped memory, or NULL
 };
 
 // a2 + a3 in one kernel.  A chunk is 32 tokens.
@@ -236,6 +237,11 @@ __global__ void __launch_bounds__(256) layout_kernel(LayoutArgs a) {
         a.totals[0] = R;
         a.totals[1] = N;
         if (R > a.capacity) report(a.status, MOE_DEVERR_CAPACITY);
+        if (a.readback) {  // for the host-synced caller, without a copy engine
+          a.readback[0] = R;
+          a.readback[1] = N;
+          a.readback[2] = *reinterpret_cast<volatile int*>(a.status);
+        }
       }
     }
     __syncthreads();
@@ -480,8 +486,9 @@ cudaError_t launch_layout_mode(const LayoutArgs& a, size_t smem, cudaStream_t s)
 }  // namespace
 
 cudaError_t launch_layout(const uint8_t* routing_map, const float* probs, const moe_layout& L,
-                          void* workspace, LayoutStep step, cudaStream_t s) {
+                          void* workspace, LayoutStep step, cudaStream_t s, int* readback) {
   LayoutArgs a;
+  a.readback = step == LayoutStep::kCounts ? readback : nullptr;
   a.map = routing_map;
   a.probs = probs;
   a.T = L.T;
