@@ -218,8 +218,12 @@ moe_status dispatch_impl(const char* who, const moe_bf16* x, const uint8_t* rout
   if ((st = check_device()) != MOE_OK) return st;
 
   cudaError_t err;
+  bool rows_done = false;  // the layout kernel did the row pass itself
   if (!rows_host) {
-    if ((err = launch_layout(routing_map, probs, *L, L->workspace, LayoutStep::kAll, stream)) != cudaSuccess)
+    const bool bf16_rows = x_disp || layout_only;
+    if ((err = launch_layout(routing_map, probs, *L, L->workspace, LayoutStep::kAll, stream, nullptr,
+                             reinterpret_cast<const uint16_t*>(x), reinterpret_cast<uint16_t*>(x_disp), H,
+                             bf16_rows ? &rows_done : nullptr)) != cudaSuccess)
       return cuda_fail(err, "dispatch: layout");
   } else {
     int32_t tot[2] = {0, 0}, dev_status = 0;
@@ -261,6 +265,7 @@ moe_status dispatch_impl(const char* who, const moe_bf16* x, const uint8_t* rout
       return cuda_fail(err, "dispatch: placement");
   }
   // the rows (or, for the layout alone, just the pad and spare rows' metadata)
+  if (rows_done) return MOE_OK;
   err = (x_disp || layout_only) ? launch_row_gather(x, *L, H, x_disp, true, nullptr, nullptr, stream)
                                 : launch_row_gather_fp8(x, *L, H, x_q, x_scale, stream);
   if (err != cudaSuccess) return cuda_fail(err, "dispatch: rows");

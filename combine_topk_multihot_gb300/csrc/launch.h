@@ -89,9 +89,14 @@ enum class LayoutStep {
 // pair.  workspace: layout_counter_bytes(T, E) + 256 bytes.
 // readback (kCounts only, may be NULL): device address of 3 ints of
 // host-mapped memory that receive R, N and the status word.
+// rows_done (kAll only, may be NULL): when the layout runs as one CTA and the
+// dispatch's row pass is small, that CTA also does the row pass (x -> x_disp,
+// or only the pad and spare rows' metadata when x_disp is NULL) and sets
+// *rows_done; otherwise *rows_done is false and the caller runs the row pass.
 cudaError_t launch_layout(const uint8_t* routing_map, const float* probs, const moe_layout& L,
                           void* workspace, LayoutStep step, cudaStream_t s,
-                          int* readback = nullptr);
+                          int* readback = nullptr, const uint16_t* x = nullptr,
+                          uint16_t* x_disp = nullptr, int H = 0, bool* rows_done = nullptr);
 // Rows of the expanded layout from token rows (a4: x -> x_disp, plus the pad /
 // spare rows' metadata when from_offsets); also the combine backward (a7)
 // with the optional routing-weight gradient (a8).  Each token row is read

@@ -86,6 +86,11 @@ __device__ bool grid_barrier(unsigned* ctr, unsigned target, int* status, int* s
   return *s_ok != 0;
 }
 
+// The single-CTA layout also does the dispatch's row pass when it has at most
+// this many items (tokens + rows) and moves at most this many bytes.
+constexpr long long LAYOUT_FUSED_ITEMS = 64;
+constexpr long long LAYOUT_FUSED_BYTES = 256 * 1024;
+
 enum LayoutMode : int {
   LAYOUT_ALL = 0,    // counts, scans, offsets and placement: one cooperative launch
   LAYOUT_COUNT = 1,  // counts, scans and offsets only (cooperative), for the host-synced path
@@ -109,7 +114,115 @@ struct LayoutArgs {
   int* token_row;
   int* status;
   int* readback;  // LAYOUT_COUNT: {R, N, status} in host-mapped memory, or NULL
+  // LAYOUT_SINGLE with rows: the CTA also does the dispatch's row pass (the
+  // copies into x_disp when it is not NULL, and the pad and spare rows)
+  bool rows;
+  const uint16_t* x;
+  uint16_t* x_disp;
+  int H;
 };
+
+// Dispatch (and the combine's backward) as a scatter, one warp per item.
+//   Items [0, T) are tokens: the warp reads the token's source row once from
+//   memory -- later passes over it hit L1 -- and writes it to each of the
+//   token's rows (token_row).  Reading each token once matters when [T, H]
+//   no longer fits in L2: a per-row gather would fetch it K times from DRAM.
+//   With DOT it also forms grad_w[r] = <src[t], o_save[r]> in fp32.
+//   Items [T, T + C) are rows: a pad or spare row is zeroed (and grad_w = 0).
+//   With META the row's validity comes from offsets / counts and the pad and
+//   spare rows get their metadata here (token -1, the sentinel expert, weight
+//   0); without it, from row_token (the combine's backward, after dispatch).
+// This is one warp's share: items first, first + stride, ...  With META,
+// s_off / s_cnt are the offsets and counts (shared memory, or global memory
+// this CTA wrote before a barrier).
+template <bool META, bool DOT>
+__device__ __forceinline__ void scatter_items(
+    long long first, long long stride, const uint16_t* __restrict__ src, int T, int K, int H, int E,
+    long long C, const int* __restrict__ token_row, const int* s_off, const int* s_cnt,
+    int* __restrict__ row_token, int* __restrict__ row_expert, float* __restrict__ row_weight,
+    uint16_t* __restrict__ dst, const uint16_t* __restrict__ o_save, float* __restrict__ grad_w) {
+  const int lane = threadIdx.x & 31;
+  const int V = H >> 8;  // 16-byte vectors per lane
+  const long long items = T + C;
+  const int R = META ? s_off[E] : 0;
+  for (long long it = first; it < items; it += stride) {
+    if (it < T) {
+      if (META && dst == nullptr) continue;  // the layout alone: no rows to copy
+      const long long t = it;
+      const uint4* s = reinterpret_cast<const uint4*>(src + t * H);
+      // The token's rows, 32 slots per load (a token's valid slots come first).
+      int r_lane = -1;
+      for (int j = 0; j < K; ++j) {
+        // (L2 load: the layout kernel itself may have just written token_row)
+        if ((j & 31) == 0) r_lane = j + lane < K ? __ldcg(token_row + t * K + j + lane) : -1;
+        const int r = __shfl_sync(FULL_MASK, r_lane, j & 31);
+        if (r < 0) break;
+        uint4* d = reinterpret_cast<uint4*>(dst + static_cast<long long>(r) * H);
+        const uint4* o = DOT ? reinterpret_cast<const uint4*>(o_save + static_cast<long long>(r) * H) : nullptr;
+        float dot = 0.f;
+        for (int v0 = 0; v0 < V; v0 += 8) {
+          uint4 buf[8], ob[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (v0 + i < V) {
+              buf[i] = __ldg(s + lane + 32 * (v0 + i));
+              if (DOT) ob[i] = __ldg(o + lane + 32 * (v0 + i));
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (v0 + i < V) {
+              d[lane + 32 * (v0 + i)] = buf[i];
+              if (DOT) {
+                const uint32_t g[4] = {buf[i].x, buf[i].y, buf[i].z, buf[i].w};
+                const uint32_t q[4] = {ob[i].x, ob[i].y, ob[i].z, ob[i].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  dot = fmaf(bf16_lo(g[k]), bf16_lo(q[k]), dot);
+                  dot = fmaf(bf16_hi(g[k]), bf16_hi(q[k]), dot);
+                }
+              }
+            }
+          }
+        }
+        if (DOT) {
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(FULL_MASK, dot, off);
+          if (lane == 0) grad_w[r] = dot;
+        }
+      }
+    } else {
+      const long long r = it - T;
+      bool pad;
+      if (META) {
+        pad = true;
+        if (r < R) {
+          int lo = 0, hi = E;  // s_off[lo] <= r < s_off[hi]
+          while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_off[mid] <= r) lo = mid; else hi = mid;
+          }
+          pad = r - s_off[lo] >= s_cnt[lo];
+        }
+      } else {
+        pad = __ldg(row_token + r) < 0;
+      }
+      if (!pad) continue;
+      if (lane == 0) {
+        if (META) {
+          row_token[r] = -1;
+          row_expert[r] = E;
+          row_weight[r] = 0.f;
+        }
+        if (DOT) grad_w[r] = 0.f;
+      }
+      if (dst == nullptr) continue;
+      uint4* d = reinterpret_cast<uint4*>(dst + r * H);
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      for (int v = 0; v < V; ++v) d[lane + 32 * v] = z;
+    }
+  }
+}
 
 // a2 + a3 in one kernel.  A chunk is 32 tokens.
 //   1. Per chunk, each expert's token count (the chunk's routing_map bytes are
@@ -310,18 +423,20 @@ __global__ void __launch_bounds__(256) layout_kernel(LayoutArgs a) {
       __syncthreads();  // before the next chunk overwrites the shared arrays
     }
   }
+  if constexpr (MODE == LAYOUT_SINGLE) {
+    if (a.rows) {
+      // every row of the layout is placed (the barrier above): the row pass,
+      // one warp per item, with the offsets in shared memory and the counts
+      // this CTA wrote
+      scatter_items<true, false>(warp, nwarps, a.x, static_cast<int>(a.T), a.K, a.H, E, a.capacity,
+                                 a.token_row, s_off, a.tokens_per_expert, a.row_token, a.row_expert,
+                                 a.row_weight, a.x_disp, nullptr, nullptr);
+    }
+  }
 }
 
-// Dispatch (and the combine's backward) as a scatter, one warp per item.
-//   Items [0, T) are tokens: the warp reads the token's source row once from
-//   memory -- later passes over it hit L1 -- and writes it to each of the
-//   token's rows (token_row).  Reading each token once matters when [T, H]
-//   no longer fits in L2: a per-row gather would fetch it K times from DRAM.
-//   With DOT it also forms grad_w[r] = <src[t], o_save[r]> in fp32.
-//   Items [T, T + C) are rows: a pad or spare row is zeroed (and grad_w = 0).
-//   With META the row's validity comes from offsets / counts and the pad and
-//   spare rows get their metadata here (token -1, the sentinel expert, weight
-//   0); without it, from row_token (the combine's backward, after dispatch).
+// The scatter as a kernel: offsets and counts staged in shared memory, then
+// one warp per item over the grid.
 template <bool META, bool DOT>
 __global__ void __launch_bounds__(256) row_scatter_kernel(
     const uint16_t* __restrict__ src, int T, int K, int H, int E, long long C,
@@ -339,88 +454,10 @@ __global__ void __launch_bounds__(256) row_scatter_kernel(
     for (int i = threadIdx.x; i < E; i += blockDim.x) s_cnt[i] = counts[i];
     __syncthreads();
   }
-  const int lane = threadIdx.x & 31;
-  const int V = H >> 8;  // 16-byte vectors per lane
-  const long long items = T + C;
-  const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-  const int R = META ? s_off[E] : 0;
-  for (long long it = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-       it < items; it += nwarps) {
-    if (it < T) {
-      if (META && dst == nullptr) continue;  // the layout alone: no rows to copy
-      const long long t = it;
-      const uint4* s = reinterpret_cast<const uint4*>(src + t * H);
-      // The token's rows, 32 slots per load (a token's valid slots come first).
-      int r_lane = -1;
-      for (int j = 0; j < K; ++j) {
-        if ((j & 31) == 0) r_lane = j + lane < K ? __ldg(token_row + t * K + j + lane) : -1;
-        const int r = __shfl_sync(FULL_MASK, r_lane, j & 31);
-        if (r < 0) break;
-        uint4* d = reinterpret_cast<uint4*>(dst + static_cast<long long>(r) * H);
-        const uint4* o = DOT ? reinterpret_cast<const uint4*>(o_save + static_cast<long long>(r) * H) : nullptr;
-        float dot = 0.f;
-        for (int v0 = 0; v0 < V; v0 += 8) {
-          uint4 buf[8], ob[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            if (v0 + i < V) {
-              buf[i] = __ldg(s + lane + 32 * (v0 + i));
-              if (DOT) ob[i] = __ldg(o + lane + 32 * (v0 + i));
-            }
-          }
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            if (v0 + i < V) {
-              d[lane + 32 * (v0 + i)] = buf[i];
-              if (DOT) {
-                const uint32_t g[4] = {buf[i].x, buf[i].y, buf[i].z, buf[i].w};
-                const uint32_t q[4] = {ob[i].x, ob[i].y, ob[i].z, ob[i].w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  dot = fmaf(bf16_lo(g[k]), bf16_lo(q[k]), dot);
-                  dot = fmaf(bf16_hi(g[k]), bf16_hi(q[k]), dot);
-                }
-              }
-            }
-          }
-        }
-        if (DOT) {
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(FULL_MASK, dot, off);
-          if (lane == 0) grad_w[r] = dot;
-        }
-      }
-    } else {
-      const long long r = it - T;
-      bool pad;
-      if (META) {
-        pad = true;
-        if (r < R) {
-          int lo = 0, hi = E;  // s_off[lo] <= r < s_off[hi]
-          while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (s_off[mid] <= r) lo = mid; else hi = mid;
-          }
-          pad = r - s_off[lo] >= s_cnt[lo];
-        }
-      } else {
-        pad = __ldg(row_token + r) < 0;
-      }
-      if (!pad) continue;
-      if (lane == 0) {
-        if (META) {
-          row_token[r] = -1;
-          row_expert[r] = E;
-          row_weight[r] = 0.f;
-        }
-        if (DOT) grad_w[r] = 0.f;
-      }
-      if (dst == nullptr) continue;
-      uint4* d = reinterpret_cast<uint4*>(dst + r * H);
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      for (int v = 0; v < V; ++v) d[lane + 32 * v] = z;
-    }
-  }
+  scatter_items<META, DOT>(static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5),
+                           static_cast<long long>(gridDim.x) * (blockDim.x >> 5), src, T, K, H, E, C,
+                           token_row, s_off, s_cnt, row_token, row_expert, row_weight, dst, o_save,
+                           grad_w);
 }
 
 }  // namespace
@@ -486,9 +523,15 @@ cudaError_t launch_layout_mode(const LayoutArgs& a, size_t smem, cudaStream_t s)
 }  // namespace
 
 cudaError_t launch_layout(const uint8_t* routing_map, const float* probs, const moe_layout& L,
-                          void* workspace, LayoutStep step, cudaStream_t s, int* readback) {
+                          void* workspace, LayoutStep step, cudaStream_t s, int* readback,
+                          const uint16_t* x, uint16_t* x_disp, int H, bool* rows_done) {
   LayoutArgs a;
   a.readback = step == LayoutStep::kCounts ? readback : nullptr;
+  a.rows = false;
+  a.x = x;
+  a.x_disp = x_disp;
+  a.H = H;
+  if (rows_done) *rows_done = false;
   a.map = routing_map;
   a.probs = probs;
   a.T = L.T;
@@ -514,8 +557,17 @@ cudaError_t launch_layout(const uint8_t* routing_map, const float* probs, const 
       // one or two chunks (T <= 64): one CTA, no barrier, no memset.  It takes
       // the chunks one after another, about 4 us each, so beyond two the
       // cooperative launch (about 15 us at any small size) is faster.
-      if (a.chunks <= 2 && smem + static_cast<size_t>(a.chunks) * a.E * sizeof(int) <= 48 * 1024)
+      if (a.chunks <= 2 && smem + static_cast<size_t>(a.chunks) * a.E * sizeof(int) <= 48 * 1024) {
+        // A decode-sized row pass (a few rows of a few KB) costs the one CTA
+        // less than a launch of its own.
+        const long long items = L.T + L.capacity;
+        const long long bytes = x_disp ? items * H * 2 : 0;
+        if (rows_done && items <= LAYOUT_FUSED_ITEMS && bytes <= LAYOUT_FUSED_BYTES) {
+          a.rows = true;
+          *rows_done = true;
+        }
         return launch_layout_mode<LAYOUT_SINGLE>(a, smem, s);
+      }
       return launch_layout_mode<LAYOUT_ALL>(a, smem, s);
     case LayoutStep::kCounts: return launch_layout_mode<LAYOUT_COUNT>(a, smem, s);
     case LayoutStep::kPlace: return launch_layout_mode<LAYOUT_PLACE>(a, smem, s);

@@ -83,6 +83,47 @@ def test_multihot_and_layout(moe, T, E, K, P, drop, dup, host_sync):
     _check_layout(g, idx, p, E, P, C)
 
 
+@pytest.mark.parametrize("T,E,K,P,drop,dup", [
+    (1, 128, 8, 1, 0.0, 0.0),       # the decode T = 1 layer
+    (4, 16, 4, 1, 0.2, 0.2),        # drops and duplicates
+    (3, 8, 2, 4, 0.0, 0.0),         # pad rows
+    (8, 8, 7, 1, 0.0, 0.0),         # 64 items: the largest row pass the layout CTA takes
+    (9, 8, 7, 1, 0.0, 0.0),         # 72 items: a separate row pass
+    (0, 8, 2, 8, 0.0, 0.0),         # no tokens: spare rows only
+])
+@pytest.mark.parametrize("layout_only", [False, True])
+def test_single_cta_row_pass(moe, T, E, K, P, drop, dup, layout_only):
+    """Sync-free layers of a few rows: the one-CTA layout kernel also copies
+    the rows and writes the pad and spare rows.  Every output buffer starts
+    out poisoned, so each row must have been written."""
+    idx, p = random_routing(T, E, K, seed=T * 11 + E, drop=drop, dup=dup)
+    H = 512
+    C = O.worst_case_capacity(T, E, K, P)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    rmap, probs, _ = moe.moe_route_to_multihot(idx.to(DEV), p.to(DEV), E, status)
+    L = moe.Layout(T, E, K, P, C, device=DEV, status=status)
+    L.row_token.fill_(12345)
+    L.row_expert.fill_(-7)
+    L.row_weight.fill_(float("nan"))
+    L.token_row.fill_(999)
+    x = torch.randn(T, H, generator=torch.Generator().manual_seed(T + 1)).to(torch.bfloat16)
+    x_disp = torch.full((C, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    if layout_only:
+        moe.moe_dispatch_layout(rmap, probs, L, host_sync=False)
+    else:
+        moe.moe_dispatch(x.to(DEV), rmap, probs, L, host_sync=False, x_disp=x_disp)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rm, pr, _ = O.route_to_multihot(idx.numpy(), p.numpy(), E)
+    Lr = O.build_layout(rm, pr, K, P, C)
+    assert L.totals.cpu().tolist() == [Lr["rows_used"], Lr["rows_valid"]]
+    for f in ("row_token", "row_expert", "row_weight"):
+        assert np.array_equal(getattr(L, f).cpu().numpy(), Lr[f]), f
+    assert np.array_equal(L.token_row.cpu().numpy().reshape(T, K), Lr["token_row"])
+    if not layout_only:
+        assert np.array_equal(bits(x_disp), O.dispatch(bits(x), Lr["row_token"]))
+
+
 def test_all_invalid_routing(moe):
     T, E, K, P = 50, 8, 2, 4
     idx = -torch.ones(T, K, dtype=torch.int64)
@@ -214,6 +255,8 @@ def test_experts_match_oracle(moe, T, H, E, K, I, P):
     (4, 512, 16, 4, 256, 1),       # four tokens: up to four rows per expert
     (3, 256, 8, 2, 128, 16),       # padded groups (pad rows not written)
     (2, 4096, 8, 2, 1536, 1),      # the h4096 expert shape
+    (3, 8192, 8, 2, 128, 1),       # wide H: the A rows outgrow the CUDA-core path, tensor cores take it
+    (4, 2048, 1024, 8, 768, 1),    # E = 1024: a long expert scan, 32 active experts
     (64, 256, 8, 2, 128, 16),      # tensor-core path without saved operands
 ])
 def test_experts_inference_match_oracle(moe, T, H, E, K, I, P):
