@@ -163,10 +163,19 @@ __device__ __forceinline__ void fence_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Byte offset of 16-byte chunk c of row r in a 64-byte-swizzled box of
+// 64-byte rows (the TMA's 64-byte swizzle: chunk bits [4:5] ^= bits [7:8]).
+// Without it, 32 lanes storing their own rows hit 2 of the 8 bank groups.
+// The box must start at a 512-byte boundary.
+__device__ __forceinline__ uint32_t staged_chunk(int r, int c) {
+  return static_cast<uint32_t>(r * 64 + 16 * (c ^ ((r >> 1) & 3)));
+}
+
 // TMA stores of 32-row boxes of 64-byte rows that a warp holds one row per
 // lane (lane i holds row i as 16 words).  Each box goes through one half of
 // the warp's 4 KiB staging area (the halves alternate, recycled with
-// wait_group.read), then lane 0 stores it with the given tensor map.
+// wait_group.read), then lane 0 stores it with the given (64-byte swizzled)
+// tensor map.
 struct StagedStore {
   uint32_t base;
   uint32_t n;
@@ -177,7 +186,7 @@ struct StagedStore {
     __syncwarp();
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(buf + lane * 64 + 16 * i),
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(buf + staged_chunk(lane, i)),
                    "r"(v[4 * i]), "r"(v[4 * i + 1]), "r"(v[4 * i + 2]), "r"(v[4 * i + 3])
                    : "memory");
     fence_async_shared();

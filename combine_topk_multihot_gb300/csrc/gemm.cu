@@ -352,8 +352,8 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
     const int r_in_tile = q * 32 + lane;
     int local = 0;
     // Staged TMA store of one 32-row x 32-column bf16 box: each lane writes its
-    // row (64 bytes) into one of the warp's two staging buffers, then lane 0
-    // stores the box.  Used only when all 32 rows of the warp are valid.
+    // row (64 bytes, swizzled) into one of the warp's two staging buffers, then
+    // lane 0 stores the box.  Used only when all 32 rows of the warp are valid.
     const uint32_t my_staging = staging_u32 + (warp - 2) * 2 * 2048;  // two 2 KiB boxes
     uint32_t n_staged = 0;
     int warp_row0 = 0;
@@ -361,10 +361,9 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
       const uint32_t buf = my_staging + (n_staged & 1) * 2048;
       if (lane == 0) tma_store_wait_read<1>();
       __syncwarp();
-      const uint32_t dst = buf + lane * 64;
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 16 * i), "r"(v[4 * i]),
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(buf + staged_chunk(lane, i)), "r"(v[4 * i]),
                      "r"(v[4 * i + 1]), "r"(v[4 * i + 2]), "r"(v[4 * i + 3])
                      : "memory");
       fence_async_shared();

@@ -43,8 +43,11 @@ bool make_tma_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_
 bool make_tma_2d_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                     uint32_t box_rows);
 
-// Tensor map for TMA stores of 32-row x 32-column bf16 boxes (64-byte rows,
-// no swizzle) into a row-major [rows, cols] matrix.
+// Tensor map for TMA stores of 32-row x 32-column bf16 boxes (64-byte rows)
+// into a row-major [rows, cols] matrix.  The shared-memory box is 64-byte
+// swizzled: the 16-byte chunk c of row r sits at chunk c ^ ((r >> 1) & 3)
+// (see staged_chunk), so a warp writing one row per lane spreads over all
+// shared-memory banks.
 bool make_tma_store_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols);
 // The same for fp32: 32-row x 16-column boxes (64-byte rows).
 bool make_tma_store_2d_f32(CUtensorMap* map, void* base, uint64_t rows, uint64_t cols);
