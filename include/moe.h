@@ -22,9 +22,13 @@
  *
  * Conventions for every entry point:
  *   - Pointers named in a signature are DEVICE pointers unless the comment
- *     says "host".  The caller owns all memory; the library allocates nothing
- *     (no cudaMalloc, no pinned buffers), keeps no state between calls and
- *     holds no handles.  Row buffers hold `capacity` rows.
+ *     says "host".  The caller owns all memory; the library allocates no
+ *     device memory, keeps no state between calls and holds no handles.  Row
+ *     buffers hold `capacity` rows.  One exception, host-side only:
+ *     host-synced moe_dispatch keeps 16 bytes of mapped pinned host memory per
+ *     device, allocated on its first call and kept until the process exits.
+ *     The count kernel writes the row totals and the status word straight
+ *     into it.
  *   - bf16 tensors are passed as raw bit patterns (moe_bf16), row-major,
  *     with the last dimension contiguous and rows packed (no row stride).
  *     Every pointer must be 16-byte aligned.
