@@ -5,6 +5,8 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
+#include <chrono>
 #include <mutex>
 
 #include "common.cuh"
@@ -38,6 +40,9 @@ int g_sms[MAX_DEVICES];
 // streams.  One buffer per device, made on first use; the mutex is held from
 // the launch to the read, so concurrent host-synced calls take turns.
 std::mutex g_rb_mu;
+// The host polls the mapped buffer for this long before it falls back to a
+// stream synchronisation (the count kernel's own waits give up after 2 s).
+constexpr int READBACK_POLL_LIMIT_S = 10;
 int* g_rb_host[MAX_DEVICES];
 int* g_rb_dev[MAX_DEVICES];
 
@@ -240,14 +245,35 @@ moe_status dispatch_impl(const char* who, const moe_bf16* x, const uint8_t* rout
     if ((err = launch_layout(routing_map, probs, *L, L->workspace, LayoutStep::kCounts, stream,
                              mapped ? rb_dev : nullptr)) != cudaSuccess)
       return cuda_fail(err, "dispatch: counts");
-    if ((err = cudaStreamSynchronize(stream)) != cudaSuccess)
-      return cuda_fail(err, "dispatch: waiting for the row counts");
+    // Wait for the counts.  With the mapped buffer: until the count kernel
+    // publishes R (its other CTAs may still be finishing), or until the
+    // stream is idle without it (the kernel gave up: read the device copies).
     volatile int* rb = rb_host;
-    if (mapped && rb[0] >= 0) {
+    bool published = false;
+    if (mapped) {
+      const auto t0 = std::chrono::steady_clock::now();
+      for (unsigned spin = 0;; ++spin) {
+        if (rb[0] >= 0) {
+          published = true;
+          break;
+        }
+        if ((spin & 255u) != 255u) continue;
+        const cudaError_t q = cudaStreamQuery(stream);
+        if (q == cudaSuccess) {
+          published = rb[0] >= 0;
+          break;
+        }
+        if (q != cudaErrorNotReady) return cuda_fail(q, "dispatch: waiting for the row counts");
+        if (std::chrono::steady_clock::now() - t0 > std::chrono::seconds(READBACK_POLL_LIMIT_S)) break;
+      }
+    }
+    if (published) {
+      std::atomic_thread_fence(std::memory_order_acquire);
       tot[0] = rb[0];
       tot[1] = rb[1];
       dev_status = rb[2];
-    } else if ((err = cudaMemcpy(tot, L->totals, sizeof(tot), cudaMemcpyDeviceToHost)) != cudaSuccess ||
+    } else if ((err = cudaStreamSynchronize(stream)) != cudaSuccess ||
+               (err = cudaMemcpy(tot, L->totals, sizeof(tot), cudaMemcpyDeviceToHost)) != cudaSuccess ||
                (err = cudaMemcpy(&dev_status, L->status, sizeof(int32_t), cudaMemcpyDeviceToHost)) != cudaSuccess) {
       return cuda_fail(err, "dispatch: reading the row counts");
     }

@@ -351,9 +351,13 @@ __global__ void __launch_bounds__(256) layout_kernel(LayoutArgs a) {
         a.totals[1] = N;
         if (R > a.capacity) report(a.status, MOE_DEVERR_CAPACITY);
         if (a.readback) {  // for the host-synced caller, without a copy engine
-          a.readback[0] = R;
-          a.readback[1] = N;
-          a.readback[2] = *reinterpret_cast<volatile int*>(a.status);
+          // R goes last, after a system-scope fence: the host waits for it and
+          // then reads the other two
+          volatile int* rb = a.readback;
+          rb[1] = N;
+          rb[2] = *reinterpret_cast<volatile int*>(a.status);
+          __threadfence_system();
+          rb[0] = R;
         }
       }
     }

@@ -34,7 +34,8 @@
  *     Every pointer must be 16-byte aligned.
  *   - Every call is asynchronous and ordered on `stream` (a cudaStream_t;
  *     NULL is the legacy default stream), except moe_dispatch in host-synced
- *     mode, which synchronises `stream` once.
+ *     mode, which waits on the host once, for the row counts: everything
+ *     queued on `stream` before the call has completed when it returns.
  *   - Every call validates its arguments on the host and returns a
  *     moe_status; it never aborts the process.  moe_last_error() gives a
  *     human-readable detail of the last failure on the calling thread.
@@ -186,8 +187,9 @@ MOE_API moe_status moe_route_to_multihot(const int64_t* topk_idx, const float* t
  *   x_disp       [C, H] bf16 (out): x_disp[r] = x[row_token[r]] bit for bit;
  *                pad and spare rows are zero.
  *   rows_host    HOST int64[2] or NULL.
- *     non-NULL = host-synced (eager) mode: the call synchronises `stream`
- *       after the counts, writes rows_host[0] = R (rows used) and
+ *     non-NULL = host-synced (eager) mode: the call waits until the count
+ *       kernel has published the counts to the host (it may still be
+ *       finishing), writes rows_host[0] = R (rows used) and
  *       rows_host[1] = N (valid rows), returns MOE_ERR_BAD_INDEX if the
  *       status word has MOE_DEVERR_BAD_INDEX, or MOE_ERR_CAPACITY (before
  *       writing any row) if R > capacity.
