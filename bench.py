@@ -252,14 +252,14 @@ def run_ours(args, world, rank, local):
     ev = lambda: torch.cuda.Event(enable_timing=True)
     bwd = cfg.backward
     stages = ["multihot", "dispatch", "experts", "combine"]
-    # our kernels per step: multihot; the layout kernel (two launches when
-    # host-synced) and the row copy; the two expert GEMMs; the combine.  A
-    # sync-free layer of at most two 32-token chunks whose row pass has at most
-    # 64 items (tokens + rows) and 256 KiB lays out and copies in one kernel.
+    # our kernels per step: multihot; the layout kernel and the row copy; the
+    # two expert GEMMs; the combine.  A layer of at most two 32-token chunks
+    # whose row pass has at most 64 items (tokens + rows) and 256 KiB lays out
+    # and copies in one kernel.
     chunks = -(-T // 32)
-    single_rows = (not host_sync and not fp8 and chunks <= 2 and T + C <= 64
+    single_rows = (not fp8 and chunks <= 2 and T + C <= 64
                    and (0 if gather else (T + C) * H * 2) <= 256 * 1024)
-    dispatch_launches = 3 if host_sync else (1 if single_rows else 2)
+    dispatch_launches = 1 if single_rows else 2
     launches_per_step = 1 + dispatch_launches + 2 + 1
     if bwd:
         stages += ["combine_bwd", "experts_bwd", "dispatch_bwd", "multihot_bwd"]

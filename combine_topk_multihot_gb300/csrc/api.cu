@@ -222,79 +222,83 @@ moe_status dispatch_impl(const char* who, const moe_bf16* x, const uint8_t* rout
                 static_cast<long long>(worst), static_cast<long long>(L->capacity));
   if ((st = check_device()) != MOE_OK) return st;
 
-  cudaError_t err;
-  bool rows_done = false;  // the layout kernel did the row pass itself
-  if (!rows_host) {
-    const bool bf16_rows = x_disp || layout_only;
-    if ((err = launch_layout(routing_map, probs, *L, L->workspace, LayoutStep::kAll, stream, nullptr,
-                             reinterpret_cast<const uint16_t*>(x), reinterpret_cast<uint16_t*>(x_disp), H,
-                             bf16_rows ? &rows_done : nullptr)) != cudaSuccess)
-      return cuda_fail(err, "dispatch: layout");
-  } else {
-    int32_t tot[2] = {0, 0}, dev_status = 0;
+  // Host-synced callers get R, N and the status word through mapped pinned
+  // memory that the layout kernel writes as soon as the offsets are known.
+  int *rb_host = nullptr, *rb_dev = nullptr;
+  std::unique_lock<std::mutex> rb_lock(g_rb_mu, std::defer_lock);
+  bool mapped = false;
+  if (rows_host) {
     int dev = 0;
-    int *rb_host = nullptr, *rb_dev = nullptr;
-    std::unique_lock<std::mutex> rb_lock(g_rb_mu);
-    const bool mapped = cudaGetDevice(&dev) == cudaSuccess && readback_buffer(dev, &rb_host, &rb_dev);
+    rb_lock.lock();
+    mapped = cudaGetDevice(&dev) == cudaSuccess && readback_buffer(dev, &rb_host, &rb_dev);
     if (mapped) {
       volatile int* rb = rb_host;
-      rb[0] = rb[1] = rb[2] = -1;  // overwritten by the count kernel when it completes
+      rb[0] = rb[1] = rb[2] = -1;  // overwritten by the layout kernel
     } else {
       rb_lock.unlock();
     }
-    if ((err = launch_layout(routing_map, probs, *L, L->workspace, LayoutStep::kCounts, stream,
-                             mapped ? rb_dev : nullptr)) != cudaSuccess)
-      return cuda_fail(err, "dispatch: counts");
-    // Wait for the counts.  With the mapped buffer: until the count kernel
-    // publishes R (its other CTAs may still be finishing), or until the
-    // stream is idle without it (the kernel gave up: read the device copies).
-    volatile int* rb = rb_host;
-    bool published = false;
-    if (mapped) {
-      const auto t0 = std::chrono::steady_clock::now();
-      for (unsigned spin = 0;; ++spin) {
-        if (rb[0] >= 0) {
-          published = true;
-          break;
-        }
-        if ((spin & 255u) != 255u) continue;
-        const cudaError_t q = cudaStreamQuery(stream);
-        if (q == cudaSuccess) {
-          published = rb[0] >= 0;
-          break;
-        }
-        if (q != cudaErrorNotReady) return cuda_fail(q, "dispatch: waiting for the row counts");
-        if (std::chrono::steady_clock::now() - t0 > std::chrono::seconds(READBACK_POLL_LIMIT_S)) break;
-      }
-    }
-    if (published) {
-      std::atomic_thread_fence(std::memory_order_acquire);
-      tot[0] = rb[0];
-      tot[1] = rb[1];
-      dev_status = rb[2];
-    } else if ((err = cudaStreamSynchronize(stream)) != cudaSuccess ||
-               (err = cudaMemcpy(tot, L->totals, sizeof(tot), cudaMemcpyDeviceToHost)) != cudaSuccess ||
-               (err = cudaMemcpy(&dev_status, L->status, sizeof(int32_t), cudaMemcpyDeviceToHost)) != cudaSuccess) {
-      return cuda_fail(err, "dispatch: reading the row counts");
-    }
-    if (rb_lock.owns_lock()) rb_lock.unlock();
-    rows_host[0] = tot[0];
-    rows_host[1] = tot[1];
-    if (dev_status & MOE_DEVERR_TIMEOUT)
-      return fail(MOE_ERR_TIMEOUT, "the layout kernel's grid barrier timed out");
-    if (dev_status & MOE_DEVERR_BAD_INDEX)
-      return fail(MOE_ERR_BAD_INDEX, "an expert index outside [-1, E) was seen");
-    if (tot[0] > L->capacity)
-      return fail(MOE_ERR_CAPACITY, "the layout needs %d rows, capacity is %lld", tot[0],
-                  static_cast<long long>(L->capacity));
-    if ((err = launch_layout(routing_map, probs, *L, L->workspace, LayoutStep::kPlace, stream)) != cudaSuccess)
-      return cuda_fail(err, "dispatch: placement");
   }
-  // the rows (or, for the layout alone, just the pad and spare rows' metadata)
-  if (rows_done) return MOE_OK;
-  err = (x_disp || layout_only) ? launch_row_gather(x, *L, H, x_disp, true, nullptr, nullptr, stream)
-                                : launch_row_gather_fp8(x, *L, H, x_q, x_scale, stream);
-  if (err != cudaSuccess) return cuda_fail(err, "dispatch: rows");
+  // The layout, then the rows (or, for the layout alone, just the pad and
+  // spare rows' metadata), queued at once in both modes.  When the rows do
+  // not fit (host-synced, R > capacity) both kernels write nothing.
+  cudaError_t err;
+  bool rows_done = false;  // the layout kernel did the row pass itself
+  const bool bf16_rows = x_disp || layout_only;
+  if ((err = launch_layout(routing_map, probs, *L, L->workspace, stream, mapped ? rb_dev : nullptr,
+                           reinterpret_cast<const uint16_t*>(x), reinterpret_cast<uint16_t*>(x_disp), H,
+                           bf16_rows ? &rows_done : nullptr)) != cudaSuccess)
+    return cuda_fail(err, "dispatch: layout");
+  if (!rows_done) {
+    err = bf16_rows ? launch_row_gather(x, *L, H, x_disp, true, nullptr, nullptr, stream)
+                    : launch_row_gather_fp8(x, *L, H, x_q, x_scale, stream);
+    if (err != cudaSuccess) return cuda_fail(err, "dispatch: rows");
+  }
+  if (!rows_host) return MOE_OK;
+
+  // Host-synced: wait for the counts.  With the mapped buffer, until the
+  // layout kernel publishes R (the kernels behind it keep running), or until
+  // the stream is idle without it (the kernel gave up: read the device
+  // copies).
+  int32_t tot[2] = {0, 0}, dev_status = 0;
+  volatile int* rb = rb_host;
+  bool published = false;
+  if (mapped) {
+    const auto t0 = std::chrono::steady_clock::now();
+    for (unsigned spin = 0;; ++spin) {
+      if (rb[0] >= 0) {
+        published = true;
+        break;
+      }
+      if ((spin & 255u) != 255u) continue;
+      const cudaError_t q = cudaStreamQuery(stream);
+      if (q == cudaSuccess) {
+        published = rb[0] >= 0;
+        break;
+      }
+      if (q != cudaErrorNotReady) return cuda_fail(q, "dispatch: waiting for the row counts");
+      if (std::chrono::steady_clock::now() - t0 > std::chrono::seconds(READBACK_POLL_LIMIT_S)) break;
+    }
+  }
+  if (published) {
+    std::atomic_thread_fence(std::memory_order_acquire);
+    tot[0] = rb[0];
+    tot[1] = rb[1];
+    dev_status = rb[2];
+  } else if ((err = cudaStreamSynchronize(stream)) != cudaSuccess ||
+             (err = cudaMemcpy(tot, L->totals, sizeof(tot), cudaMemcpyDeviceToHost)) != cudaSuccess ||
+             (err = cudaMemcpy(&dev_status, L->status, sizeof(int32_t), cudaMemcpyDeviceToHost)) != cudaSuccess) {
+    return cuda_fail(err, "dispatch: reading the row counts");
+  }
+  if (rb_lock.owns_lock()) rb_lock.unlock();
+  rows_host[0] = tot[0];
+  rows_host[1] = tot[1];
+  if (dev_status & MOE_DEVERR_TIMEOUT)
+    return fail(MOE_ERR_TIMEOUT, "the layout kernel's grid barrier timed out");
+  if (dev_status & MOE_DEVERR_BAD_INDEX)
+    return fail(MOE_ERR_BAD_INDEX, "an expert index outside [-1, E) was seen");
+  if (tot[0] > L->capacity)
+    return fail(MOE_ERR_CAPACITY, "the layout needs %d rows, capacity is %lld", tot[0],
+                static_cast<long long>(L->capacity));
   return MOE_OK;
 }
 

@@ -75,6 +75,7 @@ __global__ void __launch_bounds__(256) row_scatter_fp8_kernel(
   const long long items = T + C;
   const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   const int R = s_off[E];
+  if (R > C) return;  // the layout placed nothing: the rows do not fit
   for (long long it = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
        it < items; it += nwarps) {
     if (it < T) {
@@ -82,7 +83,8 @@ __global__ void __launch_bounds__(256) row_scatter_fp8_kernel(
       const uint4* src = reinterpret_cast<const uint4*>(x + t * H);
       const float scale = row_scale(src, V, lane);
       for (int j0 = 0; j0 < K; j0 += 32) {
-        const int r_lane = j0 + lane < K ? __ldg(token_row + t * K + j0 + lane) : -1;
+        const int r_ld = j0 + lane < K ? __ldcg(token_row + t * K + j0 + lane) : -1;
+        const int r_lane = r_ld < C ? r_ld : -1;
         const uint32_t rows = __ballot_sync(FULL_MASK, r_lane >= 0);
         if (r_lane >= 0) x_scale[r_lane] = scale;
         for (int v = 0; v < V; ++v) {

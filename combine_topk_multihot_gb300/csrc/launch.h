@@ -82,24 +82,21 @@ inline size_t layout_counter_bytes(int32_t T, int32_t E) {
   return (b + 255) / 256 * 256;
 }
 
-enum class LayoutStep {
-  kAll,     // a2 + a3 in one cooperative launch (the sync-free path)
-  kCounts,  // a2 only: counts, per-chunk starts, offsets and totals
-  kPlace,   // a3 only, after kCounts (the host-synced path reads the totals in between)
-};
-
 // Counts, padded offsets and the stable placement of every (token, expert)
-// pair.  workspace: layout_counter_bytes(T, E) + 256 bytes.
-// readback (kCounts only, may be NULL): device address of 3 ints of
-// host-mapped memory that receive R, N and the status word.
-// rows_done (kAll only, may be NULL): when the layout runs as one CTA and the
+// pair, in one launch.  workspace: layout_counter_bytes(T, E) + 256 bytes.
+// Placement is skipped when the rows do not fit (R > capacity); the status
+// word then has MOE_DEVERR_CAPACITY.
+// readback (may be NULL): device address of 3 ints of host-mapped memory
+// that receive N and the status word, then R (written last, after a system
+// fence), as soon as the offsets are known.
+// rows_done (may be NULL): when the layout runs as one CTA and the
 // dispatch's row pass is small, that CTA also does the row pass (x -> x_disp,
 // or only the pad and spare rows' metadata when x_disp is NULL) and sets
 // *rows_done; otherwise *rows_done is false and the caller runs the row pass.
 cudaError_t launch_layout(const uint8_t* routing_map, const float* probs, const moe_layout& L,
-                          void* workspace, LayoutStep step, cudaStream_t s,
-                          int* readback = nullptr, const uint16_t* x = nullptr,
-                          uint16_t* x_disp = nullptr, int H = 0, bool* rows_done = nullptr);
+                          void* workspace, cudaStream_t s, int* readback = nullptr,
+                          const uint16_t* x = nullptr, uint16_t* x_disp = nullptr, int H = 0,
+                          bool* rows_done = nullptr);
 // Rows of the expanded layout from token rows (a4: x -> x_disp, plus the pad /
 // spare rows' metadata when from_offsets); also the combine backward (a7)
 // with the optional routing-weight gradient (a8).  Each token row is read

@@ -93,8 +93,6 @@ constexpr long long LAYOUT_FUSED_BYTES = 256 * 1024;
 
 enum LayoutMode : int {
   LAYOUT_ALL = 0,    // counts, scans, offsets and placement: one cooperative launch
-  LAYOUT_COUNT = 1,  // counts, scans and offsets only (cooperative), for the host-synced path
-  LAYOUT_PLACE = 2,  // placement only, after LAYOUT_COUNT (ordinary launch)
   LAYOUT_SINGLE = 3, // all four phases in one CTA, for layers of one or two chunks (no barrier)
 };
 
@@ -113,7 +111,7 @@ struct LayoutArgs {
   float* row_weight;
   int* token_row;
   int* status;
-  int* readback;  // LAYOUT_COUNT: {R, N, status} in host-mapped memory, or NULL
+  int* readback;  // {R, N, status} in host-mapped memory (host-synced callers), or NULL
   // LAYOUT_SINGLE with rows: the CTA also does the dispatch's row pass (the
   // copies into x_disp when it is not NULL, and the pad and spare rows)
   bool rows;
@@ -145,6 +143,7 @@ __device__ __forceinline__ void scatter_items(
   const int V = H >> 8;  // 16-byte vectors per lane
   const long long items = T + C;
   const int R = META ? s_off[E] : 0;
+  if (META && R > C) return;  // the layout placed nothing: the rows do not fit
   for (long long it = first; it < items; it += stride) {
     if (it < T) {
       if (META && dst == nullptr) continue;  // the layout alone: no rows to copy
@@ -156,7 +155,7 @@ __device__ __forceinline__ void scatter_items(
         // (L2 load: the layout kernel itself may have just written token_row)
         if ((j & 31) == 0) r_lane = j + lane < K ? __ldcg(token_row + t * K + j + lane) : -1;
         const int r = __shfl_sync(FULL_MASK, r_lane, j & 31);
-        if (r < 0) break;
+        if (r < 0 || r >= C) break;
         uint4* d = reinterpret_cast<uint4*>(dst + static_cast<long long>(r) * H);
         const uint4* o = DOT ? reinterpret_cast<const uint4*>(o_save + static_cast<long long>(r) * H) : nullptr;
         float dot = 0.f;
@@ -261,23 +260,21 @@ __global__ void __launch_bounds__(256) layout_kernel(LayoutArgs a) {
   int* s_cc = s_off + E + 1;  // LAYOUT_SINGLE: [chunks][E] counts, then each chunk's start
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
 
-  if (MODE != LAYOUT_PLACE) {
-    for (int c = blockIdx.x; c < a.chunks; c += gridDim.x) {
-      const long long t0 = static_cast<long long>(c) * LAYOUT_CHUNK;
-      const int nt = static_cast<int>(min(static_cast<long long>(LAYOUT_CHUNK), a.T - t0));
-      const uint32_t* words = reinterpret_cast<const uint32_t*>(a.map + t0 * E);
-      for (int i = threadIdx.x; i < nt * E4; i += blockDim.x) s_map32[i] = words[i];
-      __syncthreads();
-      for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int n = 0;
-        for (int tl = 0; tl < nt; ++tl) n += s_map[tl * E + e] != 0;
-        if constexpr (MODE == LAYOUT_SINGLE)
-          s_cc[c * E + e] = n;
-        else
-          a.chunk_counts[static_cast<long long>(e) * a.chunks + c] = n;
-      }
-      __syncthreads();
+  for (int c = blockIdx.x; c < a.chunks; c += gridDim.x) {
+    const long long t0 = static_cast<long long>(c) * LAYOUT_CHUNK;
+    const int nt = static_cast<int>(min(static_cast<long long>(LAYOUT_CHUNK), a.T - t0));
+    const uint32_t* words = reinterpret_cast<const uint32_t*>(a.map + t0 * E);
+    for (int i = threadIdx.x; i < nt * E4; i += blockDim.x) s_map32[i] = words[i];
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      int n = 0;
+      for (int tl = 0; tl < nt; ++tl) n += s_map[tl * E + e] != 0;
+      if constexpr (MODE == LAYOUT_SINGLE)
+        s_cc[c * E + e] = n;
+      else
+        a.chunk_counts[static_cast<long long>(e) * a.chunks + c] = n;
     }
+    __syncthreads();
   }
   if constexpr (MODE == LAYOUT_SINGLE) {
     // one CTA: each expert's per-chunk starts and total, in shared memory
@@ -291,7 +288,7 @@ __global__ void __launch_bounds__(256) layout_kernel(LayoutArgs a) {
       a.tokens_per_expert[e] = run;
     }
     __syncthreads();
-  } else if constexpr (MODE != LAYOUT_PLACE) {
+  } else {
     if (!grid_barrier(a.barrier, gridDim.x, a.status, &s_ok)) return;
     for (int e = blockIdx.x * nwarps + warp; e < E; e += gridDim.x * nwarps) {
       int* row = a.chunk_counts + static_cast<long long>(e) * a.chunks;
@@ -316,9 +313,6 @@ __global__ void __launch_bounds__(256) layout_kernel(LayoutArgs a) {
       if (lane == 0) a.tokens_per_expert[e] = run;
     }
     if (!grid_barrier(a.barrier, 2 * gridDim.x, a.status, &s_ok)) return;
-    if constexpr (MODE == LAYOUT_COUNT) {
-      if (blockIdx.x != 0) return;
-    }
   }
 
   // Padded offsets; thread i owns experts 4i .. 4i + 3 (E <= 4 * blockDim.x).
@@ -341,7 +335,7 @@ __global__ void __launch_bounds__(256) layout_kernel(LayoutArgs a) {
       excl += pad[d];
     }
     if (threadIdx.x == 0) s_off[E] = R;
-    if (MODE != LAYOUT_PLACE && blockIdx.x == 0) {
+    if (blockIdx.x == 0) {
       __syncthreads();
       int N;
       block_exclusive_scan(nsum, s_warp, &N);
@@ -363,7 +357,9 @@ __global__ void __launch_bounds__(256) layout_kernel(LayoutArgs a) {
     }
     __syncthreads();
   }
-  if constexpr (MODE != LAYOUT_COUNT) {
+  // 4. Placement, only when the rows fit: with R > capacity nothing is
+  // written (the host-synced caller then reports the capacity error).
+  if (s_off[E] <= a.capacity) {
     for (int c = blockIdx.x; c < a.chunks; c += gridDim.x) {
       const long long t0 = static_cast<long long>(c) * LAYOUT_CHUNK;
       const int nt = static_cast<int>(min(static_cast<long long>(LAYOUT_CHUNK), a.T - t0));
@@ -428,7 +424,7 @@ __global__ void __launch_bounds__(256) layout_kernel(LayoutArgs a) {
     }
   }
   if constexpr (MODE == LAYOUT_SINGLE) {
-    if (a.rows) {
+    if (a.rows && s_off[E] <= a.capacity) {
       // every row of the layout is placed (the barrier above): the row pass,
       // one warp per item, with the offsets in shared memory and the counts
       // this CTA wrote
@@ -500,10 +496,6 @@ cudaError_t launch_layout_mode(const LayoutArgs& a, size_t smem, cudaStream_t s)
     return launch_dependent(layout_kernel<MODE>, 1, 256,
                             smem + static_cast<size_t>(a.chunks) * a.E * sizeof(int), s, a);
   }
-  if (MODE == LAYOUT_PLACE) {
-    if (a.chunks == 0) return cudaSuccess;
-    return launch_dependent(layout_kernel<MODE>, a.chunks, 256, smem, s, a);
-  }
   cudaError_t err = cudaMemsetAsync(a.barrier, 0, sizeof(unsigned), s);
   if (err != cudaSuccess) return err;
   // Enough CTAs for one chunk each (phases 1 and 4) and one warp per expert
@@ -527,10 +519,10 @@ cudaError_t launch_layout_mode(const LayoutArgs& a, size_t smem, cudaStream_t s)
 }  // namespace
 
 cudaError_t launch_layout(const uint8_t* routing_map, const float* probs, const moe_layout& L,
-                          void* workspace, LayoutStep step, cudaStream_t s, int* readback,
-                          const uint16_t* x, uint16_t* x_disp, int H, bool* rows_done) {
+                          void* workspace, cudaStream_t s, int* readback, const uint16_t* x,
+                          uint16_t* x_disp, int H, bool* rows_done) {
   LayoutArgs a;
-  a.readback = step == LayoutStep::kCounts ? readback : nullptr;
+  a.readback = readback;
   a.rows = false;
   a.x = x;
   a.x_disp = x_disp;
@@ -556,27 +548,21 @@ cudaError_t launch_layout(const uint8_t* routing_map, const float* probs, const 
   a.token_row = L.token_row;
   a.status = L.status;
   const size_t smem = layout_smem_bytes(L.E);
-  switch (step) {
-    case LayoutStep::kAll:
-      // one or two chunks (T <= 64): one CTA, no barrier, no memset.  It takes
-      // the chunks one after another, about 4 us each, so beyond two the
-      // cooperative launch (about 15 us at any small size) is faster.
-      if (a.chunks <= 2 && smem + static_cast<size_t>(a.chunks) * a.E * sizeof(int) <= 48 * 1024) {
-        // A decode-sized row pass (a few rows of a few KB) costs the one CTA
-        // less than a launch of its own.
-        const long long items = L.T + L.capacity;
-        const long long bytes = x_disp ? items * H * 2 : 0;
-        if (rows_done && items <= LAYOUT_FUSED_ITEMS && bytes <= LAYOUT_FUSED_BYTES) {
-          a.rows = true;
-          *rows_done = true;
-        }
-        return launch_layout_mode<LAYOUT_SINGLE>(a, smem, s);
-      }
-      return launch_layout_mode<LAYOUT_ALL>(a, smem, s);
-    case LayoutStep::kCounts: return launch_layout_mode<LAYOUT_COUNT>(a, smem, s);
-    case LayoutStep::kPlace: return launch_layout_mode<LAYOUT_PLACE>(a, smem, s);
+  // One or two chunks (T <= 64): one CTA, no barrier, no memset.  It takes
+  // the chunks one after another, about 4 us each, so beyond two the
+  // cooperative launch (about 15 us at any small size) is faster.
+  if (a.chunks <= 2 && smem + static_cast<size_t>(a.chunks) * a.E * sizeof(int) <= 48 * 1024) {
+    // A decode-sized row pass (a few rows of a few KB) costs the one CTA
+    // less than a launch of its own.
+    const long long items = L.T + L.capacity;
+    const long long bytes = x_disp ? items * H * 2 : 0;
+    if (rows_done && items <= LAYOUT_FUSED_ITEMS && bytes <= LAYOUT_FUSED_BYTES) {
+      a.rows = true;
+      *rows_done = true;
+    }
+    return launch_layout_mode<LAYOUT_SINGLE>(a, smem, s);
   }
-  return cudaErrorInvalidValue;
+  return launch_layout_mode<LAYOUT_ALL>(a, smem, s);
 }
 
 cudaError_t launch_row_gather(const uint16_t* src, const moe_layout& L, int H, uint16_t* dst,
