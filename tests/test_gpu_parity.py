@@ -6,6 +6,8 @@ Within the bf16 GEMM tolerance (max |err| <= 2e-2, rel L2 <= 5e-3): the
 expert outputs y and o and the layer output; the intermediates h and the
 gate/up pre-activations use the same bound scaled by max(1, |ref|).
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -154,6 +156,48 @@ def test_host_synced_exact_capacity(moe):
     assert rows == (R, Lr["rows_valid"])
     assert np.array_equal(L1.row_token.cpu().numpy(), Lr["row_token"])
     assert np.array_equal(bits(x_disp), O.dispatch(bits(x), Lr["row_token"]))
+
+
+@pytest.mark.parametrize("T,E,K,P", [
+    (4, 8, 2, 4),        # one CTA lays out and copies
+    (40, 8, 2, 4),       # one CTA lays out, the row kernel copies
+    (2000, 32, 4, 16),   # the cooperative layout kernel and the row kernel
+])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_host_synced_short_capacity_writes_nothing(moe, T, E, K, P, fp8):
+    """Host-synced, capacity one row short of R: MOE_ERR_CAPACITY, R and N
+    still reported, and not a single output byte written -- the kernels are
+    queued before the host knows R, so they must skip the work themselves."""
+    idx, p = random_routing(T, E, K, seed=T + E, drop=0.1)
+    Lr = O.build_layout(*O.route_to_multihot(idx.numpy(), p.numpy(), E)[:2], K, P)
+    R = Lr["rows_used"]
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    rmap, probs, _ = moe.moe_route_to_multihot(idx.to(DEV), p.to(DEV), E, status)
+    L = moe.Layout(T, E, K, P, R - 1, device=DEV, status=status)
+    for f, v in (("row_token", 12345), ("row_expert", -7), ("row_weight", 0.5), ("token_row", 999)):
+        getattr(L, f).fill_(v)
+    H = 256
+    x = torch.randn(T, H, generator=torch.Generator().manual_seed(T)).to(torch.bfloat16).to(DEV)
+    rows = (ctypes.c_int64 * 2)()
+    if fp8:
+        q = torch.full((R - 1, H), 0x5A, dtype=torch.uint8, device=DEV)
+        sc = torch.full((R - 1,), 3.0, dtype=torch.float32, device=DEV)
+        code = moe._native.lib.moe_dispatch_fp8(moe.moe._ptr(x), moe.moe._ptr(rmap), moe.moe._ptr(probs), H,
+                                                L.ref, moe.moe._ptr(q), moe.moe._ptr(sc), rows, None)
+    else:
+        xd = torch.full((R - 1, H), 7.0, dtype=torch.bfloat16, device=DEV)
+        code = moe._native.lib.moe_dispatch(moe.moe._ptr(x), moe.moe._ptr(rmap), moe.moe._ptr(probs), H,
+                                            L.ref, moe.moe._ptr(xd), rows, None)
+    torch.cuda.synchronize()
+    assert code == moe._native.MOE_ERR_CAPACITY
+    assert (rows[0], rows[1]) == (R, Lr["rows_valid"])
+    assert bool((L.row_token == 12345).all()) and bool((L.row_expert == -7).all())
+    assert bool((L.row_weight == 0.5).all()) and bool((L.token_row == 999).all())
+    if fp8:
+        assert bool((q == 0x5A).all()) and bool((sc == 3.0).all())
+    else:
+        assert bool((xd == 7.0).all())
+    assert int(status.item()) & moe._native.MOE_DEVERR_CAPACITY
 
 
 def test_sync_free_rejects_small_capacity(moe):
