@@ -89,11 +89,16 @@ __device__ bool grid_barrier(unsigned* ctr, unsigned target, int* status, int* s
 // The single-CTA layout also does the dispatch's row pass when it has at most
 // this many items (tokens + rows) and moves at most this many bytes.
 constexpr long long LAYOUT_FUSED_ITEMS = 64;
+// Layers of at most this many 32-token chunks take the barrier-free layout
+// (decode T = 256, 8 chunks: 21.1 -> 12.7 us under graph replay; at 32 chunks
+// the cooperative kernel was faster).
+constexpr int LAYOUT_REDUNDANT_CHUNKS = 8;
 constexpr long long LAYOUT_FUSED_BYTES = 256 * 1024;
 
 enum LayoutMode : int {
   LAYOUT_ALL = 0,    // counts, scans, offsets and placement: one cooperative launch
-  LAYOUT_SINGLE = 3, // all four phases in one CTA, for layers of one or two chunks (no barrier)
+  LAYOUT_SINGLE = 3, // up to 8 chunks, one CTA per chunk: each counts every chunk, then
+                     // places its own (no grid barrier; one CTA may also do the row pass)
 };
 
 struct LayoutArgs {
@@ -257,22 +262,51 @@ __global__ void __launch_bounds__(256) layout_kernel(LayoutArgs a) {
   int* s_base = reinterpret_cast<int*>(s_map32 + E);                   // [E], likewise
   uint32_t* s_emask = s_map32 + LAYOUT_CHUNK * E4;                     // [32][EW]
   int* s_off = reinterpret_cast<int*>(s_emask + LAYOUT_CHUNK * EW);    // [E + 1]
-  int* s_cc = s_off + E + 1;  // LAYOUT_SINGLE: [chunks][E] counts, then each chunk's start
+  int* s_tot = s_off + E + 1;  // LAYOUT_SINGLE: [E] each expert's count
+  int* s_cc = s_tot + E;       // LAYOUT_SINGLE: [chunks][E] counts, then each chunk's start
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
 
-  for (int c = blockIdx.x; c < a.chunks; c += gridDim.x) {
-    const long long t0 = static_cast<long long>(c) * LAYOUT_CHUNK;
-    const int nt = static_cast<int>(min(static_cast<long long>(LAYOUT_CHUNK), a.T - t0));
-    const uint32_t* words = reinterpret_cast<const uint32_t*>(a.map + t0 * E);
-    for (int i = threadIdx.x; i < nt * E4; i += blockDim.x) s_map32[i] = words[i];
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-      int n = 0;
-      for (int tl = 0; tl < nt; ++tl) n += s_map[tl * E + e] != 0;
-      if constexpr (MODE == LAYOUT_SINGLE)
-        s_cc[c * E + e] = n;
-      else
+  if constexpr (MODE == LAYOUT_ALL) {
+    // 1. this CTA's chunks, staged in shared memory; thread e counts column e
+    for (int c = blockIdx.x; c < a.chunks; c += gridDim.x) {
+      const long long t0 = static_cast<long long>(c) * LAYOUT_CHUNK;
+      const int nt = static_cast<int>(min(static_cast<long long>(LAYOUT_CHUNK), a.T - t0));
+      const uint32_t* words = reinterpret_cast<const uint32_t*>(a.map + t0 * E);
+      for (int i = threadIdx.x; i < nt * E4; i += blockDim.x) s_map32[i] = words[i];
+      __syncthreads();
+      for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int n = 0;
+        for (int tl = 0; tl < nt; ++tl) n += s_map[tl * E + e] != 0;
         a.chunk_counts[static_cast<long long>(e) * a.chunks + c] = n;
+      }
+      __syncthreads();
+    }
+  } else {
+    // 1. every CTA counts every chunk (no grid barrier needed): warp w takes
+    // chunks w, w + 8, ..., lane l the 4-expert words l, l + 32, ... of each
+    // token row.  A word's four map bytes become four 0/1 bytes and the 32
+    // token rows of a chunk are summed bytewise (at most 32: no carry), all
+    // 32 loads in flight together.  One thread owns each (chunk, expert) count.
+    const uint32_t* map32 = reinterpret_cast<const uint32_t*>(a.map);
+    for (int c = warp; c < a.chunks; c += nwarps) {
+      const long long t0 = static_cast<long long>(c) * LAYOUT_CHUNK;
+      const int nt = static_cast<int>(min(static_cast<long long>(LAYOUT_CHUNK), a.T - t0));
+      for (int w4 = lane; w4 < E4; w4 += 32) {
+        uint32_t wd[LAYOUT_CHUNK];
+#pragma unroll
+        for (int tl = 0; tl < LAYOUT_CHUNK; ++tl)
+          wd[tl] = tl < nt ? __ldg(map32 + (t0 + tl) * E4 + w4) : 0u;
+        uint32_t sum = 0;
+#pragma unroll
+        for (int tl = 0; tl < LAYOUT_CHUNK; ++tl) {
+          uint32_t b = wd[tl] | (wd[tl] >> 4);  // bit 0 of each byte: the byte is nonzero
+          b |= b >> 2;
+          b |= b >> 1;
+          sum += b & 0x01010101u;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) s_cc[c * E + 4 * w4 + k] = (sum >> (8 * k)) & 0xffu;
+      }
     }
     __syncthreads();
   }
@@ -285,7 +319,8 @@ __global__ void __launch_bounds__(256) layout_kernel(LayoutArgs a) {
         s_cc[c * E + e] = run;
         run += v;
       }
-      a.tokens_per_expert[e] = run;
+      s_tot[e] = run;
+      if (blockIdx.x == 0) a.tokens_per_expert[e] = run;
     }
     __syncthreads();
   } else {
@@ -321,7 +356,10 @@ __global__ void __launch_bounds__(256) layout_kernel(LayoutArgs a) {
 #pragma unroll
     for (int d = 0; d < 4; ++d) {
       const int e = 4 * threadIdx.x + d;
-      cnt[d] = e < E ? __ldcg(a.tokens_per_expert + e) : 0;
+      if constexpr (MODE == LAYOUT_SINGLE)
+        cnt[d] = e < E ? s_tot[e] : 0;
+      else
+        cnt[d] = e < E ? __ldcg(a.tokens_per_expert + e) : 0;
       pad[d] = ((cnt[d] + a.P - 1) / a.P) * a.P;
       psum += pad[d];
       nsum += cnt[d];
@@ -467,7 +505,7 @@ namespace {
 size_t layout_smem_bytes(int E) {
   return static_cast<size_t>(LAYOUT_CHUNK) * E +
          static_cast<size_t>(LAYOUT_CHUNK) * ((E + 31) / 32) * sizeof(uint32_t) +
-         static_cast<size_t>(E + 1) * sizeof(int);
+         static_cast<size_t>(2 * E + 1) * sizeof(int);
 }
 
 // CTAs of layout_kernel<MODE> resident at once on the current device with
@@ -493,7 +531,9 @@ int layout_resident_ctas(size_t smem) {
 template <int MODE>
 cudaError_t launch_layout_mode(const LayoutArgs& a, size_t smem, cudaStream_t s) {
   if (MODE == LAYOUT_SINGLE) {
-    return launch_dependent(layout_kernel<MODE>, 1, 256,
+    // one CTA per chunk (one CTA in all when it also does the row pass)
+    const int grid = a.rows || a.chunks < 1 ? 1 : a.chunks;
+    return launch_dependent(layout_kernel<MODE>, grid, 256,
                             smem + static_cast<size_t>(a.chunks) * a.E * sizeof(int), s, a);
   }
   cudaError_t err = cudaMemsetAsync(a.barrier, 0, sizeof(unsigned), s);
@@ -548,15 +588,17 @@ cudaError_t launch_layout(const uint8_t* routing_map, const float* probs, const 
   a.token_row = L.token_row;
   a.status = L.status;
   const size_t smem = layout_smem_bytes(L.E);
-  // One or two chunks (T <= 64): one CTA, no barrier, no memset.  It takes
-  // the chunks one after another, about 4 us each, so beyond two the
-  // cooperative launch (about 15 us at any small size) is faster.
-  if (a.chunks <= 2 && smem + static_cast<size_t>(a.chunks) * a.E * sizeof(int) <= 48 * 1024) {
-    // A decode-sized row pass (a few rows of a few KB) costs the one CTA
-    // less than a launch of its own.
+  // Up to LAYOUT_REDUNDANT_CHUNKS chunks (T <= 256): one CTA per chunk, each
+  // counting every chunk itself, so there is no grid barrier, no memset and
+  // no cooperative launch, and the kernel takes part in programmatic
+  // dependent launch.  Larger layers use the cooperative kernel.
+  if (a.chunks <= LAYOUT_REDUNDANT_CHUNKS &&
+      smem + static_cast<size_t>(a.chunks) * a.E * sizeof(int) <= 48 * 1024) {
+    // A decode-sized row pass (a few rows of a few KB, one or two chunks)
+    // costs a single CTA less than a launch of its own.
     const long long items = L.T + L.capacity;
     const long long bytes = x_disp ? items * H * 2 : 0;
-    if (rows_done && items <= LAYOUT_FUSED_ITEMS && bytes <= LAYOUT_FUSED_BYTES) {
+    if (rows_done && a.chunks <= 2 && items <= LAYOUT_FUSED_ITEMS && bytes <= LAYOUT_FUSED_BYTES) {
       a.rows = true;
       *rows_done = true;
     }

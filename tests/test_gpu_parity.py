@@ -75,6 +75,10 @@ def _check_layout(g, idx, p, E, P, capacity):
     (40, 8, 1, 3, 0.0, 0.0),        # topk = 1
     (33, 4, 4, 2, 0.0, 0.0),        # K = E
     (0, 8, 2, 16, 0.0, 0.0),        # no tokens
+    (65, 64, 4, 8, 0.1, 0.1),       # 3 chunks: one CTA per chunk, each counting all of them
+    (256, 128, 8, 1, 0.05, 0.05),   # 8 chunks: the largest layer laid out without a grid barrier
+    (257, 128, 8, 16, 0.0, 0.0),    # 9 chunks: the cooperative layout kernel
+    (1024, 128, 8, 1, 0.05, 0.05),  # 32 chunks
     (40000, 128, 8, 4, 0.05, 0.0),  # 1250 chunks: more than the layout kernel's resident CTAs
 ])
 @pytest.mark.parametrize("host_sync", [True, False])
