@@ -35,13 +35,14 @@ int g_cc_ok[MAX_DEVICES];    // 0 unknown, 1 compute capability 10.3, -1 other
 int g_sms[MAX_DEVICES];
 
 // The host-synced dispatch reads R, N and the status word from 16 bytes of
-// mapped pinned host memory that the count kernel writes directly, so the
+// mapped pinned host memory that the layout kernel writes directly, so the
 // readback needs no copy engine and cannot queue behind bulk copies on other
 // streams.  One buffer per device, made on first use; the mutex is held from
-// the launch to the read, so concurrent host-synced calls take turns.
+// the launch until the kernel can no longer write to it, so concurrent
+// host-synced calls take turns.
 std::mutex g_rb_mu;
 // The host polls the mapped buffer for this long before it falls back to a
-// stream synchronisation (the count kernel's own waits give up after 2 s).
+// stream synchronisation (the layout kernel's own waits give up after 2 s).
 constexpr int READBACK_POLL_LIMIT_S = 10;
 int* g_rb_host[MAX_DEVICES];
 int* g_rb_dev[MAX_DEVICES];
@@ -251,7 +252,12 @@ moe_status dispatch_impl(const char* who, const moe_bf16* x, const uint8_t* rout
   if (!rows_done) {
     err = bf16_rows ? launch_row_gather(x, *L, H, x_disp, true, nullptr, nullptr, stream)
                     : launch_row_gather_fp8(x, *L, H, x_q, x_scale, stream);
-    if (err != cudaSuccess) return cuda_fail(err, "dispatch: rows");
+    if (err != cudaSuccess) {
+      // the layout kernel may still write the readback buffer: let it finish
+      // before the buffer goes to the next caller
+      if (mapped) cudaStreamSynchronize(stream);
+      return cuda_fail(err, "dispatch: rows");
+    }
   }
   if (!rows_host) return MOE_OK;
 
