@@ -281,7 +281,10 @@ moe_status dispatch_impl(const char* who, const moe_bf16* x, const uint8_t* rout
         published = rb[0] >= 0;
         break;
       }
-      if (q != cudaErrorNotReady) return cuda_fail(q, "dispatch: waiting for the row counts");
+      if (q != cudaErrorNotReady) {
+        cudaStreamSynchronize(stream);  // as above: nothing may write the buffer afterwards
+        return cuda_fail(q, "dispatch: waiting for the row counts");
+      }
       if (std::chrono::steady_clock::now() - t0 > std::chrono::seconds(READBACK_POLL_LIMIT_S)) break;
     }
   }
