@@ -169,7 +169,8 @@ class ClockSampler:
 
 def algorithmic(cfg, counts: np.ndarray, R: int, N: int, C: int, backward: bool, fp8: bool = False,
                 gather: bool = False):
-    """Bytes / flops the layer's steps must move, per call (definitions in the design doc).
+    """Bytes / flops the layer's steps must move, per call: what each step has to
+    read and write at the least, and the experts' 2 flops per multiply-add.
     With fp8 the dispatched rows and W1 are e4m3 (1 byte) with fp32 per-row scales.
     With gather no rows are dispatched: the gate/up GEMM reads the tokens x once."""
     T, H, E, K, I = cfg.T, cfg.H, cfg.E, cfg.K, cfg.I

@@ -42,7 +42,8 @@ class LayerConfig:
     backward: bool = False   # forward plus backward
 
 
-# The workloads.  Seeds other than the tiny layer's 0 are this build's choice.
+# The workloads.  The tiny layer's seed 0 is part of its description; the
+# other seeds are fixed, arbitrary choices.
 CONFIGS = {
     "tiny": LayerConfig("tiny", T=64, H=256, E=8, K=2, I=128, P=16, seed=0),
     "qwen3_30b_a3b": LayerConfig("qwen3_30b_a3b", T=4096, H=2048, E=128, K=8, I=768, P=128, seed=1),
