@@ -27,6 +27,12 @@ namespace {
 
 constexpr int GEMV_ROWS = 4;       // rows per expert this path takes
 constexpr int GEMV_THREADS = 256;  // 8 warps
+// Four CTAs per SM (64 registers a thread): with 2.5 waves of 2 CTAs per SM
+// before, each wave paid the list, A-row and weight round trips again.  A
+// warp now loads 4 (gate/up) or 2 (down) 16-byte vectors per lane and row in
+// one round instead of 8 or 4: decode T = 1, the two kernels under graph
+// replay went from 24.3 to 21.8 us.
+constexpr int GEMV_CTAS_PER_SM = 4;
 constexpr int S1_COLS = 8;         // h columns per step-1 item (1 per warp)
 constexpr int S2_COLS = 32;        // y columns per step-2 item (4 per warp)
 
@@ -100,7 +106,7 @@ __device__ __forceinline__ uint16_t to_bf16_bits(float v) {
 }
 
 template <int STEP>
-__global__ void __launch_bounds__(GEMV_THREADS) gemv_experts_kernel(GemvArgs args) {
+__global__ void __launch_bounds__(GEMV_THREADS, GEMV_CTAS_PER_SM) gemv_experts_kernel(GemvArgs args) {
   griddep_launch_dependents();
   griddep_wait();
   extern __shared__ __align__(16) uint8_t smem[];
@@ -143,7 +149,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_experts_kernel(GemvArgs arg
       const int c = j * S1_COLS + warp;
       const uint16_t* w1 = args.w + static_cast<long long>(e) * 2 * args.I * K;
       float gu[2][GEMV_ROWS];
-      warp_dot<2, 8>(w1 + static_cast<long long>(c) * K, static_cast<long long>(args.I) * K, s_a, K, n,
+      warp_dot<2, 4>(w1 + static_cast<long long>(c) * K, static_cast<long long>(args.I) * K, s_a, K, n,
                      lane, gu);
       if (lane < n) {
         float gv = gu[0][0], uv = gu[1][0];
@@ -161,7 +167,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_experts_kernel(GemvArgs arg
       const int c0 = j * S2_COLS + warp * 4;
       const uint16_t* w2 = args.w + static_cast<long long>(e) * args.H * K;
       float o[4][GEMV_ROWS];
-      warp_dot<4, 4>(w2 + static_cast<long long>(c0) * K, K, s_a, K, n, lane, o);
+      warp_dot<4, 2>(w2 + static_cast<long long>(c0) * K, K, s_a, K, n, lane, o);
       if (lane < n) {
         const float wgt = args.row_weight[r0 + lane];
 #pragma unroll
