@@ -167,6 +167,24 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- algorithmic work
 
+def step_launches(T: int, H: int, E: int, C: int, fp8: bool, gather: bool, backward: bool) -> int:
+    """Our kernel launches in one step (the layout's counter memset is a driver
+    memset, not one of ours): the multihot kernel; the layout kernel and the row
+    copy; the two expert kernels; the combine; and with the backward the combine
+    backward, the five expert-backward kernels, the dispatch backward and the
+    multihot backward.  A layer of at most two 32-token chunks, whose one-CTA
+    layout fits 48 KiB of shared memory and whose row pass has at most 64 items
+    (tokens + rows) and 256 KiB, lays out and copies in one kernel (bf16 only)."""
+    chunks = -(-T // 32)
+    single_smem = 32 * E + 32 * (-(-E // 32)) * 4 + (2 * E + 1) * 4 + chunks * E * 4
+    single_rows = (not fp8 and chunks <= 2 and single_smem <= 48 * 1024 and T + C <= 64
+                   and (0 if gather else (T + C) * H * 2) <= 256 * 1024)
+    n = 1 + (1 if single_rows else 2) + 2 + 1
+    if backward:
+        n += 1 + 5 + 1 + 1
+    return n
+
+
 def algorithmic(cfg, counts: np.ndarray, R: int, N: int, C: int, backward: bool, fp8: bool = False,
                 gather: bool = False):
     """Bytes / flops the layer's steps must move, per call: what each step has to
@@ -253,18 +271,9 @@ def run_ours(args, world, rank, local):
     ev = lambda: torch.cuda.Event(enable_timing=True)
     bwd = cfg.backward
     stages = ["multihot", "dispatch", "experts", "combine"]
-    # our kernels per step: multihot; the layout kernel and the row copy; the
-    # two expert GEMMs; the combine.  A layer of at most two 32-token chunks
-    # whose row pass has at most 64 items (tokens + rows) and 256 KiB lays out
-    # and copies in one kernel.
-    chunks = -(-T // 32)
-    single_rows = (not fp8 and chunks <= 2 and T + C <= 64
-                   and (0 if gather else (T + C) * H * 2) <= 256 * 1024)
-    dispatch_launches = 1 if single_rows else 2
-    launches_per_step = 1 + dispatch_launches + 2 + 1
+    launches_per_step = step_launches(T, H, E, C, fp8, gather, bwd)
     if bwd:
         stages += ["combine_bwd", "experts_bwd", "dispatch_bwd", "multihot_bwd"]
-        launches_per_step += 1 + 5 + 1 + 1
         bufs["o"] = torch.empty(C, H, dtype=torch.bfloat16, device=dev)
         bufs["gu"] = torch.empty(C, 2 * I, dtype=torch.bfloat16, device=dev)
         for l, L in enumerate(layers):

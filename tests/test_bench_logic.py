@@ -1,0 +1,48 @@
+"""Host logic of bench.py that the JSON line's claims rest on, checked without a GPU:
+the number of our kernel launches per step (the `gpu_launches` claim) for each
+workload shape the bench runs, and both sides of the one-kernel dispatch limit."""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import synthetic  # noqa: E402
+from oracle import worst_case_capacity  # noqa: E402
+
+
+def _launches(name, fp8=False, gather=False):
+    c = synthetic.CONFIGS[name]
+    C = worst_case_capacity(c.T, c.E, c.K, c.P)
+    return bench.step_launches(c.T, c.H, c.E, C, fp8, gather, c.backward)
+
+
+@pytest.mark.parametrize("name,expected", [
+    ("decode_1", 5),             # multihot, one-CTA layout with the rows, 2 expert kernels, combine
+    ("decode_256", 6),           # the layout and the row copy are separate
+    ("decode_1024", 6),
+    ("qwen3_30b_a3b", 6),
+    ("qwen3_30b_a3b_16k", 6),
+    ("skewed", 6),
+    ("tiny", 6),                 # 64 tokens and 248 rows: more than 64 items
+    ("h4096", 14),               # + combine backward, 5 expert-backward kernels, dispatch and multihot backward
+])
+def test_launches_per_step(name, expected):
+    assert _launches(name) == expected
+
+
+def test_fp8_dispatch_is_never_fused():
+    assert _launches("decode_1", fp8=True) == 6
+
+
+@pytest.mark.parametrize("T,K,E,H,expected", [
+    (8, 7, 8, 512, 5),     # T + C = 8 + 56 = 64 items: one kernel
+    (9, 7, 8, 512, 6),     # 72 items
+    (1, 8, 128, 65536, 6), # 9 items, but 9 * 128 KiB of rows
+])
+def test_one_kernel_dispatch_limit(T, K, E, H, expected):
+    C = worst_case_capacity(T, E, K, 1)
+    assert bench.step_launches(T, H, E, C, False, False, False) == expected
