@@ -10,7 +10,8 @@
 // FMAs with it, so it is a stream over the active experts' weights.  A
 // 128-row tensor-core tile would carry 124 empty rows and, with only a few
 // experts active, too few tiles to keep every SM streaming.  Here the work is
-// (active expert, column slice) items spread over a persistent grid:
+// (active expert, column slice) items spread over a grid of up to 8 CTAs per
+// SM (4 resident at a time; the CTAs loop when there are more items):
 //   step 1: 8 h columns = 8 gate + 8 up rows of W1, h = bf16(silu(g) * u);
 //   step 2: 32 y columns = 32 rows of W2, y = bf16(w_row * o).
 // A warp takes 2 (step 1: gate and up) or 4 (step 2) weight rows and issues

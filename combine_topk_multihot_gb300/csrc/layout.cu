@@ -11,11 +11,16 @@
 // the sentinel expert id; Training -- the combine's gradient is gathered with
 // the same layout as the forward dispatch.
 //
-// The layout is built without atomics on the output order: a chunked
-// histogram (shared-memory counters), one scan block over (expert, chunk),
-// and a placement pass in which the thread of expert e walks the chunk's
-// tokens in order, so rows inside a group are in ascending token order and
-// the result does not depend on scheduling.
+// The layout is built without atomics on the output order: per 32-token chunk
+// each expert's count, a scan over the chunks of each expert, padded offsets,
+// and a placement pass that ranks each (token, expert) pair inside its chunk
+// by a popcount of the expert's token mask, so rows inside a group are in
+// ascending token order and the result does not depend on scheduling.  Large
+// layers run this as one cooperative launch with two bounded grid barriers;
+// layers of up to 8 chunks as one CTA per chunk that each count every chunk,
+// with no barrier.  For a host-synced caller the kernel also hands R, N and
+// the status word to the host through mapped memory as soon as the offsets are
+// known, and places nothing when the rows do not fit.
 
 #include "common.cuh"
 #include "launch.h"
