@@ -46,3 +46,19 @@ def test_fp8_dispatch_is_never_fused():
 def test_one_kernel_dispatch_limit(T, K, E, H, expected):
     C = worst_case_capacity(T, E, K, 1)
     assert bench.step_launches(T, H, E, C, False, False, False) == expected
+
+
+def test_experts_bytes_agree_with_profiled_traffic():
+    """The roofline's algorithmic byte count for the Qwen3-30B-A3B experts
+    (first layer of the bench, its layout from the oracle) is within 3 % of the
+    DRAM traffic ncu measured for the same two launches."""
+    import oracle as O
+    cfg = synthetic.CONFIGS["qwen3_30b_a3b"]
+    d = synthetic.make_layer_inputs(cfg, with_weights=False)
+    rm, pr, _ = O.route_to_multihot(d["topk_idx"].numpy(), d["topk_probs"].numpy(), cfg.E)
+    lay = O.build_layout(rm, pr, cfg.K, cfg.P)
+    R, N = lay["rows_used"], lay["rows_valid"]
+    a = bench.algorithmic(cfg, lay["tokens_per_expert"], R, N, R, backward=False)
+    measured = bench.PROFILED_TRAFFIC["qwen3_30b_a3b"]["bytes"]
+    assert abs(a["experts_bytes"] - measured) / measured < 0.03
+    assert a["experts_flops"] == 6.0 * N * cfg.H * cfg.I
