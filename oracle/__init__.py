@@ -29,7 +29,10 @@ of the FP8 dispatch and gate/up GEMM):
 
 Floating point: expert math in fp64 from the exact bf16 values, with the
 roundings the layer itself has (h and y to bf16); combine sums in fp32 in a
-fixed order and rounds once to bf16.
+fixed order and rounds once to bf16.  The expert backward is the chain rule
+of that forward in fp64 with no rounding at all (its bf16 outputs are
+rounded once at the end); the test suite holds a bf16 implementation of it
+to an element-wise forward-error bound around this exact value.
 
 Every function is pinned by ``tests/test_oracle_*.py`` against something other
 than itself (hand-written cases, library routines, closed forms, brute force,
@@ -41,7 +44,8 @@ from .moe_oracle import (OracleIndexError, OracleCapacityError, sentinel_expert,
                          route_to_multihot, counts_and_offsets, build_layout,
                          dispatch, expert_forward_f64, grouped_experts, combine,
                          combine_backward, routing_weight_grad,
-                         expert_backward_f64, grouped_experts_backward,
+                         expert_backward_f64, expert_backward_steps,
+                         grouped_experts_backward,
                          backward_scale, backward_gate_up, backward_swiglu,
                          backward_gemms,
                          dispatch_backward, route_to_multihot_backward,
@@ -55,7 +59,8 @@ __all__ = [
     "bf16_round_f64", "OracleIndexError", "OracleCapacityError", "sentinel_expert",
     "route_to_multihot", "counts_and_offsets", "build_layout", "dispatch",
     "expert_forward_f64", "grouped_experts", "combine", "combine_backward",
-    "routing_weight_grad", "expert_backward_f64", "grouped_experts_backward",
+    "routing_weight_grad", "expert_backward_f64", "expert_backward_steps",
+    "grouped_experts_backward",
     "backward_scale", "backward_gate_up", "backward_swiglu", "backward_gemms",
     "dispatch_backward", "route_to_multihot_backward", "layer_forward",
     "layer_backward", "worst_case_capacity", "router_topk", "router_topk_f64",

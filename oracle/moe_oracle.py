@@ -270,28 +270,42 @@ def routing_weight_grad(grad_y_bits, o_bits, row_expert, E) -> np.ndarray:
 
 
 # --------------------------------------------------------------------------
-# a9: expert backward (chain rule written out)
+# a9: expert backward   ([DEP] What this adds, Training: the gradients reach
+# the tokens and the weights through the experts).  The chain rule of the
+# forward above, written out in fp64 with no rounding anywhere: the forward's
+# bf16 roundings (h, y) are steps of a rounding function whose derivative is
+# taken as one, as autograd does, and the forward's saved bf16 h enters
+# dW2 as the value the forward produced.
 # --------------------------------------------------------------------------
-def backward_scale(GY, w, rnd=bf16_round_f64):
-    """G_o = rnd(w * GY): y = w o, so dL/do = w dL/dy (rounded to bf16, the
-    operand type of the backward GEMMs)."""
-    return rnd(np.asarray(w, dtype=np.float64)[:, None] * GY)
+def backward_scale(GY, w):
+    """G_o = w * GY: y = w o, so dL/do = w dL/dy."""
+    return np.asarray(w, dtype=np.float64)[:, None] * GY
 
 
-def backward_gate_up(X, W1e, I, rnd=bf16_round_f64):
-    """The forward's gate and up pre-activations as handed to the backward:
-    g = rnd(X Wg^T), u = rnd(X Wu^T)."""
-    return rnd(X @ W1e[:I].T), rnd(X @ W1e[I:].T)
+def backward_gate_up(X, W1e, I):
+    """The forward's gate and up pre-activations: g = X Wg^T, u = X Wu^T."""
+    return X @ W1e[:I].T, X @ W1e[I:].T
 
 
-def backward_swiglu(G_o, W2e, g, u, rnd=bf16_round_f64):
-    """G_h = G_o W2;  G_g = G_h * u * silu'(g),  G_u = G_h * silu(g) with
-    silu'(g) = s (1 + g (1 - s)), s = sigmoid(g).  Returns rnd([G_g | G_u])."""
-    G_h = G_o @ W2e
+def _sigmoid(z):
     with np.errstate(over="ignore"):
-        s = 1.0 / (1.0 + np.exp(-g))
+        return 1.0 / (1.0 + np.exp(-z))
+
+
+def backward_swiglu(G_o, W2e, g, u):
+    """G_h = G_o W2;  G_g = G_h * u * silu'(g),  G_u = G_h * silu(g) with
+    silu'(g) = s (1 + g (1 - s)), s = sigmoid(g).  Returns [G_g | G_u]."""
+    return expert_backward_steps_from(G_o, W2e, g, u)["G_gu"]
+
+
+def expert_backward_steps_from(G_o, W2e, g, u):
+    """The SwiGLU part of the chain rule, every intermediate kept."""
+    G_h = G_o @ W2e
+    s = _sigmoid(g)
+    silu = g * s
     dsilu = s * (1.0 + g * (1.0 - s))
-    return rnd(np.concatenate([G_h * u * dsilu, G_h * (g * s)], axis=1))
+    G_gu = np.concatenate([G_h * u * dsilu, G_h * silu], axis=1)
+    return dict(G_h=G_h, s=s, silu=silu, dsilu=dsilu, G_gu=G_gu)
 
 
 def backward_gemms(G_o, G_gu, X, h, W1e):
@@ -299,22 +313,28 @@ def backward_gemms(G_o, G_gu, X, h, W1e):
     return G_gu @ W1e, G_gu.T @ X, G_o.T @ h
 
 
-def expert_backward_f64(X, h, GY, w, W1e, W2e, I, rnd=bf16_round_f64):
+def expert_backward_steps(X, h, GY, w, W1e, W2e, I):
+    """Every step of one expert's chain rule, in fp64: G_o, g, u, G_h, the
+    SwiGLU derivative terms, G_gu = [G_g | G_u], and dX, dW1, dW2."""
+    G_o = backward_scale(GY, w)
+    g, u = backward_gate_up(X, W1e, I)
+    st = expert_backward_steps_from(G_o, W2e, g, u)
+    dX, dW1, dW2 = backward_gemms(G_o, st["G_gu"], X, h, W1e)
+    st.update(G_o=G_o, g=g, u=u, dX=dX, dW1=dW1, dW2=dW2)
+    return st
+
+
+def expert_backward_f64(X, h, GY, w, W1e, W2e, I):
     """Gradients of one expert's rows, in fp64.
 
     Forward: g = X Wg^T, u = X Wu^T, h = silu(g) u, o = h W2^T, y = w o.
     Given dL/dy = GY and the forward's h, the chain rule in four steps:
     backward_scale (G_o), backward_gate_up (g, u), backward_swiglu (G_gu =
-    [G_g | G_u]), backward_gemms (dX, dW1, dW2).  The experts are bf16 GEMMs,
-    so the operands of the backward GEMMs (G_o, G_gu) and the gate / up values
-    the forward hands to the backward are bf16: ``rnd`` rounds exactly there;
-    every product and sum is exact fp64.  Pass the identity to get the
-    real-valued chain rule.  Returns (dX [n, H], dW1 [2I, H], dW2 [H, I]).
+    [G_g | G_u]), backward_gemms (dX, dW1, dW2); every product and sum is
+    exact fp64.  Returns (dX [n, H], dW1 [2I, H], dW2 [H, I]).
     """
-    G_o = backward_scale(GY, w, rnd)
-    g, u = backward_gate_up(X, W1e, I, rnd)
-    G_gu = backward_swiglu(G_o, W2e, g, u, rnd)
-    return backward_gemms(G_o, G_gu, X, h, W1e)
+    st = expert_backward_steps(X, h, GY, w, W1e, W2e, I)
+    return st["dX"], st["dW1"], st["dW2"]
 
 
 def grouped_experts_backward(grad_y_bits, x_disp_bits, h_bits, row_expert,

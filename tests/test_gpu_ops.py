@@ -23,6 +23,8 @@ import torch
 
 import oracle as O
 import synthetic
+from tests._bounds import (SAFETY, U_B, U_F, acc, check_within, expert_backward_bound,
+                           expert_forward_h_bound)
 from tests._util import GEMM_REL_L2, assert_gemm_close, bits, random_routing
 
 pytestmark = pytest.mark.gpu
@@ -91,10 +93,62 @@ def test_ops_equal_the_direct_calls(moe, T, H, E, K, I, P, drop, dup):
     _same(got, ref, "ops vs direct")
 
 
+def _layer_grad_bounds(fwd, g_bits, W1b, W2b, I):
+    """The exact gradients of the layer (the oracle's layout, forward h and
+    fp64 chain rule, rounding nothing) and element-wise bounds on a bf16
+    implementation's: dW1, dW2 (cast to bf16 by autograd), grad_x (the
+    combine of the bf16 grad_x_disp rows) and the routing-weight gradient
+    per row (<grad_y, o> with o = h W2^T, which the implementation computes
+    from its own h and rounds to bf16)."""
+    f = O.bf16_bits_to_f64
+    L = fwd["layout"]
+    E = W1b.shape[0]
+    T, H = g_bits.shape
+    K = L["token_row"].shape[1]
+    C = L["row_token"].shape[0]
+    GYall = f(O.combine_backward(g_bits, L["row_token"]))
+    dX = np.zeros((C, H))
+    bX = np.zeros((C, H))
+    gw = np.zeros(C)
+    bgw = np.zeros(C)
+    dW1 = np.zeros((E, 2 * I, H))
+    dW2 = np.zeros((E, H, I))
+    bW1 = np.zeros_like(dW1)
+    bW2 = np.zeros_like(dW2)
+    for e in range(E):
+        R = np.flatnonzero(L["row_expert"] == e)
+        if R.size == 0:
+            continue
+        X, h, GY = f(fwd["x_disp"][R]), f(fwd["h"][R]), GYall[R]
+        W1e, W2e = f(W1b[e]), f(W2b[e])
+        hf = expert_forward_h_bound(X, W1e, I)
+        st, b = expert_backward_bound(X, h, GY, L["row_weight"][R], W1e, W2e, I, h_flips=hf,
+                                      dW_bf16=True)
+        dX[R], bX[R] = st["dX"], b["dX"]
+        dW1[e], dW2[e], bW1[e], bW2[e] = st["dW1"], st["dW2"], b["dW1"], b["dW2"]
+        o = h @ W2e.T
+        b_o = hf @ np.abs(W2e).T + acc(I) * (np.abs(h) @ np.abs(W2e).T) + U_B * np.abs(o)
+        gw[R] = np.sum(GY * o, axis=1)
+        bgw[R] = SAFETY * (np.sum(np.abs(GY) * b_o, axis=1) + acc(H) * np.sum(np.abs(GY * o), axis=1))
+    tr = L["token_row"]
+    gx = np.zeros((T, H))
+    bgx = np.zeros((T, H))
+    absum = np.zeros((T, H))
+    for j in range(K):
+        r = tr[:, j]
+        ok = r >= 0
+        gx[ok] += dX[r[ok]]
+        bgx[ok] += bX[r[ok]]
+        absum[ok] += np.abs(dX[r[ok]]) + bX[r[ok]]
+    bgx += SAFETY * (K * U_F * absum + U_B * np.abs(gx))
+    return dict(dW1=dW1, dW2=dW2, bW1=bW1, bW2=bW2, gx=gx, bgx=bgx, gw=gw, bgw=bgw)
+
+
 @pytest.mark.parametrize("T,H,E,K,I,P,drop,dup", CASES[:2])
 def test_ops_match_the_oracle_end_to_end(moe, T, H, E, K, I, P, drop, dup):
-    """Forward output within the GEMM tolerance; every gradient within
-    rel L2 5e-3 of the oracle's fp64 chain rule with bf16 operands."""
+    """Forward output within the GEMM tolerance; every gradient element-wise
+    within its error bound around the exact chain rule of the oracle's
+    forward (tests/_bounds.py), and within rel L2 5e-3 of it."""
     x, idx, p, W1, W2, g = _inputs(T, H, E, K, I, seed=7 * T + H, drop=drop, dup=dup)
     out, dx, dp, dW1, dW2 = _layer(lambda *a: moe.moe_layer(*a, pad_multiple=P), x, idx, p, W1, W2, g)
     torch.cuda.synchronize()
@@ -102,18 +156,40 @@ def test_ops_match_the_oracle_end_to_end(moe, T, H, E, K, I, P, drop, dup):
     W1b, W2b = bits(W1), bits(W2)
     C = O.worst_case_capacity(T, E, K, P)
     fwd = O.layer_forward(bits(x), idx_np, p.cpu().numpy(), W1b, W2b, I, P, capacity=C)
-    bwd = O.layer_backward(fwd, bits(g), W1b, W2b, idx_np, I)
     assert_gemm_close(bits(out), fwd["out"], "out")
+    ref = _layer_grad_bounds(fwd, bits(g), W1b, W2b, I)
 
-    def rel(gpu, ref, what):
-        gpu, ref = np.asarray(gpu, np.float64), np.asarray(ref, np.float64)
-        r = np.linalg.norm(gpu - ref) / max(np.linalg.norm(ref), 1e-30)
+    def rel(gpu, exact, what):
+        gpu, exact = np.asarray(gpu, np.float64), np.asarray(exact, np.float64)
+        r = np.linalg.norm(gpu - exact) / max(np.linalg.norm(exact), 1e-30)
         assert np.isfinite(gpu).all() and r <= GEMM_REL_L2, f"{what}: rel_l2={r:.3g}"
 
-    rel(O.bf16_bits_to_f64(bits(dx)), O.bf16_bits_to_f64(bwd["grad_x"]), "grad_x")
-    rel(dp.cpu().numpy(), bwd["grad_topk_probs"], "grad_topk_probs")
-    rel(dW1.float().cpu().numpy(), bwd["dW1"], "dW1")
-    rel(dW2.float().cpu().numpy(), bwd["dW2"], "dW2")
+    gx = O.bf16_bits_to_f64(bits(dx))
+    check_within(gx, ref["gx"], ref["bgx"], "grad_x")
+    rel(gx, ref["gx"], "grad_x")
+    for name, got in (("dW1", dW1), ("dW2", dW2)):
+        got = got.float().cpu().numpy()
+        check_within(got, ref[name], ref["b" + name[1:]], name)
+        rel(got, ref[name], name)
+    # grad_topk_probs: the routing-weight gradient of each slot's row (the
+    # winner slot of each (token, expert) pair; 0 for dropped and losing slots)
+    L = fwd["layout"]
+    exact = np.zeros((T, E))
+    bound = np.zeros((T, E))
+    ok = L["row_token"] >= 0
+    exact[L["row_token"][ok], L["row_expert"][ok]] = ref["gw"][ok]
+    bound[L["row_token"][ok], L["row_expert"][ok]] = ref["bgw"][ok]
+    win = fwd["winner_slot"]
+    ex_k = np.zeros((T, K))
+    b_k = np.zeros((T, K))
+    for t in range(T):
+        for k in range(K):
+            e = idx_np[t, k]
+            if e >= 0 and win[t, e] == k:
+                ex_k[t, k], b_k[t, k] = exact[t, e], bound[t, e]
+    gp = dp.cpu().numpy().astype(np.float64)
+    check_within(gp, ex_k, b_k, "grad_topk_probs")
+    rel(gp, ex_k, "grad_topk_probs")
 
 
 def test_opcheck_every_operator(moe):
