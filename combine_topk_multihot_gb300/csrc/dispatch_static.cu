@@ -13,8 +13,9 @@
 // the library is loaded holds its 1 MiB (+ 256 bytes) from load until the
 // process exits.
 // Host code only knows the symbol, not its device address, so the address is
-// looked up once per device with cudaGetSymbolAddress and handed to the
-// kernels through the layout's workspace pointer.
+// looked up with cudaGetSymbolAddress on the first call for each device (and
+// again after a device reset, which loads the module into a new context) and
+// handed to the kernels through the layout's workspace pointer.
 
 #include <cstdio>
 #include <mutex>
@@ -33,11 +34,43 @@ static __device__ __align__(256) int g_dispatch_scratch[STATIC_SCRATCH_INTS + 64
 
 constexpr int MAX_DEVICES = 64;
 std::mutex g_scratch_mu;
-int* g_scratch_ptr[MAX_DEVICES];  // device address of g_dispatch_scratch, per device
+// Device address of g_dispatch_scratch per device, and the unique id of the
+// context it was looked up in: after a device reset the module is loaded
+// again into a new context and the old address is stale.
+int* g_scratch_ptr[MAX_DEVICES];
+unsigned long long g_scratch_ctx[MAX_DEVICES];
 
-// Device address of the static scratch on the current device; looked up on
-// the first call for that device.
-moe_status static_scratch(int** out) {
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (driver entry points
+// reached through the runtime, so the library does not link libcuda);
+// false when there is none yet or the driver does not say.
+bool current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static bool looked_up = false;
+  if (!looked_up) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+    looked_up = true;
+  }
+  CUcontext ctx = nullptr;
+  return get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx != nullptr &&
+         get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the static scratch on the current device.  It is looked
+// up on the first call for the device, and again after the device's context
+// has changed (a device reset).  The lookup can load the library's module, so
+// it is refused while `stream` is being captured.
+moe_status static_scratch(cudaStream_t stream, int** out) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) {
@@ -48,19 +81,33 @@ moe_status static_scratch(int** out) {
   if (dev < 0 || dev >= MAX_DEVICES)
     return set_last_error(MOE_ERR_DEVICE, "moe_dispatch_static_scratch: device ordinal out of range");
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    err = cudaGetSymbolAddress(&p, g_dispatch_scratch);
-    if (err != cudaSuccess || p == nullptr) {
-      char msg[200];
-      snprintf(msg, sizeof(msg),
-               "moe_dispatch_static_scratch: cudaGetSymbolAddress of the static scratch failed: %s",
-               cudaGetErrorString(err));
-      return set_last_error(MOE_ERR_CUDA, msg);
-    }
-    g_scratch_ptr[dev] = static_cast<int*>(p);
+  unsigned long long ctx = 0;
+  const bool known_ctx = current_context_id(&ctx);
+  if (g_scratch_ptr[dev] && known_ctx && ctx == g_scratch_ctx[dev]) {
+    *out = g_scratch_ptr[dev];
+    return MOE_OK;
   }
-  *out = g_scratch_ptr[dev];
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  err = cudaStreamIsCapturing(stream, &cap);
+  if (err != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+    return set_last_error(MOE_ERR_INVALID_ARG,
+                          "moe_dispatch_static_scratch: the first call on a device (and the first "
+                          "after a device reset) looks up the static scratch's address and must not "
+                          "be made while its stream is being captured");
+  void* p = nullptr;
+  err = cudaGetSymbolAddress(&p, g_dispatch_scratch);
+  if (err != cudaSuccess || p == nullptr) {
+    char msg[200];
+    snprintf(msg, sizeof(msg),
+             "moe_dispatch_static_scratch: cudaGetSymbolAddress of the static scratch failed: %s",
+             cudaGetErrorString(err));
+    return set_last_error(MOE_ERR_CUDA, msg);
+  }
+  // Cache the address only when the context is known, so a reset is seen.
+  unsigned long long now = 0;
+  g_scratch_ptr[dev] = current_context_id(&now) ? static_cast<int*>(p) : nullptr;
+  g_scratch_ctx[dev] = now;
+  *out = static_cast<int*>(p);
   return MOE_OK;
 }
 
@@ -78,7 +125,9 @@ extern "C" moe_status moe_dispatch_static_scratch(const moe_bf16* x, const uint8
   if (L->T < 0 || L->E < 1)
     return set_last_error(MOE_ERR_INVALID_ARG, "moe_dispatch_static_scratch: bad T or E");
   const long long needed = layout_chunks(L->T) * static_cast<long long>(L->E);
-  if (needed > STATIC_SCRATCH_INTS) {
+  size_t ws_bytes = 0;
+  if (moe_layout_workspace_bytes(L->T, L->E, &ws_bytes) != MOE_OK || needed > STATIC_SCRATCH_INTS ||
+      ws_bytes > sizeof(g_dispatch_scratch)) {
     char msg[256];
     snprintf(msg, sizeof(msg),
              "moe_dispatch_static_scratch: E * ceil(T/32) = %lld counters exceeds the static "
@@ -87,7 +136,7 @@ extern "C" moe_status moe_dispatch_static_scratch(const moe_bf16* x, const uint8
     return set_last_error(MOE_ERR_UNSUPPORTED_SHAPE, msg);
   }
   int* scratch = nullptr;
-  moe_status st = static_scratch(&scratch);
+  moe_status st = static_scratch(stream, &scratch);
   if (st != MOE_OK) return st;
   // Same call as moe_dispatch; only the scratch differs.  Every counter the
   // kernels read is written earlier in the same call (the barrier counter is

@@ -255,12 +255,17 @@ MOE_API moe_status moe_quantize_fp8(const moe_bf16* src, int64_t rows, int32_t c
  *     T <= 65536); larger sizes return MOE_ERR_UNSUPPORTED_SHAPE before any
  *     work is queued.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *     (cudaGetSymbolAddress), and so does the first call after a device
+ *     reset.  Make that call before any stream capture: made while `stream`
+ *     is being captured it returns MOE_ERR_INVALID_ARG and queues nothing.
  *   - All calls share the one array and it keeps the last call's contents
  *     (every counter a call reads is written earlier in that call, so nothing
- *     needs clearing).  Calls whose work overlaps on the GPU -- on different
- *     streams, or from different host threads without ordering -- race on it
- *     and must be serialised by the caller.
+ *     needs clearing).  A call uses the array until its work on `stream` has
+ *     completed -- a host-synced call too, which returns once the row counts
+ *     are known, while its kernels may still be reading the array.  Calls
+ *     whose work overlaps on the GPU -- on different streams, or from
+ *     different host threads -- race on it: order each call after the
+ *     previous call's stream work (one shared stream, or an event).
  *   - No device memory is allocated or freed.
  */
 #define MOE_STATIC_SCRATCH_INTS 262144

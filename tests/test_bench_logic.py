@@ -62,3 +62,19 @@ def test_experts_bytes_agree_with_profiled_traffic():
     measured = bench.PROFILED_TRAFFIC["qwen3_30b_a3b"]["bytes"]
     assert abs(a["experts_bytes"] - measured) / measured < 0.03
     assert a["experts_flops"] == 6.0 * N * cfg.H * cfg.I
+
+
+@pytest.mark.parametrize("n", [1, 3, 5, 7, 20, 41])
+def test_timing_windows_cover_every_step_once(n):
+    b = bench.window_bounds(n)
+    assert b[0][0] == 0 and b[-1][1] == n
+    assert all(x[1] == y[0] for x, y in zip(b, b[1:]))
+    assert len(b) == min(5, n) and all(e > s for s, e in b)
+    sizes = [e - s for s, e in b]
+    assert max(sizes) - min(sizes) <= 1
+
+
+def test_window_summary_takes_the_median_window():
+    w = bench.window_summary([4.0, 4.4, 8.0, 4.2, 4.0], [4, 4, 4, 4, 4])
+    assert w["median_ms_per_step"] == 1.05
+    assert abs(w["spread"] - (2.0 - 1.0) / 1.05) < 1e-12

@@ -9,9 +9,20 @@ leftover counters) give exactly what moe_dispatch gives with its own
 caller-provided workspace: the layout and the dispatched rows are integer /
 bit-copy results, so the tolerance is bit-exactness.
 
+The sizes cover both kinds of layout launch: the cooperative one with grid
+barriers (T = 1000, 333) and the barrier-free one of decode-sized layers,
+with the row pass in the same kernel (T = 1) and without it (T = 200).  The
+first call on a device, which looks up the array's address, is refused while
+its stream is being captured; that is checked in a fresh process, where the
+lookup has not happened yet.
+
 This file is collected last on purpose and must also pass on its own.
 """
 import ctypes
+import os
+import subprocess
+import sys
+import textwrap
 
 import numpy as np
 import pytest
@@ -43,12 +54,15 @@ def _layout_tensors(L):
                                                "row_expert", "row_weight", "token_row")}
 
 
+@pytest.mark.parametrize("cases,P", [
+    ([(1000, 11), (333, 12)], 16),     # cooperative layout, grid barriers
+    ([(1, 13), (200, 14)], 1),         # barrier-free layout: with its row pass, then without
+])
 @pytest.mark.parametrize("host_sync", [True, False])
-def test_static_scratch_dispatch_matches_dispatch_twice(moe, host_sync):
+def test_static_scratch_dispatch_matches_dispatch_twice(moe, host_sync, cases, P):
     N = moe._native
-    E, K, P, H = 64, 4, 16, 256
-    cases = [(1000, 11), (333, 12)]      # two calls in a row, different sizes and routings
-    for T, seed in cases:
+    E, K, H = 64, 4, 256
+    for T, seed in cases:                # two calls in a row, different sizes and routings
         idx, p = _routing(T, E, K, seed)
         x = torch.randn(T, H, generator=torch.Generator().manual_seed(seed)).to(torch.bfloat16).to(DEV)
         C = moe.worst_case_rows(T, E, K, P)
@@ -94,3 +108,53 @@ def test_static_scratch_rejects_sizes_beyond_its_limit(moe):
     L = N.MoeLayout(32 * (N.MOE_STATIC_SCRATCH_INTS // E), E, 8, 1, 8)
     st = N.lib.moe_dispatch_static_scratch(None, None, None, 2048, ctypes.byref(L), None, None, None)
     assert st == N.MOE_ERR_INVALID_ARG
+
+
+_CAPTURE_CHILD = textwrap.dedent("""
+    import ctypes, sys
+    import torch
+    sys.path.insert(0, sys.argv[1])
+    import combine_topk_multihot_gb300 as m
+    N = m._native
+    assert N.lib.moe_device_check() == 0
+    T, E, K, P, H = 64, 8, 2, 1, 256
+    g = torch.Generator().manual_seed(3)
+    idx = torch.stack([torch.randperm(E, generator=g)[:K] for _ in range(T)]).cuda()
+    p = torch.rand(T, K, generator=g).cuda()
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rmap, probs, _ = m.moe_route_to_multihot(idx, p, E, status)
+    C = m.worst_case_rows(T, E, K, P)
+    lay = m.Layout(T, E, K, P, C, device="cuda", status=status)
+    lay.c.workspace = None
+    x_disp = torch.zeros(C, H, dtype=torch.bfloat16, device="cuda")
+    args = lambda s: (ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(rmap.data_ptr()),
+                      ctypes.c_void_p(probs.data_ptr()), H, ctypes.byref(lay.c),
+                      ctypes.c_void_p(x_disp.data_ptr()), None, ctypes.c_void_p(s.cuda_stream))
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        st = N.lib.moe_dispatch_static_scratch(*args(s))
+    assert st == N.MOE_ERR_INVALID_ARG, st
+    assert b"captured" in N.lib.moe_last_error()
+    # outside the capture the first call goes through and equals moe_dispatch
+    st = N.lib.moe_dispatch_static_scratch(*args(torch.cuda.current_stream()))
+    assert st == N.MOE_OK, N.last_error()
+    ref_layout = m.Layout(T, E, K, P, C, device="cuda", status=status)
+    ref_x, _ = m.moe_dispatch(x, rmap, probs, ref_layout, host_sync=False)
+    torch.cuda.synchronize()
+    assert torch.equal(x_disp.view(torch.int16), ref_x.view(torch.int16))
+    assert torch.equal(lay.row_token, ref_layout.row_token)
+    print("ok")
+""")
+
+
+def test_first_call_under_capture_is_refused(moe):
+    """In a fresh process, the first call on the device made inside a stream
+    capture returns MOE_ERR_INVALID_ARG and queues nothing; the next call,
+    outside the capture, looks the address up and matches moe_dispatch."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _CAPTURE_CHILD, root], capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
