@@ -176,18 +176,30 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- algorithmic work
 
 def step_launches(T: int, H: int, E: int, C: int, fp8: bool, gather: bool, backward: bool) -> int:
-    """Our kernel launches in one step (the layout's counter memset is a driver
-    memset, not one of ours): the multihot kernel; the layout kernel and the row
-    copy; the two expert kernels; the combine; and with the backward the combine
-    backward, the five expert-backward kernels, the dispatch backward and the
-    multihot backward.  A layer of at most two 32-token chunks, whose one-CTA
-    layout fits 48 KiB of shared memory and whose row pass has at most 64 items
-    (tokens + rows) and 256 KiB, lays out and copies in one kernel (bf16 only)."""
+    """Our kernel launches in one step (the dispatch's barrier-counter memset is
+    a driver memset, not one of ours), then the two expert kernels and the
+    combine, and with the backward the combine backward, the five
+    expert-backward kernels, the dispatch backward and the multihot backward.
+    The dispatch of a layer of more than 8 chunks of 32 tokens is one
+    cooperative kernel, which in the bf16 step also does the multihot step; the
+    --gather step runs the multihot kernel and that kernel without rows, the
+    FP8 step the multihot, layout and FP8 row kernels.  Smaller layers run the
+    multihot kernel, the barrier-free layout kernel and the row copy, except
+    that a layer of at most two chunks, whose one-CTA layout fits 48 KiB of
+    shared memory and whose row pass has at most 64 items (tokens + rows) and
+    256 KiB, lays out and copies in one kernel (bf16 only)."""
     chunks = -(-T // 32)
-    single_smem = 32 * E + 32 * (-(-E // 32)) * 4 + (2 * E + 1) * 4 + chunks * E * 4
-    single_rows = (not fp8 and chunks <= 2 and single_smem <= 48 * 1024 and T + C <= 64
-                   and (0 if gather else (T + C) * H * 2) <= 256 * 1024)
-    n = 1 + (1 if single_rows else 2) + 2 + 1
+    fused_smem = (4 * E + 2) * 4 + 8 * 128 * 4
+    if chunks > 8 and fused_smem <= 48 * 1024 and not fp8:
+        n = 1 if not gather else 2
+    elif chunks > 8:
+        n = 3
+    else:
+        single_smem = 32 * E + 32 * (-(-E // 32)) * 4 + (2 * E + 1) * 4 + chunks * E * 4
+        single_rows = (not fp8 and chunks <= 2 and single_smem <= 48 * 1024 and T + C <= 64
+                       and (0 if gather else (T + C) * H * 2) <= 256 * 1024)
+        n = 1 + (1 if single_rows else 2)
+    n += 2 + 1
     if backward:
         n += 1 + 5 + 1 + 1
     return n
@@ -213,17 +225,21 @@ def window_summary(win_ms, win_steps):
 
 
 def algorithmic(cfg, counts: np.ndarray, R: int, N: int, C: int, backward: bool, fp8: bool = False,
-                gather: bool = False):
+                gather: bool = False, fused_multihot: bool = False):
     """Bytes / flops the layer's steps must move, per call: what each step has to
     read and write at the least, and the experts' 2 flops per multiply-add.
     With fp8 the dispatched rows and W1 are e4m3 (1 byte) with fp32 per-row scales.
-    With gather no rows are dispatched: the gate/up GEMM reads the tokens x once."""
+    With gather no rows are dispatched: the gate/up GEMM reads the tokens x once.
+    With fused_multihot the dispatch call also does the multihot step (reads
+    the top-k choices, writes the multihot rows) and its bytes count there."""
     T, H, E, K, I = cfg.T, cfg.H, cfg.E, cfg.K, cfg.I
     active = int((counts > 0).sum())
     meta_disp = T * E * 1 + 4 * N + 12 * C + 4 * T * K + 8 * (E + 1)
     row_b = 1 if fp8 else 2
     disp = (meta_disp if gather else
             T * H * 2 + C * H * row_b + meta_disp + (4 * C if fp8 else 0))
+    if fused_multihot:
+        disp += T * K * 12 + T * E * 6
     comb = N * H * 2 + T * H * 2 + 4 * T * K
     w_bytes = active * (2 * I * H * row_b + H * I * 2) + (active * 2 * I * 4 if fp8 else 0)
     ex_bytes = w_bytes + (T * H * 2 if gather else N * H * row_b) + 2 * N * I * 2 + N * H * 2
@@ -299,6 +315,10 @@ def run_ours(args, world, rank, local, leg: bool = False):
         x_q = (torch.empty(C, H, dtype=torch.uint8, device=dev), torch.empty(C, dtype=torch.float32, device=dev))
     stream = torch.cuda.current_stream()
     ev = lambda: torch.cuda.Event(enable_timing=True)
+    # the bf16 path calls moe_dispatch_topk: the multihot step and the dispatch in one call
+    fused_topk = not (fp8 or gather)
+    mh = (torch.empty(T, E, dtype=torch.uint8, device=dev), torch.empty(T, E, dtype=torch.float32, device=dev),
+          torch.empty(T, E, dtype=torch.int8, device=dev))
     bwd = cfg.backward
     stages = ["multihot", "dispatch", "experts", "combine"]
     launches_per_step = step_launches(T, H, E, C, fp8, gather, bwd)
@@ -313,9 +333,19 @@ def run_ours(args, world, rank, local, leg: bool = False):
         rec = (lambda j: events[j].record(stream)) if events else (lambda j: None)
         o_buf = out if out_buf is None else out_buf
         rec(0)
-        rmap, probs, win = moe.moe_route_to_multihot(L["topk_idx"], L["topk_probs"], E, lay.status)
-        rec(1)
-        if fp8:
+        if fused_topk:  # the multihot step runs inside the dispatch call
+            rec(1)
+            _, (rmap, probs, win), _ = moe.moe_dispatch_topk(L["x"], L["topk_idx"], L["topk_probs"], lay,
+                                                             host_sync=host_sync, x_disp=x_disp, multihot=mh)
+            rec(2)
+            moe.moe_grouped_experts(x_disp, lay, L["W1"], L["W2"], out=bufs, save_o=bwd, save_gu=bwd)
+            rec(3)
+        else:
+            rmap, probs, win = moe.moe_route_to_multihot(L["topk_idx"], L["topk_probs"], E, lay.status)
+            rec(1)
+        if fused_topk:
+            pass
+        elif fp8:
             moe.moe_dispatch_fp8(L["x"], rmap, probs, lay, host_sync=host_sync, out=x_q)
             rec(2)
             moe.moe_grouped_experts_fp8(x_q[0], x_q[1], lay, L["W1q"], L["W1s"], L["W2"], out=bufs)
@@ -427,10 +457,14 @@ def run_ours(args, world, rank, local, leg: bool = False):
         sf_ev = []
         for i in range(args.warmup + args.steps):
             L = layers[i % n_layers]
-            rmap, probs, _ = moe.moe_route_to_multihot(L["topk_idx"], L["topk_probs"], E, lay_sf.status)
+            if not fused_topk:
+                rmap, probs, _ = moe.moe_route_to_multihot(L["topk_idx"], L["topk_probs"], E, lay_sf.status)
             a, b = ev(), ev()
             a.record(stream)
-            if fp8:
+            if fused_topk:
+                moe.moe_dispatch_topk(L["x"], L["topk_idx"], L["topk_probs"], lay_sf, host_sync=False,
+                                      x_disp=xd_sf, multihot=mh)
+            elif fp8:
                 moe.moe_dispatch_fp8(L["x"], rmap, probs, lay_sf, host_sync=False, out=xq_sf)
             elif gather:
                 moe.moe_dispatch_layout(rmap, probs, lay_sf, host_sync=False)
@@ -544,7 +578,8 @@ def run_ours(args, world, rank, local, leg: bool = False):
 
     # ---- roofline of the dominant step (the experts' two grouped GEMM launches)
     hbm, bf16_burst, bf16_sust, src = peaks()
-    work = [algorithmic(cfg, L["counts"], r[0], r[1], C, cfg.backward, fp8, gather) for L, r in zip(layers, rows)]
+    work = [algorithmic(cfg, L["counts"], r[0], r[1], C, cfg.backward, fp8, gather, fused_topk)
+            for L, r in zip(layers, rows)]
     mean = lambda key: float(np.mean([w[key] for w in work]))
     # per-step averages over the timed steps (layer i % n_layers)
     steps_w = [work[i % n_layers] for i in range(args.steps)]
@@ -591,7 +626,8 @@ def run_ours(args, world, rank, local, leg: bool = False):
     }
     kernels["dispatch_frac_hbm"] = kernels["dispatch_GBs"] / hbm
     if sf_us is not None:
-        sf_bytes = float(np.mean([algorithmic(cfg, w_l["counts"], r[0], r[1], worst, False, fp8, gather)["dispatch_bytes"]
+        sf_bytes = float(np.mean([algorithmic(cfg, w_l["counts"], r[0], r[1], worst, False, fp8, gather,
+                                              fused_topk)["dispatch_bytes"]
                                   for w_l, r in zip(layers, rows)]))
         kernels["dispatch_sync_free_us"] = float(np.mean(sf_us))
         kernels["dispatch_sync_free_GBs"] = sf_bytes / (kernels["dispatch_sync_free_us"] * 1e-6) / 1e9
@@ -600,6 +636,7 @@ def run_ours(args, world, rank, local, leg: bool = False):
     kernels["experts_frac_bf16_burst"] = kernels["experts_TFLOPs"] / bf16_burst
     kernels["experts_frac_bf16_sustained"] = kernels["experts_TFLOPs"] / bf16_sust
     kernels["multihot_dispatch_us"] = kernels["multihot_us"] + kernels["dispatch_us"]
+    kernels["dispatch_includes_multihot"] = fused_topk
 
     tokens = T * world * args.steps
     e2e = None

@@ -176,7 +176,8 @@ int64_t moe_worst_case_rows(int32_t T, int32_t E, int32_t K, int32_t pad_multipl
 moe_status moe_layout_workspace_bytes(int32_t T, int32_t E, size_t* bytes) {
   MOE_REQUIRE(bytes != nullptr, MOE_ERR_INVALID_ARG, "bytes is NULL");
   MOE_REQUIRE(T >= 0 && E >= 1, MOE_ERR_INVALID_ARG, "bad T/E");
-  *bytes = layout_counter_bytes(T, E) + 256;  // the counters, then the grid barrier's counter
+  // the per-chunk masks, each chunk's start, then the grid barrier's counter
+  *bytes = 2 * layout_counter_bytes(T, E) + 256;
   return MOE_OK;
 }
 
@@ -201,16 +202,23 @@ namespace {
 
 // moe_dispatch and moe_dispatch_fp8: the layout (host-synced or sync-free),
 // then the rows, in bf16 (x_disp) or as e4m3 codes with per-row scales.
+// With topk_idx non-NULL the input is the top-k choices, and routing_map /
+// probs / winner are outputs (the multihot step fused into the dispatch).
 moe_status dispatch_impl(const char* who, const moe_bf16* x, const uint8_t* routing_map,
                          const float* probs, int32_t H, const moe_layout* L, moe_bf16* x_disp,
                          uint8_t* x_q, float* x_scale, int64_t* rows_host, moe_stream_t stream,
-                         bool layout_only = false) {
+                         bool layout_only = false, const int64_t* topk_idx = nullptr,
+                         const float* topk_probs = nullptr, int8_t* winner = nullptr) {
   moe_status st = check_layout(L);
   if (st != MOE_OK) return st;
   if (layout_only) H = 256;  // no rows are copied; any valid hidden size will do
   if ((st = check_hidden(H)) != MOE_OK) return st;
   MOE_REQUIRE(L->T == 0 || ((x || layout_only) && routing_map && probs), MOE_ERR_INVALID_ARG,
               "%s: NULL input", who);
+  MOE_REQUIRE(!topk_idx || L->T == 0 || (topk_probs && winner), MOE_ERR_INVALID_ARG,
+              "%s: NULL top-k input or multihot output", who);
+  MOE_REQUIRE(aligned16(probs) && aligned16(winner), MOE_ERR_INVALID_ARG,
+              "%s: probs and winner_slot must be 16-byte aligned", who);
   MOE_REQUIRE(L->capacity == 0 || layout_only || x_disp || (x_q && x_scale), MOE_ERR_INVALID_ARG,
               "%s: NULL output rows", who);
   MOE_REQUIRE(aligned16(x) && aligned16(x_disp) && aligned16(x_q) && aligned16(routing_map),
@@ -245,10 +253,32 @@ moe_status dispatch_impl(const char* who, const moe_bf16* x, const uint8_t* rout
   cudaError_t err;
   bool rows_done = false;  // the layout kernel did the row pass itself
   const bool bf16_rows = x_disp || layout_only;
-  if ((err = launch_layout(routing_map, probs, *L, L->workspace, stream, mapped ? rb_dev : nullptr,
-                           reinterpret_cast<const uint16_t*>(x), reinterpret_cast<uint16_t*>(x_disp), H,
-                           bf16_rows ? &rows_done : nullptr)) != cudaSuccess)
+  const bool fused = bf16_rows && dispatch_fused_fits(*L);
+  const uint16_t* x16 = reinterpret_cast<const uint16_t*>(x);
+  uint16_t* xd16 = reinterpret_cast<uint16_t*>(x_disp);
+  int* rb_kernel = mapped ? rb_dev : nullptr;
+  if (topk_idx && !fused) {
+    // small layers and the FP8 rows: the multihot step first, then the layout from its map
+    if ((err = launch_multihot(topk_idx, topk_probs, L->T, L->K, L->E, const_cast<uint8_t*>(routing_map),
+                               const_cast<float*>(probs), winner, L->status, stream)) != cudaSuccess) {
+      if (mapped) rb_lock.unlock();
+      return cuda_fail(err, "dispatch: multihot");
+    }
+  }
+  if (fused) {
+    err = topk_idx ? launch_dispatch_fused_topk(topk_idx, topk_probs, const_cast<uint8_t*>(routing_map),
+                                                const_cast<float*>(probs), winner, *L, H, x16, xd16, rb_kernel,
+                                                stream)
+                   : launch_dispatch_fused_map(routing_map, probs, *L, H, x16, xd16, rb_kernel, stream);
+    if (err != cudaSuccess) {
+      if (mapped) cudaStreamSynchronize(stream);  // the kernel may still write the readback buffer
+      return cuda_fail(err, "dispatch: fused layout and rows");
+    }
+    rows_done = true;
+  } else if ((err = launch_layout(routing_map, probs, *L, L->workspace, stream, rb_kernel, x16, xd16, H,
+                                  bf16_rows ? &rows_done : nullptr)) != cudaSuccess) {
     return cuda_fail(err, "dispatch: layout");
+  }
   if (!rows_done) {
     err = bf16_rows ? launch_row_gather(x, *L, H, x_disp, true, nullptr, nullptr, stream)
                     : launch_row_gather_fp8(x, *L, H, x_q, x_scale, stream);
@@ -322,6 +352,20 @@ moe_status moe_dispatch(const moe_bf16* x, const uint8_t* routing_map, const flo
               "moe_dispatch: NULL x_disp");
   return dispatch_impl("moe_dispatch", x, routing_map, probs, H, L, x_disp, nullptr, nullptr,
                        rows_host, stream);
+}
+
+moe_status moe_dispatch_topk(const moe_bf16* x, const int64_t* topk_idx, const float* topk_probs,
+                             int32_t H, const moe_layout* L, uint8_t* routing_map, float* probs,
+                             int8_t* winner_slot, moe_bf16* x_disp, int64_t* rows_host,
+                             moe_stream_t stream) {
+  MOE_REQUIRE(L == nullptr || L->capacity == 0 || x_disp, MOE_ERR_INVALID_ARG,
+              "moe_dispatch_topk: NULL x_disp");
+  MOE_REQUIRE(L == nullptr || L->T == 0 || (topk_idx && topk_probs), MOE_ERR_INVALID_ARG,
+              "moe_dispatch_topk: NULL top-k input");
+  static const int64_t no_slots = 0;  // T == 0: marks the top-k input without reading it
+  return dispatch_impl("moe_dispatch_topk", x, routing_map, probs, H, L, x_disp, nullptr, nullptr,
+                       rows_host, stream, false, topk_idx ? topk_idx : &no_slots, topk_probs,
+                       winner_slot);
 }
 
 moe_status moe_dispatch_fp8(const moe_bf16* x, const uint8_t* routing_map, const float* probs,

@@ -1,8 +1,9 @@
 // moe_dispatch_static_scratch: moe_dispatch for callers that cannot allocate
 // device memory.
 //
-// moe_dispatch needs a small scratch buffer for its per-chunk expert counters
-// (moe_layout.workspace, E * ceil(T/32) int32, plus a grid-barrier counter).  Some callers have no way to
+// moe_dispatch needs a small scratch buffer for its per-chunk expert masks and
+// start rows (moe_layout.workspace, 2 * E * ceil(T/32) int32, plus a
+// grid-barrier counter).  Some callers have no way to
 // get one: a plugin inside an inference engine that owns every byte of the
 // device pool and hands a layer only its declared inputs and outputs, or a
 // serving loop that must never call cudaMalloc because it can synchronise the
@@ -10,7 +11,7 @@
 // fixed array that lives in the library's own device memory instead.
 //
 // The array below is a file-scope __device__ variable: every GPU on which
-// the library is loaded holds its 1 MiB (+ 256 bytes) from load until the
+// the library is loaded holds its 2 MiB (+ 256 bytes) from load until the
 // process exits.
 // Host code only knows the symbol, not its device address, so the address is
 // looked up with cudaGetSymbolAddress on the first call for each device (and
@@ -27,10 +28,11 @@ namespace moe {
 
 namespace {
 
-constexpr long long STATIC_SCRATCH_INTS = MOE_STATIC_SCRATCH_INTS;  // 1 MiB of int32 counters
+constexpr long long STATIC_SCRATCH_INTS = MOE_STATIC_SCRATCH_INTS;  // (expert, chunk) pairs
 
-// The counters, then 256 bytes for the layout kernel's grid-barrier counter.
-static __device__ __align__(256) int g_dispatch_scratch[STATIC_SCRATCH_INTS + 64];
+// Per (expert, chunk) pair a token mask and a start row (2 MiB), then 256
+// bytes for the dispatch kernel's grid-barrier counter.
+static __device__ __align__(256) int g_dispatch_scratch[2 * STATIC_SCRATCH_INTS + 64];
 
 constexpr int MAX_DEVICES = 64;
 std::mutex g_scratch_mu;
@@ -130,8 +132,8 @@ extern "C" moe_status moe_dispatch_static_scratch(const moe_bf16* x, const uint8
       ws_bytes > sizeof(g_dispatch_scratch)) {
     char msg[256];
     snprintf(msg, sizeof(msg),
-             "moe_dispatch_static_scratch: E * ceil(T/32) = %lld counters exceeds the static "
-             "scratch of %lld (T=%d, E=%d); use moe_dispatch with a caller-provided workspace",
+             "moe_dispatch_static_scratch: E * ceil(T/32) = %lld (expert, chunk) pairs exceeds the "
+             "static scratch's %lld (T=%d, E=%d); use moe_dispatch with a caller-provided workspace",
              needed, STATIC_SCRATCH_INTS, L->T, L->E);
     return set_last_error(MOE_ERR_UNSUPPORTED_SHAPE, msg);
   }

@@ -97,6 +97,20 @@ cudaError_t launch_layout(const uint8_t* routing_map, const float* probs, const 
                           void* workspace, cudaStream_t s, int* readback = nullptr,
                           const uint16_t* x = nullptr, uint16_t* x_disp = nullptr, int H = 0,
                           bool* rows_done = nullptr);
+// a1-a4 in one cooperative launch for layers of more than 8 chunks: counts,
+// offsets, placement, the pad and spare rows, and (x_disp non-NULL) the row
+// copies.  Input the multihot map (_map) or the top-k choices (_topk, which
+// also writes routing_map / probs / winner).  workspace: L.workspace, which
+// holds 2 * layout_counter_bytes(T, E) + 256 bytes.  readback as in
+// launch_layout.
+bool dispatch_fused_fits(const moe_layout& L);
+cudaError_t launch_dispatch_fused_map(const uint8_t* routing_map, const float* probs, const moe_layout& L,
+                                      int H, const uint16_t* x, uint16_t* x_disp, int* readback,
+                                      cudaStream_t s);
+cudaError_t launch_dispatch_fused_topk(const int64_t* topk_idx, const float* topk_probs,
+                                       uint8_t* routing_map, float* probs, int8_t* winner,
+                                       const moe_layout& L, int H, const uint16_t* x, uint16_t* x_disp,
+                                       int* readback, cudaStream_t s);
 // Rows of the expanded layout from token rows (a4: x -> x_disp, plus the pad /
 // spare rows' metadata when from_offsets); also the combine backward (a7)
 // with the optional routing-weight gradient (a8).  Each token row is read

@@ -23,73 +23,12 @@
 // known, and places nothing when the rows do not fit.
 
 #include "common.cuh"
+#include "coop.cuh"
 #include "launch.h"
 
 namespace moe {
 
 namespace {
-
-__device__ __forceinline__ int warp_inclusive_scan(int v, int lane) {
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(FULL_MASK, v, o);
-    if (lane >= o) v += n;
-  }
-  return v;
-}
-
-// Block-wide exclusive scan of one value per thread (blockDim.x a multiple of
-// 32, at most 1024); returns the exclusive prefix and writes the block total.
-__device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  const int incl = warp_inclusive_scan(v, lane);
-  if (lane == 31) s_warp[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const int w = lane < nwarps ? s_warp[lane] : 0;
-    const int wi = warp_inclusive_scan(w, lane);
-    s_warp[lane] = wi - w;
-    if (lane == 31) s_warp[32] = wi;
-  }
-  __syncthreads();
-  const int excl = incl - v + s_warp[warp];
-  *total = s_warp[32];
-  return excl;
-}
-
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Grid-wide barrier of a cooperative launch (every CTA is resident).  The
-// counter is zeroed before the launch and each CTA adds one per barrier, so
-// barrier n is passed once it reads n * gridDim.x.  The wait is bounded: after
-// WAIT_LIMIT_NS it reports MOE_DEVERR_TIMEOUT and returns false, and the
-// caller's CTA stops.  Data written before the barrier by other CTAs is read
-// after it with ld.global.cg (L2), never through this SM's L1.
-__device__ bool grid_barrier(unsigned* ctr, unsigned target, int* status, int* s_ok) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(ctr, 1u);
-    int ok = 1;
-    const unsigned long long t0 = global_timer_ns();
-    while (ld_acquire_gpu(ctr) < target) {
-      if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
-        report(status, MOE_DEVERR_TIMEOUT);
-        ok = 0;
-        break;
-      }
-      __nanosleep(64);
-    }
-    __threadfence();
-    *s_ok = ok;
-  }
-  __syncthreads();
-  return *s_ok != 0;
-}
 
 // The single-CTA layout also does the dispatch's row pass when it has at most
 // this many items (tokens + rows) and moves at most this many bytes.

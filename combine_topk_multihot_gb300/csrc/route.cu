@@ -8,51 +8,12 @@
 // last slot's prob winning (slots are taken in order).
 
 #include "common.cuh"
+#include "coop.cuh"
 #include "launch.h"
 
 namespace moe {
 
 namespace {
-
-// Writes token t's multihot row (routing_map, probs, winner_slot) from its K
-// slots, held by the warp as slot k in lane k % 32, register k / 32 (-1 =
-// no expert).  Lane l owns experts [e0 + 4l, e0 + 4l + 4) of each 128-expert
-// stripe, so the warp writes 128 bytes of routing_map, 512 bytes of probs and
-// 128 bytes of winner_slot per stripe with 4/16/4-byte stores.  Slots are
-// visited in order, so a duplicated expert keeps the last slot's prob.
-__device__ __forceinline__ void write_multihot_row(long long t, const int (&ek)[4],
-                                                   const float (&pk)[4], int K, int E, int lane,
-                                                   uint8_t* __restrict__ routing_map,
-                                                   float* __restrict__ probs,
-                                                   int8_t* __restrict__ winner) {
-  for (int e0 = 0; e0 < E; e0 += 128) {
-    const int eb = e0 + 4 * lane;
-    uint32_t m = 0, w = 0xffffffffu;  // 4 bytes each; winner -1 = 0xff
-    float pr[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int k = 0; k < K; ++k) {
-      const int j = k >> 5;
-      const int src_e = j == 0 ? ek[0] : j == 1 ? ek[1] : j == 2 ? ek[2] : ek[3];
-      const float src_p = j == 0 ? pk[0] : j == 1 ? pk[1] : j == 2 ? pk[2] : pk[3];
-      const int e = __shfl_sync(FULL_MASK, src_e, k & 31);
-      const float p = __shfl_sync(FULL_MASK, src_p, k & 31);
-      const unsigned d = static_cast<unsigned>(e - eb);
-      if (e >= 0 && d < 4u) {
-        m |= 1u << (8 * d);
-        w = (w & ~(0xffu << (8 * d))) | (static_cast<uint32_t>(k) << (8 * d));
-        pr[0] = d == 0 ? p : pr[0];
-        pr[1] = d == 1 ? p : pr[1];
-        pr[2] = d == 2 ? p : pr[2];
-        pr[3] = d == 3 ? p : pr[3];
-      }
-    }
-    if (eb < E) {  // E % 4 == 0, so the 4 experts are all in range
-      const long long o = t * E + eb;
-      *reinterpret_cast<uint32_t*>(routing_map + o) = m;
-      *reinterpret_cast<uint32_t*>(winner + o) = w;
-      *reinterpret_cast<float4*>(probs + o) = make_float4(pr[0], pr[1], pr[2], pr[3]);
-    }
-  }
-}
 
 // One warp per token: the K slot indices are loaded by the lanes and the row
 // is written by write_multihot_row.

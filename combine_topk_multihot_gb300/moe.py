@@ -173,6 +173,29 @@ def moe_dispatch(x: torch.Tensor, routing_map: torch.Tensor, probs: torch.Tensor
     return x_disp, ((int(rows[0]), int(rows[1])) if host_sync else None)
 
 
+def moe_dispatch_topk(x: torch.Tensor, topk_idx: torch.Tensor, topk_probs: torch.Tensor, layout: Layout,
+                      host_sync: bool = True, x_disp: Optional[torch.Tensor] = None, multihot=None,
+                      stream=None):
+    """a1-a4 in one call: the multihot step and the dispatch from the top-k
+    choices.  Returns (x_disp [C, H], (routing_map, probs, winner_slot),
+    (R, N) or None); ``multihot`` optionally gives the three output buffers."""
+    _bf16(x, "x")
+    assert topk_idx.dtype == torch.int64 and topk_probs.dtype == torch.float32
+    T, H = x.shape
+    E = layout.E
+    dev = x.device
+    if x_disp is None:
+        x_disp = torch.empty(layout.capacity, H, dtype=torch.bfloat16, device=dev)
+    if multihot is None:
+        multihot = (torch.empty(T, E, dtype=torch.uint8, device=dev), torch.empty(T, E, dtype=torch.float32, device=dev),
+                    torch.empty(T, E, dtype=torch.int8, device=dev))
+    rows = (ctypes.c_int64 * 2)() if host_sync else None
+    _check(N.lib.moe_dispatch_topk(_ptr(x), _ptr(topk_idx), _ptr(topk_probs), H, layout.ref, _ptr(multihot[0]),
+                                   _ptr(multihot[1]), _ptr(multihot[2]), _ptr(x_disp), rows, _stream(stream)),
+           "moe_dispatch_topk")
+    return x_disp, tuple(multihot), ((int(rows[0]), int(rows[1])) if host_sync else None)
+
+
 def moe_dispatch_layout(routing_map: torch.Tensor, probs: torch.Tensor, layout: Layout,
                         host_sync: bool = True, stream=None):
     """a2-a3 alone (no rows copied): fills ``layout``; returns (R, N) or None."""

@@ -204,6 +204,27 @@ MOE_API moe_status moe_dispatch(const moe_bf16* x, const uint8_t* routing_map, c
                         int64_t* rows_host, moe_stream_t stream);
 
 /*
+ * a1-a4 in one call: moe_route_to_multihot followed by moe_dispatch, from the
+ * top-k choices.  [HEP] Changelog (top-k indices become multihot routing
+ * data) and the passages of moe_dispatch.
+ *   topk_idx, topk_probs: [T, K] int64 / fp32, as for moe_route_to_multihot
+ *                (an index outside [-1, E) sets MOE_DEVERR_BAD_INDEX and
+ *                counts as -1).
+ *   routing_map, probs, winner_slot: [T, E] (out, required, 16-byte
+ *                aligned): the multihot outputs of moe_route_to_multihot, for
+ *                the backward.
+ *   x, L, x_disp, rows_host, stream: as for moe_dispatch, with the same
+ *                modes, results and errors.
+ * Layers of more than 8 chunks of 32 tokens run all of it as one cooperative
+ * kernel (the multihot rows, counts, offsets, placement and row copies);
+ * smaller ones as the multihot kernel followed by moe_dispatch's kernels.
+ */
+MOE_API moe_status moe_dispatch_topk(const moe_bf16* x, const int64_t* topk_idx,
+                                     const float* topk_probs, int32_t H, const moe_layout* L,
+                                     uint8_t* routing_map, float* probs, int8_t* winner_slot,
+                                     moe_bf16* x_disp, int64_t* rows_host, moe_stream_t stream);
+
+/*
  * a2-a3 alone: the layout of moe_dispatch (counts, offsets, totals, row
  * metadata, with the pad and spare rows' sentinel metadata) without copying
  * any rows -- for moe_grouped_experts_gather, which reads the tokens itself.
@@ -247,10 +268,10 @@ MOE_API moe_status moe_quantize_fp8(const moe_bf16* src, int64_t rows, int32_t c
  * because it can synchronise the device.
  *
  * Arguments, results and errors are those of moe_dispatch, except that
- * L->workspace is ignored (it may be NULL): the per-chunk expert counters
- * live in a static device array inside the library, MOE_STATIC_SCRATCH_INTS
- * int32 (1 MiB, plus 256 bytes for a barrier counter) per GPU, held from
- * library load until the process exits.
+ * L->workspace is ignored (it may be NULL): the per-chunk expert masks and
+ * start rows live in a static device array inside the library,
+ * 2 * MOE_STATIC_SCRATCH_INTS int32 (2 MiB, plus 256 bytes for a barrier
+ * counter) per GPU, held from library load until the process exits.
  *   - Limit: E * ceil(T / 32) <= MOE_STATIC_SCRATCH_INTS (E = 128 allows
  *     T <= 65536); larger sizes return MOE_ERR_UNSUPPORTED_SHAPE before any
  *     work is queued.

@@ -22,13 +22,13 @@ def _launches(name, fp8=False, gather=False):
 
 @pytest.mark.parametrize("name,expected", [
     ("decode_1", 5),             # multihot, one-CTA layout with the rows, 2 expert kernels, combine
-    ("decode_256", 6),           # the layout and the row copy are separate
-    ("decode_1024", 6),
-    ("qwen3_30b_a3b", 6),
-    ("qwen3_30b_a3b_16k", 6),
-    ("skewed", 6),
+    ("decode_256", 6),           # 8 chunks: multihot, layout and row copy separate
+    ("decode_1024", 4),          # 32 chunks: one dispatch kernel (multihot to rows), experts, combine
+    ("qwen3_30b_a3b", 4),
+    ("qwen3_30b_a3b_16k", 4),
+    ("skewed", 4),
     ("tiny", 6),                 # 64 tokens and 248 rows: more than 64 items
-    ("h4096", 14),               # + combine backward, 5 expert-backward kernels, dispatch and multihot backward
+    ("h4096", 12),               # + combine backward, 5 expert-backward kernels, dispatch and multihot backward
 ])
 def test_launches_per_step(name, expected):
     assert _launches(name) == expected
@@ -36,6 +36,11 @@ def test_launches_per_step(name, expected):
 
 def test_fp8_dispatch_is_never_fused():
     assert _launches("decode_1", fp8=True) == 6
+    assert _launches("qwen3_30b_a3b", fp8=True) == 6      # multihot, layout, FP8 rows
+
+
+def test_gather_step_runs_the_multihot_kernel_and_the_layout():
+    assert _launches("qwen3_30b_a3b", gather=True) == 5
 
 
 @pytest.mark.parametrize("T,K,E,H,expected", [

@@ -130,6 +130,96 @@ def test_single_cta_row_pass(moe, T, E, K, P, drop, dup, layout_only):
         assert np.array_equal(bits(x_disp), O.dispatch(bits(x), Lr["row_token"]))
 
 
+LAYOUT_CASES = [
+    (1, 8, 2, 16, 0.0, 0.0),        # single token
+    (77, 12, 3, 5, 0.2, 0.2),       # ragged chunk tail, drops, duplicates
+    (256, 128, 8, 1, 0.05, 0.05),   # 8 chunks: the multihot kernel, then the barrier-free layout
+    (257, 128, 8, 16, 0.0, 0.0),    # 9 chunks: one cooperative kernel for all of it
+    (513, 32, 8, 128, 0.1, 0.1),    # several chunks, ragged tail, drops, duplicates
+    (700, 1024, 4, 1, 0.0, 0.0),    # the largest E (8 stripes of 128 experts per token row)
+    (300, 16, 16, 3, 0.1, 0.3),     # K = E, duplicates
+    (333, 64, 40, 2, 0.2, 0.2),     # K > 32: slots in two registers per lane
+    (4096, 128, 8, 128, 0.0, 0.0),  # the Qwen3-30B-A3B routing shape
+    (40000, 128, 8, 4, 0.05, 0.0),  # more chunks than resident CTAs
+    (0, 8, 2, 16, 0.0, 0.0),        # no tokens
+]
+
+
+@pytest.mark.parametrize("T,E,K,P,drop,dup", LAYOUT_CASES)
+@pytest.mark.parametrize("host_sync", [True, False])
+def test_dispatch_topk_matches_oracle(moe, T, E, K, P, drop, dup, host_sync):
+    """moe_dispatch_topk (the multihot step fused into the dispatch): the
+    multihot outputs, the layout and the rows bit for bit against the oracle,
+    with every row buffer poisoned first so each entry must be written."""
+    idx, p = random_routing(T, E, K, seed=T * 5 + E + K, drop=drop, dup=dup)
+    H = 512 if T < 5000 else 256
+    C = O.worst_case_capacity(T, E, K, P)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    L = moe.Layout(T, E, K, P, C, device=DEV, status=status)
+    L.row_token.fill_(12345)
+    L.row_expert.fill_(-7)
+    L.row_weight.fill_(float("nan"))
+    L.token_row.fill_(999)
+    x = torch.randn(T, H, generator=torch.Generator().manual_seed(T + 3)).to(torch.bfloat16)
+    x_disp = torch.full((C, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    mh = (torch.full((T, E), 7, dtype=torch.uint8, device=DEV),
+          torch.full((T, E), float("nan"), dtype=torch.float32, device=DEV),
+          torch.full((T, E), 5, dtype=torch.int8, device=DEV))
+    _, mh, rows = moe.moe_dispatch_topk(x.to(DEV), idx.to(DEV), p.to(DEV), L, host_sync=host_sync,
+                                        x_disp=x_disp, multihot=mh)
+    torch.cuda.synchronize()
+    g = dict(rmap=mh[0], probs=mh[1], win=mh[2], L=L, x=x, x_disp=x_disp, rows=rows, status=status)
+    _check_layout(g, idx, p, E, P, C)
+
+
+@pytest.mark.parametrize("T,E,K,P", [(257, 128, 8, 16), (3000, 64, 6, 32)])
+def test_fused_dispatch_writes_every_row(moe, T, E, K, P):
+    """moe_dispatch on layers of more than 8 chunks (the cooperative kernel
+    that places and copies in one launch), sync-free: poisoned row buffers
+    and rows, so every valid, pad and spare row must be written."""
+    idx, p = random_routing(T, E, K, seed=T + K, drop=0.1, dup=0.1)
+    H = 768
+    C = O.worst_case_capacity(T, E, K, P)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    rmap, probs, _ = moe.moe_route_to_multihot(idx.to(DEV), p.to(DEV), E, status)
+    L = moe.Layout(T, E, K, P, C, device=DEV, status=status)
+    L.row_token.fill_(12345)
+    L.row_expert.fill_(-7)
+    L.row_weight.fill_(float("nan"))
+    L.token_row.fill_(999)
+    x = torch.randn(T, H, generator=torch.Generator().manual_seed(T)).to(torch.bfloat16)
+    x_disp = torch.full((C, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    moe.moe_dispatch(x.to(DEV), rmap, probs, L, host_sync=False, x_disp=x_disp)
+    torch.cuda.synchronize()
+    g = dict(rmap=rmap, probs=probs, win=moe.moe_route_to_multihot(idx.to(DEV), p.to(DEV), E, status)[2],
+             L=L, x=x, x_disp=x_disp, rows=None, status=status)
+    _check_layout(g, idx, p, E, P, C)
+
+
+@pytest.mark.parametrize("T", [40, 600])
+def test_dispatch_topk_bad_index(moe, T):
+    E, K, P = 16, 2, 4
+    idx, p = random_routing(T, E, K, seed=T)
+    idx[5, 1] = E + 3
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    L = moe.Layout(T, E, K, P, O.worst_case_capacity(T, E, K, P), device=DEV, status=status)
+    x = torch.zeros(T, 256, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_dispatch_topk(x, idx.to(DEV), p.to(DEV), L, host_sync=True)
+    assert ei.value.code == moe._native.MOE_ERR_BAD_INDEX
+    # sync-free: the status bit, and the bad slot dropped as a -1 slot would be
+    status.zero_()
+    _, mh, _ = moe.moe_dispatch_topk(x, idx.to(DEV), p.to(DEV), L, host_sync=False)
+    torch.cuda.synchronize()
+    assert int(status.item()) & moe._native.MOE_DEVERR_BAD_INDEX
+    idx2 = idx.clone()
+    idx2[5, 1] = -1
+    rm, pr, _ = O.route_to_multihot(idx2.numpy(), p.numpy(), E)
+    assert np.array_equal(mh[0].cpu().numpy(), rm)
+    Lr = O.build_layout(rm, pr, K, P, L.capacity)
+    assert np.array_equal(L.row_token.cpu().numpy(), Lr["row_token"])
+
+
 def test_all_invalid_routing(moe):
     T, E, K, P = 50, 8, 2, 4
     idx = -torch.ones(T, K, dtype=torch.int64)
