@@ -176,8 +176,7 @@ int64_t moe_worst_case_rows(int32_t T, int32_t E, int32_t K, int32_t pad_multipl
 moe_status moe_layout_workspace_bytes(int32_t T, int32_t E, size_t* bytes) {
   MOE_REQUIRE(bytes != nullptr, MOE_ERR_INVALID_ARG, "bytes is NULL");
   MOE_REQUIRE(T >= 0 && E >= 1, MOE_ERR_INVALID_ARG, "bad T/E");
-  // the per-chunk masks, each chunk's start, then the grid barrier's counter
-  *bytes = 2 * layout_counter_bytes(T, E) + 256;
+  *bytes = dispatch_workspace_bytes(T, E);
   return MOE_OK;
 }
 

@@ -35,9 +35,12 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
   return excl;
 }
 
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+// A relaxed gpu-scope load: it reads the value in L2 but, unlike an acquire,
+// orders nothing, so a spin on it leaves the SM's L1 and memory pipeline to
+// the other CTAs on the SM.  A spin ends with one fence (the acquire).
+__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned* p) {
   unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
@@ -54,7 +57,7 @@ static __device__ bool grid_barrier(unsigned* ctr, unsigned target, int* status,
     atomicAdd(ctr, 1u);
     int ok = 1;
     const unsigned long long t0 = global_timer_ns();
-    while (ld_acquire_gpu(ctr) < target) {
+    while (ld_relaxed_gpu(ctr) < target) {
       if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
         report(status, MOE_DEVERR_TIMEOUT);
         ok = 0;
@@ -62,7 +65,45 @@ static __device__ bool grid_barrier(unsigned* ctr, unsigned target, int* status,
       }
       __nanosleep(64);
     }
+    __threadfence();  // the acquire of everything written before the barrier
+    *s_ok = ok;
+  }
+  __syncthreads();
+  return *s_ok != 0;
+}
+
+// Words of the replicated grid barrier: an arrival counter, then REP release
+// flags, each in its own 128-byte line, so that the waiting CTAs poll REP
+// different lines instead of one.
+constexpr int BARRIER_REP = 8;
+constexpr int BARRIER_WORDS = 32 * (1 + BARRIER_REP);  // 1152 bytes, zeroed before the launch
+
+// Grid-wide barrier number n (1, 2, ...) of a cooperative launch.  Each CTA
+// adds one to the counter; the CTA whose addition completes barrier n (the
+// counter reaching n * gridDim.x) sets every release flag to n, and the others
+// wait for flag (blockIdx.x % REP) to reach n.  Bounded like grid_barrier.
+static __device__ bool grid_barrier_rep(unsigned* words, unsigned n, int* status, int* s_ok) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
     __threadfence();
+    const unsigned old = atomicAdd(words, 1u);
+    int ok = 1;
+    if (old == n * gridDim.x - 1) {
+      __threadfence();  // one fence, then the flags: a release of everything before it
+      for (int i = 0; i < BARRIER_REP; ++i) reinterpret_cast<volatile unsigned*>(words)[32 * (1 + i)] = n;
+    } else {
+      const unsigned* flag = words + 32 * (1 + (blockIdx.x % BARRIER_REP));
+      const unsigned long long t0 = global_timer_ns();
+      while (ld_relaxed_gpu(flag) < n) {
+        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+          report(status, MOE_DEVERR_TIMEOUT);
+          ok = 0;
+          break;
+        }
+        __nanosleep(100);
+      }
+    }
+    __threadfence();  // the acquire of everything written before the barrier
     *s_ok = ok;
   }
   __syncthreads();

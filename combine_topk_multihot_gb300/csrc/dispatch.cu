@@ -13,8 +13,7 @@
 //
 // One launch, every CTA resident, two bounded grid barriers:
 //   A. Per 32-token chunk, each expert's 32-bit token mask (shared-memory
-//      atomics).  From the top-k choices the same pass also writes the
-//      token's multihot row (routing_map, probs, winner_slot).
+//      atomics).
 //   -- barrier --
 //   B. One warp per expert: each chunk's start inside the expert's group (an
 //      exclusive scan of the masks' popcounts) and the expert's count.
@@ -23,12 +22,24 @@
 //      (block scans); CTA 0 writes offsets and totals and hands R, N and the
 //      status word to a host-synced caller through mapped memory.
 //   D. Items: the T tokens, then the C - N pad and spare rows, one warp each.
-//      A token's warp finds its experts in ascending order, places each pair
+//      A token's warp (from the top-k choices, after writing the token's
+//      multihot row: routing_map, probs, winner_slot) finds its experts in
+//      ascending order, places each pair
 //      at offsets[e] + start[e][chunk] + popcount(mask below the token),
-//      writes the rows' metadata and token_row, and stores the token's x row
-//      (held in registers since the start of the kernel for the warp's first
-//      token: its load overlaps phases A-C) into each of its rows.  A pad or
-//      spare row is zeroed and gets the sentinel metadata.
+//      writes the rows' metadata and token_row, puts the token's x row into
+//      its 4 KiB shared-memory slot, and one lane hands each of the token's
+//      rows to the TMA engine as a bulk copy (cp.async.bulk shared -> global),
+//      so a warp issues a few instructions per row.  A pad or spare row is a
+//      bulk copy of a zeroed slot and gets the sentinel metadata.
+// The two barriers release the CTAs through replicated flags and phase B
+// publishes each count in replicated copies, so the 600-odd CTAs do not all
+// poll or read one L2 line.  Nothing is loaded ahead for phase D: in-kernel
+// %globaltimer stamps at T = 4096 showed that loading each warp's first x row
+// before barrier 1 (16.8 MB at once) stretched phase A from about 2 to 12 us,
+// because it fills the memory pipeline of the SMs whose CTAs are still in
+// phase A.  The multihot rows are written in phase D for the same reason: as
+// stores in phase A, whose new L2 lines wait for the write-back of the
+// previous kernel's dirty lines, they added about 6 us to it.
 // No atomic decides a position, so the result does not depend on scheduling,
 // and rows inside a group are in ascending token order.  When the rows do not
 // fit (R > capacity) phase D writes nothing.
@@ -43,8 +54,16 @@ namespace {
 
 constexpr int FD_THREADS = 256;
 constexpr int FD_WARPS = FD_THREADS / 32;
-constexpr int FD_PF = 8;         // 16-byte vectors per lane of x kept in registers (H <= 2048 whole)
+constexpr int FD_PF = 8;         // 16-byte vectors per lane of one 4 KiB piece of a row
 constexpr int FD_MAX_K = 128;    // slots of the per-warp row list (K <= 127)
+constexpr int FD_SLOT = 32 * FD_PF * 16;  // bytes of a warp's staging slot (4 KiB)
+constexpr int FD_REP = BARRIER_REP;       // copies of each count, one per group of CTAs
+static_assert(BARRIER_WORDS * 4 <= FUSED_BARRIER_BYTES, "barrier words fit their workspace region");
+
+__device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
+               : "memory");
+}
 
 enum FusedInput : int { IN_MAP = 0, IN_TOPK = 1 };
 
@@ -61,7 +80,8 @@ struct FusedArgs {
   long long capacity;
   uint32_t* masks;    // [E][chunks] token mask of each chunk
   int* starts;        // [E][chunks] the chunk's first row inside the expert's group
-  unsigned* barrier;  // zeroed before the launch
+  unsigned* barrier;  // BARRIER_WORDS, zeroed before the launch
+  int* counts_rep;    // [FD_REP][E] copies of tokens_per_expert
   int* tokens_per_expert;
   int* offsets;
   int* totals;
@@ -111,29 +131,27 @@ __device__ __forceinline__ int pair_row(const FusedArgs& a, const int* s_off, lo
 
 template <int IN>
 __global__ void __launch_bounds__(FD_THREADS, 4) dispatch_fused_kernel(FusedArgs a) {
-  extern __shared__ __align__(16) int fd_smem[];
+  extern __shared__ __align__(128) uint8_t fd_smem[];
   __shared__ int s_warp[33];
   __shared__ int s_ok;
   const int E = a.E, K = a.K;
-  uint32_t* s_tmask = reinterpret_cast<uint32_t*>(fd_smem);  // [E]
-  int* s_off = fd_smem + E;                                   // [E + 1]
-  int* s_cnt = s_off + E + 1;                                 // [E]
-  int* s_pad = s_cnt + E;                                     // [E + 1] pad rows before expert e
-  int* s_rows = s_pad + E + 1;                                // [FD_WARPS][FD_MAX_K]
+  // staging slots first (16-byte aligned for the bulk copies), then the tables
+  uint8_t* s_slots = fd_smem;                                            // [FD_WARPS][FD_SLOT]
+  uint8_t* s_zero = fd_smem + FD_WARPS * FD_SLOT;                        // [FD_SLOT] zeros
+  uint32_t* s_tmask = reinterpret_cast<uint32_t*>(s_zero + FD_SLOT);     // [E]
+  int* s_off = reinterpret_cast<int*>(s_tmask + E);                      // [E + 1]
+  int* s_cnt = s_off + E + 1;                                            // [E]
+  int* s_pad = s_cnt + E;                                                // [E + 1] pad rows before e
+  int* s_rows = s_pad + E + 1;                                           // [FD_WARPS][FD_MAX_K]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const long long gwarp = static_cast<long long>(blockIdx.x) * FD_WARPS + warp;
   const long long gwarps = static_cast<long long>(gridDim.x) * FD_WARPS;
   const int V = a.H >> 8;  // 16-byte vectors per lane of one row
 
-  // The warp's first token item is token gwarp: load its row of x now, so the
-  // load is in flight during phases A-C.
-  uint4 xr[FD_PF];
-  const bool have_first = a.x != nullptr && gwarp < a.T;
-  if (have_first) {
-    const uint4* src = reinterpret_cast<const uint4*>(a.x + gwarp * a.H);
-#pragma unroll
-    for (int i = 0; i < FD_PF; ++i)
-      if (i < V) xr[i] = __ldg(src + lane + 32 * i);
+  if (a.x_disp) {  // the zero slot of the pad and spare rows
+    for (int i = threadIdx.x; i < FD_SLOT / 16; i += FD_THREADS)
+      reinterpret_cast<uint4*>(s_zero)[i] = make_uint4(0, 0, 0, 0);
+    fence_async_shared();
   }
 
   // ---- A. per chunk, each expert's token mask
@@ -153,12 +171,36 @@ __global__ void __launch_bounds__(FD_THREADS, 4) dispatch_fused_kernel(FusedArgs
         for (int d = 0; d < 4; ++d)
           if ((w >> (8 * d)) & 0xffu) atomicOr(s_tmask + e0 + d, 1u << tl);
       }
+    } else if (K <= 32) {
+      // the warp's four tokens (warp, warp + 8, ...): every slot load issued at once
+      int em[4];
+      float pm[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int tl = warp + FD_WARPS * m;
+        em[m] = -1;
+        pm[m] = 0.f;
+        if (tl < nt && lane < K) {
+          const long long o = (t0 + tl) * K + lane;
+          long long v = __ldg(a.topk_idx + o);
+          pm[m] = __ldg(a.topk_probs + o);
+          if (v < -1 || v >= E) {
+            report(a.status, MOE_DEVERR_BAD_INDEX);
+            v = -1;
+          }
+          em[m] = static_cast<int>(v);
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int tl = warp + FD_WARPS * m;
+        if (tl < nt && em[m] >= 0) atomicOr(s_tmask + em[m], 1u << tl);
+      }
     } else {
       for (int tl = warp; tl < nt; tl += FD_WARPS) {
         int ek[4];
         float pk[4];
         load_slots(a, t0 + tl, lane, ek, pk, true);
-        if (a.map_out) write_multihot_row(t0 + tl, ek, pk, K, E, lane, a.map_out, a.probs_out, a.winner_out);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           if (ek[j] >= 0) atomicOr(s_tmask + ek[j], 1u << tl);
@@ -169,7 +211,8 @@ __global__ void __launch_bounds__(FD_THREADS, 4) dispatch_fused_kernel(FusedArgs
       a.masks[static_cast<long long>(e) * a.chunks + c] = s_tmask[e];
     __syncthreads();  // before the next chunk clears s_tmask
   }
-  if (!grid_barrier(a.barrier, gridDim.x, a.status, &s_ok)) return;
+
+  if (!grid_barrier_rep(a.barrier, 1, a.status, &s_ok)) return;
 
   // ---- B. per expert, each chunk's start in the group and the count
   for (long long e = gwarp; e < E; e += gwarps) {
@@ -193,17 +236,19 @@ __global__ void __launch_bounds__(FD_THREADS, 4) dispatch_fused_kernel(FusedArgs
       }
     }
     if (lane == 0) a.tokens_per_expert[e] = run;
+    if (lane < FD_REP) a.counts_rep[lane * E + e] = run;
   }
-  if (!grid_barrier(a.barrier, 2 * gridDim.x, a.status, &s_ok)) return;
+  if (!grid_barrier_rep(a.barrier, 2, a.status, &s_ok)) return;
 
   // ---- C. padded offsets and pad-row prefixes; thread i owns experts 4i .. 4i + 3
   int R, pad_total;
   {
+    const int* counts = a.counts_rep + (blockIdx.x % FD_REP) * E;
     int cnt[4], padded[4], psum = 0, qsum = 0;
 #pragma unroll
     for (int d = 0; d < 4; ++d) {
       const int e = 4 * threadIdx.x + d;
-      cnt[d] = e < E ? __ldcg(a.tokens_per_expert + e) : 0;
+      cnt[d] = e < E ? __ldcg(counts + e) : 0;
       padded[d] = ((cnt[d] + a.P - 1) / a.P) * a.P;
       psum += padded[d];
       qsum += padded[d] - cnt[d];
@@ -251,6 +296,9 @@ __global__ void __launch_bounds__(FD_THREADS, 4) dispatch_fused_kernel(FusedArgs
   const long long N = R - pad_total;
   const long long items = a.T + (C - N);
   int* rows = s_rows + warp * FD_MAX_K;
+  const uint32_t slot = smem_u32(s_slots + warp * FD_SLOT);
+  const uint32_t zero = smem_u32(s_zero);
+  const long long row_bytes = 2LL * a.H;
   for (long long it = gwarp; it < items; it += gwarps) {
     if (it < a.T) {
       const long long t = it;
@@ -292,6 +340,8 @@ __global__ void __launch_bounds__(FD_THREADS, 4) dispatch_fused_kernel(FusedArgs
         int ek[4];
         float pk[4];
         load_slots(a, t, lane, ek, pk, false);
+        // the token's multihot row, for the backward (nothing in this kernel reads it)
+        write_multihot_row(t, ek, pk, K, E, lane, a.map_out, a.probs_out, a.winner_out);
         // A slot is its expert's winner unless a later slot names the same expert.
         bool win[4] = {ek[0] >= 0, ek[1] >= 0, ek[2] >= 0, ek[3] >= 0};
         for (int k2 = 0; k2 < K; ++k2) {
@@ -329,24 +379,34 @@ __global__ void __launch_bounds__(FD_THREADS, 4) dispatch_fused_kernel(FusedArgs
       for (int j = n + lane; j < K; j += 32) a.token_row[t * K + j] = -1;
       __syncwarp();
       if (a.x == nullptr) continue;
-      // the copies: x[t] into each of the token's rows
+      // x[t] into each of the token's rows, 4 KiB at a time: the lanes put the
+      // piece into the warp's slot, one lane bulk-copies it to every row
       const uint4* src = reinterpret_cast<const uint4*>(a.x + t * a.H);
       for (int v0 = 0; v0 < V; v0 += FD_PF) {
-        if (v0 > 0 || t != gwarp) {
+        const int nv = min(FD_PF, V - v0);
+        uint4 xr[FD_PF];
 #pragma unroll
-          for (int i = 0; i < FD_PF; ++i)
-            if (v0 + i < V) xr[i] = __ldg(src + lane + 32 * (v0 + i));
-        }
-        for (int j = 0; j < n; ++j) {
-          const int r = rows[j];
-          if (r < 0 || r >= C) continue;
-          uint4* d = reinterpret_cast<uint4*>(a.x_disp + static_cast<long long>(r) * a.H);
+        for (int i = 0; i < FD_PF; ++i)
+          if (i < nv) xr[i] = __ldg(src + lane + 32 * (v0 + i));
+        if (lane == 0) tma_store_wait_read<0>();  // the slot's previous copies have read it
+        __syncwarp();
 #pragma unroll
-          for (int i = 0; i < FD_PF; ++i)
-            if (v0 + i < V) d[lane + 32 * (v0 + i)] = xr[i];
+        for (int i = 0; i < FD_PF; ++i)
+          if (i < nv)
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(slot + 16 * (lane + 32 * i)),
+                         "r"(xr[i].x), "r"(xr[i].y), "r"(xr[i].z), "r"(xr[i].w)
+                         : "memory");
+        fence_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+          for (int j = 0; j < n; ++j) {
+            const int r = rows[j];
+            if (r < 0 || r >= C) continue;
+            bulk_store(reinterpret_cast<uint8_t*>(a.x_disp) + r * row_bytes + 512LL * v0, slot, 512u * nv);
+          }
+          tma_store_commit();
         }
       }
-      __syncwarp();  // rows[] is rewritten by the warp's next token
     } else {
       // pad item p: a pad row of some expert's group, or a spare row after R
       const long long p = it - a.T;
@@ -361,22 +421,24 @@ __global__ void __launch_bounds__(FD_THREADS, 4) dispatch_fused_kernel(FusedArgs
       } else {
         r = R + (p - pad_total);
       }
-      if (r >= C) continue;
-      if (lane == 0) {
-        a.row_token[r] = -1;
-        a.row_expert[r] = E;
-        a.row_weight[r] = 0.f;
-      }
+      if (r >= C || lane != 0) continue;
+      a.row_token[r] = -1;
+      a.row_expert[r] = E;
+      a.row_weight[r] = 0.f;
       if (a.x_disp == nullptr) continue;
-      uint4* d = reinterpret_cast<uint4*>(a.x_disp + r * a.H);
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      for (int v = 0; v < V; ++v) d[lane + 32 * v] = z;
+      for (int v0 = 0; v0 < V; v0 += FD_PF)
+        bulk_store(reinterpret_cast<uint8_t*>(a.x_disp) + r * row_bytes + 512LL * v0, zero,
+                   512u * min(FD_PF, V - v0));
+      tma_store_commit();
     }
   }
+  if (lane == 0) tma_store_wait_all();  // every bulk copy done before the CTA exits
+  __syncwarp();
 }
 
 size_t fused_smem_bytes(int E) {
-  return (static_cast<size_t>(4) * E + 2) * sizeof(int) + static_cast<size_t>(FD_WARPS) * FD_MAX_K * sizeof(int);
+  return static_cast<size_t>(FD_WARPS + 1) * FD_SLOT + (static_cast<size_t>(4) * E + 2) * sizeof(int) +
+         static_cast<size_t>(FD_WARPS) * FD_MAX_K * sizeof(int);
 }
 
 // CTAs of dispatch_fused_kernel<IN> resident at once on the current device
@@ -402,12 +464,23 @@ int fused_resident_ctas(size_t smem) {
 template <int IN>
 cudaError_t launch_fused(FusedArgs& a, void* workspace, cudaStream_t s) {
   const size_t cb = layout_counter_bytes(a.T, a.E);
-  a.masks = static_cast<uint32_t*>(workspace);
-  a.starts = reinterpret_cast<int*>(static_cast<char*>(workspace) + cb);
-  a.barrier = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + 2 * cb);
-  cudaError_t err = cudaMemsetAsync(a.barrier, 0, sizeof(unsigned), s);
+  char* ws = static_cast<char*>(workspace);
+  a.masks = reinterpret_cast<uint32_t*>(ws);
+  a.starts = reinterpret_cast<int*>(ws + cb);
+  a.barrier = reinterpret_cast<unsigned*>(ws + 2 * cb);
+  a.counts_rep = reinterpret_cast<int*>(ws + 2 * cb + FUSED_BARRIER_BYTES);
+  cudaError_t err = cudaMemsetAsync(a.barrier, 0, BARRIER_WORDS * sizeof(unsigned), s);
   if (err != cudaSuccess) return err;
   const size_t smem = fused_smem_bytes(a.E);
+  static bool configured[64][2] = {};
+  int dev = 0;
+  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64 || !configured[dev][IN]) {
+    err = cudaFuncSetAttribute(dispatch_fused_kernel<IN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(fused_smem_bytes(1024)));
+    if (err != cudaSuccess) return err;
+    if (dev >= 0 && dev < 64) configured[dev][IN] = true;
+  }
   // every resident CTA: phase D has T + (C - N) warp items
   const long long items = a.T + a.capacity;
   const long long want = (items + FD_WARPS - 1) / FD_WARPS;
@@ -453,7 +526,7 @@ void fill_common(FusedArgs& a, const moe_layout& L, int H, const uint16_t* x, ui
 bool dispatch_fused_fits(const moe_layout& L) {
   // the cooperative launch is for layers of more than 8 chunks (smaller ones
   // take the barrier-free layout) whose per-CTA arrays fit shared memory
-  return layout_chunks(L.T) > 8 && fused_smem_bytes(L.E) <= 48 * 1024;
+  return layout_chunks(L.T) > 8 && fused_smem_bytes(L.E) <= fused_smem_bytes(1024);
 }
 
 cudaError_t launch_dispatch_fused_map(const uint8_t* routing_map, const float* probs, const moe_layout& L,

@@ -11,7 +11,7 @@
 // fixed array that lives in the library's own device memory instead.
 //
 // The array below is a file-scope __device__ variable: every GPU on which
-// the library is loaded holds its 2 MiB (+ 256 bytes) from load until the
+// the library is loaded holds its 2 MiB (+ 33 KiB) from load until the
 // process exits.
 // Host code only knows the symbol, not its device address, so the address is
 // looked up with cudaGetSymbolAddress on the first call for each device (and
@@ -30,9 +30,10 @@ namespace {
 
 constexpr long long STATIC_SCRATCH_INTS = MOE_STATIC_SCRATCH_INTS;  // (expert, chunk) pairs
 
-// Per (expert, chunk) pair a token mask and a start row (2 MiB), then 256
-// bytes for the dispatch kernel's grid-barrier counter.
-static __device__ __align__(256) int g_dispatch_scratch[2 * STATIC_SCRATCH_INTS + 64];
+// Per (expert, chunk) pair a token mask and a start row (2 MiB), then the
+// dispatch kernel's grid-barrier words and 8 copies of up to 1024 expert
+// counts (33 KiB).
+static __device__ __align__(256) int g_dispatch_scratch[2 * STATIC_SCRATCH_INTS + (1280 + 8 * 1024 * 4) / 4];
 
 constexpr int MAX_DEVICES = 64;
 std::mutex g_scratch_mu;

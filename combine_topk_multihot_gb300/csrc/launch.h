@@ -97,12 +97,20 @@ cudaError_t launch_layout(const uint8_t* routing_map, const float* probs, const 
                           void* workspace, cudaStream_t s, int* readback = nullptr,
                           const uint16_t* x = nullptr, uint16_t* x_disp = nullptr, int H = 0,
                           bool* rows_done = nullptr);
+// Workspace of the dispatch (moe_layout.workspace): per (expert, chunk) a
+// token mask and a start row, then the fused kernel's grid-barrier words,
+// then 8 copies of the per-expert counts.
+constexpr size_t FUSED_BARRIER_BYTES = 1280;
+inline size_t dispatch_workspace_bytes(int32_t T, int32_t E) {
+  const size_t rep = (static_cast<size_t>(8) * E * sizeof(int32_t) + 255) / 256 * 256;
+  return 2 * layout_counter_bytes(T, E) + FUSED_BARRIER_BYTES + rep;
+}
+
 // a1-a4 in one cooperative launch for layers of more than 8 chunks: counts,
 // offsets, placement, the pad and spare rows, and (x_disp non-NULL) the row
 // copies.  Input the multihot map (_map) or the top-k choices (_topk, which
 // also writes routing_map / probs / winner).  workspace: L.workspace, which
-// holds 2 * layout_counter_bytes(T, E) + 256 bytes.  readback as in
-// launch_layout.
+// holds dispatch_workspace_bytes(T, E).  readback as in launch_layout.
 bool dispatch_fused_fits(const moe_layout& L);
 cudaError_t launch_dispatch_fused_map(const uint8_t* routing_map, const float* probs, const moe_layout& L,
                                       int H, const uint16_t* x, uint16_t* x_disp, int* readback,

@@ -270,8 +270,9 @@ MOE_API moe_status moe_quantize_fp8(const moe_bf16* src, int64_t rows, int32_t c
  * Arguments, results and errors are those of moe_dispatch, except that
  * L->workspace is ignored (it may be NULL): the per-chunk expert masks and
  * start rows live in a static device array inside the library,
- * 2 * MOE_STATIC_SCRATCH_INTS int32 (2 MiB, plus 256 bytes for a barrier
- * counter) per GPU, held from library load until the process exits.
+ * 2 * MOE_STATIC_SCRATCH_INTS int32 (2 MiB, plus 33 KiB for the kernel's
+ * barrier words and count copies) per GPU, held from library load until the
+ * process exits.
  *   - Limit: E * ceil(T / 32) <= MOE_STATIC_SCRATCH_INTS (E = 128 allows
  *     T <= 65536); larger sizes return MOE_ERR_UNSUPPORTED_SHAPE before any
  *     work is queued.
