@@ -333,8 +333,7 @@ def run_ours(args, world, rank, local, leg: bool = False):
         rec = (lambda j: events[j].record(stream)) if events else (lambda j: None)
         o_buf = out if out_buf is None else out_buf
         rec(0)
-        if fused_topk:  # the multihot step runs inside the dispatch call
-            rec(1)
+        if fused_topk:  # the multihot step runs inside the dispatch call (its stage is 0)
             _, (rmap, probs, win), _ = moe.moe_dispatch_topk(L["x"], L["topk_idx"], L["topk_probs"], lay,
                                                              host_sync=host_sync, x_disp=x_disp, multihot=mh)
             rec(2)
@@ -416,7 +415,9 @@ def run_ours(args, world, rank, local, leg: bool = False):
         units = [(cycle.replay, n_layers)] * (args.steps // n_layers) + \
                 [(graphs[i].replay, 1) for i in range(args.steps % n_layers)]
     else:
-        units = [((lambda i=i: step(layers[i % n_layers], step_events[i])), 1) for i in range(args.steps)]
+        # no per-stage events inside the timed windows: each event record is a
+        # gap on the stream; the stage split comes from a separate pass below
+        units = [((lambda i=i: step(layers[i % n_layers])), 1) for i in range(args.steps)]
     bounds = window_bounds(len(units))
     w_ev = [ev() for _ in range(len(bounds) + 1)]
     with ClockSampler(local) as clk:
@@ -436,10 +437,20 @@ def run_ours(args, world, rank, local, leg: bool = False):
                              [sum(n for _, n in units[a:b]) for a, b in bounds])
     ms_step_max = max_over_ranks(windows["median_ms_per_step"], world)
     ms_max = max_over_ranks(ms, world)
+    if graphs is None:
+        # the per-stage split: the same steps again, each stage between two events
+        for i in range(args.steps):
+            step(layers[i % n_layers], step_events[i])
+        torch.cuda.synchronize()
     per = {k: [] for k in stages}
     for evs in step_events:
         for j, k in enumerate(stages):
-            per[k].append(evs[j].elapsed_time(evs[j + 1]))
+            if fused_topk and j == 0:      # multihot: inside the dispatch
+                per[k].append(0.0)
+            elif fused_topk and j == 1:    # dispatch: from the step's first event
+                per[k].append(evs[0].elapsed_time(evs[2]))
+            else:
+                per[k].append(evs[j].elapsed_time(evs[j + 1]))
     status = int(lay.status.item())
     if status:
         raise RuntimeError(f"device status word set: {status}")
