@@ -178,8 +178,9 @@ class ClockSampler:
 def step_launches(T: int, H: int, E: int, C: int, fp8: bool, gather: bool, backward: bool) -> int:
     """Our kernel launches in one step (the dispatch's barrier-counter memset is
     a driver memset, not one of ours), then the two expert kernels and the
-    combine, and with the backward the combine backward, the five
-    expert-backward kernels, the dispatch backward and the multihot backward.
+    combine, and with the backward the combine backward (which also applies the
+    routing weight), the four expert-backward GEMMs, the dispatch backward and
+    the multihot backward.
     The dispatch of a layer of more than 8 chunks of 32 tokens is one
     cooperative kernel, which in the bf16 step also does the multihot step; the
     --gather step runs the multihot kernel and that kernel without rows, the
@@ -201,7 +202,7 @@ def step_launches(T: int, H: int, E: int, C: int, fp8: bool, gather: bool, backw
         n = 1 + (1 if single_rows else 2)
     n += 2 + 1
     if backward:
-        n += 1 + 5 + 1 + 1
+        n += 1 + 4 + 1 + 1
     return n
 
 
@@ -249,9 +250,10 @@ def algorithmic(cfg, counts: np.ndarray, R: int, N: int, C: int, backward: bool,
     if backward:
         out["combine_bwd_bytes"] = T * H * 2 + C * H * 2 + N * H * 2 + 4 * C
         out["dispatch_bwd_bytes"] = N * H * 2 + T * H * 2 + T * E * 4
-        # scale, dgrad1 (W2, gu), dgrad2 (W1), wgrad2, wgrad1 (fp32 dW written)
+        # dgrad1 (W2, gu), dgrad2 (W1), wgrad2, wgrad1 (fp32 dW written); G_o
+        # comes from the combine backward's scatter
         out["experts_bwd_bytes"] = (w_bytes + 2 * w_bytes  # weights read, fp32 dW written
-                                    + N * H * 2 * 4        # grad_y, G_o (w + 2 r), x_disp
+                                    + N * H * 2 * 3        # G_o (2 reads), x_disp
                                     + N * 2 * I * 2 * 4    # gu read, G_gu (w + 2 r)
                                     + N * I * 2 + N * H * 2)  # h read, grad_x_disp written
         out["experts_bwd_flops"] = 12.0 * N * H * I
@@ -362,10 +364,12 @@ def run_ours(args, world, rank, local, leg: bool = False):
         moe.moe_combine(bufs["y"], lay, out=o_buf)
         rec(4)
         if bwd:
-            grad_y, grad_w = moe.moe_combine_backward(L["grad_out"], lay, o_save=bufs["o"])
+            # the routing weight goes onto the gradient in the combine backward's
+            # scatter (G_o = w * grad_y), so the experts' backward needs no scaling pass
+            g_o, grad_w = moe.moe_combine_backward(L["grad_out"], lay, o_save=bufs["o"], scaled=True)
             rec(5)
-            gxd, dW1, dW2 = moe.moe_grouped_experts_backward(grad_y, x_disp, bufs["h"], bufs["gu"], lay,
-                                                             L["W1"], L["W2"])
+            gxd, dW1, dW2 = moe.moe_grouped_experts_backward(g_o, x_disp, bufs["h"], bufs["gu"], lay,
+                                                             L["W1"], L["W2"], scaled=True)
             rec(6)
             grad_x, grad_probs = moe.moe_dispatch_backward(gxd, lay, grad_w)
             rec(7)
@@ -618,7 +622,7 @@ def run_ours(args, world, rank, local, leg: bool = False):
     roof["algorithmic_bytes"] = ex_bytes
     roof["kernel"] = ("experts: grouped_gemm_kernel<0> (gate/up + SwiGLU" + (", e4m3 operands" if fp8 else "")
                       + ") + grouped_gemm_kernel<1> (down x weight)"
-                      + (" + the backward's scale_rows + 4 bwd_gemm_kernel launches" if bwd else ""))
+                      + (" + the backward's 4 bwd_gemm_kernel launches" if bwd else ""))
     roof["peak_source"] = src
     roof["tensor_frac_of_burst"] = ex_flops / (ex_us * 1e-6) / 1e12 / bf16_burst
 

@@ -72,9 +72,12 @@ SIGNATURES = {
     "moe_grouped_experts": (c_int32, [_P, _LP, c_int32, c_int32, _P, _P, _P, _P, _P, _P, _P]),
     "moe_combine": (c_int32, [_P, _LP, c_int32, _P, _P]),
     "moe_combine_backward": (c_int32, [_P, _P, _LP, c_int32, _P, _P, _P]),
+    "moe_combine_backward_scaled": (c_int32, [_P, _P, _LP, c_int32, _P, _P, _P]),
     "moe_dispatch_backward": (c_int32, [_P, _P, _LP, c_int32, _P, _P, _P]),
     "moe_experts_backward_workspace_bytes": (c_int32, [c_int64, c_int32, c_int32, ctypes.POINTER(c_size_t)]),
     "moe_grouped_experts_backward": (c_int32, [_P, _P, _P, _P, _LP, c_int32, c_int32, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_grouped_experts_backward_scaled": (c_int32, [_P, _P, _P, _P, _LP, c_int32, c_int32, _P, _P, _P, _P, _P,
+                                                      _P, _P]),
     "moe_selftest_wait_timeout": (c_int32, [_P, c_int64, _P, _P]),
     "moe_route_to_multihot_backward": (c_int32, [_P, _P, _P, c_int32, c_int32, c_int32, _P, _P]),
 }

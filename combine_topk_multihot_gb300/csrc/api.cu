@@ -468,22 +468,77 @@ moe_status moe_combine(const moe_bf16* y_disp, const moe_layout* L, int32_t H, m
   return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_combine launch");
 }
 
-moe_status moe_combine_backward(const moe_bf16* grad_out, const moe_bf16* o_save,
-                                const moe_layout* L, int32_t H, moe_bf16* grad_y, float* grad_w,
-                                moe_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+moe_status combine_backward_impl(const char* who, const moe_bf16* grad_out, const moe_bf16* o_save,
+                                 const moe_layout* L, int32_t H, moe_bf16* grad_y, float* grad_w,
+                                 moe_stream_t stream, bool scale) {
   moe_status st = check_layout(L);
   if (st != MOE_OK) return st;
   if ((st = check_hidden(H)) != MOE_OK) return st;
-  MOE_REQUIRE(L->capacity == 0 || (grad_out && grad_y), MOE_ERR_INVALID_ARG,
-              "moe_combine_backward: NULL pointer");
-  MOE_REQUIRE(!grad_w || o_save, MOE_ERR_INVALID_ARG,
-              "moe_combine_backward: grad_w needs o_save");
+  MOE_REQUIRE(L->capacity == 0 || (grad_out && grad_y), MOE_ERR_INVALID_ARG, "%s: NULL pointer", who);
+  MOE_REQUIRE(!grad_w || o_save, MOE_ERR_INVALID_ARG, "%s: grad_w needs o_save", who);
   MOE_REQUIRE(aligned16(grad_out) && aligned16(grad_y) && aligned16(o_save), MOE_ERR_INVALID_ARG,
-              "moe_combine_backward: pointers must be 16-byte aligned");
+              "%s: pointers must be 16-byte aligned", who);
   if ((st = check_device()) != MOE_OK) return st;
-  cudaError_t err = launch_row_gather(grad_out, *L, H, grad_y, false, o_save, grad_w, stream);
-  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_combine_backward launch");
+  cudaError_t err = launch_row_gather(grad_out, *L, H, grad_y, false, o_save, grad_w, stream, scale);
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, who);
 }
+
+moe_status experts_backward_impl(const char* who, const moe_bf16* grad_y, const moe_bf16* x_disp,
+                                 const moe_bf16* h, const moe_bf16* gu_save, const moe_layout* L,
+                                 int32_t H, int32_t I, const moe_bf16* W1, const moe_bf16* W2,
+                                 moe_bf16* grad_x_disp, float* dW1, float* dW2, void* workspace,
+                                 moe_stream_t stream, bool g_o_given) {
+  moe_status st = check_layout(L);
+  if (st != MOE_OK) return st;
+  if ((st = check_hidden(H)) != MOE_OK) return st;
+  MOE_REQUIRE(I > 0 && I % 128 == 0, MOE_ERR_UNSUPPORTED_SHAPE,
+              "the intermediate size must be a positive multiple of 128 (got %d)", I);
+  MOE_REQUIRE(W1 && W2 && dW1 && dW2 && workspace, MOE_ERR_INVALID_ARG,
+              "%s: NULL weight, weight-gradient or workspace pointer", who);
+  MOE_REQUIRE(L->capacity == 0 || (grad_y && x_disp && h && gu_save && grad_x_disp),
+              MOE_ERR_INVALID_ARG, "%s: NULL row buffer", who);
+  MOE_REQUIRE(aligned16(grad_y) && aligned16(x_disp) && aligned16(h) && aligned16(gu_save) &&
+                  aligned16(W1) && aligned16(W2) && aligned16(grad_x_disp) && aligned16(dW1) &&
+                  aligned16(dW2),
+              MOE_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", who);
+  if ((st = check_device()) != MOE_OK) return st;
+  cudaError_t err = launch_experts_backward(grad_y, x_disp, h, gu_save, *L, H, I, W1, W2, grad_x_disp,
+                                            dW1, dW2, workspace, stream, g_o_given);
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err, who);
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_combine_backward_scaled(const moe_bf16* grad_out, const moe_bf16* o_save,
+                                       const moe_layout* L, int32_t H, moe_bf16* g_o, float* grad_w,
+                                       moe_stream_t stream) {
+  return combine_backward_impl("moe_combine_backward_scaled", grad_out, o_save, L, H, g_o, grad_w, stream,
+                               true);
+}
+
+moe_status moe_grouped_experts_backward_scaled(const moe_bf16* g_o, const moe_bf16* x_disp,
+                                               const moe_bf16* h, const moe_bf16* gu_save,
+                                               const moe_layout* L, int32_t H, int32_t I,
+                                               const moe_bf16* W1, const moe_bf16* W2,
+                                               moe_bf16* grad_x_disp, float* dW1, float* dW2,
+                                               void* workspace, moe_stream_t stream) {
+  return experts_backward_impl("moe_grouped_experts_backward_scaled", g_o, x_disp, h, gu_save, L, H, I, W1,
+                               W2, grad_x_disp, dW1, dW2, workspace, stream, true);
+}
+
+moe_status moe_combine_backward(const moe_bf16* grad_out, const moe_bf16* o_save,
+                                const moe_layout* L, int32_t H, moe_bf16* grad_y, float* grad_w,
+                                moe_stream_t stream) {
+  return combine_backward_impl("moe_combine_backward", grad_out, o_save, L, H, grad_y, grad_w, stream,
+                               false);
+}
+
 
 moe_status moe_dispatch_backward(const moe_bf16* grad_x_disp, const float* grad_w,
                                  const moe_layout* L, int32_t H, moe_bf16* grad_x,
@@ -560,23 +615,8 @@ moe_status moe_grouped_experts_backward(const moe_bf16* grad_y, const moe_bf16* 
                                         const moe_bf16* W1, const moe_bf16* W2,
                                         moe_bf16* grad_x_disp, float* dW1, float* dW2,
                                         void* workspace, moe_stream_t stream) {
-  moe_status st = check_layout(L);
-  if (st != MOE_OK) return st;
-  if ((st = check_hidden(H)) != MOE_OK) return st;
-  MOE_REQUIRE(I > 0 && I % 128 == 0, MOE_ERR_UNSUPPORTED_SHAPE,
-              "the intermediate size must be a positive multiple of 128 (got %d)", I);
-  MOE_REQUIRE(W1 && W2 && dW1 && dW2 && workspace, MOE_ERR_INVALID_ARG,
-              "moe_grouped_experts_backward: NULL weight, weight-gradient or workspace pointer");
-  MOE_REQUIRE(L->capacity == 0 || (grad_y && x_disp && h && gu_save && grad_x_disp),
-              MOE_ERR_INVALID_ARG, "moe_grouped_experts_backward: NULL row buffer");
-  MOE_REQUIRE(aligned16(grad_y) && aligned16(x_disp) && aligned16(h) && aligned16(gu_save) &&
-                  aligned16(W1) && aligned16(W2) && aligned16(grad_x_disp) && aligned16(dW1) &&
-                  aligned16(dW2),
-              MOE_ERR_INVALID_ARG, "moe_grouped_experts_backward: pointers must be 16-byte aligned");
-  if ((st = check_device()) != MOE_OK) return st;
-  cudaError_t err = launch_experts_backward(grad_y, x_disp, h, gu_save, *L, H, I, W1, W2,
-                                            grad_x_disp, dW1, dW2, workspace, stream);
-  return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_grouped_experts_backward launch");
+  return experts_backward_impl("moe_grouped_experts_backward", grad_y, x_disp, h, gu_save, L, H, I, W1, W2,
+                               grad_x_disp, dW1, dW2, workspace, stream, false);
 }
 
 }  // extern "C"

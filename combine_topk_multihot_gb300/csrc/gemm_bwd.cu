@@ -88,10 +88,10 @@ struct Smem {
 // 32 rows x 64 bytes: 32 bf16 or 16 fp32 columns).
 constexpr int STAGING_BYTES = EPI_WARPS * 4096;
 
-template <int BN>
+template <int BN, bool PAIR = false>
 constexpr size_t smem_bytes(int stages, int E) {
-  return 1024 + static_cast<size_t>(stages) * Cfg<BN>::STAGE_BYTES + STAGING_BYTES + sizeof(Smem) +
-         static_cast<size_t>(3 * E + 2) * sizeof(int);
+  return 1024 + static_cast<size_t>(stages) * (PAIR ? A_BYTES + Cfg<BN>::B_BYTES / 2 : Cfg<BN>::STAGE_BYTES) +
+         STAGING_BYTES + sizeof(Smem) + static_cast<size_t>(3 * E + 2) * sizeof(int);
 }
 
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -133,12 +133,22 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
 //   A is K-major (rows of the expert), B is MN-major (the expert's weight).
 // GROUP_K = true: tiles are (expert, M block, N block); both operands are
 //   MN-major slices of the expert's rows, the contraction runs over the rows.
-template <bool GROUP_K, int BN, int EPI, int STAGES>
+// PAIR: clusters of two CTAs, tiles of 256 M rows (the expert's rows, or the
+//   M extent of a weight gradient): each CTA loads its own 128 of them and
+//   one half (128) of the tile's N columns, the even CTA issues cta_group::2
+//   MMAs for the pair, each CTA's epilogue takes its own 128 rows (as in the
+//   forward kernel's pairs).  Used with 256-column tiles and no K-line
+//   masking, so that neither CTA touches shared memory the other's MMAs read.
+template <bool GROUP_K, int BN, int EPI, int STAGES, bool PAIR = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmOut, const BwdArgs args) {
-  constexpr int STAGE_BYTES = Cfg<BN>::STAGE_BYTES;
-  constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN) | (GROUP_K ? (1u << 15) : 0u) | (1u << 16);
+  static_assert(!PAIR || BN == 256, "CTA pairs take 256-column tiles");
+  constexpr int B_BYTES = PAIR ? Cfg<BN>::B_BYTES / 2 : Cfg<BN>::B_BYTES;
+  constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr int RB = PAIR ? 2 * BM : BM;  // M rows of a tile
+  constexpr int B_BOXES = (PAIR ? BN / 2 : BN) / 64;
+  constexpr uint32_t IDESC = idesc_bf16_f32(RB, BN) | (GROUP_K ? (1u << 15) : 0u) | (1u << 16);
   // K-major A: 8-row groups 1 KiB apart, next 16-wide K slice 32 bytes on.
   // MN-major A / B: 64-wide MN blocks 8 KiB apart, 8-deep K groups 1 KiB
   // apart, next 16-deep K slice two groups (2 KiB) on.
@@ -158,6 +168,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t staging_u32 = tiles_u32 + STAGES * STAGE_BYTES;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = args.E;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // the even CTA of a pair issues the MMAs
+  const int tile0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int tstep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -166,7 +179,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.tfull[i]), 1);
-      mbar_init(smem_u32(&s.tempty[i]), EPI_WARPS);
+      mbar_init(smem_u32(&s.tempty[i]), PAIR ? 2 * EPI_WARPS : EPI_WARPS);
     }
     mbar_init(smem_u32(&s.drain), 1);
     s.abort = 0;
@@ -175,7 +188,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmOut);
   }
-  if (warp == 1) tmem_alloc(smem_u32(&s.tmem_base), TMEM_COLS);
+  if (warp == 1) {
+    if constexpr (PAIR)
+      tmem_alloc_pair(smem_u32(&s.tmem_base), TMEM_COLS);
+    else
+      tmem_alloc(smem_u32(&s.tmem_base), TMEM_COLS);
+  }
   for (int e = threadIdx.x; e <= E; e += NUM_THREADS) s_off[e] = args.offsets[e];
   for (int e = threadIdx.x; e < E; e += NUM_THREADS) s_cnt[e] = args.counts[e];
   __syncthreads();
@@ -184,7 +202,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int e0 = 0; e0 < E; e0 += 32) {
       const int e = e0 + lane;
       int n = 0;
-      if (e < E) n = GROUP_K ? args.m_tiles * args.n_tiles : ((s_cnt[e] + BM - 1) / BM) * args.n_tiles;
+      if (e < E) n = GROUP_K ? args.m_tiles * args.n_tiles : ((s_cnt[e] + RB - 1) / RB) * args.n_tiles;
       int incl = n;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -201,6 +219,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();  // both CTAs' barriers exist before either signals the other
   tc_fence_after();
 
   const int total = s.total_tiles;
@@ -214,34 +233,56 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       long long issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = tile0; tile < total && ok; tile += tstep) {
         const Tile t = decode(s_pre, E, args.n_tiles, tile);
         const int kbs = GROUP_K ? (s_cnt[t.e] + BK - 1) / BK : args.k_blocks;
+        const int m0 = t.mt * RB + static_cast<int>(rank) * BM;         // this CTA's M rows
+        const int n0 = t.nt * BN + static_cast<int>(rank) * (BN / 2);   // (pair) this CTA's N half
         for (int kb = 0; kb < kbs; ++kb) {
           if (!mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, abort_flag)) { ok = false; break; }
           const uint32_t full = smem_u32(&s.full[stage]);
           const uint32_t a_dst = tiles_u32 + stage * STAGE_BYTES;
           const uint32_t b_dst = a_dst + A_BYTES;
-          mbar_arrive_expect_tx(full, STAGE_BYTES);
-          if (GROUP_K) {
-            const int k_row = s_off[t.e] + kb * BK;
-            tma_load_2d(a_dst, &tmA, t.mt * BM, k_row, full);
-            tma_load_2d(a_dst + MN_BOX_BYTES, &tmA, t.mt * BM + 64, k_row, full);
+          if constexpr (PAIR) {
+            // both CTAs' loads complete on the even CTA's barrier, which expects them all
+            const uint32_t full0 = mapa_shared(full, 0);
+            if (rank == 0) mbar_arrive_expect_tx(full, 2 * STAGE_BYTES);
+            if (GROUP_K) {
+              const int k_row = s_off[t.e] + kb * BK;
+              tma_load_2d_pair(a_dst, &tmA, m0, k_row, full0);
+              tma_load_2d_pair(a_dst + MN_BOX_BYTES, &tmA, m0 + 64, k_row, full0);
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_2d(b_dst + j * MN_BOX_BYTES, &tmB, t.nt * BN + 64 * j, k_row, full);
+              for (int j = 0; j < B_BOXES; ++j)
+                tma_load_2d_pair(b_dst + j * MN_BOX_BYTES, &tmB, n0 + 64 * j, k_row, full0);
+            } else {
+              tma_load_2d_pair(a_dst, &tmA, kb * BK, s_off[t.e] + m0, full0);
+              const int k_row = t.e * args.b_rows_per_expert + kb * BK;
+#pragma unroll
+              for (int j = 0; j < B_BOXES; ++j)
+                tma_load_2d_pair(b_dst + j * MN_BOX_BYTES, &tmB, n0 + 64 * j, k_row, full0);
+            }
           } else {
-            tma_load_2d(a_dst, &tmA, kb * BK, s_off[t.e] + t.mt * BM, full);
-            const int k_row = t.e * args.b_rows_per_expert + kb * BK;
+            mbar_arrive_expect_tx(full, STAGE_BYTES);
+            if (GROUP_K) {
+              const int k_row = s_off[t.e] + kb * BK;
+              tma_load_2d(a_dst, &tmA, t.mt * BM, k_row, full);
+              tma_load_2d(a_dst + MN_BOX_BYTES, &tmA, t.mt * BM + 64, k_row, full);
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_2d(b_dst + j * MN_BOX_BYTES, &tmB, t.nt * BN + 64 * j, k_row, full);
+              for (int j = 0; j < BN / 64; ++j)
+                tma_load_2d(b_dst + j * MN_BOX_BYTES, &tmB, t.nt * BN + 64 * j, k_row, full);
+            } else {
+              tma_load_2d(a_dst, &tmA, kb * BK, s_off[t.e] + t.mt * BM, full);
+              const int k_row = t.e * args.b_rows_per_expert + kb * BK;
+#pragma unroll
+              for (int j = 0; j < BN / 64; ++j)
+                tma_load_2d(b_dst + j * MN_BOX_BYTES, &tmB, t.nt * BN + 64 * j, k_row, full);
+            }
           }
           ++issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
-      if (!ok) {
+      if (!ok && (!PAIR || rank == 0)) {
         for (int i = 0; i < STAGES && i < issued; ++i) {
           if (--stage < 0) { stage = STAGES - 1; phase ^= 1u; }
           mbar_wait_drain(smem_u32(&s.full[stage]), phase);
@@ -249,13 +290,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     __syncwarp();
+  } else if (warp == 1 && PAIR && rank != 0) {
+    // ================= the odd CTA of a pair: no MMAs; wait for the even CTA's last ones =================
+    if (lane == 0 && !mbar_wait_drain(smem_u32(&s.drain), 0)) *abort_flag = 1;
+    __syncwarp();
   } else if (warp == 1) {
     // ================= MMA warp (lane 0 issues; the warp zeroes tail K lines) =================
     int stage = 0;
     uint32_t phase = 0;
     int local = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++local) {
+    for (int tile = tile0; tile < total && ok; tile += tstep, ++local) {
       const Tile t = decode(s_pre, E, args.n_tiles, tile);
       const int count = s_cnt[t.e];
       const int kbs = GROUP_K ? (count + BK - 1) / BK : args.k_blocks;
@@ -294,18 +339,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
             const uint64_t a_desc = sdesc_sw128(a_addr + kk * A_STEP, A_LBO, 1024);
             const uint64_t b_desc = sdesc_sw128(b_addr + kk * B_STEP, B_LBO, 1024);
-            tc_mma_bf16(d_tmem, a_desc, b_desc, IDESC, (kb | kk) != 0);
+            if constexpr (PAIR)
+              tc_mma_bf16_pair(d_tmem, a_desc, b_desc, IDESC, (kb | kk) != 0);
+            else
+              tc_mma_bf16(d_tmem, a_desc, b_desc, IDESC, (kb | kk) != 0);
           }
-          tc_commit(smem_u32(&s.empty[stage]));
+          if constexpr (PAIR)
+            tc_commit_pair(smem_u32(&s.empty[stage]));
+          else
+            tc_commit(smem_u32(&s.empty[stage]));
         }
         __syncwarp();
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
-      if (ok && lane == 0) tc_commit(smem_u32(&s.tfull[buf]));
+      if (ok && lane == 0) {
+        if constexpr (PAIR)
+          tc_commit_pair(smem_u32(&s.tfull[buf]));
+        else
+          tc_commit(smem_u32(&s.tfull[buf]));
+      }
       __syncwarp();
     }
     if (lane == 0) {
-      tc_commit(smem_u32(&s.drain));
+      if constexpr (PAIR)
+        tc_commit_pair(smem_u32(&s.drain));
+      else
+        tc_commit(smem_u32(&s.drain));
       if (!mbar_wait_drain(smem_u32(&s.drain), 0)) *abort_flag = 1;
     }
     __syncwarp();
@@ -319,7 +378,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int r_in_tile = q * 32 + lane;
     StagedStore st{staging_u32 + (warp - 2) * 4096, 0u, lane};
     int local = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
+    for (int tile = tile0; tile < total; tile += tstep, ++local) {
       const Tile t = decode(s_pre, E, args.n_tiles, tile);
       const int buf = local & 1;
       const uint32_t use = (local >> 1) & 1;
@@ -328,7 +387,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t tb = tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
       if (GROUP_K) {
         // dW rows of expert e: rows (e * m_total + m) of the [E * m_total, n_total] output
-        const int out_row0 = t.e * args.m_total + t.mt * BM + q * 32;
+        const int out_row0 = t.e * args.m_total + t.mt * RB + static_cast<int>(rank) * BM + q * 32;
         const bool empty = s_cnt[t.e] == 0;
 #pragma unroll 1
         for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
@@ -346,11 +405,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       } else {
         // rows written: the expert's group (valid and pad rows) inside the tile
-        const int group_row = t.mt * BM + r_in_tile;
+        const int group_row = t.mt * RB + static_cast<int>(rank) * BM + r_in_tile;
         const bool valid = group_row < s_off[t.e + 1] - s_off[t.e];
         const bool full_warp = __all_sync(FULL_MASK, valid);
         const long long row = static_cast<long long>(s_off[t.e]) + group_row;
-        const int warp_row0 = s_off[t.e] + t.mt * BM + q * 32;
+        const int warp_row0 = s_off[t.e] + t.mt * RB + static_cast<int>(rank) * BM + q * 32;
         const int col0 = t.nt * BN;
 #pragma unroll 1
         for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
@@ -420,15 +479,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&s.tempty[buf]));
+      if (lane == 0) {
+        if constexpr (PAIR)
+          mbar_arrive_cluster(mapa_shared(smem_u32(&s.tempty[buf]), 0));  // the MMA issuer's barrier
+        else
+          mbar_arrive(smem_u32(&s.tempty[buf]));
+      }
     }
     st.finish();
   }
 
   tc_fence_before();
   __syncthreads();
+  // a pair: neither CTA frees its tensor memory or leaves while the pair's
+  // MMAs, loads or barrier signals may still reach it
+  if constexpr (PAIR) cluster_sync_all();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+  if (warp == 1) {
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, TMEM_COLS);
+  }
   if (threadIdx.x == 0 && s.abort) report(args.status, MOE_DEVERR_TIMEOUT);
 }
 
@@ -463,39 +535,75 @@ __global__ void __launch_bounds__(256) scale_rows_kernel(const uint16_t* __restr
   }
 }
 
-template <bool GROUP_K, int BN, int EPI, int STAGES>
+template <bool GROUP_K, int BN, int EPI, int STAGES, bool PAIR = false>
 cudaError_t launch_bwd_stages(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
                               const BwdArgs& args, cudaStream_t s) {
+  auto kernel = bwd_gemm_kernel<GROUP_K, BN, EPI, STAGES, PAIR>;
   static bool configured[64] = {};
+  static int pair_grid[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    err = cudaFuncSetAttribute(bwd_gemm_kernel<GROUP_K, BN, EPI, STAGES>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  bwd_gemm_kernel<GROUP_K, BN, EPI, STAGES><<<sm_count(), NUM_THREADS, smem_bytes<BN>(STAGES, args.E), s>>>(
-      a, b, out, args);
-  return cudaGetLastError();
+  const size_t smem = smem_bytes<BN, PAIR>(STAGES, args.E);
+  if constexpr (!PAIR) {
+    kernel<<<sm_count(), NUM_THREADS, smem, s>>>(a, b, out, args);
+    return cudaGetLastError();
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // persistent: as many pairs as can be resident at once (a pair needs two
+    // free SMs of one GPC), at most one CTA per SM
+    int grid = dev >= 0 && dev < 64 ? pair_grid[dev] : 0;
+    if (grid == 0) {
+      cfg.gridDim = dim3(sm_count() & ~1);
+      int clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess || clusters < 1)
+        clusters = sm_count() / 2;
+      grid = 2 * (clusters < sm_count() / 2 ? clusters : sm_count() / 2);
+      if (dev >= 0 && dev < 64) pair_grid[dev] = grid;
+    }
+    cfg.gridDim = dim3(grid);
+    return cudaLaunchKernelEx(&cfg, kernel, a, b, out, args);
+  }
 }
 
-// The deepest ring that fits beside the staging and the per-expert tables.
-template <bool GROUP_K, int BN, int EPI>
+// The deepest ring that fits beside the staging and the per-expert tables
+// (a pair's 32 KiB stages: six; 48 KiB stages: four).
+template <bool GROUP_K, int BN, int EPI, bool PAIR = false>
 cudaError_t launch_bwd(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
                        const BwdArgs& args, cudaStream_t s) {
-  constexpr int MS = Cfg<BN>::MAX_STAGES;
-  if (smem_bytes<BN>(MS, args.E) <= static_cast<size_t>(SMEM_LIMIT))
-    return launch_bwd_stages<GROUP_K, BN, EPI, MS>(a, b, out, args, s);
-  return launch_bwd_stages<GROUP_K, BN, EPI, MS - 1>(a, b, out, args, s);
+  constexpr int MS = PAIR ? 6 : Cfg<BN>::MAX_STAGES;
+  if (smem_bytes<BN, PAIR>(MS, args.E) <= static_cast<size_t>(SMEM_LIMIT))
+    return launch_bwd_stages<GROUP_K, BN, EPI, MS, PAIR>(a, b, out, args, s);
+  return launch_bwd_stages<GROUP_K, BN, EPI, MS - 1, PAIR>(a, b, out, args, s);
 }
 
+// 256-column tiles where N allows, on CTA pairs when the layer has rows for
+// them (pair): the M-grouped dgrads always, the K-grouped wgrads when M is a
+// multiple of 256 and no K lines need masking.
 template <bool GROUP_K, int EPI>
 cudaError_t launch_bwd_bn(int n_total, const CUtensorMap& a, const CUtensorMap& b,
-                          const CUtensorMap& out, BwdArgs args, cudaStream_t s) {
+                          const CUtensorMap& out, BwdArgs args, cudaStream_t s, bool pair) {
   if (n_total % 256 == 0) {
     args.n_tiles = n_total / 256;
+    if (pair && (!GROUP_K || (args.m_total % 256 == 0 && !args.zero_tail))) {
+      if (GROUP_K) args.m_tiles = args.m_total / 256;
+      return launch_bwd<GROUP_K, 256, EPI, true>(a, b, out, args, s);
+    }
     return launch_bwd<GROUP_K, 256, EPI>(a, b, out, args, s);
   }
   args.n_tiles = n_total / 128;
@@ -514,14 +622,16 @@ cudaError_t launch_experts_backward(const uint16_t* grad_y, const uint16_t* x_di
                                     const uint16_t* h, const uint16_t* gu_save, const moe_layout& L,
                                     int H, int I, const uint16_t* W1, const uint16_t* W2,
                                     uint16_t* grad_x_disp, float* dW1, float* dW2, void* workspace,
-                                    cudaStream_t s) {
+                                    cudaStream_t s, bool g_o_given) {
   const long long C = L.capacity;
   const int E = L.E;
   uintptr_t ws = (reinterpret_cast<uintptr_t>(workspace) + 255) & ~static_cast<uintptr_t>(255);
-  uint16_t* g_o = reinterpret_cast<uint16_t*>(ws);
+  // g_o_given: grad_y already holds G_o = bf16(w * grad_y) (the scaled combine
+  // backward wrote it), so the scaling pass is skipped
+  uint16_t* g_o = g_o_given ? const_cast<uint16_t*>(grad_y) : reinterpret_cast<uint16_t*>(ws);
   uint16_t* g_gu = reinterpret_cast<uint16_t*>(ws + ((static_cast<size_t>(C) * H * 2 + 255) / 256) * 256);
 
-  if (C > 0) {
+  if (C > 0 && !g_o_given) {
     const long long need = (C + 7) / 8;
     const int blocks = static_cast<int>(need < 8LL * sm_count() ? need : 8LL * sm_count());
     scale_rows_kernel<<<blocks, 256, 0, s>>>(grad_y, L.row_token, L.row_weight, L.totals, C, H, g_o);
@@ -529,6 +639,10 @@ cudaError_t launch_experts_backward(const uint16_t* grad_y, const uint16_t* x_di
     if (err != cudaSuccess) return err;
   }
 
+  // CTA pairs for layers with rows for every SM, as in the forward: at least
+  // as many experts' 256-column tiles as SMs
+  const long long pairs_rows = static_cast<long long>(L.T) * L.K;
+  const bool pair = (pairs_rows < E ? pairs_rows : E) * (I / 128) >= sm_count();
   BwdArgs base{};
   base.counts = L.tokens_per_expert;
   base.offsets = L.offsets;
@@ -550,7 +664,7 @@ cudaError_t launch_experts_backward(const uint16_t* grad_y, const uint16_t* x_di
     a.out_bf16 = g_gu;
     a.ld_out = 2 * I;
     a.gu = gu_save;
-    err = launch_bwd_bn<false, EPI_DSWIGLU>(I, mA, mB, mO, a, s);
+    err = launch_bwd_bn<false, EPI_DSWIGLU>(I, mA, mB, mO, a, s, pair);
     if (err != cudaSuccess) return err;
 
     // dgrad2: grad_x_disp = G_gu W1
@@ -563,7 +677,7 @@ cudaError_t launch_experts_backward(const uint16_t* grad_y, const uint16_t* x_di
     a.b_rows_per_expert = 2 * I;
     a.out_bf16 = grad_x_disp;
     a.ld_out = H;
-    err = launch_bwd_bn<false, EPI_BF16>(H, mA, mB, mO, a, s);
+    err = launch_bwd_bn<false, EPI_BF16>(H, mA, mB, mO, a, s, pair);
     if (err != cudaSuccess) return err;
   }
 
@@ -585,7 +699,7 @@ cudaError_t launch_experts_backward(const uint16_t* grad_y, const uint16_t* x_di
     a.m_total = H;
     a.n_total = I;
     a.out_f32 = dW2;
-    err = launch_bwd_bn<true, EPI_F32>(I, mA, mB, mO, a, s);
+    err = launch_bwd_bn<true, EPI_F32>(I, mA, mB, mO, a, s, pair);
     if (err != cudaSuccess) return err;
   }
   // wgrad1: dW1[e] = G_gu^T x_disp   (M = 2I, N = H)
@@ -606,7 +720,7 @@ cudaError_t launch_experts_backward(const uint16_t* grad_y, const uint16_t* x_di
     a.m_total = 2 * I;
     a.n_total = H;
     a.out_f32 = dW1;
-    err = launch_bwd_bn<true, EPI_F32>(H, mA, mB, mO, a, s);
+    err = launch_bwd_bn<true, EPI_F32>(H, mA, mB, mO, a, s, pair);
   }
   return err;
 }

@@ -123,9 +123,10 @@ cudaError_t launch_dispatch_fused_topk(const int64_t* topk_idx, const float* top
 // spare rows' metadata when from_offsets); also the combine backward (a7)
 // with the optional routing-weight gradient (a8).  Each token row is read
 // once and scattered to the token's rows; pad / spare rows are zeroed.
+// With scale (combine backward only) each row gets bf16(row_weight * src).
 cudaError_t launch_row_gather(const uint16_t* src, const moe_layout& L, int H, uint16_t* dst,
                               bool write_row_meta, const uint16_t* o_save, float* grad_w,
-                              cudaStream_t s);
+                              cudaStream_t s, bool scale = false);
 // Per-token ordered sum of rows (a6 / a10), optional grad_probs scatter.
 cudaError_t launch_combine(const uint16_t* rows, const moe_layout& L, int H, uint16_t* out,
                            const float* grad_w, float* grad_probs, cudaStream_t s);
@@ -171,6 +172,6 @@ cudaError_t launch_experts_backward(const uint16_t* grad_y, const uint16_t* x_di
                                     const uint16_t* h, const uint16_t* gu_save, const moe_layout& L,
                                     int H, int I, const uint16_t* W1, const uint16_t* W2,
                                     uint16_t* grad_x_disp, float* dW1, float* dW2, void* workspace,
-                                    cudaStream_t s);
+                                    cudaStream_t s, bool g_o_given = false);
 
 }  // namespace moe

@@ -74,7 +74,10 @@ struct LayoutArgs {
 //   memory -- later passes over it hit L1 -- and writes it to each of the
 //   token's rows (token_row).  Reading each token once matters when [T, H]
 //   no longer fits in L2: a per-row gather would fetch it K times from DRAM.
-//   With DOT it also forms grad_w[r] = <src[t], o_save[r]> in fp32.
+//   With DOT it also forms grad_w[r] = <src[t], o_save[r]> in fp32.  With
+//   SCALE the row gets bf16(row_weight[r] * src[t]) instead of src[t] (the
+//   combine's backward handing the experts dL/do = w dL/dy directly; the dot
+//   uses the unscaled src).
 //   Items [T, T + C) are rows: a pad or spare row is zeroed (and grad_w = 0).
 //   With META the row's validity comes from offsets / counts and the pad and
 //   spare rows get their metadata here (token -1, the sentinel expert, weight
@@ -82,7 +85,7 @@ struct LayoutArgs {
 // This is one warp's share: items first, first + stride, ...  With META,
 // s_off / s_cnt are the offsets and counts (shared memory, or global memory
 // this CTA wrote before a barrier).
-template <bool META, bool DOT>
+template <bool META, bool DOT, bool SCALE = false>
 __device__ __forceinline__ void scatter_items(
     long long first, long long stride, const uint16_t* __restrict__ src, int T, int K, int H, int E,
     long long C, const int* __restrict__ token_row, const int* s_off, const int* s_cnt,
@@ -107,6 +110,7 @@ __device__ __forceinline__ void scatter_items(
         if (r < 0 || r >= C) break;
         uint4* d = reinterpret_cast<uint4*>(dst + static_cast<long long>(r) * H);
         const uint4* o = DOT ? reinterpret_cast<const uint4*>(o_save + static_cast<long long>(r) * H) : nullptr;
+        const float w = SCALE ? __ldg(row_weight + r) : 0.f;
         float dot = 0.f;
         for (int v0 = 0; v0 < V; v0 += 8) {
           uint4 buf[8], ob[8];
@@ -120,7 +124,15 @@ __device__ __forceinline__ void scatter_items(
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             if (v0 + i < V) {
-              d[lane + 32 * (v0 + i)] = buf[i];
+              if (SCALE) {
+                const uint4 a = buf[i];
+                d[lane + 32 * (v0 + i)] = make_uint4(pack_bf16x2(w * bf16_lo(a.x), w * bf16_hi(a.x)),
+                                                     pack_bf16x2(w * bf16_lo(a.y), w * bf16_hi(a.y)),
+                                                     pack_bf16x2(w * bf16_lo(a.z), w * bf16_hi(a.z)),
+                                                     pack_bf16x2(w * bf16_lo(a.w), w * bf16_hi(a.w)));
+              } else {
+                d[lane + 32 * (v0 + i)] = buf[i];
+              }
               if (DOT) {
                 const uint32_t g[4] = {buf[i].x, buf[i].y, buf[i].z, buf[i].w};
                 const uint32_t q[4] = {ob[i].x, ob[i].y, ob[i].z, ob[i].w};
@@ -419,7 +431,7 @@ __global__ void __launch_bounds__(256) layout_kernel(LayoutArgs a) {
 
 // The scatter as a kernel: offsets and counts staged in shared memory, then
 // one warp per item over the grid.
-template <bool META, bool DOT>
+template <bool META, bool DOT, bool SCALE = false>
 __global__ void __launch_bounds__(256) row_scatter_kernel(
     const uint16_t* __restrict__ src, int T, int K, int H, int E, long long C,
     const int* __restrict__ token_row, const int* __restrict__ offsets,
@@ -436,7 +448,7 @@ __global__ void __launch_bounds__(256) row_scatter_kernel(
     for (int i = threadIdx.x; i < E; i += blockDim.x) s_cnt[i] = counts[i];
     __syncthreads();
   }
-  scatter_items<META, DOT>(static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5),
+  scatter_items<META, DOT, SCALE>(static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5),
                            static_cast<long long>(gridDim.x) * (blockDim.x >> 5), src, T, K, H, E, C,
                            token_row, s_off, s_cnt, row_token, row_expert, row_weight, dst, o_save,
                            grad_w);
@@ -553,7 +565,7 @@ cudaError_t launch_layout(const uint8_t* routing_map, const float* probs, const 
 
 cudaError_t launch_row_gather(const uint16_t* src, const moe_layout& L, int H, uint16_t* dst,
                               bool from_offsets, const uint16_t* o_save, float* grad_w,
-                              cudaStream_t s) {
+                              cudaStream_t s, bool scale) {
   const long long C = L.capacity;
   const long long items = static_cast<long long>(L.T) + C;
   if (items == 0) return cudaSuccess;
@@ -566,6 +578,14 @@ cudaError_t launch_row_gather(const uint16_t* src, const moe_layout& L, int H, u
                             H, L.E, C, L.token_row, L.offsets, L.tokens_per_expert, L.row_token,
                             L.row_expert, L.row_weight, dst, static_cast<const uint16_t*>(nullptr),
                             static_cast<float*>(nullptr));
+  } else if (grad_w && scale) {
+    row_scatter_kernel<false, true, true><<<blocks, threads, 0, s>>>(
+        src, L.T, L.K, H, L.E, C, L.token_row, nullptr, nullptr, L.row_token, nullptr, L.row_weight,
+        dst, o_save, grad_w);
+  } else if (scale) {
+    row_scatter_kernel<false, false, true><<<blocks, threads, 0, s>>>(
+        src, L.T, L.K, H, L.E, C, L.token_row, nullptr, nullptr, L.row_token, nullptr, L.row_weight,
+        dst, nullptr, nullptr);
   } else if (grad_w) {
     row_scatter_kernel<false, true><<<blocks, threads, 0, s>>>(
         src, L.T, L.K, H, L.E, C, L.token_row, nullptr, nullptr, L.row_token, nullptr, nullptr,

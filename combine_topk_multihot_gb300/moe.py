@@ -298,14 +298,17 @@ def moe_combine(y_disp: torch.Tensor, layout: Layout, out: Optional[torch.Tensor
 
 
 def moe_combine_backward(grad_out: torch.Tensor, layout: Layout, o_save: Optional[torch.Tensor] = None,
-                         stream=None):
-    """a7 (+a8 when o_save is given): returns (grad_y [C, H], grad_w [C] or None)."""
+                         stream=None, scaled: bool = False):
+    """a7 (+a8 when o_save is given): returns (grad_y [C, H], grad_w [C] or None).
+    With ``scaled`` (moe_combine_backward_scaled) the rows are G_o = bf16(w * grad_y)
+    instead, for moe_grouped_experts_backward(..., scaled=True)."""
     H = grad_out.shape[1]
     grad_y = torch.empty(layout.capacity, H, dtype=torch.bfloat16, device=grad_out.device)
     grad_w = (torch.empty(layout.capacity, dtype=torch.float32, device=grad_out.device)
               if o_save is not None else None)
-    _check(N.lib.moe_combine_backward(_ptr(grad_out), _ptr(o_save), layout.ref, H, _ptr(grad_y),
-                                      _ptr(grad_w), _stream(stream)), "moe_combine_backward")
+    fn = N.lib.moe_combine_backward_scaled if scaled else N.lib.moe_combine_backward
+    _check(fn(_ptr(grad_out), _ptr(o_save), layout.ref, H, _ptr(grad_y), _ptr(grad_w), _stream(stream)),
+           "moe_combine_backward_scaled" if scaled else "moe_combine_backward")
     return grad_y, grad_w
 
 
@@ -336,10 +339,13 @@ def moe_route_to_multihot_backward(grad_probs: torch.Tensor, topk_idx: torch.Ten
 
 def moe_grouped_experts_backward(grad_y: torch.Tensor, x_disp: torch.Tensor, h: torch.Tensor,
                                  gu_save: torch.Tensor, layout: Layout, W1: torch.Tensor,
-                                 W2: torch.Tensor, stream=None, return_operands: bool = False):
+                                 W2: torch.Tensor, stream=None, return_operands: bool = False,
+                                 scaled: bool = False):
     """a9: returns (grad_x_disp [C, H] bf16, dW1 [E, 2I, H] fp32, dW2 [E, H, I] fp32),
     plus, with return_operands, views of the workspace's G_o [C, H] and
-    [G_g | G_u] [C, 2I] (bf16, valid rows)."""
+    [G_g | G_u] [C, 2I] (bf16, valid rows).  With ``scaled``
+    (moe_grouped_experts_backward_scaled) ``grad_y`` is G_o from
+    moe_combine_backward(..., scaled=True), and the G_o returned is ``grad_y``."""
     E, twoI, H = W1.shape
     I = twoI // 2
     dev = grad_y.device
@@ -350,17 +356,17 @@ def moe_grouped_experts_backward(grad_y: torch.Tensor, x_disp: torch.Tensor, h: 
     grad_x_disp = torch.empty(layout.capacity, H, dtype=torch.bfloat16, device=dev)
     dW1 = torch.empty(E, 2 * I, H, dtype=torch.float32, device=dev)
     dW2 = torch.empty(E, H, I, dtype=torch.float32, device=dev)
-    _check(N.lib.moe_grouped_experts_backward(_ptr(grad_y), _ptr(x_disp), _ptr(h), _ptr(gu_save),
-                                              layout.ref, H, I, _ptr(W1), _ptr(W2), _ptr(grad_x_disp),
-                                              _ptr(dW1), _ptr(dW2), _ptr(ws), _stream(stream)),
-           "moe_grouped_experts_backward")
+    fn = N.lib.moe_grouped_experts_backward_scaled if scaled else N.lib.moe_grouped_experts_backward
+    _check(fn(_ptr(grad_y), _ptr(x_disp), _ptr(h), _ptr(gu_save), layout.ref, H, I, _ptr(W1), _ptr(W2),
+              _ptr(grad_x_disp), _ptr(dW1), _ptr(dW2), _ptr(ws), _stream(stream)),
+           "moe_grouped_experts_backward_scaled" if scaled else "moe_grouped_experts_backward")
     if not return_operands:
         return grad_x_disp, dW1, dW2
     C = layout.capacity
     base = (-ws.data_ptr()) % 256
     go_bytes = C * H * 2
     gu_off = base + (go_bytes + 255) // 256 * 256
-    G_o = ws[base:base + go_bytes].view(torch.bfloat16).view(C, H)
+    G_o = grad_y if scaled else ws[base:base + go_bytes].view(torch.bfloat16).view(C, H)
     G_gu = ws[gu_off:gu_off + C * 2 * I * 2].view(torch.bfloat16).view(C, 2 * I)
     return grad_x_disp, dW1, dW2, G_o, G_gu
 

@@ -171,10 +171,11 @@ def _(y, lay, T, top_k, pad_multiple, num_experts):
 @torch.library.custom_op(f"{NS}::combine_backward", mutates_args=(), device_types="cuda")
 def combine_backward(grad_out: Tensor, o_save: Tensor, lay: List[Tensor], T: int, top_k: int,
                      pad_multiple: int, num_experts: int) -> Tuple[Tensor, Tensor]:
-    """(grad_y [C, H], grad_w fp32 [C]): grad_out sent along the forward's
-    layout, and each row's routing-weight gradient."""
+    """(G_o [C, H], grad_w fp32 [C]): grad_out sent along the forward's layout
+    with each row's routing weight applied (G_o = w * grad_y, the gradient of
+    the experts' pre-weight output), and each row's routing-weight gradient."""
     L = _layout(T, num_experts, top_k, pad_multiple, lay)
-    return _m.moe_combine_backward(grad_out.contiguous(), L, o_save=o_save)
+    return _m.moe_combine_backward(grad_out.contiguous(), L, o_save=o_save, scaled=True)
 
 
 @combine_backward.register_fake
@@ -185,17 +186,18 @@ def _(grad_out, o_save, lay, T, top_k, pad_multiple, num_experts):
 
 
 @torch.library.custom_op(f"{NS}::experts_backward", mutates_args=(), device_types="cuda")
-def experts_backward(grad_y: Tensor, x_disp: Tensor, h: Tensor, gu_save: Tensor, W1: Tensor,
+def experts_backward(g_o: Tensor, x_disp: Tensor, h: Tensor, gu_save: Tensor, W1: Tensor,
                      W2: Tensor, lay: List[Tensor], T: int, top_k: int,
                      pad_multiple: int) -> Tuple[Tensor, Tensor, Tensor]:
-    """(grad_x_disp [C, H] bf16, dW1 fp32 [E, 2I, H], dW2 fp32 [E, H, I])."""
+    """(grad_x_disp [C, H] bf16, dW1 fp32 [E, 2I, H], dW2 fp32 [E, H, I]) from
+    combine_backward's G_o."""
     L = _layout(T, W1.shape[0], top_k, pad_multiple, lay)
-    return _m.moe_grouped_experts_backward(grad_y, x_disp, h, gu_save, L, W1.contiguous(),
-                                           W2.contiguous())
+    return _m.moe_grouped_experts_backward(g_o, x_disp, h, gu_save, L, W1.contiguous(),
+                                           W2.contiguous(), scaled=True)
 
 
 @experts_backward.register_fake
-def _(grad_y, x_disp, h, gu_save, W1, W2, lay, T, top_k, pad_multiple):
+def _(g_o, x_disp, h, gu_save, W1, W2, lay, T, top_k, pad_multiple):
     return (x_disp.new_empty(x_disp.shape),
             torch.empty(W1.shape, dtype=torch.float32, device=W1.device),
             torch.empty(W2.shape, dtype=torch.float32, device=W2.device))
@@ -257,8 +259,8 @@ class MoELayerFunction(torch.autograd.Function):
     def backward(ctx, grad_out, _grad_status):
         topk_idx, win, x_disp, h, o, gu, W1, W2, *lay = ctx.saved_tensors
         T, K, E, P = ctx.meta
-        grad_y, grad_w = _ops.combine_backward(grad_out, o, lay, T, K, P, E)
-        gxd, dW1, dW2 = _ops.experts_backward(grad_y, x_disp, h, gu, W1, W2, lay, T, K, P)
+        g_o, grad_w = _ops.combine_backward(grad_out, o, lay, T, K, P, E)
+        gxd, dW1, dW2 = _ops.experts_backward(g_o, x_disp, h, gu, W1, W2, lay, T, K, P)
         grad_x, grad_probs = _ops.dispatch_backward(gxd, grad_w, lay, T, K, P, E)
         grad_topk = _ops.route_to_multihot_backward(grad_probs, topk_idx, win)
         return grad_x, None, grad_topk, dW1.to(W1.dtype), dW2.to(W2.dtype), None

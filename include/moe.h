@@ -378,6 +378,21 @@ MOE_API moe_status moe_combine_backward(const moe_bf16* grad_out, const moe_bf16
                                 moe_bf16* grad_y, float* grad_w, moe_stream_t stream);
 
 /*
+ * a7 + a8 with the routing weight applied: as moe_combine_backward, but each
+ * valid row receives G_o[r] = bf16(row_weight[r] * grad_out[row_token[r]])
+ * -- the gradient with respect to the experts' pre-weight output o, since
+ * y = w_r * o ([DEP] Expanded layout: the experts apply the weights;
+ * Training) -- instead of grad_y; pad and spare rows are zero.  grad_w is
+ * still the dot of the unscaled gradient with o_save, as in
+ * moe_combine_backward.  Feed G_o to moe_grouped_experts_backward_scaled,
+ * which then skips its own scaling pass (one read and one write of [C, H]
+ * fewer).  Arguments and errors as in moe_combine_backward.
+ */
+MOE_API moe_status moe_combine_backward_scaled(const moe_bf16* grad_out, const moe_bf16* o_save,
+                                               const moe_layout* L, int32_t H, moe_bf16* g_o,
+                                               float* grad_w, moe_stream_t stream);
+
+/*
  * a10 + the weight-gradient scatter.  [DEP] Training (both the tokens and
  * the routing weights receive gradients).
  *   grad_x_disp [C, H] bf16: dL/d x_disp.
@@ -436,6 +451,20 @@ MOE_API moe_status moe_grouped_experts_backward(const moe_bf16* grad_y, const mo
                                                 const moe_bf16* W1, const moe_bf16* W2,
                                                 moe_bf16* grad_x_disp, float* dW1, float* dW2,
                                                 void* workspace, moe_stream_t stream);
+
+/*
+ * a9 from G_o: moe_grouped_experts_backward with g_o [C, H] bf16 (written by
+ * moe_combine_backward_scaled) in place of grad_y; the routing weight is
+ * already applied, so no scaling pass runs and the workspace's G_o region is
+ * not written.  Arguments, outputs and errors otherwise as in
+ * moe_grouped_experts_backward.
+ */
+MOE_API moe_status moe_grouped_experts_backward_scaled(const moe_bf16* g_o, const moe_bf16* x_disp,
+                                                       const moe_bf16* h, const moe_bf16* gu_save,
+                                                       const moe_layout* L, int32_t H, int32_t I,
+                                                       const moe_bf16* W1, const moe_bf16* W2,
+                                                       moe_bf16* grad_x_disp, float* dW1, float* dW2,
+                                                       void* workspace, moe_stream_t stream);
 
 /*
  * Failure-detection self-test.  Runs one CTA whose wait on an mbarrier can

@@ -165,3 +165,35 @@ def test_expert_backward_full_size_h4096_sampled(moe):
     re = L.row_expert.cpu().numpy()
     rows = np.sort(np.random.default_rng(1).choice(np.flatnonzero(rt >= 0), 512, replace=False))
     _check_rows_dx(rows, re, fwd.x_disp, fwd.h, grad_y, rw, W1, W2, I, gxd)
+
+
+@pytest.mark.parametrize("T,H,E,K,I,P", [
+    (300, 512, 8, 2, 256, 16),      # 256-column tiles (CTA pairs) in dgrad, single CTAs in wgrad
+    (2000, 512, 40, 4, 512, 128),   # CTA pairs in every GEMM (P % 64 == 0)
+    (64, 256, 8, 2, 128, 16),       # 128-column tiles
+])
+def test_scaled_backward_equals_unscaled(moe, T, H, E, K, I, P):
+    """moe_combine_backward_scaled + moe_grouped_experts_backward_scaled (the
+    routing weight applied in the combine backward's scatter) give bit for
+    bit what moe_combine_backward + moe_grouped_experts_backward give: G_o is
+    bf16(w * grad_out) in both, computed from the same values."""
+    idx, p = random_routing(T, E, K, seed=T + E, drop=0.1)
+    gen = torch.Generator().manual_seed(T)
+    x = torch.randn(T, H, generator=gen).to(torch.bfloat16).to(DEV)
+    W1 = (torch.randn(E, 2 * I, H, generator=gen) * 0.02).to(torch.bfloat16).to(DEV)
+    W2 = (torch.randn(E, H, I, generator=gen) * 0.02).to(torch.bfloat16).to(DEV)
+    g = torch.randn(T, H, generator=gen).to(torch.bfloat16).to(DEV)
+    fwd = moe.moe_layer_forward(x, idx.to(DEV), p.to(DEV), W1, W2, P, host_sync=False, save_for_backward=True)
+    gy, gw = moe.moe_combine_backward(g, fwd.layout, o_save=fwd.o)
+    a = moe.moe_grouped_experts_backward(gy, fwd.x_disp, fwd.h, fwd.gu, fwd.layout, W1, W2, return_operands=True)
+    go, gw2 = moe.moe_combine_backward(g, fwd.layout, o_save=fwd.o, scaled=True)
+    b = moe.moe_grouped_experts_backward(go, fwd.x_disp, fwd.h, fwd.gu, fwd.layout, W1, W2, return_operands=True,
+                                         scaled=True)
+    torch.cuda.synchronize()
+    assert int(fwd.layout.status.item()) == 0
+    valid = fwd.layout.row_token >= 0
+    assert torch.equal(gw, gw2)
+    assert torch.equal(a[3][valid].view(torch.int16), go[valid].view(torch.int16))   # G_o
+    assert not go[~valid].any()                                                       # pad / spare rows zero
+    assert torch.equal(a[0][valid].view(torch.int16), b[0][valid].view(torch.int16))  # grad_x_disp
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])                        # dW1, dW2
