@@ -15,7 +15,6 @@ if not os.path.exists(_LIB_PATH):
         f"the CUDA library {_LIB_PATH} is not built; run "
         "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc)")
 
-lib = ctypes.CDLL(_LIB_PATH)
 
 c_int32 = ctypes.c_int32
 c_int64 = ctypes.c_int64
@@ -34,6 +33,8 @@ MOE_ERR_CUDA = 7
 MOE_DEVERR_BAD_INDEX = 1
 MOE_DEVERR_CAPACITY = 2
 MOE_DEVERR_TIMEOUT = 4
+MOE_DEVERR_BOUNDS = 8
+MOE_BUILD_BOUNDS_CHECKS = 1
 MOE_STATIC_SCRATCH_INTS = 262144
 
 
@@ -56,6 +57,7 @@ SIGNATURES = {
     "moe_status_string": (ctypes.c_char_p, [c_int32]),
     "moe_last_error": (ctypes.c_char_p, []),
     "moe_device_check": (c_int32, []),
+    "moe_build_flags": (ctypes.c_uint32, []),
     "moe_worst_case_rows": (c_int64, [c_int32, c_int32, c_int32, c_int32]),
     "moe_layout_workspace_bytes": (c_int32, [c_int32, c_int32, ctypes.POINTER(c_size_t)]),
     "moe_router_topk": (c_int32, [_P, c_int32, c_int32, c_int32, _P, _P, _P, _P, _P, _P]),
@@ -82,10 +84,18 @@ SIGNATURES = {
     "moe_route_to_multihot_backward": (c_int32, [_P, _P, _P, c_int32, c_int32, c_int32, _P, _P]),
 }
 
-for _name, (_res, _args) in SIGNATURES.items():
-    _fn = getattr(lib, _name)
-    _fn.restype = _res
-    _fn.argtypes = _args
+def load(path: str) -> ctypes.CDLL:
+    """Opens a copy of the library (the normal build, or the bounds-checked
+    libmoe_bounds.so) with the ABI's signatures attached."""
+    handle = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(handle, name)
+        fn.restype = res
+        fn.argtypes = args
+    return handle
+
+
+lib = load(_LIB_PATH)
 
 
 def status_string(code: int) -> str:

@@ -41,23 +41,39 @@ def _deps():
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+# Library variants: the normal one, and "bounds", compiled with MOE_DEBUG_BOUNDS
+# (device-side checks of layout-derived indices, reported as MOE_DEVERR_BOUNDS;
+# a debugging aid, not the product path).
+VARIANTS = {"": ("libmoe.so", OUT, ()), "bounds": ("libmoe_bounds.so", os.path.join(OUT, "bounds"),
+                                                   ("-DMOE_DEBUG_BOUNDS",))}
+
+
+def library_path(variant: str = "") -> str:
+    name, _, _ = VARIANTS[variant]
+    return os.path.join(OUT, name)
+
+
+def up_to_date(variant: str = "") -> bool:
+    lib = library_path(variant)
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile (if needed) and return the path of libmoe.so."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(OUT, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), variant: str = "") -> str:
+    """Compile (if needed) and return the path of the library (libmoe.so, or
+    with variant="bounds" the bounds-checked libmoe_bounds.so)."""
+    lib_path = library_path(variant)
+    _, obj_dir, variant_flags = VARIANTS[variant]
+    if not force and up_to_date(variant):
+        return lib_path
+    os.makedirs(obj_dir, exist_ok=True)
     nvcc = _nvcc()
     jobs = []
     for src in _sources():
-        obj = os.path.join(OUT, os.path.basename(src)[:-3] + ".o")
-        jobs.append((src, obj, [nvcc, *CFLAGS, *extra_flags, "-c", src, "-o", obj]))
+        obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
+        jobs.append((src, obj, [nvcc, *CFLAGS, *variant_flags, *extra_flags, "-c", src, "-o", obj]))
 
     def run(job):
         src, obj, cmd = job
@@ -74,13 +90,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         for log in logs:
             if log.strip():
                 print(log, file=sys.stderr)
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *[j[1] for j in jobs], "-cudart", "static"]
     p = subprocess.run(cmd, capture_output=True, text=True)
     if p.returncode != 0:
         raise RuntimeError(f"link failed:\n{p.stdout}\n{p.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

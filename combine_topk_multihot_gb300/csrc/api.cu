@@ -168,6 +168,14 @@ const char* moe_last_error(void) { return g_last_error; }
 
 moe_status moe_device_check(void) { return check_device(); }
 
+uint32_t moe_build_flags(void) {
+#ifdef MOE_DEBUG_BOUNDS
+  return MOE_BUILD_BOUNDS_CHECKS;
+#else
+  return 0u;
+#endif
+}
+
 int64_t moe_worst_case_rows(int32_t T, int32_t E, int32_t K, int32_t pad_multiple) {
   if (T < 0 || E < 1 || K < 1 || pad_multiple < 1) return -1;
   return static_cast<int64_t>(T) * K + static_cast<int64_t>(E) * (pad_multiple - 1);

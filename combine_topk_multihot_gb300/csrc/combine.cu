@@ -47,7 +47,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
                                                       int K, int H, uint16_t* __restrict__ out,
                                                       const int* __restrict__ row_expert,
                                                       const float* __restrict__ grad_w,
-                                                      float* __restrict__ grad_probs, int E) {
+                                                      float* __restrict__ grad_probs, int E,
+                                                      long long C, int* status) {
   griddep_launch_dependents();
   griddep_wait();
   const int lane = threadIdx.x & 31;
@@ -64,6 +65,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
     for (int jj = 0; jj < 4; ++jj) {
       const int k = lane + 32 * jj;
       tr[jj] = k < K ? __ldg(token_row + t * K + k) : -1;
+      if (!MOE_IN_BOUNDS(tr[jj] < C, status)) tr[jj] = -1;
       n += __popc(__ballot_sync(FULL_MASK, tr[jj] >= 0));
     }
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -89,7 +91,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
         const int r = tr[jj];
-        if (r >= 0) gp[row_expert[r]] = grad_w ? grad_w[r] : 0.f;
+        if (r >= 0 && MOE_IN_BOUNDS(row_expert[r] >= 0 && row_expert[r] < E, status))
+          gp[row_expert[r]] = grad_w ? grad_w[r] : 0.f;
       }
     }
   }
@@ -106,11 +109,12 @@ cudaError_t launch_combine(const uint16_t* rows, const moe_layout& L, int H, uin
   const int blocks = static_cast<int>(need < 8LL * sm_count() ? need : 8LL * sm_count());
   if (grad_probs) {
     combine_kernel<true><<<blocks, threads, 0, s>>>(rows, L.token_row, L.T, L.K, H, out,
-                                                    L.row_expert, grad_w, grad_probs, L.E);
+                                                    L.row_expert, grad_w, grad_probs, L.E,
+                                                    static_cast<long long>(L.capacity), L.status);
   } else {
     return launch_dependent(combine_kernel<false>, blocks, threads, 0, s, rows, L.token_row, L.T, L.K,
                             H, out, static_cast<const int*>(nullptr), static_cast<const float*>(nullptr),
-                            static_cast<float*>(nullptr), L.E);
+                            static_cast<float*>(nullptr), L.E, static_cast<long long>(L.capacity), L.status);
   }
   return cudaGetLastError();
 }

@@ -38,6 +38,26 @@ __device__ __forceinline__ void report(int* status, int bits) {
   if (status) atomicOr(status, bits);
 }
 
+// Device-side bounds checks, compiled in only by a build with
+// MOE_DEBUG_BOUNDS (the library variant libmoe_bounds.so): an index a kernel
+// derived from the layout (a row from token_row or from the placement, an
+// expert) is checked against its buffer before the access; a failed check
+// skips the access and ORs MOE_DEVERR_BOUNDS into the status word.  In the
+// normal build MOE_IN_BOUNDS(...) is the constant true and the checks cost
+// nothing.  The checks sit in the dispatch, the row scatters and the combine;
+// the tensor-core kernels carry none (their rows come from the offsets, and a
+// data-dependent branch beside their warp-collective tcgen05 instructions is
+// kept out of them), so their code is the same in both builds.
+__device__ __forceinline__ bool bounds_ok(bool ok, int* status) {
+  if (!ok) report(status, MOE_DEVERR_BOUNDS);
+  return ok;
+}
+#ifdef MOE_DEBUG_BOUNDS
+#define MOE_IN_BOUNDS(cond, status) (::moe::bounds_ok((cond), (status)))
+#else
+#define MOE_IN_BOUNDS(cond, status) true
+#endif
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(FD_THREADS, 4) dispatch_fused_kernel(FusedArgs
               const int r = pair_row(a, s_off, t, e);
               rows[j] = r;
               a.token_row[t * K + j] = r;
-              if (r < C) {
+              if (MOE_IN_BOUNDS(r >= 0 && r < C, a.status) && r < C) {
                 a.row_token[r] = static_cast<int>(t);
                 a.row_expert[r] = e;
                 a.row_weight[r] = __ldg(a.probs + t * E + e);
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(FD_THREADS, 4) dispatch_fused_kernel(FusedArgs
             const int r = pair_row(a, s_off, t, ek[j]);
             rows[rank[j]] = r;
             a.token_row[t * K + rank[j]] = r;
-            if (r < C) {
+            if (MOE_IN_BOUNDS(r >= 0 && r < C && rank[j] < K, a.status) && r < C) {
               a.row_token[r] = static_cast<int>(t);
               a.row_expert[r] = ek[j];
               a.row_weight[r] = pk[j];
@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(FD_THREADS, 4) dispatch_fused_kernel(FusedArgs
       } else {
         r = R + (p - pad_total);
       }
-      if (r >= C || lane != 0) continue;
+      if (lane != 0 || !MOE_IN_BOUNDS(r >= 0 && r < C, a.status) || r >= C) continue;
       a.row_token[r] = -1;
       a.row_expert[r] = E;
       a.row_weight[r] = 0.f;

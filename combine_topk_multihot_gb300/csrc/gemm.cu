@@ -426,7 +426,11 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
       const Tile t = decode_tile(s_pre, E, args.n_tiles, tile);
       const int buf = local & 1;
       const uint32_t use = (local >> 1) & 1;
-      if (!mbar_wait(smem_u32(&s.tfull[buf]), use, abort_flag)) break;
+      // every lane waits, then the warp leaves together if any lane's wait ran
+      // out: lanes leaving one by one would strand the others at the
+      // warp-wide instructions below
+      const bool ready = mbar_wait(smem_u32(&s.tfull[buf]), use, abort_flag);
+      if (!__all_sync(FULL_MASK, ready)) break;
       tc_fence_after();
       const int group_row = t.mt * RB + static_cast<int>(rank) * BM + r_in_tile;
       // rows written: the valid rows, plus (write_pad) the pad rows of the

@@ -69,6 +69,7 @@ struct BwdArgs {
   float* out_f32;            // K-grouped: [E, m_total, n_total]
   int zero_tail;             // K-grouped: zero the K lines past an expert's count
   int* status;
+  long long capacity;        // rows of the row buffers (bounds-checked builds)
 };
 
 // Barriers and scalars; the per-expert tables (offsets [E+1], counts [E],
@@ -382,7 +383,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const Tile t = decode(s_pre, E, args.n_tiles, tile);
       const int buf = local & 1;
       const uint32_t use = (local >> 1) & 1;
-      if (!mbar_wait(smem_u32(&s.tfull[buf]), use, abort_flag)) break;
+      // every lane waits, then the warp leaves together if any lane's wait ran out
+      const bool ready = mbar_wait(smem_u32(&s.tfull[buf]), use, abort_flag);
+      if (!__all_sync(FULL_MASK, ready)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
       if (GROUP_K) {
@@ -644,6 +647,7 @@ cudaError_t launch_experts_backward(const uint16_t* grad_y, const uint16_t* x_di
   const long long pairs_rows = static_cast<long long>(L.T) * L.K;
   const bool pair = (pairs_rows < E ? pairs_rows : E) * (I / 128) >= sm_count();
   BwdArgs base{};
+  base.capacity = C;
   base.counts = L.tokens_per_expert;
   base.offsets = L.offsets;
   base.E = E;

@@ -90,7 +90,8 @@ __device__ __forceinline__ void scatter_items(
     long long first, long long stride, const uint16_t* __restrict__ src, int T, int K, int H, int E,
     long long C, const int* __restrict__ token_row, const int* s_off, const int* s_cnt,
     int* __restrict__ row_token, int* __restrict__ row_expert, float* __restrict__ row_weight,
-    uint16_t* __restrict__ dst, const uint16_t* __restrict__ o_save, float* __restrict__ grad_w) {
+    uint16_t* __restrict__ dst, const uint16_t* __restrict__ o_save, float* __restrict__ grad_w,
+    int* status = nullptr) {
   const int lane = threadIdx.x & 31;
   const int V = H >> 8;  // 16-byte vectors per lane
   const long long items = T + C;
@@ -107,7 +108,7 @@ __device__ __forceinline__ void scatter_items(
         // (L2 load: the layout kernel itself may have just written token_row)
         if ((j & 31) == 0) r_lane = j + lane < K ? __ldcg(token_row + t * K + j + lane) : -1;
         const int r = __shfl_sync(FULL_MASK, r_lane, j & 31);
-        if (r < 0 || r >= C) break;
+        if (r < 0 || !MOE_IN_BOUNDS(r < C, status) || r >= C) break;
         uint4* d = reinterpret_cast<uint4*>(dst + static_cast<long long>(r) * H);
         const uint4* o = DOT ? reinterpret_cast<const uint4*>(o_save + static_cast<long long>(r) * H) : nullptr;
         const float w = SCALE ? __ldg(row_weight + r) : 0.f;
@@ -424,7 +425,7 @@ __global__ void __launch_bounds__(256) layout_kernel(LayoutArgs a) {
       // this CTA wrote
       scatter_items<true, false>(warp, nwarps, a.x, static_cast<int>(a.T), a.K, a.H, E, a.capacity,
                                  a.token_row, s_off, a.tokens_per_expert, a.row_token, a.row_expert,
-                                 a.row_weight, a.x_disp, nullptr, nullptr);
+                                 a.row_weight, a.x_disp, nullptr, nullptr, a.status);
     }
   }
 }
@@ -437,7 +438,7 @@ __global__ void __launch_bounds__(256) row_scatter_kernel(
     const int* __restrict__ token_row, const int* __restrict__ offsets,
     const int* __restrict__ counts, int* __restrict__ row_token, int* __restrict__ row_expert,
     float* __restrict__ row_weight, uint16_t* __restrict__ dst, const uint16_t* __restrict__ o_save,
-    float* __restrict__ grad_w) {
+    float* __restrict__ grad_w, int* status) {
   griddep_launch_dependents();
   griddep_wait();
   extern __shared__ int s_meta[];  // META: offsets [E+1], counts [E]
@@ -451,7 +452,7 @@ __global__ void __launch_bounds__(256) row_scatter_kernel(
   scatter_items<META, DOT, SCALE>(static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5),
                            static_cast<long long>(gridDim.x) * (blockDim.x >> 5), src, T, K, H, E, C,
                            token_row, s_off, s_cnt, row_token, row_expert, row_weight, dst, o_save,
-                           grad_w);
+                           grad_w, status);
 }
 
 }  // namespace
@@ -577,23 +578,23 @@ cudaError_t launch_row_gather(const uint16_t* src, const moe_layout& L, int H, u
     return launch_dependent(row_scatter_kernel<true, false>, blocks, threads, smem, s, src, L.T, L.K,
                             H, L.E, C, L.token_row, L.offsets, L.tokens_per_expert, L.row_token,
                             L.row_expert, L.row_weight, dst, static_cast<const uint16_t*>(nullptr),
-                            static_cast<float*>(nullptr));
+                            static_cast<float*>(nullptr), L.status);
   } else if (grad_w && scale) {
     row_scatter_kernel<false, true, true><<<blocks, threads, 0, s>>>(
         src, L.T, L.K, H, L.E, C, L.token_row, nullptr, nullptr, L.row_token, nullptr, L.row_weight,
-        dst, o_save, grad_w);
+        dst, o_save, grad_w, L.status);
   } else if (scale) {
     row_scatter_kernel<false, false, true><<<blocks, threads, 0, s>>>(
         src, L.T, L.K, H, L.E, C, L.token_row, nullptr, nullptr, L.row_token, nullptr, L.row_weight,
-        dst, nullptr, nullptr);
+        dst, nullptr, nullptr, L.status);
   } else if (grad_w) {
     row_scatter_kernel<false, true><<<blocks, threads, 0, s>>>(
         src, L.T, L.K, H, L.E, C, L.token_row, nullptr, nullptr, L.row_token, nullptr, nullptr,
-        dst, o_save, grad_w);
+        dst, o_save, grad_w, L.status);
   } else {
     row_scatter_kernel<false, false><<<blocks, threads, 0, s>>>(
         src, L.T, L.K, H, L.E, C, L.token_row, nullptr, nullptr, L.row_token, nullptr, nullptr,
-        dst, nullptr, nullptr);
+        dst, nullptr, nullptr, L.status);
   }
   return cudaGetLastError();
 }

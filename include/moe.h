@@ -82,6 +82,10 @@ typedef enum moe_status {
 #define MOE_DEVERR_BAD_INDEX 1
 #define MOE_DEVERR_CAPACITY  2
 #define MOE_DEVERR_TIMEOUT   4
+/* Set only by the bounds-checked build of the library (moe_build_flags() has
+ * MOE_BUILD_BOUNDS_CHECKS): a kernel found an index it derived from the
+ * layout outside its buffer and skipped the access. */
+#define MOE_DEVERR_BOUNDS    8
 
 /* Name of a status code (static string). */
 MOE_API const char* moe_status_string(moe_status status);
@@ -91,6 +95,13 @@ MOE_API const char* moe_last_error(void);
 
 /* MOE_OK if the current CUDA device is compute capability 10.3, else MOE_ERR_DEVICE. */
 MOE_API moe_status moe_device_check(void);
+
+/* How this copy of the library was built: MOE_BUILD_BOUNDS_CHECKS when its
+ * kernels check the indices they derive from the layout against their
+ * buffers (the debugging build, compiled with MOE_DEBUG_BOUNDS; results are
+ * the same as the normal build's, MOE_DEVERR_BOUNDS flags a failed check). */
+#define MOE_BUILD_BOUNDS_CHECKS 1u
+MOE_API uint32_t moe_build_flags(void);
 
 /* Rows a sync-free buffer needs so that no routing can overflow it:
  * T*K (every slot valid) + E*(pad_multiple-1) (every group padded).
