@@ -50,6 +50,9 @@ CONFIGS = {
     "qwen3_30b_a3b_16k": LayerConfig("qwen3_30b_a3b_16k", T=16384, H=2048, E=128, K=8, I=768, P=128, seed=1),
     "h4096": LayerConfig("h4096", T=16384, H=4096, E=128, K=8, I=1536, P=128, seed=2, backward=True),
     "skewed": LayerConfig("skewed", T=16384, H=2048, E=128, K=8, I=768, P=128, seed=3, zipf_s=1.2, drop=0.05),
+    # the h4096 expert shape (about 1024 rows per expert) on 16 experts: a few
+    # GB on the device, small enough for detailed profiler captures
+    "h4096_small": LayerConfig("h4096_small", T=2048, H=4096, E=16, K=8, I=1536, P=128, seed=2, backward=True),
     "decode_1": LayerConfig("decode_1", T=1, H=2048, E=128, K=8, I=768, P=1, seed=5, sync_free=True),
     "decode_256": LayerConfig("decode_256", T=256, H=2048, E=128, K=8, I=768, P=1, seed=260, sync_free=True),
     "decode_1024": LayerConfig("decode_1024", T=1024, H=2048, E=128, K=8, I=768, P=1, seed=1028, sync_free=True),
