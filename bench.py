@@ -45,8 +45,8 @@ PROFILED_TRAFFIC = {
     "qwen3_30b_a3b": {"src": "33c16159a3a133ca", "bytes": (986.011904 + 47.470080 + 465.243904 + 113.445888) * 1e6,
                       "profile": "profiles/experts_gemm_qwen3_30b_a3b_T4096.md"},
 }
-GEMM_SOURCES = ("combine_topk_multihot_gb300/csrc/gemm.cu", "combine_topk_multihot_gb300/csrc/common.cuh",
-                "combine_topk_multihot_gb300/csrc/tma.cu")
+GEMM_SOURCES = ("combine_topk_multihot_gb300/csrc/gemm.cu", "combine_topk_multihot_gb300/csrc/gemm_pair.cu",
+                "combine_topk_multihot_gb300/csrc/common.cuh", "combine_topk_multihot_gb300/csrc/tma.cu")
 
 
 def profiled_traffic(workload: str):
@@ -174,6 +174,26 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- algorithmic work
+
+def experts_kernel_label(cfg, fp8: bool, gather: bool, backward: bool) -> str:
+    """Which expert GEMM kernels a bench step runs, as the library picks them
+    for layers with rows for every SM: bf16 layers that save for the backward,
+    or average at most 384 rows per expert, take pair_gemm_kernel (CTA pairs,
+    expert rows on the MMA's N side); other bf16 layers the CTA-pair form of
+    grouped_gemm_kernel; e4m3 operands and the gathered A its one-CTA form."""
+    wide = min(cfg.T * cfg.K, cfg.E) * (cfg.I // 128) >= 152
+    if cfg.T <= 4 and not backward and not fp8:
+        fwd = "experts: gemv_experts_kernel<1> (gate/up + SwiGLU) + gemv_experts_kernel<2> (down x weight), CUDA cores"
+    elif fp8 or gather or not wide:
+        fwd = ("experts: grouped_gemm_kernel<0> (gate/up + SwiGLU" + (", e4m3 operands" if fp8 else "")
+               + (", A gathered" if gather else "") + ("" if wide else ", 64-column tiles")
+               + ") + grouped_gemm_kernel<1> (down x weight)")
+    elif backward or cfg.T * cfg.K <= 384 * cfg.E:
+        fwd = "experts: pair_gemm_kernel<0> (gate/up + SwiGLU) + pair_gemm_kernel<1> (down x weight)"
+    else:
+        fwd = "experts: grouped_gemm_kernel<0> (gate/up + SwiGLU, CTA pairs) + grouped_gemm_kernel<1> (down x weight)"
+    return fwd + (" + the backward's 4 bwd_gemm_kernel launches" if backward else "")
+
 
 def step_launches(T: int, H: int, E: int, C: int, fp8: bool, gather: bool, backward: bool) -> int:
     """Our kernel launches in one step (the dispatch's barrier-counter memset is
@@ -620,9 +640,7 @@ def run_ours(args, world, rank, local, leg: bool = False):
                               "dram__bytes_write.sum of the two launches; reported while the kernel "
                               "sources still hash to the profiled ones)") if roof["traffic"] else None
     roof["algorithmic_bytes"] = ex_bytes
-    roof["kernel"] = ("experts: grouped_gemm_kernel<0> (gate/up + SwiGLU" + (", e4m3 operands" if fp8 else "")
-                      + ") + grouped_gemm_kernel<1> (down x weight)"
-                      + (" + the backward's 4 bwd_gemm_kernel launches" if bwd else ""))
+    roof["kernel"] = experts_kernel_label(cfg, fp8, gather, bwd)
     roof["peak_source"] = src
     roof["tensor_frac_of_burst"] = ex_flops / (ex_us * 1e-6) / 1e12 / bf16_burst
 

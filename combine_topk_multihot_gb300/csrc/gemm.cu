@@ -732,6 +732,18 @@ Shape pick_shape(const moe_layout& L, int I, bool write_pad) {
   return stored <= 32 ? Shape::kNarrowShortA : Shape::kNarrow;
 }
 
+// Which CTA-pair kernel takes a bf16 layer.  The expert rows sit on the
+// MMA's N side (gemm_pair.cu) when the forward saves its operands for the
+// backward -- its staged stores of g, u and o are the faster ones -- or when
+// the experts average at most 384 rows, where 256-row tiles on the M side
+// would spend up to half of their MMAs on rows past an expert's end.  With
+// more rows per expert that waste is small, and the M-side tiles of this
+// file ran a few percent faster back to back (T = 16384, 1024 rows each).
+bool rows_on_n(const moe_layout& L, bool saves) {
+  const long long pairs = static_cast<long long>(L.T) * L.K;
+  return saves || pairs <= 384LL * L.E;
+}
+
 template <int OPS>
 cudaError_t experts_forward_any(const void* x_disp, const float* x_scale, const moe_layout& L,
                                 int H, int I, const void* W1, const float* W1_scale,
@@ -739,10 +751,13 @@ cudaError_t experts_forward_any(const void* x_disp, const float* x_scale, const 
                                 uint16_t* gu_save, cudaStream_t s) {
   switch (pick_shape(L, I, gu_save != nullptr)) {
     case Shape::kWide:
-      if constexpr (OPS == OPS_BF16)  // bf16 layers with rows for every SM: CTA pairs
+      if constexpr (OPS == OPS_BF16) {  // bf16 layers with rows for every SM: CTA pairs
+        if (rows_on_n(L, gu_save != nullptr || o_save != nullptr))
+          return launch_experts_forward_pair(static_cast<const uint16_t*>(x_disp), L, H, I,
+                                             static_cast<const uint16_t*>(W1), W2, h, y, o_save, gu_save, s);
         return experts_forward<256, 128, OPS, false, true>(x_disp, x_scale, L, H, I, W1, W1_scale, W2, h,
                                                            y, o_save, gu_save, s);
-      else
+      } else
         return experts_forward<256, 128, OPS>(x_disp, x_scale, L, H, I, W1, W1_scale, W2, h, y,
                                               o_save, gu_save, s);
     case Shape::kNarrow:

@@ -43,12 +43,19 @@ bool make_tma_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_
 bool make_tma_2d_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                     uint32_t box_rows);
 
+// Tensor map of the gate/up weights W1 [E, 2I, H] (bf16) read as boxes of
+// 64 features x {gate, up} x 64 columns of one expert, interleaved: box row
+// 2j is gate row f + j, box row 2j + 1 up row f + j (128-byte swizzle).
+bool make_tma_w1_gate_up(CUtensorMap* map, const void* W1, uint64_t E, uint64_t I, uint64_t H);
+
 // Tensor map for TMA stores of 32-row x 32-column bf16 boxes (64-byte rows)
 // into a row-major [rows, cols] matrix.  The shared-memory box is 64-byte
 // swizzled: the 16-byte chunk c of row r sits at chunk c ^ ((r >> 1) & 3)
 // (see staged_chunk), so a warp writing one row per lane spreads over all
 // shared-memory banks.
 bool make_tma_store_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols);
+// The same for 32-row x 16-column bf16 boxes (32-byte rows, no swizzle).
+bool make_tma_store_2d_bf16_16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols);
 // The same for fp32: 32-row x 16-column boxes (64-byte rows).
 bool make_tma_store_2d_f32(CUtensorMap* map, void* base, uint64_t rows, uint64_t cols);
 
@@ -136,6 +143,14 @@ cudaError_t launch_experts_forward(const uint16_t* x_disp, const moe_layout& L, 
                                    const uint16_t* W1, const uint16_t* W2, uint16_t* h,
                                    uint16_t* y, uint16_t* o_save, uint16_t* gu_save,
                                    cudaStream_t s);
+
+// a5 (bf16) on CTA pairs with each expert's rows on the MMA's N side, for
+// layers with rows for every SM: the accumulator is W[e] x_disp^T, tiles of
+// 256 weight rows by up to 256 expert rows in multiples of 16.
+cudaError_t launch_experts_forward_pair(const uint16_t* x_disp, const moe_layout& L, int H, int I,
+                                        const uint16_t* W1, const uint16_t* W2, uint16_t* h,
+                                        uint16_t* y, uint16_t* o_save, uint16_t* gu_save,
+                                        cudaStream_t s);
 
 // a5 on the CUDA cores for layers with at most 4 rows per expert (T <= 4)
 // and nothing saved for a backward: weight streaming with warp dot products.

@@ -55,6 +55,19 @@ bool make_tma_2d_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_tma_w1_gate_up(CUtensorMap* map, const void* W1, uint64_t E, uint64_t I, uint64_t H) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || E == 0 || I == 0 || H == 0) return false;
+  // dimensions innermost first: k, gate/up, feature, expert
+  const cuuint64_t dims[4] = {H, 2, I, E};
+  const cuuint64_t strides[3] = {I * H * 2, H * 2, 2 * I * H * 2};
+  const cuuint32_t box[4] = {64, 2, 64, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(W1), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_tma_store_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols) {
   EncodeTiledFn fn = encode_fn();
   if (!fn || rows == 0 || cols == 0) return false;
@@ -64,6 +77,18 @@ bool make_tma_store_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, u
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tma_store_2d_bf16_16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows == 0 || cols == 0) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {16, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -396,10 +396,14 @@ def test_experts_match_oracle(moe, T, H, E, K, I, P):
     (3, 8192, 8, 2, 128, 1),       # wide H: the A rows outgrow the CUDA-core path, tensor cores take it
     (4, 2048, 1024, 8, 768, 1),    # E = 1024: a long expert scan, 32 active experts
     (64, 256, 8, 2, 128, 16),      # tensor-core path without saved operands
+    (1500, 512, 40, 8, 512, 1),    # CTA pairs, expert rows on the MMA's N side: ~300 rows each, ragged last chunks
+    (2048, 512, 16, 8, 1536, 128), # CTA pairs, expert rows on the M side: ~1024 rows per expert
 ])
 def test_experts_inference_match_oracle(moe, T, H, E, K, I, P):
     """Inference (nothing saved for a backward): layers with at most four rows
-    per expert take the CUDA-core path, larger ones the tensor cores."""
+    per expert take the CUDA-core path, larger ones the tensor cores; layers
+    with rows for every SM take CTA pairs, with the expert rows on the N side
+    of the MMA up to 384 rows per expert on average and on the M side above."""
     idx, p, x, W1, W2, C, fwd = _experts_case(moe, T, H, E, K, I, P, seed=3 * T + H, save=False)
     Lr = O.build_layout(*O.route_to_multihot(idx.numpy(), p.numpy(), E)[:2], K, P, C)
     xd = bits(fwd.x_disp)
