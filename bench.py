@@ -177,10 +177,12 @@ class ClockSampler:
 
 def experts_kernel_label(cfg, fp8: bool, gather: bool, backward: bool) -> str:
     """Which expert GEMM kernels a bench step runs, as the library picks them
-    for layers with rows for every SM: bf16 layers that save for the backward,
-    or average at most 384 rows per expert, take pair_gemm_kernel (CTA pairs,
-    expert rows on the MMA's N side); other bf16 layers the CTA-pair form of
-    grouped_gemm_kernel; e4m3 operands and the gathered A its one-CTA form."""
+    for layers with rows for every SM: bf16 layers averaging at most 64 rows
+    per expert take grouped_gemm_kernel with one CTA per tile; those that save
+    for the backward, or average at most 384 rows per expert, pair_gemm_kernel
+    (CTA pairs, expert rows on the MMA's N side); other bf16 layers the
+    CTA-pair form of grouped_gemm_kernel; e4m3 operands and the gathered A its
+    one-CTA form."""
     wide = min(cfg.T * cfg.K, cfg.E) * (cfg.I // 128) >= 152
     if cfg.T <= 4 and not backward and not fp8:
         fwd = "experts: gemv_experts_kernel<1> (gate/up + SwiGLU) + gemv_experts_kernel<2> (down x weight), CUDA cores"
@@ -188,6 +190,8 @@ def experts_kernel_label(cfg, fp8: bool, gather: bool, backward: bool) -> str:
         fwd = ("experts: grouped_gemm_kernel<0> (gate/up + SwiGLU" + (", e4m3 operands" if fp8 else "")
                + (", A gathered" if gather else "") + ("" if wide else ", 64-column tiles")
                + ") + grouped_gemm_kernel<1> (down x weight)")
+    elif cfg.T * cfg.K <= 64 * cfg.E:
+        fwd = "experts: grouped_gemm_kernel<0> (gate/up + SwiGLU, one CTA per tile) + grouped_gemm_kernel<1> (down x weight)"
     elif backward or cfg.T * cfg.K <= 384 * cfg.E:
         fwd = "experts: pair_gemm_kernel<0> (gate/up + SwiGLU) + pair_gemm_kernel<1> (down x weight)"
     else:

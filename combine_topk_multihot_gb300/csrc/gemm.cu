@@ -732,16 +732,27 @@ Shape pick_shape(const moe_layout& L, int I, bool write_pad) {
   return stored <= 32 ? Shape::kNarrowShortA : Shape::kNarrow;
 }
 
-// Which CTA-pair kernel takes a bf16 layer.  The expert rows sit on the
-// MMA's N side (gemm_pair.cu) when the forward saves its operands for the
-// backward -- its staged stores of g, u and o are the faster ones -- or when
-// the experts average at most 384 rows, where 256-row tiles on the M side
-// would spend up to half of their MMAs on rows past an expert's end.  With
-// more rows per expert that waste is small, and the M-side tiles of this
-// file ran a few percent faster back to back (T = 16384, 1024 rows each).
-bool rows_on_n(const moe_layout& L, bool saves) {
+// Which kernel takes a bf16 layer with rows for every SM (all from
+// host-known sizes, so the sync-free path needs no row counts):
+//   * at most 64 rows per expert on average: one CTA per tile.  The step is a
+//     weight stream, and a CTA's four 48 KiB stages hold 128 KiB of weights in
+//     flight per SM, where a pair's 32 KiB stages hold 96 KiB (decode T = 256:
+//     206 against 215 us);
+//   * the forward saves its operands for the backward, or at most 384 rows
+//     per expert: CTA pairs with the expert rows on the MMA's N side
+//     (gemm_pair.cu) -- their staged stores of g, u and o are the faster
+//     ones, and 256-row tiles on the M side would spend up to half of their
+//     MMAs on rows past an expert's end;
+//   * otherwise CTA pairs with the rows on the M side: with ~1024 rows per
+//     expert that waste is small, and these tiles ran a few percent faster
+//     back to back (T = 16384).
+enum class WideKernel { kSingle, kPairRowsN, kPairRowsM };
+
+WideKernel wide_kernel(const moe_layout& L, bool saves) {
   const long long pairs = static_cast<long long>(L.T) * L.K;
-  return saves || pairs <= 384LL * L.E;
+  if (pairs <= 64LL * L.E) return WideKernel::kSingle;
+  if (saves || pairs <= 384LL * L.E) return WideKernel::kPairRowsN;
+  return WideKernel::kPairRowsM;
 }
 
 template <int OPS>
@@ -751,12 +762,19 @@ cudaError_t experts_forward_any(const void* x_disp, const float* x_scale, const 
                                 uint16_t* gu_save, cudaStream_t s) {
   switch (pick_shape(L, I, gu_save != nullptr)) {
     case Shape::kWide:
-      if constexpr (OPS == OPS_BF16) {  // bf16 layers with rows for every SM: CTA pairs
-        if (rows_on_n(L, gu_save != nullptr || o_save != nullptr))
-          return launch_experts_forward_pair(static_cast<const uint16_t*>(x_disp), L, H, I,
-                                             static_cast<const uint16_t*>(W1), W2, h, y, o_save, gu_save, s);
-        return experts_forward<256, 128, OPS, false, true>(x_disp, x_scale, L, H, I, W1, W1_scale, W2, h,
-                                                           y, o_save, gu_save, s);
+      if constexpr (OPS == OPS_BF16) {
+        switch (wide_kernel(L, gu_save != nullptr || o_save != nullptr)) {
+          case WideKernel::kPairRowsN:
+            return launch_experts_forward_pair(static_cast<const uint16_t*>(x_disp), L, H, I,
+                                               static_cast<const uint16_t*>(W1), W2, h, y, o_save, gu_save, s);
+          case WideKernel::kPairRowsM:
+            return experts_forward<256, 128, OPS, false, true>(x_disp, x_scale, L, H, I, W1, W1_scale, W2, h,
+                                                               y, o_save, gu_save, s);
+          case WideKernel::kSingle:
+            break;
+        }
+        return experts_forward<256, 128, OPS>(x_disp, x_scale, L, H, I, W1, W1_scale, W2, h, y, o_save,
+                                              gu_save, s);
       } else
         return experts_forward<256, 128, OPS>(x_disp, x_scale, L, H, I, W1, W1_scale, W2, h, y,
                                               o_save, gu_save, s);
