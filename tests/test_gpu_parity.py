@@ -388,6 +388,46 @@ def test_experts_match_oracle(moe, T, H, E, K, I, P):
     assert_gemm_close(bits(fwd.out), O.combine(y, Lr["token_row"]), "out")
 
 
+@pytest.mark.parametrize("save", [True, False])
+def test_experts_skewed_layer_matches_oracle(moe, save):
+    """A skewed layer on CTA pairs (log-Zipf router bias, 5 % dropped slots, 40
+    experts): the largest expert has over a thousand rows, so its tiles take
+    many 256-row chunks and a ragged last one, next to experts with a few
+    rows.  With the operands saved (training) the rows sit on the MMA's N
+    side and the pad rows are written as zeros; in inference the layer
+    averages about 300 rows per expert, which takes the same kernel."""
+    T, H, E, K, I, P = 3000, 512, 40, 4, 512, 16
+    idx, p = synthetic.make_routing(T, E, K, seed=11, zipf_s=1.2, drop=0.05)
+    counts = np.bincount(idx[idx >= 0].numpy().ravel(), minlength=E)
+    assert counts.max() > 1000 and counts.min() < 64  # the shape the test is about
+    gen = torch.Generator().manual_seed(12)
+    x = torch.randn(T, H, generator=gen).to(torch.bfloat16)
+    W1 = (torch.randn(E, 2 * I, H, generator=gen) * 0.02).to(torch.bfloat16)
+    W2 = (torch.randn(E, H, I, generator=gen) * 0.02).to(torch.bfloat16)
+    C = O.worst_case_capacity(T, E, K, P)
+    fwd = moe.moe_layer_forward(x.to(DEV), idx.to(DEV), p.to(DEV), W1.to(DEV), W2.to(DEV), P,
+                                capacity=C, save_for_backward=save)
+    torch.cuda.synchronize()
+    assert int(fwd.layout.status.item()) == 0
+    Lr = O.build_layout(*O.route_to_multihot(idx.numpy(), p.numpy(), E)[:2], K, P, C)
+    xd = bits(fwd.x_disp)
+    assert np.array_equal(xd, O.dispatch(bits(x), Lr["row_token"]))
+    y, h, o = O.grouped_experts(xd, Lr["row_expert"], Lr["row_weight"], bits(W1), bits(W2), I)
+    valid = Lr["row_token"] >= 0
+    assert_gemm_close(bits(fwd.h)[valid], h[valid], "h", intermediate=True)
+    assert_gemm_close(bits(fwd.y)[valid], y[valid], "y")
+    if save:
+        assert_gemm_close(bits(fwd.o)[valid], o[valid], "o_save")
+        # pad rows inside each group come out zero in every saved output
+        pad = np.zeros(C, dtype=bool)
+        offs, cnt = Lr["offsets"], Lr["tokens_per_expert"]
+        for e in range(E):
+            pad[offs[e] + cnt[e]:offs[e + 1]] = True
+        for name in ("h", "y", "o", "gu"):
+            assert not bits(getattr(fwd, name))[pad].any(), name
+    assert_gemm_close(bits(fwd.out), O.combine(y, Lr["token_row"]), "out")
+
+
 @pytest.mark.parametrize("T,H,E,K,I,P", [
     (1, 2048, 128, 8, 768, 1),     # the decode T = 1 layer: CUDA-core path
     (4, 512, 16, 4, 256, 1),       # four tokens: up to four rows per expert
