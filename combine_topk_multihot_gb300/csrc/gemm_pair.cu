@@ -52,14 +52,16 @@ namespace moe {
 namespace {
 
 constexpr int BK = 64;                           // bf16 elements per 128-byte swizzled row
+constexpr int KSUB = 2;                          // 64-column sub-tiles per stage (K = 128)
 constexpr int UMMA_K = 16;                       // K per tcgen05.mma for 16-bit inputs
 constexpr int MAX_N = 256;                       // expert rows per tile
 constexpr int EPI_WARPS = 8;
 constexpr int NUM_THREADS = 32 * (2 + EPI_WARPS);
 constexpr int MAX_STAGES = 8;
 constexpr int SMEM_LIMIT = 232448;
-constexpr int W_BYTES = 128 * BK * 2;            // a CTA's 128 weight rows of one stage
-constexpr int R_BYTES = (MAX_N / 2) * BK * 2;    // its up to 128 expert rows
+constexpr int W_SUB = 128 * BK * 2;              // a CTA's 128 weight rows x 64 columns
+constexpr int W_BYTES = KSUB * W_SUB;            // ... x 128 columns: one stage
+constexpr int R_BYTES = KSUB * (MAX_N / 2) * BK * 2;  // its up to 128 expert rows x 128 columns
 constexpr int STAGE_BYTES = W_BYTES + R_BYTES;
 constexpr int TMEM_COLS = 2 * MAX_N;             // double-buffered accumulator
 constexpr int STAGING_PER_WARP = 4096;           // epilogue staging for TMA stores
@@ -142,12 +144,14 @@ struct RowMaps {
   const CUtensorMap* box[4];
 };
 
-// The loads of one tile: for each k-block, wait for a free stage, then load
-// the CTA's 128 weight rows and its ROWS expert rows, all completing on the
-// even CTA's barrier, which expects both CTAs' bytes.  The rows come as one
-// box of ROWS rounded up to 32 (the MMA reads only the first ROWS; the rest
-// are the next rows of the layout, or zeros past its end): one TMA operation
-// fewer per box saved costs more than the extra bytes.  ROWS is a template
+// The loads of one tile: for each 128-column K step, wait for a free stage,
+// then load the CTA's 128 weight rows and its ROWS expert rows, all
+// completing on the even CTA's barrier, which expects both CTAs' bytes.  Each
+// operand comes as one TMA box of two 64-column sub-tiles: a CTA's TMA engine
+// takes a roughly fixed time per box, so 32 KiB boxes stream twice as fast
+// from L2 as 16 KiB ones (a probe: 134 against 71 GB/s per SM).  The rows box
+// is ROWS rounded up to 32 (the MMA reads only the first ROWS; the rest are
+// the next rows of the layout, or zeros past its end).  ROWS is a template
 // argument so that the issue sequence has a constant shape (with the box
 // choice made at run time the same loads ran about a quarter slower).
 template <int ROWS, int EPI, int STAGES>
@@ -156,7 +160,7 @@ __device__ __forceinline__ bool load_tile(const CUtensorMap* tmW, const RowMaps&
                                           int& stage, uint32_t& phase, long long& issued,
                                           volatile int* abort_flag) {
   constexpr int BOX = (ROWS + 31) / 32 * 32;
-  constexpr uint32_t TX = 2u * static_cast<uint32_t>(W_BYTES + BOX * BK * 2);
+  constexpr uint32_t TX = 2u * static_cast<uint32_t>(W_BYTES + KSUB * BOX * BK * 2);
   const int r0 = t.row0 + static_cast<int>(rank) * ROWS;
   const int w_row = EPI == EPI_SWIGLU ? t.fb * 128 + static_cast<int>(rank) * 64
                                       : t.e * w_rows_per_expert + t.fb * 256 + static_cast<int>(rank) * 128;
@@ -168,10 +172,10 @@ __device__ __forceinline__ bool load_tile(const CUtensorMap* tmW, const RowMaps&
     const uint32_t r_dst = w_dst + W_BYTES;
     if (rank == 0) mbar_arrive_expect_tx(full, TX);
     if constexpr (EPI == EPI_SWIGLU)
-      tma_load_4d_pair(w_dst, tmW, kb * BK, 0, w_row, t.e, full0);
+      tma_load_5d_pair(w_dst, tmW, 0, 0, w_row, t.e, kb * KSUB, full0);
     else
-      tma_load_2d_pair(w_dst, tmW, kb * BK, w_row, full0);
-    tma_load_2d_pair(r_dst, rm.box[BOX / 32 - 1], kb * BK, r0, full0);
+      tma_load_3d_pair(w_dst, tmW, 0, w_row, kb * KSUB, full0);
+    tma_load_3d_pair(r_dst, rm.box[BOX / 32 - 1], 0, r0, kb * KSUB, full0);
     ++issued;
     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
   }
@@ -196,23 +200,27 @@ __device__ __forceinline__ bool load_tile_n(const CUtensorMap* tmW, const RowMap
 #undef MOE_LOAD_N
 }
 
-// The MMAs of one tile: for each k-block, wait for its stage, issue the
-// pair's MMAs of 256 x N x 16 along the 128-byte rows, free the stage.  N is
-// a template argument so that the instruction descriptor is a compile-time
-// constant.
+// The MMAs of one tile: for each K step, wait for its stage, issue the
+// pair's MMAs of 256 x N x 16 along each sub-tile's 128-byte rows, free the
+// stage.  N is a template argument so that the instruction descriptor is a
+// compile-time constant (and so is the rows box's sub-tile stride).
 template <int N, int STAGES>
 __device__ __forceinline__ bool mma_tile(uint32_t d_tmem, uint32_t tiles_u32, Smem& s, int k_blocks,
                                          int& stage, uint32_t& phase, volatile int* abort_flag) {
   constexpr uint32_t IDESC = idesc_bf16_f32(2 * 128, N);
+  constexpr int R_SUB = (N / 2 + 31) / 32 * 32 * BK * 2;  // bytes of one sub-tile of the rows box
   for (int kb = 0; kb < k_blocks; ++kb) {
     if (!mbar_wait(smem_u32(&s.full[stage]), phase, abort_flag)) return false;
     tc_fence_after();
     const uint32_t w_addr = tiles_u32 + stage * STAGE_BYTES;
-    const uint64_t a_desc = sdesc_k_sw128(w_addr);
-    const uint64_t b_desc = sdesc_k_sw128(w_addr + W_BYTES);
 #pragma unroll
-    for (int kk = 0; kk < BK / UMMA_K; ++kk)  // 32 bytes along K per step
-      tc_mma_bf16_pair(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, IDESC, (kb | kk) != 0);
+    for (int j = 0; j < KSUB; ++j) {
+      const uint64_t a_desc = sdesc_k_sw128(w_addr + j * W_SUB);
+      const uint64_t b_desc = sdesc_k_sw128(w_addr + W_BYTES + j * R_SUB);
+#pragma unroll
+      for (int kk = 0; kk < BK / UMMA_K; ++kk)  // 32 bytes along K per step
+        tc_mma_bf16_pair(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, IDESC, (kb | j | kk) != 0);
+    }
     tc_commit_pair(smem_u32(&s.empty[stage]));  // frees the stage in both CTAs
     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
   }
@@ -598,20 +606,20 @@ cudaError_t launch_stages(const CUtensorMap& w, const CUtensorMap (&r)[4], const
   return cudaLaunchKernelEx(&cfg, kernel, w, r[0], r[1], r[2], r[3], st0, st1, args);
 }
 
-// Six 32 KiB stages when they fit beside the staging and the per-expert
-// tables, else five (E above about 200).
+// Three 64 KiB stages when they fit beside the staging and the per-expert
+// tables, else two (E above about 150).
 template <int EPI>
 cudaError_t launch_pair_gemm(const CUtensorMap& w, const CUtensorMap (&r)[4], const CUtensorMap& st0,
                              const CUtensorMap& st1, const PairArgs& args, cudaStream_t s) {
-  if (smem_bytes(6, args.E) <= static_cast<size_t>(SMEM_LIMIT))
-    return launch_stages<EPI, 6>(w, r, st0, st1, args, s);
-  return launch_stages<EPI, 5>(w, r, st0, st1, args, s);
+  if (smem_bytes(3, args.E) <= static_cast<size_t>(SMEM_LIMIT))
+    return launch_stages<EPI, 3>(w, r, st0, st1, args, s);
+  return launch_stages<EPI, 2>(w, r, st0, st1, args, s);
 }
 
 bool row_maps(CUtensorMap (&r)[4], const void* base, uint64_t rows, uint64_t cols) {
   const uint32_t boxes[4] = {32, 64, 96, 128};
   for (int i = 0; i < 4; ++i)
-    if (!make_tma_2d_bf16(&r[i], base, rows, cols, boxes[i])) return false;
+    if (!make_tma_rows_k128(&r[i], base, rows, cols, boxes[i])) return false;
   return true;
 }
 
@@ -624,8 +632,8 @@ cudaError_t launch_experts_forward_pair(const uint16_t* x_disp, const moe_layout
   if (L.capacity == 0) return cudaSuccess;
   const uint64_t C = static_cast<uint64_t>(L.capacity);
   CUtensorMap mW1, mW2, mX[4], mH[4], sH, sGU, sY, sO;
-  if (!make_tma_w1_gate_up(&mW1, W1, L.E, I, H) ||
-      !make_tma_2d_bf16(&mW2, W2, static_cast<uint64_t>(L.E) * H, I, 128) || !row_maps(mX, x_disp, C, H) ||
+  if (!make_tma_w1_gate_up_k128(&mW1, W1, L.E, I, H) ||
+      !make_tma_rows_k128(&mW2, W2, static_cast<uint64_t>(L.E) * H, I, 128) || !row_maps(mX, x_disp, C, H) ||
       !row_maps(mH, h, C, I) || !make_tma_store_2d_bf16_16(&sH, h, C, I) ||
       !make_tma_store_2d_bf16(&sY, y, C, H))
     return cudaErrorInvalidValue;
@@ -640,7 +648,7 @@ cudaError_t launch_experts_forward_pair(const uint16_t* x_disp, const moe_layout
   g1.offsets = L.offsets;
   g1.row_weight = L.row_weight;
   g1.E = L.E;
-  g1.k_blocks = H / BK;
+  g1.k_blocks = H / (KSUB * BK);
   g1.n_fblocks = I / 128;  // a 256-row block of W1 is 128 gate and 128 up rows
   g1.w_rows_per_expert = 2 * I;
   g1.out0 = h;
@@ -654,7 +662,7 @@ cudaError_t launch_experts_forward_pair(const uint16_t* x_disp, const moe_layout
   if (err != cudaSuccess) return err;
 
   PairArgs g2 = g1;
-  g2.k_blocks = I / BK;
+  g2.k_blocks = I / (KSUB * BK);
   g2.n_fblocks = H / 256;
   g2.w_rows_per_expert = H;
   g2.out0 = y;

@@ -43,10 +43,16 @@ bool make_tma_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_
 bool make_tma_2d_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                     uint32_t box_rows);
 
-// Tensor map of the gate/up weights W1 [E, 2I, H] (bf16) read as boxes of
-// 64 features x {gate, up} x 64 columns of one expert, interleaved: box row
-// 2j is gate row f + j, box row 2j + 1 up row f + j (128-byte swizzle).
-bool make_tma_w1_gate_up(CUtensorMap* map, const void* W1, uint64_t E, uint64_t I, uint64_t H);
+// Tensor maps whose boxes carry 128 columns of K as two 64-column sub-tiles
+// (128-byte swizzle; sub-tile j follows sub-tile j - 1 in shared memory), so
+// one TMA operation moves a whole 128-wide K step:
+//   * the gate/up weights W1 [E, 2I, H] (bf16): 64 features x {gate, up} x
+//     128 columns of one expert, interleaved -- sub-tile row 2j is gate row
+//     f + j, row 2j + 1 up row f + j (H % 128 == 0);
+//   * a row-major bf16 matrix [rows, cols]: box_rows rows x 128 columns
+//     (cols % 128 == 0); reads past the last row return zeros.
+bool make_tma_w1_gate_up_k128(CUtensorMap* map, const void* W1, uint64_t E, uint64_t I, uint64_t H);
+bool make_tma_rows_k128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 
 // Tensor map for TMA stores of 32-row x 32-column bf16 boxes (64-byte rows)
 // into a row-major [rows, cols] matrix.  The shared-memory box is 64-byte

@@ -55,15 +55,28 @@ bool make_tma_2d_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool make_tma_w1_gate_up(CUtensorMap* map, const void* W1, uint64_t E, uint64_t I, uint64_t H) {
+bool make_tma_w1_gate_up_k128(CUtensorMap* map, const void* W1, uint64_t E, uint64_t I, uint64_t H) {
   EncodeTiledFn fn = encode_fn();
-  if (!fn || E == 0 || I == 0 || H == 0) return false;
-  // dimensions innermost first: k, gate/up, feature, expert
-  const cuuint64_t dims[4] = {H, 2, I, E};
-  const cuuint64_t strides[3] = {I * H * 2, H * 2, 2 * I * H * 2};
-  const cuuint32_t box[4] = {64, 2, 64, 1};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(W1), dims, strides, box,
+  if (!fn || E == 0 || I == 0 || H == 0 || H % 128) return false;
+  // dimensions innermost first: 64 columns, gate/up, feature, expert, 64-column block
+  const cuuint64_t dims[5] = {64, 2, I, E, H / 64};
+  const cuuint64_t strides[4] = {I * H * 2, H * 2, 2 * I * H * 2, 128};
+  const cuuint32_t box[5] = {64, 2, 64, 1, 2};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(W1), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tma_rows_k128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows == 0 || cols == 0 || cols % 128) return false;
+  // dimensions innermost first: 64 columns, row, 64-column block
+  const cuuint64_t dims[3] = {64, rows, cols / 64};
+  const cuuint64_t strides[2] = {cols * 2, 128};
+  const cuuint32_t box[3] = {64, box_rows, 2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
