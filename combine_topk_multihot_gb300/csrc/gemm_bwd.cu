@@ -248,19 +248,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // both CTAs' loads complete on the even CTA's barrier, which expects them all
             const uint32_t full0 = mapa_shared(full, 0);
             if (rank == 0) mbar_arrive_expect_tx(full, 2 * STAGE_BYTES);
+            // an MN-major operand's 64-wide blocks come as one 3-D box (64
+            // columns x 64 K lines x 2 blocks, the blocks 8 KiB apart in shared
+            // memory): one TMA operation instead of two
+            static_assert(B_BOXES == 2, "the pair's N half is two 64-wide blocks");
             if (GROUP_K) {
               const int k_row = s_off[t.e] + kb * BK;
-              tma_load_2d_pair(a_dst, &tmA, m0, k_row, full0);
-              tma_load_2d_pair(a_dst + MN_BOX_BYTES, &tmA, m0 + 64, k_row, full0);
-#pragma unroll
-              for (int j = 0; j < B_BOXES; ++j)
-                tma_load_2d_pair(b_dst + j * MN_BOX_BYTES, &tmB, n0 + 64 * j, k_row, full0);
+              tma_load_3d_pair(a_dst, &tmA, 0, k_row, m0 / 64, full0);
+              tma_load_3d_pair(b_dst, &tmB, 0, k_row, n0 / 64, full0);
             } else {
               tma_load_2d_pair(a_dst, &tmA, kb * BK, s_off[t.e] + m0, full0);
               const int k_row = t.e * args.b_rows_per_expert + kb * BK;
-#pragma unroll
-              for (int j = 0; j < B_BOXES; ++j)
-                tma_load_2d_pair(b_dst + j * MN_BOX_BYTES, &tmB, n0 + 64 * j, k_row, full0);
+              tma_load_3d_pair(b_dst, &tmB, 0, k_row, n0 / 64, full0);
             }
           } else {
             mbar_arrive_expect_tx(full, STAGE_BYTES);
@@ -598,14 +597,17 @@ cudaError_t launch_bwd(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
 // 256-column tiles where N allows, on CTA pairs when the layer has rows for
 // them (pair): the M-grouped dgrads always, the K-grouped wgrads when M is a
 // multiple of 256 and no K lines need masking.
+// a3 / b3: the operands' maps for the pair kernel, whose MN-major operands
+// load two 64-wide blocks per box (make_tma_rows_k128 with 64-line boxes).
 template <bool GROUP_K, int EPI>
-cudaError_t launch_bwd_bn(int n_total, const CUtensorMap& a, const CUtensorMap& b,
-                          const CUtensorMap& out, BwdArgs args, cudaStream_t s, bool pair) {
+cudaError_t launch_bwd_bn(int n_total, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& a3,
+                          const CUtensorMap& b3, const CUtensorMap& out, BwdArgs args, cudaStream_t s,
+                          bool pair) {
   if (n_total % 256 == 0) {
     args.n_tiles = n_total / 256;
     if (pair && (!GROUP_K || (args.m_total % 256 == 0 && !args.zero_tail))) {
       if (GROUP_K) args.m_tiles = args.m_total / 256;
-      return launch_bwd<GROUP_K, 256, EPI, true>(a, b, out, args, s);
+      return launch_bwd<GROUP_K, 256, EPI, true>(a3, b3, out, args, s);
     }
     return launch_bwd<GROUP_K, 256, EPI>(a, b, out, args, s);
   }
@@ -657,9 +659,10 @@ cudaError_t launch_experts_backward(const uint16_t* grad_y, const uint16_t* x_di
 
   if (C > 0) {
     // dgrad1: G_gu = SwiGLU'(G_o W2)
-    CUtensorMap mA, mB, mO;
+    CUtensorMap mA, mB, mB3, mO;
     if (!make_tma_2d_bf16(&mA, g_o, C, H, 128) ||
         !make_tma_2d_bf16(&mB, W2, static_cast<uint64_t>(E) * H, I, 64) ||
+        !make_tma_rows_k128(&mB3, W2, static_cast<uint64_t>(E) * H, I, 64) ||
         !make_tma_store_2d_bf16(&mO, g_gu, C, 2 * I))
       return cudaErrorInvalidValue;
     BwdArgs a = base;
@@ -668,12 +671,13 @@ cudaError_t launch_experts_backward(const uint16_t* grad_y, const uint16_t* x_di
     a.out_bf16 = g_gu;
     a.ld_out = 2 * I;
     a.gu = gu_save;
-    err = launch_bwd_bn<false, EPI_DSWIGLU>(I, mA, mB, mO, a, s, pair);
+    err = launch_bwd_bn<false, EPI_DSWIGLU>(I, mA, mB, mA, mB3, mO, a, s, pair);
     if (err != cudaSuccess) return err;
 
     // dgrad2: grad_x_disp = G_gu W1
     if (!make_tma_2d_bf16(&mA, g_gu, C, 2 * I, 128) ||
         !make_tma_2d_bf16(&mB, W1, static_cast<uint64_t>(E) * 2 * I, H, 64) ||
+        !make_tma_rows_k128(&mB3, W1, static_cast<uint64_t>(E) * 2 * I, H, 64) ||
         !make_tma_store_2d_bf16(&mO, grad_x_disp, C, H))
       return cudaErrorInvalidValue;
     a = base;
@@ -681,16 +685,18 @@ cudaError_t launch_experts_backward(const uint16_t* grad_y, const uint16_t* x_di
     a.b_rows_per_expert = 2 * I;
     a.out_bf16 = grad_x_disp;
     a.ld_out = H;
-    err = launch_bwd_bn<false, EPI_BF16>(H, mA, mB, mO, a, s, pair);
+    err = launch_bwd_bn<false, EPI_BF16>(H, mA, mB, mA, mB3, mO, a, s, pair);
     if (err != cudaSuccess) return err;
   }
 
   // wgrad2: dW2[e] = G_o^T h     (M = H, N = I, K = the expert's rows)
   {
-    CUtensorMap mA, mB, mO;
+    CUtensorMap mA, mB, mA3, mB3, mO;
     const uint64_t rows = C > 0 ? static_cast<uint64_t>(C) : 1;
-    if (!make_tma_2d_bf16(&mA, C > 0 ? static_cast<const void*>(g_o) : static_cast<const void*>(dW2), rows, H, 64) ||
-        !make_tma_2d_bf16(&mB, C > 0 ? static_cast<const void*>(h) : static_cast<const void*>(dW2), rows, I, 64) ||
+    const void* a_src = C > 0 ? static_cast<const void*>(g_o) : static_cast<const void*>(dW2);
+    const void* b_src = C > 0 ? static_cast<const void*>(h) : static_cast<const void*>(dW2);
+    if (!make_tma_2d_bf16(&mA, a_src, rows, H, 64) || !make_tma_2d_bf16(&mB, b_src, rows, I, 64) ||
+        !make_tma_rows_k128(&mA3, a_src, rows, H, 64) || !make_tma_rows_k128(&mB3, b_src, rows, I, 64) ||
         !make_tma_store_2d_f32(&mO, dW2, static_cast<uint64_t>(E) * H, I))
       return cudaErrorInvalidValue;
     BwdArgs a = base;
@@ -703,15 +709,17 @@ cudaError_t launch_experts_backward(const uint16_t* grad_y, const uint16_t* x_di
     a.m_total = H;
     a.n_total = I;
     a.out_f32 = dW2;
-    err = launch_bwd_bn<true, EPI_F32>(I, mA, mB, mO, a, s, pair);
+    err = launch_bwd_bn<true, EPI_F32>(I, mA, mB, mA3, mB3, mO, a, s, pair);
     if (err != cudaSuccess) return err;
   }
   // wgrad1: dW1[e] = G_gu^T x_disp   (M = 2I, N = H)
   {
-    CUtensorMap mA, mB, mO;
+    CUtensorMap mA, mB, mA3, mB3, mO;
     const uint64_t rows = C > 0 ? static_cast<uint64_t>(C) : 1;
-    if (!make_tma_2d_bf16(&mA, C > 0 ? static_cast<const void*>(g_gu) : static_cast<const void*>(dW1), rows, 2 * I, 64) ||
-        !make_tma_2d_bf16(&mB, C > 0 ? static_cast<const void*>(x_disp) : static_cast<const void*>(dW1), rows, H, 64) ||
+    const void* a_src = C > 0 ? static_cast<const void*>(g_gu) : static_cast<const void*>(dW1);
+    const void* b_src = C > 0 ? static_cast<const void*>(x_disp) : static_cast<const void*>(dW1);
+    if (!make_tma_2d_bf16(&mA, a_src, rows, 2 * I, 64) || !make_tma_2d_bf16(&mB, b_src, rows, H, 64) ||
+        !make_tma_rows_k128(&mA3, a_src, rows, 2 * I, 64) || !make_tma_rows_k128(&mB3, b_src, rows, H, 64) ||
         !make_tma_store_2d_f32(&mO, dW1, static_cast<uint64_t>(E) * 2 * I, H))
       return cudaErrorInvalidValue;
     BwdArgs a = base;
@@ -724,7 +732,7 @@ cudaError_t launch_experts_backward(const uint16_t* grad_y, const uint16_t* x_di
     a.m_total = 2 * I;
     a.n_total = H;
     a.out_f32 = dW1;
-    err = launch_bwd_bn<true, EPI_F32>(H, mA, mB, mO, a, s, pair);
+    err = launch_bwd_bn<true, EPI_F32>(H, mA, mB, mA3, mB3, mO, a, s, pair);
   }
   return err;
 }
