@@ -135,6 +135,11 @@ __global__ void __launch_bounds__(FD_THREADS, 4) dispatch_fused_kernel(FusedArgs
   __shared__ int s_warp[33];
   __shared__ int s_ok;
   const int E = a.E, K = a.K;
+  // The next kernel (the experts, launched for programmatic dependent launch)
+  // may be scheduled now: it sets up on the SMs this grid frees and waits for
+  // the whole grid's completion before it reads any of its outputs.  This
+  // kernel itself follows a memset in stream order, so it waits for nothing.
+  griddep_launch_dependents();
   // staging slots first (16-byte aligned for the bulk copies), then the tables
   uint8_t* s_slots = fd_smem;                                            // [FD_WARPS][FD_SLOT]
   uint8_t* s_zero = fd_smem + FD_WARPS * FD_SLOT;                        // [FD_SLOT] zeros
