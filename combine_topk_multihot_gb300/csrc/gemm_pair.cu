@@ -154,27 +154,44 @@ struct RowMaps {
 // the next rows of the layout, or zeros past its end).  ROWS is a template
 // argument so that the issue sequence has a constant shape (with the box
 // choice made at run time the same loads ran about a quarter slower).
+// Transaction bytes of one stage of a tile with N expert rows, both CTAs.
+__device__ __forceinline__ uint32_t stage_tx(int n) {
+  const int box = (n / 2 + 31) / 32 * 32;
+  return 2u * static_cast<uint32_t>(W_BYTES + KSUB * box * BK * 2);
+}
+
+// The weight box of one stage (the CTA's 128 weight rows, 128 columns of K).
+template <int EPI>
+__device__ __forceinline__ void load_weights(const CUtensorMap* tmW, const Tile& t, uint32_t rank, int w_rows_per_expert,
+                                             uint32_t w_dst, int kb, uint32_t full0) {
+  const int w_row = EPI == EPI_SWIGLU ? t.fb * 128 + static_cast<int>(rank) * 64
+                                      : t.e * w_rows_per_expert + t.fb * 256 + static_cast<int>(rank) * 128;
+  if constexpr (EPI == EPI_SWIGLU)
+    tma_load_5d_pair(w_dst, tmW, 0, 0, w_row, t.e, kb * KSUB, full0);
+  else
+    tma_load_3d_pair(w_dst, tmW, 0, w_row, kb * KSUB, full0);
+}
+
+// pre: the leading stages of this tile whose weight box (and the stage's
+// expected bytes) were issued already; only their rows remain.
 template <int ROWS, int EPI, int STAGES>
 __device__ __forceinline__ bool load_tile(const CUtensorMap* tmW, const RowMaps& rm, const Tile& t, uint32_t rank,
                                           uint32_t tiles_u32, Smem& s, int k_blocks, int w_rows_per_expert,
                                           int& stage, uint32_t& phase, long long& issued,
-                                          volatile int* abort_flag) {
+                                          volatile int* abort_flag, int pre) {
   constexpr int BOX = (ROWS + 31) / 32 * 32;
   constexpr uint32_t TX = 2u * static_cast<uint32_t>(W_BYTES + KSUB * BOX * BK * 2);
   const int r0 = t.row0 + static_cast<int>(rank) * ROWS;
-  const int w_row = EPI == EPI_SWIGLU ? t.fb * 128 + static_cast<int>(rank) * 64
-                                      : t.e * w_rows_per_expert + t.fb * 256 + static_cast<int>(rank) * 128;
   for (int kb = 0; kb < k_blocks; ++kb) {
-    if (!mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, abort_flag)) return false;
     const uint32_t full = smem_u32(&s.full[stage]);
     const uint32_t full0 = mapa_shared(full, 0);
     const uint32_t w_dst = tiles_u32 + stage * STAGE_BYTES;
     const uint32_t r_dst = w_dst + W_BYTES;
-    if (rank == 0) mbar_arrive_expect_tx(full, TX);
-    if constexpr (EPI == EPI_SWIGLU)
-      tma_load_5d_pair(w_dst, tmW, 0, 0, w_row, t.e, kb * KSUB, full0);
-    else
-      tma_load_3d_pair(w_dst, tmW, 0, w_row, kb * KSUB, full0);
+    if (kb >= pre) {
+      if (!mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, abort_flag)) return false;
+      if (rank == 0) mbar_arrive_expect_tx(full, TX);
+      load_weights<EPI>(tmW, t, rank, w_rows_per_expert, w_dst, kb, full0);
+    }
     tma_load_3d_pair(r_dst, rm.box[BOX / 32 - 1], 0, r0, kb * KSUB, full0);
     ++issued;
     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -186,11 +203,11 @@ template <int EPI, int STAGES>
 __device__ __forceinline__ bool load_tile_n(const CUtensorMap* tmW, const RowMaps& rm, const Tile& t, uint32_t rank,
                                             uint32_t tiles_u32, Smem& s, int k_blocks, int w_rows_per_expert,
                                             int& stage, uint32_t& phase, long long& issued,
-                                            volatile int* abort_flag) {
+                                            volatile int* abort_flag, int pre) {
 #define MOE_LOAD_N(NN)                                                                                     \
   case NN / 16:                                                                                            \
     return load_tile<NN / 2, EPI, STAGES>(tmW, rm, t, rank, tiles_u32, s, k_blocks, w_rows_per_expert, stage, \
-                                          phase, issued, abort_flag);
+                                          phase, issued, abort_flag, pre);
   switch (t.n >> 4) {
     MOE_LOAD_N(16) MOE_LOAD_N(32) MOE_LOAD_N(48) MOE_LOAD_N(64) MOE_LOAD_N(80) MOE_LOAD_N(96)
     MOE_LOAD_N(112) MOE_LOAD_N(128) MOE_LOAD_N(144) MOE_LOAD_N(160) MOE_LOAD_N(176) MOE_LOAD_N(192)
@@ -270,7 +287,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t rank = cluster_ctarank();  // the even CTA of a pair issues the MMAs
   const int tile0 = static_cast<int>(blockIdx.x >> 1);
   const int tstep = static_cast<int>(gridDim.x >> 1);
-  griddep_launch_dependents();
 
   // ---- set-up: barriers, tensor memory, the device-side tile list
   if (threadIdx.x == 0) {
@@ -294,7 +310,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tmS0);
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(&s.tmem_base), TMEM_COLS);
-  griddep_wait();  // the layout, the dispatched rows (and h) come from earlier kernels
+  // Launch order.  Each launch lets its dependents start only once its own
+  // wait has returned, so a running down-projection CTA implies that the
+  // dispatch, two launches back, has completed.  The gate/up launch waits here
+  // for the dispatch (the layout and the rows).  The down-projection launch
+  // reads the layout now and waits for the gate/up launch's h only in its
+  // producer, after it has issued its first stages' weight boxes, so its
+  // set-up and first weight loads overlap the gate/up launch's last tiles.
+  if constexpr (EPI == EPI_SWIGLU) {
+    griddep_wait();
+    griddep_launch_dependents();
+  }
   for (int e = threadIdx.x; e <= E; e += blockDim.x) s_off[e] = args.offsets[e];
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = args.counts[e];
   __syncthreads();
@@ -334,11 +360,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       long long issued = 0;
       bool ok = true;
       const RowMaps rm{{&tmR32, &tmR64, &tmR96, &tmR128}};
+      int pre = 0;  // leading stages of the first tile whose weights are already on their way
+      if constexpr (EPI == EPI_WEIGHTED) {
+        if (tile0 < total) {
+          const Tile t = decode_tile(s_off, s_cnt, s_pre, E, args.n_fblocks, args.write_pad, tile0);
+          pre = args.k_blocks < STAGES ? args.k_blocks : STAGES;
+          for (int kb = 0; kb < pre; ++kb) {  // fresh stages: nothing to wait for
+            const uint32_t full = smem_u32(&s.full[kb]);
+            if (rank == 0) mbar_arrive_expect_tx(full, stage_tx(t.n));
+            load_weights<EPI>(&tmW, t, rank, args.w_rows_per_expert, tiles_u32 + kb * STAGE_BYTES, kb,
+                              mapa_shared(full, 0));
+          }
+        }
+        griddep_wait();  // h comes from the gate/up launch
+        griddep_launch_dependents();
+      }
       for (int tile = tile0; tile < total && ok; tile += tstep) {
         const Tile t = decode_tile(s_off, s_cnt, s_pre, E, args.n_fblocks, args.write_pad, tile);
         // this CTA loads t.n / 2 expert rows (a multiple of 8): rows t.row0 + rank * t.n / 2 on
         ok = load_tile_n<EPI, STAGES>(&tmW, rm, t, rank, tiles_u32, s, args.k_blocks, args.w_rows_per_expert,
-                                      stage, phase, issued, abort_flag);
+                                      stage, phase, issued, abort_flag, tile == tile0 ? pre : 0);
       }
       if (!ok && rank == 0) {
         // drain: wait for the loads of the last (up to STAGES) issued stages
