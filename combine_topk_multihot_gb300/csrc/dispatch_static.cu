@@ -43,32 +43,6 @@ std::mutex g_scratch_mu;
 int* g_scratch_ptr[MAX_DEVICES];
 unsigned long long g_scratch_ctx[MAX_DEVICES];
 
-using CtxGetCurrentFn = CUresult (*)(CUcontext*);
-using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
-
-// Unique id of the calling thread's current context (driver entry points
-// reached through the runtime, so the library does not link libcuda);
-// false when there is none yet or the driver does not say.
-bool current_context_id(unsigned long long* id) {
-  static CtxGetCurrentFn get_current = nullptr;
-  static CtxGetIdFn get_id = nullptr;
-  static bool looked_up = false;
-  if (!looked_up) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess && q == cudaDriverEntryPointSuccess)
-      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess && q == cudaDriverEntryPointSuccess)
-      get_id = reinterpret_cast<CtxGetIdFn>(p);
-    looked_up = true;
-  }
-  CUcontext ctx = nullptr;
-  return get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx != nullptr &&
-         get_id(ctx, id) == CUDA_SUCCESS;
-}
-
 // Device address of the static scratch on the current device.  It is looked
 // up on the first call for the device, and again after the device's context
 // has changed (a device reset).  The lookup can load the library's module, so
@@ -115,6 +89,33 @@ moe_status static_scratch(cudaStream_t stream, int** out) {
 }
 
 }  // namespace
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (driver entry points
+// reached through the runtime, so the library does not link libcuda);
+// false when there is none yet or the driver does not say.
+bool current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static bool looked_up = false;
+  if (!looked_up) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+    looked_up = true;
+  }
+  CUcontext ctx = nullptr;
+  return get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx != nullptr &&
+         get_id(ctx, id) == CUDA_SUCCESS;
+}
+
 
 }  // namespace moe
 

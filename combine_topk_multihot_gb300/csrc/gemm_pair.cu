@@ -44,10 +44,27 @@
 // backward) the pad rows of its group, which come out zero from the zero pad
 // rows of x_disp.  Spare rows are never written.
 
+#include <atomic>
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 
 namespace moe {
+
+// Readiness of h per row chunk (an expert's 256-row chunk), so that the down
+// launch can start a tile as soon as the gate/up tiles of its chunk are
+// written rather than when the whole gate/up launch has finished: each
+// gate/up epilogue warp adds one to its tile's chunk once its stores of the
+// tile have completed, and the down launch's producer waits for the count of
+// all the chunk's gate/up tiles.  16 slots rotate between launch pairs (a
+// launch pair's down launch clears its slot as its last CTA finishes, so a
+// slot is clean for its next use 16 launch pairs later).  2 x 128 KiB of
+// device memory per GPU, held from library load until the process exits.
+constexpr int HR_SLOTS = 16;
+constexpr int HR_CAP = 2048;  // row chunks per layer
+static __device__ __align__(128) int g_h_ready[HR_SLOTS][HR_CAP];
+static __device__ unsigned int g_h_done[HR_SLOTS];
 
 namespace {
 
@@ -84,6 +101,9 @@ struct PairArgs {
   int I;                   // GEMM1: offset of the up half in gu_save
   int write_pad;           // also cover the pad rows of each expert's group
   int* status;
+  int* ready;              // per row chunk: h-ready signals (NULL: the down launch waits for the whole gate/up launch)
+  unsigned int* done;      // the down launch's finished CTAs; the last one clears `ready`
+  int ready_target;        // signals that make a chunk ready: gate/up tiles per chunk x 16 epilogue warps
 };
 
 // Barriers and scalars; the per-expert tables (offsets [E+1], counts [E],
@@ -97,6 +117,7 @@ struct Smem {
   uint32_t tmem_base;
   int abort;
   int total_tiles;
+  int last;  // the down launch's last CTA (it clears the readiness counters)
 };
 
 constexpr size_t smem_bytes(int stages, int E) {
@@ -109,6 +130,7 @@ struct Tile {
   int row0;    // first expert row of the chunk (row of the expanded layout)
   int rows;    // expert rows of the chunk
   int n;       // MMA N: rows rounded up to 16
+  int chunk;   // the chunk's index among all experts' chunks
 };
 
 // Rows an expert's tiles cover: its valid rows, or its whole padded group.
@@ -132,6 +154,7 @@ __device__ __forceinline__ Tile decode_tile(const int* s_off, const int* s_cnt, 
   t.e = lo;
   t.fb = local - chunk * n_fb;
   t.row0 = s_off[lo] + chunk * MAX_N;
+  t.chunk = s_pre[lo] / n_fb + chunk;
   t.rows = ne - chunk * MAX_N < MAX_N ? ne - chunk * MAX_N : MAX_N;
   t.n = (t.rows + 15) & ~15;
   return t;
@@ -258,6 +281,24 @@ __device__ __forceinline__ bool mma_tile_n(int n, uint32_t d_tmem, uint32_t tile
 #undef MOE_MMA_N
 }
 
+// Waits until *counter reaches target (acquire at GPU scope).  Bounded like
+// every wait of the kernel: false (and the CTA's abort flag raised) if it
+// runs past the limit or another role of the CTA has given up.
+__device__ __forceinline__ bool wait_ready(const int* counter, int target, volatile int* abort_flag) {
+  if (ld_acquire_gpu(counter) >= target) return true;
+  const unsigned long long t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (ld_acquire_gpu(counter) >= target) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
 __device__ __forceinline__ uint16_t bf16_bits(float v) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
@@ -361,6 +402,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       const RowMaps rm{{&tmR32, &tmR64, &tmR96, &tmR128}};
       int pre = 0;  // leading stages of the first tile whose weights are already on their way
+      const bool fine = EPI == EPI_WEIGHTED && args.ready != nullptr;
       if constexpr (EPI == EPI_WEIGHTED) {
         if (tile0 < total) {
           const Tile t = decode_tile(s_off, s_cnt, s_pre, E, args.n_fblocks, args.write_pad, tile0);
@@ -372,11 +414,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                               mapa_shared(full, 0));
           }
         }
-        griddep_wait();  // h comes from the gate/up launch
+        if (!fine) griddep_wait();  // h comes from the gate/up launch
         griddep_launch_dependents();
       }
       for (int tile = tile0; tile < total && ok; tile += tstep) {
         const Tile t = decode_tile(s_off, s_cnt, s_pre, E, args.n_fblocks, args.write_pad, tile);
+        if (fine) {
+          // this chunk's h rows are written (bounded wait), then read them with TMA
+          if (!wait_ready(args.ready + t.chunk, args.ready_target, abort_flag)) { ok = false; break; }
+          fence_proxy_async_global();
+        }
         // this CTA loads t.n / 2 expert rows (a multiple of 8): rows t.row0 + rank * t.n / 2 on
         ok = load_tile_n<EPI, STAGES>(&tmW, rm, t, rank, tiles_u32, s, args.k_blocks, args.w_rows_per_expert,
                                       stage, phase, issued, abort_flag, tile == tile0 ? pre : 0);
@@ -584,6 +631,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // hand the accumulator back to the MMA issuer (its barrier is in the even
       // CTA) without waiting for this warp's global stores to complete
       if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&s.tempty[buf]), 0));
+      if constexpr (EPI == EPI_SWIGLU) {
+        if (args.ready != nullptr) {
+          // this warp's part of the tile's h is in memory: its bulk stores have
+          // completed, and the lanes' direct stores are ordered before lane 0's
+          // release by the warp barrier above
+          if (lane == 0) {
+            tma_store_wait_all();
+            fence_proxy_async_global();
+            red_release_gpu_add(args.ready + t.chunk, 1);
+          }
+          __syncwarp();
+        }
+      }
     }
     if (lane == 0) tma_store_wait_all();  // every store done before the CTA exits
     __syncwarp();
@@ -597,6 +657,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
   if (threadIdx.x == 0 && s.abort) report(args.status, MOE_DEVERR_TIMEOUT);
+  if constexpr (EPI == EPI_WEIGHTED) {
+    if (args.ready != nullptr) {
+      // the last CTA of the down launch (every CTA has read its counters by
+      // now) clears the slot's counters for their next use
+      if (threadIdx.x == 0) {
+        __threadfence();
+        s.last = atomicAdd(args.done, 1u) == gridDim.x - 1;
+      }
+      __syncthreads();
+      if (s.last) {
+        const int n_chunks = total / args.n_fblocks;
+        for (int i = threadIdx.x; i < n_chunks; i += blockDim.x) args.ready[i] = 0;
+        if (threadIdx.x == 0) *args.done = 0u;
+        __threadfence();
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------- host side
@@ -657,6 +734,45 @@ cudaError_t launch_pair_gemm(const CUtensorMap& w, const CUtensorMap (&r)[4], co
   return launch_stages<EPI, 2>(w, r, st0, st1, args, s);
 }
 
+std::mutex g_ready_mu;
+int* g_ready_ptr[64];
+unsigned int* g_done_ptr[64];
+unsigned long long g_ready_ctx[64];
+std::atomic<unsigned int> g_ready_next{0};
+
+// A slot of readiness counters on the current device, or false.  Their
+// device address is looked up on the first use on each device (and again
+// after a device reset); the lookup can load the library's module, so a first
+// use while `stream` is being captured goes without (the down launch then
+// waits for the whole gate/up launch).
+bool ready_counters(cudaStream_t stream, int** ready, unsigned int** done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  unsigned long long ctx = 0;
+  const bool known_ctx = current_context_id(&ctx);
+  std::lock_guard<std::mutex> lock(g_ready_mu);
+  if (g_ready_ptr[dev] == nullptr || !known_ctx || g_ready_ctx[dev] != ctx) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+      cudaGetLastError();
+      return false;
+    }
+    void* r = nullptr;
+    void* d = nullptr;
+    if (cudaGetSymbolAddress(&r, g_h_ready) != cudaSuccess || cudaGetSymbolAddress(&d, g_h_done) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    g_ready_ptr[dev] = static_cast<int*>(r);
+    g_done_ptr[dev] = static_cast<unsigned int*>(d);
+    g_ready_ctx[dev] = ctx;
+  }
+  const unsigned int slot = g_ready_next.fetch_add(1u) % HR_SLOTS;
+  *ready = g_ready_ptr[dev] + static_cast<size_t>(slot) * HR_CAP;
+  *done = g_done_ptr[dev] + slot;
+  return true;
+}
+
 bool row_maps(CUtensorMap (&r)[4], const void* base, uint64_t rows, uint64_t cols) {
   const uint32_t boxes[4] = {32, 64, 96, 128};
   for (int i = 0; i < 4; ++i)
@@ -699,6 +815,15 @@ cudaError_t launch_experts_forward_pair(const uint16_t* x_disp, const moe_layout
   g1.I = I;
   g1.write_pad = gu_save != nullptr;  // training: the backward reads the pad rows
   g1.status = L.status;
+  // readiness counters when the layer's row chunks fit a slot (at most one
+  // chunk per expert more than its rows / 256)
+  const long long rows_bound = static_cast<long long>(L.T) * L.K +
+                               (g1.write_pad ? static_cast<long long>(L.E) * (L.pad_multiple - 1) : 0);
+  if (rows_bound / MAX_N + L.E + 1 <= HR_CAP && !ready_counters(s, &g1.ready, &g1.done)) {
+    g1.ready = nullptr;
+    g1.done = nullptr;
+  }
+  g1.ready_target = (I / 128) * 2 * EPI_WARPS;
   cudaError_t err = launch_pair_gemm<EPI_SWIGLU>(mW1, mX, sH, sGU, g1, s);
   if (err != cudaSuccess) return err;
 
@@ -710,7 +835,14 @@ cudaError_t launch_experts_forward_pair(const uint16_t* x_disp, const moe_layout
   g2.ld0 = H;
   g2.out1 = o_save;
   g2.ld1 = H;
-  return launch_pair_gemm<EPI_WEIGHTED>(mW2, mH, sY, sO, g2, s);
+  err = launch_pair_gemm<EPI_WEIGHTED>(mW2, mH, sY, sO, g2, s);
+  if (err != cudaSuccess && g2.ready != nullptr) {
+    // the down launch, which clears the slot, did not start: clear it here
+    // so that its next use does not see this use's signals
+    cudaMemsetAsync(g2.ready, 0, sizeof(int) * HR_CAP, s);
+    cudaMemsetAsync(g2.done, 0, sizeof(unsigned int), s);
+  }
+  return err;
 }
 
 }  // namespace moe

@@ -65,6 +65,12 @@ bool make_tma_store_2d_bf16_16(CUtensorMap* map, const void* base, uint64_t rows
 // The same for fp32: 32-row x 16-column boxes (64-byte rows).
 bool make_tma_store_2d_f32(CUtensorMap* map, void* base, uint64_t rows, uint64_t cols);
 
+// Unique id of the calling thread's current CUDA context; false when there is
+// none yet or the driver does not say.  The device addresses of the library's
+// static arrays are cached per device and looked up again when it changes
+// (a device reset loads the module into a new context).
+bool current_context_id(unsigned long long* id);
+
 // Records `text` as this thread's moe_last_error() and returns `st`.
 moe_status set_last_error(moe_status st, const char* text);
 
