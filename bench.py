@@ -176,13 +176,12 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- algorithmic work
 
 def experts_kernel_label(cfg, fp8: bool, gather: bool, backward: bool) -> str:
-    """Which expert GEMM kernels a bench step runs, as the library picks them
-    for layers with rows for every SM: bf16 layers averaging at most 64 rows
-    per expert take grouped_gemm_kernel with one CTA per tile; those that save
-    for the backward, or average at most 384 rows per expert, pair_gemm_kernel
-    (CTA pairs, expert rows on the MMA's N side); other bf16 layers the
-    CTA-pair form of grouped_gemm_kernel; e4m3 operands and the gathered A its
-    one-CTA form."""
+    """Which expert GEMM kernels a bench step runs, as the library picks them:
+    bf16 layers with rows for every SM take pair_gemm_kernel (CTA pairs,
+    expert rows on the MMA's N side) above 64 rows per expert on average and
+    grouped_gemm_kernel (one CTA per tile) up to that; e4m3 operands, the
+    gathered A and small layers grouped_gemm_kernel; T <= 4 in inference the
+    CUDA-core gemv_experts_kernel."""
     wide = min(cfg.T * cfg.K, cfg.E) * (cfg.I // 128) >= 152
     if cfg.T <= 4 and not backward and not fp8:
         fwd = "experts: gemv_experts_kernel<1> (gate/up + SwiGLU) + gemv_experts_kernel<2> (down x weight), CUDA cores"
@@ -192,10 +191,8 @@ def experts_kernel_label(cfg, fp8: bool, gather: bool, backward: bool) -> str:
                + ") + grouped_gemm_kernel<1> (down x weight)")
     elif cfg.T * cfg.K <= 64 * cfg.E:
         fwd = "experts: grouped_gemm_kernel<0> (gate/up + SwiGLU, one CTA per tile) + grouped_gemm_kernel<1> (down x weight)"
-    elif backward or cfg.T * cfg.K <= 384 * cfg.E:
-        fwd = "experts: pair_gemm_kernel<0> (gate/up + SwiGLU) + pair_gemm_kernel<1> (down x weight)"
     else:
-        fwd = "experts: grouped_gemm_kernel<0> (gate/up + SwiGLU, CTA pairs) + grouped_gemm_kernel<1> (down x weight)"
+        fwd = "experts: pair_gemm_kernel<0> (gate/up + SwiGLU) + pair_gemm_kernel<1> (down x weight)"
     return fwd + (" + the backward's 4 bwd_gemm_kernel launches" if backward else "")
 
 

@@ -12,6 +12,11 @@
 //          epilogue h = bf16(silu(g) * u)            (optionally g, u saved)
 //   GEMM2:  o = h W2[e]^T,  epilogue y = bf16(w_row * o)   (optionally o saved)
 //
+// This kernel takes the layers the CTA-pair kernel (gemm_pair.cu) does not:
+// bf16 layers averaging at most 64 rows per expert (or with too few rows for
+// every SM, in 64-column tiles), e4m3 gate/up operands, and the A rows
+// gathered straight from the tokens.
+//
 // Design (one CTA per SM, persistent):
 //   * the tile list is built on the device from tokens_per_expert / offsets,
 //     so no host sync is needed and the launch can be graph-captured; an
@@ -142,28 +147,18 @@ __device__ __forceinline__ Tile decode_tile(const int* tile_prefix, int E, int n
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
 
-// PAIR: the kernel runs as clusters of two CTAs on two SMs.  A tile is 256
-// rows: each CTA loads its own 128 rows of A and one half of the tile's B
-// columns (the gate or the up box of GEMM1, the first or second 128 output
-// columns of GEMM2), the even CTA issues one cta_group::2 MMA of M = 256 for
-// the pair, and each CTA's epilogue reads its own 128 rows from its own
-// tensor memory.  A stage then holds 32 KiB instead of 48, so six stages fit,
-// and each SM moves a third fewer operand bytes per multiply-add.
-template <int EPI, int BN, int A_ROWS, int STAGES, int OPS, bool GATHER, bool PAIR = false>
+template <int EPI, int BN, int A_ROWS, int STAGES, int OPS, bool GATHER>
 __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmOut, const GemmArgs args) {
   static_assert(STAGES <= MAX_STAGES, "barrier slots");
-  static_assert(!PAIR || (OPS == OPS_BF16 && !GATHER && A_ROWS == BM && BN == 256),
-                "CTA pairs: bf16 operands loaded by TMA, 128-row A boxes, 256-column tiles");
   using F = Fwd<BN, A_ROWS>;
   constexpr int A_BYTES = F::A_BYTES;
-  constexpr int B_BYTES = PAIR ? F::B_BYTES / 2 : F::B_BYTES;  // a CTA of a pair holds half of B
+  constexpr int B_BYTES = F::B_BYTES;
   constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   constexpr int TMEM_COLS = F::TMEM_COLS;
-  constexpr int RB = PAIR ? 2 * BM : BM;  // rows of a tile
-  constexpr uint32_t IDESC = OPS == OPS_E4M3 ? F::IDESC_E4M3 : (PAIR ? idesc_bf16_f32(RB, BN) : F::IDESC);
+  constexpr uint32_t IDESC = OPS == OPS_E4M3 ? F::IDESC_E4M3 : F::IDESC;
   constexpr int BKE = OPS == OPS_E4M3 ? 128 : BK;   // K elements per 128-byte row of a stage
   static_assert(OPS == OPS_BF16 || EPI == EPI_SWIGLU, "e4m3 operands only in the gate/up GEMM");
   static_assert(!GATHER || (OPS == OPS_BF16 && EPI == EPI_SWIGLU && A_ROWS == BM),
@@ -180,9 +175,6 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = args.E;
-  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // the even CTA of a pair issues the MMAs
-  const int tile0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int tstep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   griddep_launch_dependents();
 
   // ---- set-up: barriers, tensor memory, the device-side tile list
@@ -195,7 +187,7 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.tfull[i]), 1);
       // a pair's accumulator is free once the epilogue warps of both CTAs have read it
-      mbar_init(smem_u32(&s.tempty[i]), PAIR ? 2 * EPI_WARPS : EPI_WARPS);
+      mbar_init(smem_u32(&s.tempty[i]), EPI_WARPS);
     }
     mbar_init(smem_u32(&s.drain), 1);
     s.abort = 0;
@@ -204,12 +196,7 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmOut);
   }
-  if (warp == 1) {
-    if constexpr (PAIR)
-      tmem_alloc_pair(smem_u32(&s.tmem_base), TMEM_COLS);
-    else
-      tmem_alloc(smem_u32(&s.tmem_base), TMEM_COLS);
-  }
+  if (warp == 1) tmem_alloc(smem_u32(&s.tmem_base), TMEM_COLS);
   griddep_wait();  // the layout, the dispatched rows (and h) come from earlier kernels
   for (int e = threadIdx.x; e <= E; e += blockDim.x) s_off[e] = args.offsets[e];
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = args.counts[e];
@@ -221,7 +208,7 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
       // rows an expert's tiles cover: its valid rows, or with the pad rows
       // written (training) its whole padded group
       const int rows_e = e < E ? (args.write_pad ? s_off[e + 1] - s_off[e] : s_cnt[e]) : 0;
-      const int n = ((rows_e + RB - 1) / RB) * args.n_tiles;
+      const int n = ((rows_e + BM - 1) / BM) * args.n_tiles;
       int incl = n;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -238,8 +225,6 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  // a pair: both CTAs' barriers are initialised before either signals the other's
-  if constexpr (PAIR) cluster_sync_all();
   tc_fence_after();
 
   const int total = s.total_tiles;
@@ -301,32 +286,24 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
       uint32_t phase = 0;
       long long issued = 0;
       bool ok = true;
-      for (int tile = tile0; tile < total && ok; tile += tstep) {
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         const Tile t = decode_tile(s_pre, E, args.n_tiles, tile);
-        const int a_row = s_off[t.e] + t.mt * RB + static_cast<int>(rank) * BM;
+        const int a_row = s_off[t.e] + t.mt * BM;
         const int b_row = t.e * args.b_rows_per_expert + t.nt * args.b_tile_step;
         for (int kb = 0; kb < args.k_blocks; ++kb) {
           if (!mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, abort_flag)) { ok = false; break; }
           const uint32_t full = smem_u32(&s.full[stage]);
           const uint32_t a_dst = tiles_u32 + stage * STAGE_BYTES;
           const uint32_t b_dst = a_dst + A_BYTES;
-          if constexpr (PAIR) {
-            // both CTAs' loads complete on the even CTA's barrier, which expects them all
-            const uint32_t full0 = mapa_shared(full, 0);
-            if (rank == 0) mbar_arrive_expect_tx(full, 2 * STAGE_BYTES);
-            tma_load_2d_pair(a_dst, &tmA, kb * BKE, a_row, full0);
-            tma_load_2d_pair(b_dst, &tmB, kb * BKE, b_row + (rank ? args.b_second_off : 0), full0);
-          } else {
-            mbar_arrive_expect_tx(full, STAGE_BYTES);
-            tma_load_2d(a_dst, &tmA, kb * BKE, a_row, full);
-            tma_load_2d(b_dst, &tmB, kb * BKE, b_row, full);
-            tma_load_2d(b_dst + B_BYTES / 2, &tmB, kb * BKE, b_row + args.b_second_off, full);
-          }
+          mbar_arrive_expect_tx(full, STAGE_BYTES);
+          tma_load_2d(a_dst, &tmA, kb * BKE, a_row, full);
+          tma_load_2d(b_dst, &tmB, kb * BKE, b_row, full);
+          tma_load_2d(b_dst + B_BYTES / 2, &tmB, kb * BKE, b_row + args.b_second_off, full);
           ++issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
-      if (!ok && (!PAIR || rank == 0)) {
+      if (!ok) {
         // drain: wait for the loads of the last (up to STAGES) issued stages
         for (int i = 0; i < STAGES && i < issued; ++i) {
           if (--stage < 0) { stage = STAGES - 1; phase ^= 1u; }
@@ -336,17 +313,13 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ================= MMA issuer (the even CTA of a pair) =================
-    if (lane == 0 && PAIR && rank != 0) {
-      // the odd CTA of a pair issues nothing; it waits until the even CTA's
-      // last MMAs, which write its tensor memory, have completed
-      if (!mbar_wait_drain(smem_u32(&s.drain), 0)) *abort_flag = 1;
-    } else if (lane == 0) {
+    // ================= MMA issuer =================
+    if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
-      for (int tile = tile0; tile < total && ok; tile += tstep, ++local) {
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++local) {
         const int buf = local & 1;
         const uint32_t use = (local >> 1) & 1;
         if (!mbar_wait(smem_u32(&s.tempty[buf]), use ^ 1u, abort_flag)) { ok = false; break; }
@@ -365,30 +338,17 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
             // (16 bf16 or 32 e4m3 elements)
             if constexpr (OPS == OPS_E4M3)
               tc_mma_e4m3(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, IDESC, (kb | kk) != 0);
-            else if constexpr (PAIR)
-              tc_mma_bf16_pair(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, IDESC, (kb | kk) != 0);
             else
               tc_mma_bf16(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, IDESC, (kb | kk) != 0);
           }
-          if constexpr (PAIR)
-            tc_commit_pair(smem_u32(&s.empty[stage]));  // frees the stage in both CTAs
-          else
-            tc_commit(smem_u32(&s.empty[stage]));
+          tc_commit(smem_u32(&s.empty[stage]));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
-        if (ok) {
-          if constexpr (PAIR)
-            tc_commit_pair(smem_u32(&s.tfull[buf]));
-          else
-            tc_commit(smem_u32(&s.tfull[buf]));
-        }
+        if (ok) tc_commit(smem_u32(&s.tfull[buf]));
       }
       // make sure every MMA this thread issued has finished before anyone
-      // frees tensor memory or shared memory (in both CTAs of a pair)
-      if constexpr (PAIR)
-        tc_commit_pair(smem_u32(&s.drain));
-      else
-        tc_commit(smem_u32(&s.drain));
+      // frees tensor memory or shared memory
+      tc_commit(smem_u32(&s.drain));
       if (!mbar_wait_drain(smem_u32(&s.drain), 0)) *abort_flag = 1;
     }
     __syncwarp();
@@ -422,7 +382,7 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
       }
       ++n_staged;
     };
-    for (int tile = tile0; tile < total; tile += tstep, ++local) {
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
       const Tile t = decode_tile(s_pre, E, args.n_tiles, tile);
       const int buf = local & 1;
       const uint32_t use = (local >> 1) & 1;
@@ -432,13 +392,13 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
       const bool ready = mbar_wait(smem_u32(&s.tfull[buf]), use, abort_flag);
       if (!__all_sync(FULL_MASK, ready)) break;
       tc_fence_after();
-      const int group_row = t.mt * RB + static_cast<int>(rank) * BM + r_in_tile;
+      const int group_row = t.mt * BM + r_in_tile;
       // rows written: the valid rows, plus (write_pad) the pad rows of the
       // expert's group, which come out zero from the zero pad rows of x_disp
       const bool valid = group_row < (args.write_pad ? s_off[t.e + 1] - s_off[t.e] : s_cnt[t.e]);
       const bool full_warp = __all_sync(FULL_MASK, valid);
       const long long row = static_cast<long long>(s_off[t.e]) + group_row;
-      warp_row0 = s_off[t.e] + t.mt * RB + static_cast<int>(rank) * BM + q * 32;
+      warp_row0 = s_off[t.e] + t.mt * BM + q * 32;
       const uint32_t tb = tmem_base + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
       if (EPI == EPI_SWIGLU) {
         // columns [0, BN/2) gate, [BN/2, BN) up, for h columns nt*BN/2 + [0, BN/2);
@@ -538,12 +498,7 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        if constexpr (PAIR)
-          mbar_arrive_cluster(mapa_shared(smem_u32(&s.tempty[buf]), 0));  // the MMA issuer's barrier
-        else
-          mbar_arrive(smem_u32(&s.tempty[buf]));
-      }
+      if (lane == 0) mbar_arrive(smem_u32(&s.tempty[buf]));
     }
     if (lane == 0) tma_store_wait_all();
     __syncwarp();
@@ -551,52 +506,17 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  // a pair: neither CTA frees its tensor memory or leaves while the pair's
-  // MMAs, loads or barrier signals may still reach it
-  if constexpr (PAIR) cluster_sync_all();
   tc_fence_after();
-  if (warp == 1) {
-    if constexpr (PAIR)
-      tmem_dealloc_pair(tmem_base, TMEM_COLS);
-    else
-      tmem_dealloc(tmem_base, TMEM_COLS);
-  }
+  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
   if (threadIdx.x == 0 && s.abort) report(args.status, MOE_DEVERR_TIMEOUT);
 }
 
 // ---------------------------------------------------------------- host side
 
-// Persistent grid of a pair kernel: two CTAs per cluster that can be resident
-// at once (a cluster needs two free SMs of one GPC), at most one per SM.
-template <typename Kernel>
-int pair_grid(Kernel kernel, size_t smem) {
-  static int cached[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(sm_count() & ~1);
-  cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = smem;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess || clusters < 1)
-    clusters = sm_count() / 2;
-  const int grid = 2 * (clusters < sm_count() / 2 ? clusters : sm_count() / 2);
-  if (dev >= 0 && dev < 64) cached[dev] = grid;
-  return grid;
-}
-
-template <int EPI, int BN, int A_ROWS, int STAGES, int OPS, bool GATHER, bool PAIR = false>
+template <int EPI, int BN, int A_ROWS, int STAGES, int OPS, bool GATHER>
 cudaError_t launch_gemm_stages(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
                                const GemmArgs& args, cudaStream_t s) {
-  auto kernel = grouped_gemm_kernel<EPI, BN, A_ROWS, STAGES, OPS, GATHER, PAIR>;
+  auto kernel = grouped_gemm_kernel<EPI, BN, A_ROWS, STAGES, OPS, GATHER>;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -606,55 +526,26 @@ cudaError_t launch_gemm_stages(const CUtensorMap& a, const CUtensorMap& b, const
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  constexpr int stage_bytes = PAIR ? Fwd<BN, A_ROWS>::A_BYTES + Fwd<BN, A_ROWS>::B_BYTES / 2
-                                   : Fwd<BN, A_ROWS>::STAGE_BYTES;
-  const size_t smem = smem_bytes(STAGES, stage_bytes, args.E);
-  if constexpr (!PAIR) {
-    return launch_dependent(kernel, sm_count(), GATHER ? NUM_THREADS_GATHER : NUM_THREADS, smem, s, a, b,
-                            out, args);
-  } else {
-    const int grid = pair_grid(kernel, smem);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid > 0 ? grid : 2);
-    cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = 2;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kernel, a, b, out, args);
-  }
+  const size_t smem = smem_bytes(STAGES, Fwd<BN, A_ROWS>::STAGE_BYTES, args.E);
+  return launch_dependent(kernel, sm_count(), GATHER ? NUM_THREADS_GATHER : NUM_THREADS, smem, s, a, b, out,
+                          args);
 }
 
 // The ring depth of Fwd when it fits beside the staging and the per-expert
-// tables, else one stage less (E above about 200).  A CTA pair's 32 KiB
-// stages fit six deep (five for large E).
-template <int EPI, int BN, int A_ROWS, int OPS = OPS_BF16, bool GATHER = false, bool PAIR = false>
+// tables, else one stage less (E above about 200).
+template <int EPI, int BN, int A_ROWS, int OPS = OPS_BF16, bool GATHER = false>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
                         const GemmArgs& args, cudaStream_t s) {
   using F = Fwd<BN, A_ROWS>;
-  if constexpr (PAIR) {
-    constexpr int sb = F::A_BYTES + F::B_BYTES / 2;
-    if (smem_bytes(6, sb, args.E) <= static_cast<size_t>(SMEM_LIMIT))
-      return launch_gemm_stages<EPI, BN, A_ROWS, 6, OPS, GATHER, true>(a, b, out, args, s);
-    return launch_gemm_stages<EPI, BN, A_ROWS, 5, OPS, GATHER, true>(a, b, out, args, s);
-  } else {
-    if (smem_bytes(F::STAGES, F::STAGE_BYTES, args.E) <= static_cast<size_t>(SMEM_LIMIT))
-      return launch_gemm_stages<EPI, BN, A_ROWS, F::STAGES, OPS, GATHER>(a, b, out, args, s);
-    return launch_gemm_stages<EPI, BN, A_ROWS, F::STAGES - 1, OPS, GATHER>(a, b, out, args, s);
-  }
+  if (smem_bytes(F::STAGES, F::STAGE_BYTES, args.E) <= static_cast<size_t>(SMEM_LIMIT))
+    return launch_gemm_stages<EPI, BN, A_ROWS, F::STAGES, OPS, GATHER>(a, b, out, args, s);
+  return launch_gemm_stages<EPI, BN, A_ROWS, F::STAGES - 1, OPS, GATHER>(a, b, out, args, s);
 }
 
 // GEMM1 reads A (x_disp rows) and B (W1) as bf16, or as e4m3 codes with
 // fp32 scales per A row and per W1 row, or (GATHER) A straight from the
 // tokens x by row_token; GEMM2 is bf16.
-template <int BN, int A_ROWS, int OPS, bool GATHER = false, bool PAIR = false>
+template <int BN, int A_ROWS, int OPS, bool GATHER = false>
 cudaError_t experts_forward(const void* x_disp, const float* x_scale, const moe_layout& L, int H,
                             int I, const void* W1, const float* W1_scale, const uint16_t* W2,
                             uint16_t* h, uint16_t* y, uint16_t* o_save, uint16_t* gu_save,
@@ -698,7 +589,7 @@ cudaError_t experts_forward(const void* x_disp, const float* x_scale, const moe_
   g1.row_token = L.row_token;
   g1.capacity = L.capacity;
   g1.H = H;
-  cudaError_t err = launch_gemm<EPI_SWIGLU, BN, A_ROWS, OPS, GATHER, PAIR>(mA1, mB1, mH, g1, s);
+  cudaError_t err = launch_gemm<EPI_SWIGLU, BN, A_ROWS, OPS, GATHER>(mA1, mB1, mH, g1, s);
   if (err != cudaSuccess) return err;
 
   GemmArgs g2 = g1;
@@ -713,7 +604,7 @@ cudaError_t experts_forward(const void* x_disp, const float* x_scale, const moe_
   g2.ld1 = H;
   g2.a_scale = nullptr;
   g2.b_scale = nullptr;
-  return launch_gemm<EPI_WEIGHTED, BN, A_ROWS, OPS_BF16, false, PAIR>(mA2, mB2, mY, g2, s);
+  return launch_gemm<EPI_WEIGHTED, BN, A_ROWS, OPS_BF16, false>(mA2, mB2, mY, g2, s);
 }
 
 // The tile shape for a layer (all from host-known sizes, so the sync-free
@@ -732,27 +623,17 @@ Shape pick_shape(const moe_layout& L, int I, bool write_pad) {
   return stored <= 32 ? Shape::kNarrowShortA : Shape::kNarrow;
 }
 
-// Which kernel takes a bf16 layer with rows for every SM (all from
-// host-known sizes, so the sync-free path needs no row counts):
-//   * at most 64 rows per expert on average: one CTA per tile.  The step is a
-//     weight stream, and a CTA's four 48 KiB stages hold 128 KiB of weights in
-//     flight per SM, where a pair's 32 KiB stages hold 96 KiB (decode T = 256:
-//     206 against 215 us);
-//   * the forward saves its operands for the backward, or at most 384 rows
-//     per expert: CTA pairs with the expert rows on the MMA's N side
-//     (gemm_pair.cu) -- their staged stores of g, u and o are the faster
-//     ones, and 256-row tiles on the M side would spend up to half of their
-//     MMAs on rows past an expert's end;
-//   * otherwise CTA pairs with the rows on the M side: with ~1024 rows per
-//     expert that waste is small, and these tiles ran a few percent faster
-//     back to back (T = 16384).
-enum class WideKernel { kSingle, kPairRowsN, kPairRowsM };
-
-WideKernel wide_kernel(const moe_layout& L, bool saves) {
+// Which kernel takes a bf16 layer with rows for every SM (from host-known
+// sizes, so the sync-free path needs no row counts): at most 64 rows per
+// expert on average, one CTA per tile -- the step is a weight stream, and a
+// CTA's four 48 KiB stages hold 128 KiB of weights in flight per SM where a
+// pair's stages hold 96 KiB (decode T = 256: 206 against 215 us); otherwise
+// CTA pairs with the expert rows on the MMA's N side (gemm_pair.cu).  (CTA
+// pairs with the rows on the M side, 256-row tiles, ran slower at every
+// size: 301 against 296 us at T = 4096, 830 against 809 us at T = 16384.)
+bool wide_single_cta(const moe_layout& L) {
   const long long pairs = static_cast<long long>(L.T) * L.K;
-  if (pairs <= 64LL * L.E) return WideKernel::kSingle;
-  if (saves || pairs <= 384LL * L.E) return WideKernel::kPairRowsN;
-  return WideKernel::kPairRowsM;
+  return pairs <= 64LL * L.E;
 }
 
 template <int OPS>
@@ -763,16 +644,9 @@ cudaError_t experts_forward_any(const void* x_disp, const float* x_scale, const 
   switch (pick_shape(L, I, gu_save != nullptr)) {
     case Shape::kWide:
       if constexpr (OPS == OPS_BF16) {
-        switch (wide_kernel(L, gu_save != nullptr || o_save != nullptr)) {
-          case WideKernel::kPairRowsN:
-            return launch_experts_forward_pair(static_cast<const uint16_t*>(x_disp), L, H, I,
-                                               static_cast<const uint16_t*>(W1), W2, h, y, o_save, gu_save, s);
-          case WideKernel::kPairRowsM:
-            return experts_forward<256, 128, OPS, false, true>(x_disp, x_scale, L, H, I, W1, W1_scale, W2, h,
-                                                               y, o_save, gu_save, s);
-          case WideKernel::kSingle:
-            break;
-        }
+        if (!wide_single_cta(L))
+          return launch_experts_forward_pair(static_cast<const uint16_t*>(x_disp), L, H, I,
+                                             static_cast<const uint16_t*>(W1), W2, h, y, o_save, gu_save, s);
         return experts_forward<256, 128, OPS>(x_disp, x_scale, L, H, I, W1, W1_scale, W2, h, y, o_save,
                                               gu_save, s);
       } else

@@ -436,14 +436,14 @@ def test_experts_skewed_layer_matches_oracle(moe, save):
     (3, 8192, 8, 2, 128, 1),       # wide H: the A rows outgrow the CUDA-core path, tensor cores take it
     (4, 2048, 1024, 8, 768, 1),    # E = 1024: a long expert scan, 32 active experts
     (64, 256, 8, 2, 128, 16),      # tensor-core path without saved operands
-    (1500, 512, 40, 8, 512, 1),    # CTA pairs, expert rows on the MMA's N side: ~300 rows each, ragged last chunks
-    (2048, 512, 16, 8, 1536, 128), # CTA pairs, expert rows on the M side: ~1024 rows per expert
+    (1500, 512, 40, 8, 512, 1),    # CTA pairs: ~300 rows per expert, ragged last chunks
+    (2048, 512, 16, 8, 1536, 128), # CTA pairs: ~1024 rows per expert, four full 256-row chunks each
 ])
 def test_experts_inference_match_oracle(moe, T, H, E, K, I, P):
     """Inference (nothing saved for a backward): layers with at most four rows
     per expert take the CUDA-core path, larger ones the tensor cores; layers
-    with rows for every SM take CTA pairs, with the expert rows on the N side
-    of the MMA up to 384 rows per expert on average and on the M side above."""
+    with rows for every SM and more than 64 rows per expert take CTA pairs
+    with the expert rows on the MMA's N side."""
     idx, p, x, W1, W2, C, fwd = _experts_case(moe, T, H, E, K, I, P, seed=3 * T + H, save=False)
     Lr = O.build_layout(*O.route_to_multihot(idx.numpy(), p.numpy(), E)[:2], K, P, C)
     xd = bits(fwd.x_disp)
