@@ -21,16 +21,16 @@
 // e.g. 2 x 144 for 272 rows, was slower: MMAs with N between 128 and 256
 // ran below the rate of N = 256.)
 //
-// GEMM1 loads the gate and up rows of W1 interleaved (a 4-D tensor map):
+// GEMM1 loads the gate and up rows of W1 interleaved (a 5-D tensor map):
 // weight row 2j of a CTA's 128 is gate row f + j and row 2j + 1 is up row
 // f + j.  Lanes 2j and 2j + 1 of tensor memory then hold the gate and up
 // values of one h column, and the SwiGLU pairs them with one shuffle.
 //
 // Roles (one CTA per SM, clusters of two, persistent over a tile list built
 // on the device from the counts and offsets, so no host sync is needed):
-//   * warp 0 issues the TMA loads of both operands into a ring of 32 KiB
-//     stages (weights 16 KiB, expert rows up to 16 KiB), completing on the
-//     even CTA's barrier;
+//   * warp 0 issues the TMA loads of both operands into a ring of 64 KiB
+//     stages of 128 K columns (weights 32 KiB, expert rows up to 32 KiB),
+//     completing on the even CTA's barrier;
 //   * warp 1 of the even CTA issues the pair's tcgen05.mma (cta_group::2);
 //   * warps 2-9 are the epilogue: two warps per 32-lane quarter of tensor
 //     memory, taking alternate 32-column chunks.  An epilogue thread holds
@@ -740,23 +740,24 @@ unsigned int* g_done_ptr[64];
 unsigned long long g_ready_ctx[64];
 std::atomic<unsigned int> g_ready_next{0};
 
-// A slot of readiness counters on the current device, or false.  Their
-// device address is looked up on the first use on each device (and again
-// after a device reset); the lookup can load the library's module, so a first
-// use while `stream` is being captured goes without (the down launch then
-// waits for the whole gate/up launch).
+// A slot of readiness counters on the current device, or false.  A launch
+// pair that is being captured into a graph goes without (the down launch then
+// waits for the whole gate/up launch): a graph would keep the slot it was
+// captured with for every replay, while eager launch pairs on other streams
+// go on rotating through all the slots.  The counters' device address is
+// looked up on the first use on each device (and again after a device reset).
 bool ready_counters(cudaStream_t stream, int** ready, unsigned int** done) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+    cudaGetLastError();
+    return false;
+  }
   unsigned long long ctx = 0;
   const bool known_ctx = current_context_id(&ctx);
   std::lock_guard<std::mutex> lock(g_ready_mu);
   if (g_ready_ptr[dev] == nullptr || !known_ctx || g_ready_ctx[dev] != ctx) {
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
-      cudaGetLastError();
-      return false;
-    }
     void* r = nullptr;
     void* d = nullptr;
     if (cudaGetSymbolAddress(&r, g_h_ready) != cudaSuccess || cudaGetSymbolAddress(&d, g_h_done) != cudaSuccess) {

@@ -218,10 +218,13 @@ def test_opcheck_every_operator(moe):
         torch.library.opcheck(op, args, test_utils=utils)
 
 
-def test_cuda_graph_replay_equals_eager(moe):
+@pytest.mark.parametrize("T,H,E,K,I,P", [
+    (256, 512, 8, 2, 256, 16),    # one-CTA expert tiles
+    (1500, 512, 40, 8, 512, 16),  # CTA-pair expert tiles; eager with per-chunk readiness, captured without
+])
+def test_cuda_graph_replay_equals_eager(moe, T, H, E, K, I, P):
     """Forward + backward captured once after an eager warm-up, replayed on
     new inputs copied into the static ones: replay == eager, bit for bit."""
-    T, H, E, K, I, P = 256, 512, 8, 2, 256, 16
     W1, W2 = synthetic.make_weights(E, H, I, 4, device=DEV)
     W1.requires_grad_(True)
     W2.requires_grad_(True)

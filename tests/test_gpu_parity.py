@@ -393,9 +393,9 @@ def test_experts_skewed_layer_matches_oracle(moe, save):
     """A skewed layer on CTA pairs (log-Zipf router bias, 5 % dropped slots, 40
     experts): the largest expert has over a thousand rows, so its tiles take
     many 256-row chunks and a ragged last one, next to experts with a few
-    rows.  With the operands saved (training) the rows sit on the MMA's N
-    side and the pad rows are written as zeros; in inference the layer
-    averages about 300 rows per expert, which takes the same kernel."""
+    rows.  The layer averages 300 rows per expert, so with and without saved
+    operands it runs the kernel with the expert rows on the MMA's N side;
+    with them (training) the pad rows are written as zeros."""
     T, H, E, K, I, P = 3000, 512, 40, 4, 512, 16
     idx, p = synthetic.make_routing(T, E, K, seed=11, zipf_s=1.2, drop=0.05)
     counts = np.bincount(idx[idx >= 0].numpy().ravel(), minlength=E)
