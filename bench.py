@@ -59,6 +59,7 @@ def profiled_traffic(workload: str):
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return rec["bytes"] if h.hexdigest()[:16] == rec["src"] else None
+CLOCK_EXTRA_S = 0.6
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -154,10 +155,12 @@ class ClockSampler:
                 self.proc.kill()
             self._reader.join(timeout=5)
 
-    def summary(self):
+    def summary(self, upto=None):
+        """Median SM clock, the maximum and the throttle reasons seen, over the
+        first ``upto`` samples (all when None)."""
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in self.lines:
+        for l in (self.lines if upto is None else self.lines[:upto]):
             f = [x.strip() for x in l.split(",")]
             if len(f) < 9:
                 continue
@@ -456,6 +459,15 @@ def run_ours(args, world, rank, local, leg: bool = False):
             w_ev[wi + 1].record(stream)
         t1.record(stream)
         torch.cuda.synchronize()
+        n_timed_samples = len(clk.lines)
+        # A timed region of a few ms sees one or two clock samples; the same
+        # steps, repeated untimed for about CLOCK_EXTRA_S more, give the clock
+        # record a longer look at the GPU under this load (reported apart).
+        t_end = time.time() + CLOCK_EXTRA_S
+        while time.time() < t_end:
+            for fn, _ in units:
+                fn()
+            torch.cuda.synchronize()
     barrier(world)
     ms = t0.elapsed_time(t1)
     windows = window_summary([w_ev[i].elapsed_time(w_ev[i + 1]) for i in range(len(bounds))],
@@ -709,7 +721,9 @@ def run_ours(args, world, rank, local, leg: bool = False):
         "roofline": roof,
         "kernels": kernels,
     }
-    res["clocks"] = clk.summary()
+    res["clocks"] = clk.summary(n_timed_samples)
+    res["clocks_extended"] = dict(clk.summary(), window=f"the timed region and {CLOCK_EXTRA_S} s of the same "
+                                                         "steps repeated right after it, untimed")
     return res
 
 

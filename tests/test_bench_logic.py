@@ -83,3 +83,17 @@ def test_window_summary_takes_the_median_window():
     w = bench.window_summary([4.0, 4.4, 8.0, 4.2, 4.0], [4, 4, 4, 4, 4])
     assert w["median_ms_per_step"] == 1.05
     assert abs(w["spread"] - (2.0 - 1.0) / 1.05) < 1e-12
+
+
+def test_clock_summary_of_the_timed_samples_and_of_all():
+    """The timed region's clock record uses only the samples taken up to its
+    end; the extended record (the same steps repeated after it) all of them,
+    with every throttle reason seen."""
+    c = bench.ClockSampler(0)
+    row = "0, {sm}, 2070, 900, 0x0, Not Active, Not Active, Not Active, {cap}\n"
+    c.lines = [row.format(sm=2070, cap="Not Active"), row.format(sm=2070, cap="Not Active"),
+               row.format(sm=1800, cap="Active"), "garbled\n"]
+    timed = c.summary(2)
+    assert timed == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 2}
+    every = c.summary()
+    assert every["samples"] == 3 and every["reasons"] == ["sw_power_cap"] and every["sm_mhz"] == 2070.0
