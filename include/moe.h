@@ -319,13 +319,22 @@ MOE_API moe_status moe_dispatch_static_scratch(const moe_bf16* x, const uint8_t*
  *           the routing-weight gradient needs.
  *   gu_save [C, 2I] bf16 (out, nullable): bf16 of the gate and up
  *           pre-activations, which the expert backward needs.
- * Each expert's rows are computed in 128-row tiles (ceil(count / 128) of
- * them).  The valid rows are written.  When gu_save is given (training), the
- * pad rows of each expert's group that its tiles cover are written too, and
- * come out as zeros in h, y, o_save and gu_save because moe_dispatch leaves
- * x_disp's pad rows zero and their weight is 0; without gu_save they are not
- * touched.  Spare rows (R..C-1) are never written.  The row counts are read on
- * the device, so the call never synchronises and can be captured.
+ * Above 64 rows per expert on average (T*K > 64*E) each expert's rows are
+ * computed in chunks of up to 256 on CTA pairs; smaller layers in 128-row
+ * tiles, one CTA each.  The valid rows are written.  When gu_save is given
+ * (training), the pad rows of each expert's group are written too (with
+ * 128-row tiles, those the tiles cover), and come out as zeros in h, y, o_save
+ * and gu_save because moe_dispatch leaves x_disp's pad rows zero and their
+ * weight is 0; without gu_save they are not touched.  Spare rows (R..C-1) are
+ * never written.  The row counts are read on the device, so the call never
+ * synchronises and can be captured.
+ * On CTA pairs an eager call takes one of 16 slots of row-chunk readiness
+ * counters (static device memory of the library, 2 x 128 KiB per GPU), so
+ * that the down projection can start on a chunk as soon as its h is written;
+ * a call being captured into a graph takes none and waits for the whole
+ * gate/up launch instead.  Calls on one stream are ordered; more than 16 such
+ * calls in flight at once on different streams would share a slot, so order
+ * them (one stream, or events).
  */
 MOE_API moe_status moe_grouped_experts(const moe_bf16* x_disp, const moe_layout* L,
                                int32_t H, int32_t I,
