@@ -360,7 +360,8 @@ def _experts_case(moe, T, H, E, K, I, P, seed, drop=0.0, save=True):
     # the cases above have few experts with rows, so the GEMMs take 64-column
     # tiles; these have enough for 256-column tiles on every SM
     (64, 256, 64, 4, 384, 16),     # 256-column tiles, a few rows per expert
-    (2000, 512, 40, 4, 512, 1),    # 256-column tiles, two 128-row tiles per expert
+    (2000, 512, 40, 4, 512, 1),    # CTA pairs, rows on N: ~200 rows per expert, one chunk each
+    (2304, 256, 256, 8, 128, 16),  # CTA pairs with two stages (E = 256: the per-expert tables take the third)
     (700, 256, 1024, 4, 128, 1),   # the largest E: per-expert tables take a pipeline stage
 ])
 def test_experts_match_oracle(moe, T, H, E, K, I, P):
@@ -438,6 +439,7 @@ def test_experts_skewed_layer_matches_oracle(moe, save):
     (64, 256, 8, 2, 128, 16),      # tensor-core path without saved operands
     (1500, 512, 40, 8, 512, 1),    # CTA pairs: ~300 rows per expert, ragged last chunks
     (2048, 512, 16, 8, 1536, 128), # CTA pairs: ~1024 rows per expert, four full 256-row chunks each
+    (2304, 256, 256, 8, 128, 1),   # CTA pairs with two stages (E = 256), ~72 rows per expert
 ])
 def test_experts_inference_match_oracle(moe, T, H, E, K, I, P):
     """Inference (nothing saved for a backward): layers with at most four rows
