@@ -15,8 +15,10 @@ namespace moe {
 
 namespace {
 
-__device__ __forceinline__ int pick4(const int (&a)[4], int j) {
-  return j == 0 ? a[0] : j == 1 ? a[1] : j == 2 ? a[2] : a[3];
+template <int KW>
+__device__ __forceinline__ int pick4(const int (&a)[KW], int j) {
+  if constexpr (KW == 1) return a[0];
+  else return j == 0 ? a[0] : j == 1 ? a[1] : j == 2 ? a[2] : a[3];
 }
 
 __device__ __forceinline__ void acc_add(float (&acc)[8], const uint4& v) {
@@ -40,8 +42,9 @@ __device__ __forceinline__ uint4 acc_pack(const float (&acc)[8]) {
 // (up to 8 at a time) are loaded before they are added, in row order, so an
 // item costs one memory round trip; T * H/256 items keep every SM busy even
 // at small T.  With SCATTER, the warp of chunk 0 also writes the token's
-// grad_probs row.
-template <bool SCATTER>
+// grad_probs row.  KW: 32-slot words of a token's row list (1 for K <= 32,
+// else 4).
+template <bool SCATTER, int KW>
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ rows,
                                                       const int* __restrict__ token_row, int T,
                                                       int K, int H, uint16_t* __restrict__ out,
@@ -55,26 +58,39 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
   const int V = H >> 8;  // 512-byte chunks per row
   const long long items = static_cast<long long>(T) * V;
   const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-  for (long long it = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-       it < items; it += nwarps) {
+  // The token_row entries of the warp's next item are loaded while the
+  // current item's rows are, so that an item costs one memory round trip
+  // rather than two (its row list, then its rows).
+  auto load_rows_of = [&](long long item, int (&dst)[KW]) {
+    const long long tt = item / V;
+#pragma unroll
+    for (int jj = 0; jj < KW; ++jj) {
+      const int k = lane + 32 * jj;
+      dst[jj] = item < items && k < K ? __ldg(token_row + tt * K + k) : -1;
+    }
+  };
+  long long it = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  int tr_next[KW];
+  load_rows_of(it, tr_next);
+  for (; it < items; it += nwarps) {
     const long long t = it / V;
     const int v = static_cast<int>(it - t * V);
-    int tr[4];
+    int tr[KW];
     int n = 0;
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      const int k = lane + 32 * jj;
-      tr[jj] = k < K ? __ldg(token_row + t * K + k) : -1;
+    for (int jj = 0; jj < KW; ++jj) {
+      tr[jj] = tr_next[jj];
       if (!MOE_IN_BOUNDS(tr[jj] < C, status)) tr[jj] = -1;
       n += __popc(__ballot_sync(FULL_MASK, tr[jj] >= 0));
     }
+    load_rows_of(it + nwarps, tr_next);
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int j0 = 0; j0 < n; j0 += 8) {
       uint4 b[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int j = j0 + i;
-        const int r = __shfl_sync(FULL_MASK, pick4(tr, j >> 5), j & 31);
+        const int r = __shfl_sync(FULL_MASK, pick4<KW>(tr, j >> 5), j & 31);
         if (j < n)
           b[i] = __ldg(reinterpret_cast<const uint4*>(rows + static_cast<long long>(r) * H) + lane + 32 * v);
       }
@@ -89,7 +105,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
         *reinterpret_cast<float4*>(gp + e) = make_float4(0.f, 0.f, 0.f, 0.f);
       __syncwarp();
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
+      for (int jj = 0; jj < KW; ++jj) {
         const int r = tr[jj];
         if (r >= 0 && MOE_IN_BOUNDS(row_expert[r] >= 0 && row_expert[r] < E, status))
           gp[row_expert[r]] = grad_w ? grad_w[r] : 0.f;
@@ -107,16 +123,24 @@ cudaError_t launch_combine(const uint16_t* rows, const moe_layout& L, int H, uin
   const long long items = static_cast<long long>(L.T) * (H >> 8);
   const long long need = (items + 7) / 8;
   const int blocks = static_cast<int>(need < 8LL * sm_count() ? need : 8LL * sm_count());
+  const long long C = static_cast<long long>(L.capacity);
   if (grad_probs) {
-    combine_kernel<true><<<blocks, threads, 0, s>>>(rows, L.token_row, L.T, L.K, H, out,
-                                                    L.row_expert, grad_w, grad_probs, L.E,
-                                                    static_cast<long long>(L.capacity), L.status);
-  } else {
-    return launch_dependent(combine_kernel<false>, blocks, threads, 0, s, rows, L.token_row, L.T, L.K,
-                            H, out, static_cast<const int*>(nullptr), static_cast<const float*>(nullptr),
-                            static_cast<float*>(nullptr), L.E, static_cast<long long>(L.capacity), L.status);
+    if (L.K <= 32)
+      combine_kernel<true, 1><<<blocks, threads, 0, s>>>(rows, L.token_row, L.T, L.K, H, out, L.row_expert, grad_w,
+                                                         grad_probs, L.E, C, L.status);
+    else
+      combine_kernel<true, 4><<<blocks, threads, 0, s>>>(rows, L.token_row, L.T, L.K, H, out, L.row_expert, grad_w,
+                                                         grad_probs, L.E, C, L.status);
+    return cudaGetLastError();
   }
-  return cudaGetLastError();
+  const int* no_expert = nullptr;
+  const float* no_grad_w = nullptr;
+  float* no_grad_probs = nullptr;
+  if (L.K <= 32)
+    return launch_dependent(combine_kernel<false, 1>, blocks, threads, 0, s, rows, L.token_row, L.T, L.K, H, out,
+                            no_expert, no_grad_w, no_grad_probs, L.E, C, L.status);
+  return launch_dependent(combine_kernel<false, 4>, blocks, threads, 0, s, rows, L.token_row, L.T, L.K, H, out,
+                          no_expert, no_grad_w, no_grad_probs, L.E, C, L.status);
 }
 
 }  // namespace moe
