@@ -129,6 +129,10 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint3
                : "memory");
 }
 
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until every cp.async group this thread committed has landed.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // The mbarrier's pending count drops by one once every cp.async this thread
 // issued so far has landed (the arrival is counted in the barrier's init count).
 __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {

@@ -22,15 +22,16 @@
 //      (block scans); CTA 0 writes offsets and totals and hands R, N and the
 //      status word to a host-synced caller through mapped memory.
 //   D. Items: the T tokens, then the C - N pad and spare rows, one warp each.
-//      A token's warp (from the top-k choices, after writing the token's
-//      multihot row: routing_map, probs, winner_slot) finds its experts in
-//      ascending order, places each pair
-//      at offsets[e] + start[e][chunk] + popcount(mask below the token),
-//      writes the rows' metadata and token_row, puts the token's x row into
-//      its 4 KiB shared-memory slot, and one lane hands each of the token's
-//      rows to the TMA engine as a bulk copy (cp.async.bulk shared -> global),
-//      so a warp issues a few instructions per row.  A pad or spare row is a
-//      bulk copy of a zeroed slot and gets the sentinel metadata.
+//      A token's warp starts copying the token's x row into its 4 KiB
+//      shared-memory slot (cp.async), then (from the top-k choices, after
+//      writing the token's multihot row: routing_map, probs, winner_slot)
+//      finds its experts in ascending order, places each pair
+//      at offsets[e] + start[e][chunk] + popcount(mask below the token) and
+//      writes the rows' metadata and token_row while the copy lands; one lane
+//      then hands each of the token's rows to the TMA engine as a bulk copy
+//      (cp.async.bulk shared -> global), so a warp issues a few instructions
+//      per row.  A pad or spare row is a bulk copy of a zeroed slot and gets
+//      the sentinel metadata.
 // The two barriers release the CTAs through replicated flags and phase B
 // publishes each count in replicated copies, so the 600-odd CTAs do not all
 // poll or read one L2 line.  Nothing is loaded ahead for phase D: in-kernel
@@ -307,6 +308,18 @@ __global__ void __launch_bounds__(FD_THREADS, 4) dispatch_fused_kernel(FusedArgs
   for (long long it = gwarp; it < items; it += gwarps) {
     if (it < a.T) {
       const long long t = it;
+      // the first 4 KiB of x[t] start into the warp's slot now (cp.async, no
+      // registers held) and land while the token's rows are placed below
+      const uint4* src = a.x ? reinterpret_cast<const uint4*>(a.x + t * a.H) : nullptr;
+      if (src) {
+        if (lane == 0) tma_store_wait_read<0>();  // the slot's previous copies have read it
+        __syncwarp();
+        const int nv = min(FD_PF, V);
+#pragma unroll
+        for (int i = 0; i < FD_PF; ++i)
+          if (i < nv) cp_async_16(slot + 16 * (lane + 32 * i), src + lane + 32 * i, 16u);
+        cp_async_commit();
+      }
       int n = 0;  // the token's rows, in ascending expert order, go to rows[0 .. n)
       if constexpr (IN == IN_MAP) {
         const int E4 = E >> 2;
@@ -385,22 +398,26 @@ __global__ void __launch_bounds__(FD_THREADS, 4) dispatch_fused_kernel(FusedArgs
       __syncwarp();
       if (a.x == nullptr) continue;
       // x[t] into each of the token's rows, 4 KiB at a time: the lanes put the
-      // piece into the warp's slot, one lane bulk-copies it to every row
-      const uint4* src = reinterpret_cast<const uint4*>(a.x + t * a.H);
+      // piece into the warp's slot (the first one is already on its way), one
+      // lane bulk-copies it to every row
       for (int v0 = 0; v0 < V; v0 += FD_PF) {
         const int nv = min(FD_PF, V - v0);
-        uint4 xr[FD_PF];
+        if (v0 == 0) {
+          cp_async_wait_all();
+        } else {
+          uint4 xr[FD_PF];
 #pragma unroll
-        for (int i = 0; i < FD_PF; ++i)
-          if (i < nv) xr[i] = __ldg(src + lane + 32 * (v0 + i));
-        if (lane == 0) tma_store_wait_read<0>();  // the slot's previous copies have read it
-        __syncwarp();
+          for (int i = 0; i < FD_PF; ++i)
+            if (i < nv) xr[i] = __ldg(src + lane + 32 * (v0 + i));
+          if (lane == 0) tma_store_wait_read<0>();  // the slot's previous copies have read it
+          __syncwarp();
 #pragma unroll
-        for (int i = 0; i < FD_PF; ++i)
-          if (i < nv)
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(slot + 16 * (lane + 32 * i)),
-                         "r"(xr[i].x), "r"(xr[i].y), "r"(xr[i].z), "r"(xr[i].w)
-                         : "memory");
+          for (int i = 0; i < FD_PF; ++i)
+            if (i < nv)
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(slot + 16 * (lane + 32 * i)),
+                           "r"(xr[i].x), "r"(xr[i].y), "r"(xr[i].z), "r"(xr[i].w)
+                           : "memory");
+        }
         fence_async_shared();
         __syncwarp();
         if (lane == 0) {
