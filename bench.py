@@ -208,15 +208,15 @@ def step_launches(T: int, H: int, E: int, C: int, fp8: bool, gather: bool, backw
     The dispatch of a layer of more than 8 chunks of 32 tokens is one
     cooperative kernel, which in the bf16 step also does the multihot step; the
     --gather step runs the multihot kernel and that kernel without rows, the
-    FP8 step the multihot, layout and FP8 row kernels.  Smaller layers run the
+    FP8 step the multihot kernel and that kernel with e4m3 rows.  Smaller layers run the
     multihot kernel, the barrier-free layout kernel and the row copy, except
     that a layer of at most two chunks, whose one-CTA layout fits 48 KiB of
     shared memory and whose row pass has at most 64 items (tokens + rows) and
     256 KiB, lays out and copies in one kernel (bf16 only)."""
     chunks = -(-T // 32)
     fused_smem = (4 * E + 2) * 4 + 8 * 128 * 4
-    if chunks > 8 and fused_smem <= 48 * 1024 and not fp8:
-        n = 1 if not gather else 2
+    if chunks > 8 and fused_smem <= 48 * 1024:
+        n = 2 if (gather or fp8) else 1
     elif chunks > 8:
         n = 3
     else:

@@ -260,12 +260,13 @@ moe_status dispatch_impl(const char* who, const moe_bf16* x, const uint8_t* rout
   cudaError_t err;
   bool rows_done = false;  // the layout kernel did the row pass itself
   const bool bf16_rows = x_disp || layout_only;
-  const bool fused = bf16_rows && dispatch_fused_fits(*L);
+  const bool fp8_rows = !bf16_rows && x_q != nullptr;
+  const bool fused = (bf16_rows || (fp8_rows && !topk_idx)) && dispatch_fused_fits(*L);
   const uint16_t* x16 = reinterpret_cast<const uint16_t*>(x);
   uint16_t* xd16 = reinterpret_cast<uint16_t*>(x_disp);
   int* rb_kernel = mapped ? rb_dev : nullptr;
   if (topk_idx && !fused) {
-    // small layers and the FP8 rows: the multihot step first, then the layout from its map
+    // small layers and the FP8 rows from the top-k: the multihot step first, then the layout from its map
     if ((err = launch_multihot(topk_idx, topk_probs, L->T, L->K, L->E, const_cast<uint8_t*>(routing_map),
                                const_cast<float*>(probs), winner, L->status, stream)) != cudaSuccess) {
       if (mapped) rb_lock.unlock();
@@ -276,7 +277,9 @@ moe_status dispatch_impl(const char* who, const moe_bf16* x, const uint8_t* rout
     err = topk_idx ? launch_dispatch_fused_topk(topk_idx, topk_probs, const_cast<uint8_t*>(routing_map),
                                                 const_cast<float*>(probs), winner, *L, H, x16, xd16, rb_kernel,
                                                 stream)
-                   : launch_dispatch_fused_map(routing_map, probs, *L, H, x16, xd16, rb_kernel, stream);
+                   : fp8_rows ? launch_dispatch_fused_map_fp8(routing_map, probs, *L, H, x16, x_q, x_scale, rb_kernel,
+                                                              stream)
+                              : launch_dispatch_fused_map(routing_map, probs, *L, H, x16, xd16, rb_kernel, stream);
     if (err != cudaSuccess) {
       if (mapped) cudaStreamSynchronize(stream);  // the kernel may still write the readback buffer
       return cuda_fail(err, "dispatch: fused layout and rows");

@@ -47,6 +47,7 @@
 
 #include "common.cuh"
 #include "coop.cuh"
+#include "fp8_quant.cuh"
 #include "launch.h"
 
 namespace moe {
@@ -93,6 +94,8 @@ struct FusedArgs {
   int* status;
   int* readback;      // {R, N, status} in host-mapped memory, or NULL
   uint16_t* x_disp;
+  uint8_t* x_q;       // FP8 rows: e4m3 codes [C, H] and one fp32 scale per row [C]
+  float* x_scale;
 };
 
 // Token t's K slots, slot k in lane k % 32, register k / 32 (-1 = none); an
@@ -130,7 +133,9 @@ __device__ __forceinline__ int pair_row(const FusedArgs& a, const int* s_off, lo
   return s_off[e] + __ldcg(a.starts + i) + __popc(m & ((1u << tl) - 1u));
 }
 
-template <int IN>
+// FP8: the rows are written as e4m3 codes with one scale per row (the
+// rowwise format of fp8_quant.cuh) to x_q / x_scale instead of bf16 to x_disp.
+template <int IN, bool FP8>
 __global__ void __launch_bounds__(FD_THREADS, 4) dispatch_fused_kernel(FusedArgs a) {
   extern __shared__ __align__(128) uint8_t fd_smem[];
   __shared__ int s_warp[33];
@@ -154,7 +159,7 @@ __global__ void __launch_bounds__(FD_THREADS, 4) dispatch_fused_kernel(FusedArgs
   const long long gwarps = static_cast<long long>(gridDim.x) * FD_WARPS;
   const int V = a.H >> 8;  // 16-byte vectors per lane of one row
 
-  if (a.x_disp) {  // the zero slot of the pad and spare rows
+  if (FP8 ? a.x_q != nullptr : a.x_disp != nullptr) {  // the zero slot of the pad and spare rows
     for (int i = threadIdx.x; i < FD_SLOT / 16; i += FD_THREADS)
       reinterpret_cast<uint4*>(s_zero)[i] = make_uint4(0, 0, 0, 0);
     fence_async_shared();
@@ -311,7 +316,7 @@ __global__ void __launch_bounds__(FD_THREADS, 4) dispatch_fused_kernel(FusedArgs
       // the first 4 KiB of x[t] start into the warp's slot now (cp.async, no
       // registers held) and land while the token's rows are placed below
       const uint4* src = a.x ? reinterpret_cast<const uint4*>(a.x + t * a.H) : nullptr;
-      if (src) {
+      if (!FP8 && src) {
         if (lane == 0) tma_store_wait_read<0>();  // the slot's previous copies have read it
         __syncwarp();
         const int nv = min(FD_PF, V);
@@ -397,6 +402,38 @@ __global__ void __launch_bounds__(FD_THREADS, 4) dispatch_fused_kernel(FusedArgs
       for (int j = n + lane; j < K; j += 32) a.token_row[t * K + j] = -1;
       __syncwarp();
       if (a.x == nullptr) continue;
+      if constexpr (FP8) {
+        // the token's codes, quantized once with the row's scale, 2 KiB at a
+        // time into the warp's slot, one lane bulk-copying them to every row
+        const float scale = row_scale(src, V, lane);
+        for (int j = lane; j < n; j += 32) {
+          const int r = rows[j];
+          if (r >= 0 && r < C) a.x_scale[r] = scale;
+        }
+        for (int v0 = 0; v0 < V; v0 += FD_PF) {
+          const int nv = min(FD_PF, V - v0);
+          if (lane == 0) tma_store_wait_read<0>();  // the slot's previous copies have read it
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < FD_PF; ++i)
+            if (i < nv) {
+              const uint2 c = quantize8(__ldg(src + lane + 32 * (v0 + i)), scale);
+              asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(slot + 8 * (lane + 32 * i)), "r"(c.x), "r"(c.y)
+                           : "memory");
+            }
+          fence_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            for (int j = 0; j < n; ++j) {
+              const int r = rows[j];
+              if (r < 0 || r >= C) continue;
+              bulk_store(a.x_q + r * a.H + 256LL * v0, slot, 256u * nv);
+            }
+            tma_store_commit();
+          }
+        }
+        continue;
+      }
       // x[t] into each of the token's rows, 4 KiB at a time: the lanes put the
       // piece into the warp's slot (the first one is already on its way), one
       // lane bulk-copies it to every row
@@ -447,10 +484,17 @@ __global__ void __launch_bounds__(FD_THREADS, 4) dispatch_fused_kernel(FusedArgs
       a.row_token[r] = -1;
       a.row_expert[r] = E;
       a.row_weight[r] = 0.f;
-      if (a.x_disp == nullptr) continue;
-      for (int v0 = 0; v0 < V; v0 += FD_PF)
-        bulk_store(reinterpret_cast<uint8_t*>(a.x_disp) + r * row_bytes + 512LL * v0, zero,
-                   512u * min(FD_PF, V - v0));
+      if constexpr (FP8) {
+        if (a.x_q == nullptr) continue;
+        a.x_scale[r] = 0.f;  // zero codes, scale 0
+        for (int v0 = 0; v0 < V; v0 += FD_PF)
+          bulk_store(a.x_q + r * a.H + 256LL * v0, zero, 256u * min(FD_PF, V - v0));
+      } else {
+        if (a.x_disp == nullptr) continue;
+        for (int v0 = 0; v0 < V; v0 += FD_PF)
+          bulk_store(reinterpret_cast<uint8_t*>(a.x_disp) + r * row_bytes + 512LL * v0, zero,
+                     512u * min(FD_PF, V - v0));
+      }
       tma_store_commit();
     }
   }
@@ -463,9 +507,9 @@ size_t fused_smem_bytes(int E) {
          static_cast<size_t>(FD_WARPS) * FD_MAX_K * sizeof(int);
 }
 
-// CTAs of dispatch_fused_kernel<IN> resident at once on the current device
-// (the last answer is kept per thread).
-template <int IN>
+// CTAs of dispatch_fused_kernel<IN, FP8> resident at once on the current
+// device (the last answer is kept per thread).
+template <int IN, bool FP8>
 int fused_resident_ctas(size_t smem) {
   static thread_local int last_dev = -1;
   static thread_local size_t last_smem = 0;
@@ -474,7 +518,7 @@ int fused_resident_ctas(size_t smem) {
   cudaGetDevice(&dev);
   if (dev == last_dev && smem == last_smem) return last_ctas;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_fused_kernel<IN>, FD_THREADS, smem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_fused_kernel<IN, FP8>, FD_THREADS, smem) !=
           cudaSuccess || per_sm < 1)
     per_sm = 1;
   last_dev = dev;
@@ -483,7 +527,7 @@ int fused_resident_ctas(size_t smem) {
   return last_ctas;
 }
 
-template <int IN>
+template <int IN, bool FP8 = false>
 cudaError_t launch_fused(FusedArgs& a, void* workspace, cudaStream_t s) {
   const size_t cb = layout_counter_bytes(a.T, a.E);
   char* ws = static_cast<char*>(workspace);
@@ -494,14 +538,14 @@ cudaError_t launch_fused(FusedArgs& a, void* workspace, cudaStream_t s) {
   cudaError_t err = cudaMemsetAsync(a.barrier, 0, BARRIER_WORDS * sizeof(unsigned), s);
   if (err != cudaSuccess) return err;
   const size_t smem = fused_smem_bytes(a.E);
-  static bool configured[64][2] = {};
+  static bool configured[64] = {};  // one table per instantiation
   int dev = 0;
   if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
-  if (dev < 0 || dev >= 64 || !configured[dev][IN]) {
-    err = cudaFuncSetAttribute(dispatch_fused_kernel<IN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    err = cudaFuncSetAttribute(dispatch_fused_kernel<IN, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(fused_smem_bytes(1024)));
     if (err != cudaSuccess) return err;
-    if (dev >= 0 && dev < 64) configured[dev][IN] = true;
+    if (dev >= 0 && dev < 64) configured[dev] = true;
   }
   // phase D has T + (C - N) warp items, and N is at most T * K; a CTA per 8
   // of them, at most every resident CTA (more CTAs than the work needs only
@@ -510,7 +554,7 @@ cudaError_t launch_fused(FusedArgs& a, void* workspace, cudaStream_t s) {
   const long long tk = static_cast<long long>(a.T) * a.K;
   const long long items = a.T + (a.capacity > tk ? a.capacity - tk : 0);
   const long long want = (items + FD_WARPS - 1) / FD_WARPS;
-  const int resident = fused_resident_ctas<IN>(smem);
+  const int resident = fused_resident_ctas<IN, FP8>(smem);
   const int grid = static_cast<int>(want < resident ? (want > a.chunks ? want : a.chunks) : resident);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid > 0 ? grid : 1);
@@ -522,7 +566,7 @@ cudaError_t launch_fused(FusedArgs& a, void* workspace, cudaStream_t s) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, dispatch_fused_kernel<IN>, a);
+  return cudaLaunchKernelEx(&cfg, dispatch_fused_kernel<IN, FP8>, a);
 }
 
 void fill_common(FusedArgs& a, const moe_layout& L, int H, const uint16_t* x, uint16_t* x_disp,
@@ -563,6 +607,19 @@ cudaError_t launch_dispatch_fused_map(const uint8_t* routing_map, const float* p
   a.map = routing_map;
   a.probs = probs;
   return launch_fused<IN_MAP>(a, L.workspace, s);
+}
+
+cudaError_t launch_dispatch_fused_map_fp8(const uint8_t* routing_map, const float* probs, const moe_layout& L,
+                                          int H, const uint16_t* x, uint8_t* x_q, float* x_scale, int* readback,
+                                          cudaStream_t s) {
+  FusedArgs a = {};
+  fill_common(a, L, H, x, nullptr, readback);
+  a.x = x;
+  a.x_q = x_q;
+  a.x_scale = x_scale;
+  a.map = routing_map;
+  a.probs = probs;
+  return launch_fused<IN_MAP, true>(a, L.workspace, s);
 }
 
 cudaError_t launch_dispatch_fused_topk(const int64_t* topk_idx, const float* topk_probs,

@@ -11,47 +11,13 @@
 // ...  A first pass finds the row's amax (warp max), a second re-reads the
 // row (now in L1), converts it and stores 8 codes per vector.
 
-#include <cuda_fp8.h>
-
 #include "common.cuh"
+#include "fp8_quant.cuh"
 #include "launch.h"
 
 namespace moe {
 
 namespace {
-
-constexpr float E4M3_MAX = 448.0f;
-
-__device__ __forceinline__ float bf16_abs_max8(uint4 q) {
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-  float m = 0.f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
-  return m;
-}
-
-__device__ __forceinline__ uint32_t e4m3_of(float v) {
-  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
-}
-
-// 8 bf16 values / scale -> 8 e4m3 codes, in element order (lowest byte first).
-__device__ __forceinline__ uint2 quantize8(uint4 q, float scale) {
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-  uint32_t c[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    c[i] = e4m3_of(bf16_lo(w[i]) / scale) | (e4m3_of(bf16_hi(w[i]) / scale) << 8);
-  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-}
-
-// The scale of a warp-owned row (V vectors per lane).
-__device__ __forceinline__ float row_scale(const uint4* src, int V, int lane) {
-  float amax = 0.f;
-  for (int v = 0; v < V; ++v) amax = fmaxf(amax, bf16_abs_max8(__ldg(src + lane + 32 * v)));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(FULL_MASK, amax, o));
-  return amax > 0.f ? amax / E4M3_MAX : 1.0f;
-}
 
 // a4 in e4m3.  Items [0, T): tokens -- the token's row is quantized once and
 // its codes and scale written to each of its rows.  Items [T, T + C): rows --

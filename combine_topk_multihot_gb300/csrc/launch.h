@@ -134,6 +134,11 @@ bool dispatch_fused_fits(const moe_layout& L);
 cudaError_t launch_dispatch_fused_map(const uint8_t* routing_map, const float* probs, const moe_layout& L,
                                       int H, const uint16_t* x, uint16_t* x_disp, int* readback,
                                       cudaStream_t s);
+// The same from a multihot map, with the rows as e4m3 codes and one fp32
+// scale per row (x_q [capacity, H], x_scale [capacity]).
+cudaError_t launch_dispatch_fused_map_fp8(const uint8_t* routing_map, const float* probs, const moe_layout& L,
+                                          int H, const uint16_t* x, uint8_t* x_q, float* x_scale, int* readback,
+                                          cudaStream_t s);
 cudaError_t launch_dispatch_fused_topk(const int64_t* topk_idx, const float* topk_probs,
                                        uint8_t* routing_map, float* probs, int8_t* winner,
                                        const moe_layout& L, int H, const uint16_t* x, uint16_t* x_disp,

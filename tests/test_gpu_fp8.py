@@ -44,8 +44,12 @@ def test_quantize_rows_bit_exact(moe, rows, cols, scale):
 
 
 @pytest.mark.parametrize("host_sync", [True, False])
-@pytest.mark.parametrize("T,H,E,K,P,drop", [(64, 256, 8, 2, 16, 0.0), (513, 512, 32, 8, 128, 0.1),
-                                            (1, 2048, 128, 8, 1, 0.0)])
+@pytest.mark.parametrize("T,H,E,K,P,drop", [
+    (64, 256, 8, 2, 16, 0.0),      # two chunks: the layout kernel, then the FP8 row kernel
+    (513, 512, 32, 8, 128, 0.1),   # 17 chunks: the fused cooperative dispatch writes the e4m3 rows
+    (600, 4096, 16, 4, 64, 0.05),  # fused, each row in two 2 KiB pieces of codes
+    (1, 2048, 128, 8, 1, 0.0),
+])
 def test_dispatch_fp8_bit_exact(moe, T, H, E, K, P, drop, host_sync):
     idx, p = random_routing(T, E, K, seed=T + H, drop=drop)
     x = torch.randn(T, H, generator=torch.Generator().manual_seed(T)).to(torch.bfloat16)
