@@ -208,7 +208,7 @@ def step_launches(T: int, H: int, E: int, C: int, fp8: bool, gather: bool, backw
     The dispatch of a layer of more than 8 chunks of 32 tokens is one
     cooperative kernel, which in the bf16 step also does the multihot step; the
     --gather step runs the multihot kernel and that kernel without rows, the
-    FP8 step the multihot kernel and that kernel with e4m3 rows.  Smaller layers run the
+    FP8 step that kernel with e4m3 rows (the multihot step included).  Smaller layers run the
     multihot kernel, the barrier-free layout kernel and the row copy, except
     that a layer of at most two chunks, whose one-CTA layout fits 48 KiB of
     shared memory and whose row pass has at most 64 items (tokens + rows) and
@@ -216,7 +216,7 @@ def step_launches(T: int, H: int, E: int, C: int, fp8: bool, gather: bool, backw
     chunks = -(-T // 32)
     fused_smem = (4 * E + 2) * 4 + 8 * 128 * 4
     if chunks > 8 and fused_smem <= 48 * 1024:
-        n = 2 if (gather or fp8) else 1
+        n = 2 if gather else 1
     elif chunks > 8:
         n = 3
     else:
@@ -341,8 +341,9 @@ def run_ours(args, world, rank, local, leg: bool = False):
         x_q = (torch.empty(C, H, dtype=torch.uint8, device=dev), torch.empty(C, dtype=torch.float32, device=dev))
     stream = torch.cuda.current_stream()
     ev = lambda: torch.cuda.Event(enable_timing=True)
-    # the bf16 path calls moe_dispatch_topk: the multihot step and the dispatch in one call
-    fused_topk = not (fp8 or gather)
+    # the bf16 and FP8 paths call moe_dispatch_topk(_fp8): the multihot step and
+    # the dispatch in one call
+    fused_topk = not gather
     mh = (torch.empty(T, E, dtype=torch.uint8, device=dev), torch.empty(T, E, dtype=torch.float32, device=dev),
           torch.empty(T, E, dtype=torch.int8, device=dev))
     bwd = cfg.backward
@@ -359,7 +360,13 @@ def run_ours(args, world, rank, local, leg: bool = False):
         rec = (lambda j: events[j].record(stream)) if events else (lambda j: None)
         o_buf = out if out_buf is None else out_buf
         rec(0)
-        if fused_topk:  # the multihot step runs inside the dispatch call (its stage is 0)
+        if fused_topk and fp8:  # the multihot step runs inside the dispatch call (its stage is 0)
+            _, _, (rmap, probs, win), _ = moe.moe_dispatch_topk_fp8(L["x"], L["topk_idx"], L["topk_probs"], lay,
+                                                                    host_sync=host_sync, out=x_q, multihot=mh)
+            rec(2)
+            moe.moe_grouped_experts_fp8(x_q[0], x_q[1], lay, L["W1q"], L["W1s"], L["W2"], out=bufs)
+            rec(3)
+        elif fused_topk:
             _, (rmap, probs, win), _ = moe.moe_dispatch_topk(L["x"], L["topk_idx"], L["topk_probs"], lay,
                                                              host_sync=host_sync, x_disp=x_disp, multihot=mh)
             rec(2)
@@ -370,11 +377,6 @@ def run_ours(args, world, rank, local, leg: bool = False):
             rec(1)
         if fused_topk:
             pass
-        elif fp8:
-            moe.moe_dispatch_fp8(L["x"], rmap, probs, lay, host_sync=host_sync, out=x_q)
-            rec(2)
-            moe.moe_grouped_experts_fp8(x_q[0], x_q[1], lay, L["W1q"], L["W1s"], L["W2"], out=bufs)
-            rec(3)
         elif gather:
             moe.moe_dispatch_layout(rmap, probs, lay, host_sync=host_sync)
             rec(2)
@@ -509,11 +511,12 @@ def run_ours(args, world, rank, local, leg: bool = False):
                 rmap, probs, _ = moe.moe_route_to_multihot(L["topk_idx"], L["topk_probs"], E, lay_sf.status)
             a, b = ev(), ev()
             a.record(stream)
-            if fused_topk:
+            if fused_topk and fp8:
+                moe.moe_dispatch_topk_fp8(L["x"], L["topk_idx"], L["topk_probs"], lay_sf, host_sync=False,
+                                          out=xq_sf, multihot=mh)
+            elif fused_topk:
                 moe.moe_dispatch_topk(L["x"], L["topk_idx"], L["topk_probs"], lay_sf, host_sync=False,
                                       x_disp=xd_sf, multihot=mh)
-            elif fp8:
-                moe.moe_dispatch_fp8(L["x"], rmap, probs, lay_sf, host_sync=False, out=xq_sf)
             elif gather:
                 moe.moe_dispatch_layout(rmap, probs, lay_sf, host_sync=False)
             else:

@@ -70,6 +70,7 @@ SIGNATURES = {
     "moe_grouped_experts_fp8": (c_int32, [_P, _P, _LP, c_int32, c_int32, _P, _P, _P, _P, _P, _P]),
     "moe_dispatch": (c_int32, [_P, _P, _P, c_int32, _LP, _P, ctypes.POINTER(c_int64), _P]),
     "moe_dispatch_topk": (c_int32, [_P, _P, _P, c_int32, _LP, _P, _P, _P, _P, ctypes.POINTER(c_int64), _P]),
+    "moe_dispatch_topk_fp8": (c_int32, [_P, _P, _P, c_int32, _LP, _P, _P, _P, _P, _P, ctypes.POINTER(c_int64), _P]),
     "moe_dispatch_static_scratch": (c_int32, [_P, _P, _P, c_int32, _LP, _P, ctypes.POINTER(c_int64), _P]),
     "moe_grouped_experts": (c_int32, [_P, _LP, c_int32, c_int32, _P, _P, _P, _P, _P, _P, _P]),
     "moe_combine": (c_int32, [_P, _LP, c_int32, _P, _P]),

@@ -261,12 +261,12 @@ moe_status dispatch_impl(const char* who, const moe_bf16* x, const uint8_t* rout
   bool rows_done = false;  // the layout kernel did the row pass itself
   const bool bf16_rows = x_disp || layout_only;
   const bool fp8_rows = !bf16_rows && x_q != nullptr;
-  const bool fused = (bf16_rows || (fp8_rows && !topk_idx)) && dispatch_fused_fits(*L);
+  const bool fused = (bf16_rows || fp8_rows) && dispatch_fused_fits(*L);
   const uint16_t* x16 = reinterpret_cast<const uint16_t*>(x);
   uint16_t* xd16 = reinterpret_cast<uint16_t*>(x_disp);
   int* rb_kernel = mapped ? rb_dev : nullptr;
   if (topk_idx && !fused) {
-    // small layers and the FP8 rows from the top-k: the multihot step first, then the layout from its map
+    // small layers: the multihot step first, then the layout from its map
     if ((err = launch_multihot(topk_idx, topk_probs, L->T, L->K, L->E, const_cast<uint8_t*>(routing_map),
                                const_cast<float*>(probs), winner, L->status, stream)) != cudaSuccess) {
       if (mapped) rb_lock.unlock();
@@ -274,12 +274,16 @@ moe_status dispatch_impl(const char* who, const moe_bf16* x, const uint8_t* rout
     }
   }
   if (fused) {
-    err = topk_idx ? launch_dispatch_fused_topk(topk_idx, topk_probs, const_cast<uint8_t*>(routing_map),
-                                                const_cast<float*>(probs), winner, *L, H, x16, xd16, rb_kernel,
-                                                stream)
-                   : fp8_rows ? launch_dispatch_fused_map_fp8(routing_map, probs, *L, H, x16, x_q, x_scale, rb_kernel,
-                                                              stream)
-                              : launch_dispatch_fused_map(routing_map, probs, *L, H, x16, xd16, rb_kernel, stream);
+    if (topk_idx)
+      err = fp8_rows ? launch_dispatch_fused_topk_fp8(topk_idx, topk_probs, const_cast<uint8_t*>(routing_map),
+                                                      const_cast<float*>(probs), winner, *L, H, x16, x_q, x_scale,
+                                                      rb_kernel, stream)
+                     : launch_dispatch_fused_topk(topk_idx, topk_probs, const_cast<uint8_t*>(routing_map),
+                                                  const_cast<float*>(probs), winner, *L, H, x16, xd16, rb_kernel,
+                                                  stream);
+    else
+      err = fp8_rows ? launch_dispatch_fused_map_fp8(routing_map, probs, *L, H, x16, x_q, x_scale, rb_kernel, stream)
+                     : launch_dispatch_fused_map(routing_map, probs, *L, H, x16, xd16, rb_kernel, stream);
     if (err != cudaSuccess) {
       if (mapped) cudaStreamSynchronize(stream);  // the kernel may still write the readback buffer
       return cuda_fail(err, "dispatch: fused layout and rows");
@@ -376,6 +380,19 @@ moe_status moe_dispatch_topk(const moe_bf16* x, const int64_t* topk_idx, const f
   return dispatch_impl("moe_dispatch_topk", x, routing_map, probs, H, L, x_disp, nullptr, nullptr,
                        rows_host, stream, false, topk_idx ? topk_idx : &no_slots, topk_probs,
                        winner_slot);
+}
+
+moe_status moe_dispatch_topk_fp8(const moe_bf16* x, const int64_t* topk_idx, const float* topk_probs,
+                                 int32_t H, const moe_layout* L, uint8_t* routing_map, float* probs,
+                                 int8_t* winner_slot, uint8_t* x_disp_q, float* x_disp_scale, int64_t* rows_host,
+                                 moe_stream_t stream) {
+  MOE_REQUIRE(L == nullptr || L->capacity == 0 || (x_disp_q && x_disp_scale), MOE_ERR_INVALID_ARG,
+              "moe_dispatch_topk_fp8: NULL x_disp_q or x_disp_scale");
+  MOE_REQUIRE(L == nullptr || L->T == 0 || (topk_idx && topk_probs), MOE_ERR_INVALID_ARG,
+              "moe_dispatch_topk_fp8: NULL top-k input");
+  static const int64_t no_slots = 0;  // T == 0: marks the top-k input without reading it
+  return dispatch_impl("moe_dispatch_topk_fp8", x, routing_map, probs, H, L, nullptr, x_disp_q, x_disp_scale,
+                       rows_host, stream, false, topk_idx ? topk_idx : &no_slots, topk_probs, winner_slot);
 }
 
 moe_status moe_dispatch_fp8(const moe_bf16* x, const uint8_t* routing_map, const float* probs,

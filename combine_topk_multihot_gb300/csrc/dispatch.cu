@@ -636,4 +636,21 @@ cudaError_t launch_dispatch_fused_topk(const int64_t* topk_idx, const float* top
   return launch_fused<IN_TOPK>(a, L.workspace, s);
 }
 
+cudaError_t launch_dispatch_fused_topk_fp8(const int64_t* topk_idx, const float* topk_probs,
+                                           uint8_t* routing_map, float* probs, int8_t* winner,
+                                           const moe_layout& L, int H, const uint16_t* x, uint8_t* x_q,
+                                           float* x_scale, int* readback, cudaStream_t s) {
+  FusedArgs a = {};
+  fill_common(a, L, H, x, nullptr, readback);
+  a.x = x;
+  a.x_q = x_q;
+  a.x_scale = x_scale;
+  a.topk_idx = topk_idx;
+  a.topk_probs = topk_probs;
+  a.map_out = routing_map;
+  a.probs_out = probs;
+  a.winner_out = winner;
+  return launch_fused<IN_TOPK, true>(a, L.workspace, s);
+}
+
 }  // namespace moe

@@ -143,6 +143,10 @@ cudaError_t launch_dispatch_fused_topk(const int64_t* topk_idx, const float* top
                                        uint8_t* routing_map, float* probs, int8_t* winner,
                                        const moe_layout& L, int H, const uint16_t* x, uint16_t* x_disp,
                                        int* readback, cudaStream_t s);
+cudaError_t launch_dispatch_fused_topk_fp8(const int64_t* topk_idx, const float* topk_probs,
+                                           uint8_t* routing_map, float* probs, int8_t* winner,
+                                           const moe_layout& L, int H, const uint16_t* x, uint8_t* x_q,
+                                           float* x_scale, int* readback, cudaStream_t s);
 // Rows of the expanded layout from token rows (a4: x -> x_disp, plus the pad /
 // spare rows' metadata when from_offsets); also the combine backward (a7)
 // with the optional routing-weight gradient (a8).  Each token row is read

@@ -240,6 +240,31 @@ def moe_dispatch_fp8(x: torch.Tensor, routing_map: torch.Tensor, probs: torch.Te
     return q, sc, ((int(rows[0]), int(rows[1])) if host_sync else None)
 
 
+def moe_dispatch_topk_fp8(x: torch.Tensor, topk_idx: torch.Tensor, topk_probs: torch.Tensor, layout: Layout,
+                          host_sync: bool = True, out=None, multihot=None, stream=None):
+    """a1-a4 in one call with e4m3 rows: the multihot step and the FP8
+    dispatch from the top-k choices.  Returns (x_disp_q uint8 [C, H],
+    x_disp_scale fp32 [C], (routing_map, probs, winner_slot), (R, N) or None);
+    ``out`` optionally gives the two row buffers, ``multihot`` the three
+    multihot outputs."""
+    _bf16(x, "x")
+    assert topk_idx.dtype == torch.int64 and topk_probs.dtype == torch.float32
+    T, H = x.shape
+    E = layout.E
+    C = layout.capacity
+    dev = x.device
+    q = out[0] if out is not None else torch.empty(C, H, dtype=torch.uint8, device=dev)
+    sc = out[1] if out is not None else torch.empty(C, dtype=torch.float32, device=dev)
+    if multihot is None:
+        multihot = (torch.empty(T, E, dtype=torch.uint8, device=dev), torch.empty(T, E, dtype=torch.float32, device=dev),
+                    torch.empty(T, E, dtype=torch.int8, device=dev))
+    rows = (ctypes.c_int64 * 2)() if host_sync else None
+    _check(N.lib.moe_dispatch_topk_fp8(_ptr(x), _ptr(topk_idx), _ptr(topk_probs), H, layout.ref, _ptr(multihot[0]),
+                                       _ptr(multihot[1]), _ptr(multihot[2]), _ptr(q), _ptr(sc), rows,
+                                       _stream(stream)), "moe_dispatch_topk_fp8")
+    return q, sc, tuple(multihot), ((int(rows[0]), int(rows[1])) if host_sync else None)
+
+
 def moe_quantize_fp8(src: torch.Tensor, stream=None):
     """Rowwise e4m3 of a bf16 tensor whose last dimension is the row: returns
     (codes uint8, same shape; scales fp32, shape[:-1])."""

@@ -262,6 +262,24 @@ MOE_API moe_status moe_dispatch_fp8(const moe_bf16* x, const uint8_t* routing_ma
                                     moe_stream_t stream);
 
 /*
+ * a1-a4 in one call with FP8 rows: moe_route_to_multihot followed by
+ * moe_dispatch_fp8, from the top-k choices.  The passages of both.
+ *   topk_idx, topk_probs, routing_map, probs, winner_slot: as for
+ *                moe_dispatch_topk.
+ *   x, L, x_disp_q, x_disp_scale, rows_host, stream: as for
+ *                moe_dispatch_fp8, with the same modes, results and errors.
+ * Layers of more than 8 chunks of 32 tokens run all of it as one cooperative
+ * kernel (the multihot rows, counts, offsets, placement, the e4m3 codes and
+ * scales); smaller ones as the multihot kernel followed by moe_dispatch_fp8's
+ * kernels.
+ */
+MOE_API moe_status moe_dispatch_topk_fp8(const moe_bf16* x, const int64_t* topk_idx,
+                                         const float* topk_probs, int32_t H, const moe_layout* L,
+                                         uint8_t* routing_map, float* probs, int8_t* winner_slot,
+                                         uint8_t* x_disp_q, float* x_disp_scale, int64_t* rows_host,
+                                         moe_stream_t stream);
+
+/*
  * Rowwise e4m3 quantization of a bf16 matrix [rows, cols] (cols a multiple
  * of 256, src and codes 16-byte aligned), with the rule of moe_dispatch_fp8:
  * codes [rows, cols] uint8 and scales [rows] fp32 (out).  For the gate/up

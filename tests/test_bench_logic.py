@@ -36,7 +36,7 @@ def test_launches_per_step(name, expected):
 
 def test_fp8_dispatch_is_fused_above_eight_chunks():
     assert _launches("decode_1", fp8=True) == 6           # multihot, layout, FP8 rows
-    assert _launches("qwen3_30b_a3b", fp8=True) == 5      # multihot, the fused dispatch with e4m3 rows
+    assert _launches("qwen3_30b_a3b", fp8=True) == 4      # the fused dispatch (multihot included) with e4m3 rows
 
 
 def test_gather_step_runs_the_multihot_kernel_and_the_layout():

@@ -6,8 +6,8 @@ workspaces -- is the middle of a larger allocation whose 4 KiB on either side
 hold a canary byte.  One whole layer runs through the C ABI (multihot,
 dispatch in both modes and from the top-k, both expert forwards, combine,
 both combine backwards, both expert backwards, dispatch and multihot
-backward, the FP8 dispatch and gate/up GEMM, the gathered gate/up GEMM, the
-router), then every canary must be intact and the status word clear.  The
+backward, the FP8 dispatch (from the multihot map and from the top-k) and
+gate/up GEMM, the gathered gate/up GEMM, the router), then every canary must be intact and the status word clear.  The
 shapes cover the one-CTA and cooperative layouts, one-CTA and CTA-pair GEMM
 tiles, 128-row tiles with ragged groups, and the CUDA-core decode experts.
 """
@@ -123,6 +123,11 @@ def test_no_write_outside_any_output(moe, T, H, E, K, I, P):
     Lq = _layout(moe, g, T, E, K, P, C)
     xq, xs = g((C, H), torch.uint8), g((C,), torch.float32)
     assert N.lib.moe_dispatch_fp8(_p(x), _p(rmap), _p(probs), H, Lq.ref, _p(xq), _p(xs), None, st()) == 0
+    Lq2 = _layout(moe, g, T, E, K, P, C)
+    xq2, xs2 = g((C, H), torch.uint8), g((C,), torch.float32)
+    m3 = g((T, E), torch.uint8), g((T, E), torch.float32), g((T, E), torch.int8)
+    assert N.lib.moe_dispatch_topk_fp8(_p(x), _p(idx), _p(p), H, Lq2.ref, _p(m3[0]), _p(m3[1]), _p(m3[2]),
+                                       _p(xq2), _p(xs2), rows, st()) == 0
     h4, y4 = g((C, I), bf), g((C, H), bf)
     assert N.lib.moe_grouped_experts_fp8(_p(xq), _p(xs), Lq.ref, H, I, _p(w1q), _p(w1s), _p(W2), _p(h4),
                                          _p(y4), st()) == 0

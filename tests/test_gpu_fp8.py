@@ -69,6 +69,39 @@ def test_dispatch_fp8_bit_exact(moe, T, H, E, K, P, drop, host_sync):
     assert int(status.item()) == 0
 
 
+@pytest.mark.parametrize("host_sync", [True, False])
+@pytest.mark.parametrize("T,H,E,K,P,drop,dup", [
+    (64, 256, 8, 2, 16, 0.0, 0.0),       # two chunks: the multihot kernel, the layout, the FP8 rows
+    (513, 512, 32, 8, 128, 0.1, 0.05),   # one cooperative kernel from the top-k, drops and duplicates
+    (600, 4096, 16, 4, 64, 0.05, 0.0),   # the same, two 2 KiB pieces of codes per row
+])
+def test_dispatch_topk_fp8_bit_exact(moe, T, H, E, K, P, drop, dup, host_sync):
+    """moe_dispatch_topk_fp8 = moe_route_to_multihot + moe_dispatch_fp8: the
+    multihot outputs, the layout, the codes and the scales all equal the
+    oracle's."""
+    idx, p = random_routing(T, E, K, seed=T + H + 1, drop=drop, dup=dup)
+    x = torch.randn(T, H, generator=torch.Generator().manual_seed(T + 1)).to(torch.bfloat16)
+    C = O.worst_case_capacity(T, E, K, P)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    L = moe.Layout(T, E, K, P, C, device=DEV, status=status)
+    q, sc, (rmap, probs, win), rows = moe.moe_dispatch_topk_fp8(x.to(DEV), idx.to(DEV), p.to(DEV), L,
+                                                                host_sync=host_sync)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rm, pr, wn = O.route_to_multihot(idx.numpy(), p.numpy(), E)
+    assert np.array_equal(rmap.cpu().numpy(), rm)
+    assert np.array_equal(probs.cpu().numpy(), pr)
+    assert np.array_equal(win.cpu().numpy(), wn)
+    Lr = O.build_layout(rm, pr, K, P, C)
+    for k in ("row_token", "row_expert", "token_row"):
+        assert np.array_equal(getattr(L, k).cpu().numpy().reshape(np.shape(Lr[k])), Lr[k]), k
+    if host_sync:
+        assert rows == (Lr["rows_used"], Lr["rows_valid"])
+    ref_q, ref_s = O.dispatch_fp8(bits(x), Lr["row_token"])
+    assert np.array_equal(q.cpu().numpy(), ref_q)
+    assert np.array_equal(sc.cpu().numpy(), ref_s)
+
+
 def _run_fp8_experts(moe, x, idx, p, W1, W2, E, K, P, host_sync=True):
     """The FP8 path on the GPU: multihot, FP8 dispatch, W1 quantization, experts."""
     T, H = x.shape
