@@ -144,6 +144,7 @@ def _check_fp8_experts(L, out, x, idx, p, W1, W2, E, K, P, I, experts=None, rows
     (300, 512, 8, 2, 256, 16),      # 64-column tiles, several 128-row tiles
     (5, 1024, 8, 4, 384, 1),        # 64-column tiles with a 32-row A slot
     (2000, 512, 40, 4, 512, 1),     # 256-column tiles, two 128-row tiles per expert
+    (2304, 256, 256, 8, 128, 1),    # 256 experts: the per-expert tables take a pipeline stage
 ])
 def test_experts_fp8_match_oracle(moe, T, H, E, K, I, P):
     seed = T + 7 * I
