@@ -1,5 +1,6 @@
 // a1-a4 in one cooperative launch: from the top-k choices (or the multihot
-// routing map) to the expanded layout with every row copied.
+// routing map) to the expanded layout with every row copied, as bf16 or (the
+// FP8 dispatch) as e4m3 codes with one scale per row.
 //
 // "feat: add hybridep (NVIDIA-NeMo/Automodel #1333)", Changelog: top-k indices
 // become multihot routing data (a routing_map and fp32 per-(token, expert)
