@@ -72,20 +72,35 @@ def test_dispatch_fp8_bit_exact(moe, T, H, E, K, P, drop, host_sync):
 @pytest.mark.parametrize("host_sync", [True, False])
 @pytest.mark.parametrize("T,H,E,K,P,drop,dup", [
     (64, 256, 8, 2, 16, 0.0, 0.0),       # two chunks: the multihot kernel, the layout, the FP8 rows
+    (256, 512, 128, 8, 1, 0.05, 0.05),   # 8 chunks: the multihot kernel, then the barrier-free layout
     (513, 512, 32, 8, 128, 0.1, 0.05),   # one cooperative kernel from the top-k, drops and duplicates
     (600, 4096, 16, 4, 64, 0.05, 0.0),   # the same, two 2 KiB pieces of codes per row
+    (333, 512, 64, 40, 2, 0.2, 0.2),     # K > 32: slots in two registers per lane
+    (700, 256, 1024, 4, 1, 0.0, 0.0),    # the largest E
+    (40000, 256, 128, 8, 4, 0.05, 0.0),  # more chunks than resident CTAs
+    (0, 256, 8, 2, 16, 0.0, 0.0),        # no tokens: spare rows only
 ])
 def test_dispatch_topk_fp8_bit_exact(moe, T, H, E, K, P, drop, dup, host_sync):
     """moe_dispatch_topk_fp8 = moe_route_to_multihot + moe_dispatch_fp8: the
     multihot outputs, the layout, the codes and the scales all equal the
-    oracle's."""
+    oracle's, with every output buffer poisoned first so that each entry must
+    be written."""
     idx, p = random_routing(T, E, K, seed=T + H + 1, drop=drop, dup=dup)
     x = torch.randn(T, H, generator=torch.Generator().manual_seed(T + 1)).to(torch.bfloat16)
     C = O.worst_case_capacity(T, E, K, P)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     L = moe.Layout(T, E, K, P, C, device=DEV, status=status)
+    L.row_token.fill_(12345)
+    L.row_expert.fill_(-7)
+    L.row_weight.fill_(float("nan"))
+    L.token_row.fill_(999)
+    q = torch.full((C, H), 0x7F, dtype=torch.uint8, device=DEV)
+    sc = torch.full((C,), float("nan"), dtype=torch.float32, device=DEV)
+    mh = (torch.full((T, E), 7, dtype=torch.uint8, device=DEV),
+          torch.full((T, E), float("nan"), dtype=torch.float32, device=DEV),
+          torch.full((T, E), 5, dtype=torch.int8, device=DEV))
     q, sc, (rmap, probs, win), rows = moe.moe_dispatch_topk_fp8(x.to(DEV), idx.to(DEV), p.to(DEV), L,
-                                                                host_sync=host_sync)
+                                                                host_sync=host_sync, out=(q, sc), multihot=mh)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     rm, pr, wn = O.route_to_multihot(idx.numpy(), p.numpy(), E)
@@ -95,6 +110,7 @@ def test_dispatch_topk_fp8_bit_exact(moe, T, H, E, K, P, drop, dup, host_sync):
     Lr = O.build_layout(rm, pr, K, P, C)
     for k in ("row_token", "row_expert", "token_row"):
         assert np.array_equal(getattr(L, k).cpu().numpy().reshape(np.shape(Lr[k])), Lr[k]), k
+    assert np.array_equal(L.row_weight.cpu().numpy(), Lr["row_weight"])
     if host_sync:
         assert rows == (Lr["rows_used"], Lr["rows_valid"])
     ref_q, ref_s = O.dispatch_fp8(bits(x), Lr["row_token"])
