@@ -457,6 +457,48 @@ def test_experts_inference_match_oracle(moe, T, H, E, K, I, P):
 
 
 @pytest.mark.parametrize("save", [False, True])
+def test_pair_gemm_repeated_launches_identical(moe, save):
+    """Forty launch pairs of the CTA-pair GEMMs back to back on one stream:
+    each pair takes the next of the 16 rotating slots of row-chunk readiness
+    counters, which the down launch's last CTA clears for its next use.  A slot
+    left dirty would let a down tile read h before it is written; every
+    output must equal the first launch's bit for bit, and the first the
+    oracle's within the bf16 tolerance."""
+    T, H, E, K, I, P = 1500, 512, 40, 8, 512, 16
+    idx, p = random_routing(T, E, K, seed=77, drop=0.05)
+    gen = torch.Generator().manual_seed(78)
+    x = torch.randn(T, H, generator=gen).to(torch.bfloat16)
+    W1 = (torch.randn(E, 2 * I, H, generator=gen) * 0.02).to(torch.bfloat16).to(DEV)
+    W2 = (torch.randn(E, H, I, generator=gen) * 0.02).to(torch.bfloat16).to(DEV)
+    C = O.worst_case_capacity(T, E, K, P)
+    L = moe.Layout(T, E, K, P, C, device=DEV)
+    xd, _, _ = moe.moe_dispatch_topk(x.to(DEV), idx.to(DEV), p.to(DEV), L, host_sync=False)
+    first = moe.moe_grouped_experts(xd, L, W1, W2, save_o=save, save_gu=save)
+    ref = {k: v.clone() for k, v in first.items() if v is not None}
+    valid_t = L.row_token >= 0  # the rows every launch writes
+    outs = [dict(h=torch.empty_like(ref["h"]), y=torch.empty_like(ref["y"])) for _ in range(2)]
+    for n in range(40):
+        o = outs[n % 2]
+        o["h"].fill_(float("nan"))
+        o["y"].fill_(float("nan"))
+        if save:
+            o["o"], o["gu"] = torch.empty_like(ref["o"]), torch.empty_like(ref["gu"])
+        moe.moe_grouped_experts(xd, L, W1, W2, save_o=save, save_gu=save, out=o)
+        if n % 2:
+            torch.cuda.synchronize()
+            for k in ("h", "y"):
+                for oo in outs:
+                    assert torch.equal(oo[k][valid_t].view(torch.int16), ref[k][valid_t].view(torch.int16)), (n, k)
+    torch.cuda.synchronize()
+    assert int(L.status.item()) == 0
+    Lr = O.build_layout(*O.route_to_multihot(idx.numpy(), p.numpy(), E)[:2], K, P, C)
+    y, h, _ = O.grouped_experts(bits(xd), Lr["row_expert"], Lr["row_weight"], bits(W1), bits(W2), I)
+    valid = Lr["row_token"] >= 0
+    assert_gemm_close(bits(ref["h"])[valid], h[valid], "h", intermediate=True)
+    assert_gemm_close(bits(ref["y"])[valid], y[valid], "y")
+
+
+@pytest.mark.parametrize("save", [False, True])
 def test_experts_sentinel_rows(moe, save):
     """Spare rows (R..C-1) are never written by the experts.  Pad rows inside
     an expert's group are left untouched in inference and written as zeros
